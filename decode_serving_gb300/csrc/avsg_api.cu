@@ -1,0 +1,578 @@
+// The C interface declared in avsg.h: handle life cycle, argument checks,
+// device-state layout, and the order in which a step's kernels are enqueued.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <vector>
+
+#include "avsg_internal.cuh"
+
+using namespace avsg;
+
+struct avsg_handle_s {
+  avsg_config cfg{};
+  DeviceState ds{};
+  int device = 0, num_sms = 0, gather_ctas = 0, splits_cap = 0, target_ctas = 0, tile_rows = 0;
+  void* dev_block = nullptr;
+  size_t dev_bytes = 0;
+  const void* host_k = nullptr;
+  const void* host_v = nullptr;
+  bool reg_k = false, reg_v = false;
+  bool no_reuse = false;
+  bool has_t = false;
+  int32_t last_t = -1;
+  bool latched = false;
+  cudaStream_t last_stream = nullptr;
+  cudaError_t cuda_err = cudaSuccess;
+  uint64_t steps = 0, selected = 0, host_misses = 0;
+  float scale_log2 = 0.f;
+  int32_t* slot_scratch = nullptr;  // [U][max_union] when the caller passes no slot map
+  uint8_t* hit_scratch = nullptr;   // [U][max_union]
+  int32_t* stage_sel = nullptr;     // avsg_step_host staging
+  float* stage_q = nullptr;
+  float* stage_out = nullptr;
+  // profiling
+  bool prof = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  struct Rec {
+    int kernel;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  double prof_ms[4] = {0, 0, 0, 0};
+  uint64_t prof_launches[4] = {0, 0, 0, 0};
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+int fail_cuda(avsg_handle h, cudaError_t e) {
+  if (h) h->cuda_err = e;
+  return AVSG_ERR_CUDA;
+}
+
+int pow2_at_least(int64_t x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+int log2_exact(int p) {
+  int l = 0;
+  while ((1 << l) < p) ++l;
+  return l;
+}
+
+// Carves one device allocation into aligned arrays.
+struct Carver {
+  size_t off = 0;
+  template <typename T>
+  size_t take(T** slot, size_t count) {
+    off = (off + kAlign - 1) / kAlign * kAlign;
+    const size_t at = off;
+    off += sizeof(T) * (count ? count : 1);
+    *slot = reinterpret_cast<T*>(at);  // offset for now, rebased later
+    return at;
+  }
+};
+
+template <typename T>
+void rebase(T** p, void* base) {
+  *p = reinterpret_cast<T*>(static_cast<char*>(base) + reinterpret_cast<size_t>(*p));
+}
+
+// Maps caller host memory for device reads: mapped allocations are used in
+// place, anything else is registered here (and unregistered on destroy).
+int map_host(avsg_handle h, const void* p, size_t bytes, const unsigned char** dptr, bool* registered) {
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e == cudaSuccess && attr.type == cudaMemoryTypeHost && attr.devicePointer) {
+    *dptr = static_cast<const unsigned char*>(attr.devicePointer);
+    *registered = false;
+    return AVSG_OK;
+  }
+  cudaGetLastError();
+  e = cudaHostRegister(const_cast<void*>(p), bytes, cudaHostRegisterMapped | cudaHostRegisterReadOnly);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    e = cudaHostRegister(const_cast<void*>(p), bytes, cudaHostRegisterMapped);
+  }
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  *registered = true;
+  void* d = nullptr;
+  e = cudaHostGetDevicePointer(&d, const_cast<void*>(p), 0);
+  if (e != cudaSuccess) {
+    cudaHostUnregister(const_cast<void*>(p));
+    *registered = false;
+    return fail_cuda(h, e);
+  }
+  *dptr = static_cast<const unsigned char*>(d);
+  return AVSG_OK;
+}
+
+void release(avsg_handle h) {
+  if (!h) return;
+  for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
+  if (h->dev_block) cudaFree(h->dev_block);
+  if (h->reg_k && h->host_k) cudaHostUnregister(const_cast<void*>(h->host_k));
+  if (h->reg_v && h->host_v) cudaHostUnregister(const_cast<void*>(h->host_v));
+  delete h;
+}
+
+// Splits of a (unit, token)'s entries over CTAs: about target_ctas CTAs in all,
+// each with at least one tile of rows.
+int attn_splits(const avsg_handle h, int n_tok, int k) {
+  const int64_t pairs = (int64_t)h->ds.U * n_tok;
+  int64_t s = (h->target_ctas + pairs - 1) / pairs;
+  const int64_t by_rows = ((int64_t)k * h->ds.ET + h->tile_rows - 1) / h->tile_rows;
+  if (s > by_rows) s = by_rows;
+  if (s > h->splits_cap) s = h->splits_cap;
+  return (int)(s < 1 ? 1 : s);
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  const int x = atoi(v);
+  return x > 0 ? x : dflt;
+}
+
+}  // namespace
+
+namespace {
+
+int init_state(avsg_handle h, cudaStream_t st) {
+  const DeviceState& s = h->ds;
+  const size_t ub = (size_t)s.U * s.B;
+  cudaError_t e = cudaSuccess;
+#define AVSG_SET(ptr, val, bytes) \
+  if (e == cudaSuccess) e = cudaMemsetAsync((ptr), (val), (bytes), st)
+  AVSG_SET(s.kbuf, 0, (size_t)s.U * s.B * s.ek);
+  if (s.ev) AVSG_SET(s.vbuf, 0, (size_t)s.U * s.B * s.ev);
+  if (!h->no_reuse) {
+    AVSG_SET(s.tag, 0xFF, ub * 4);
+    AVSG_SET(s.last, 0xFF, ub * 4);
+    AVSG_SET(s.seen, 0, ub * 4);
+    AVSG_SET(s.htab, 0xFF, (size_t)s.U * s.HS * sizeof(int2));
+    AVSG_SET(s.hused, 0, (size_t)s.U * 4);
+    AVSG_SET(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
+    AVSG_SET(s.mcount, 0, (size_t)s.U * 4);
+  }
+  AVSG_SET(s.desc_count, 0, 4);
+  AVSG_SET(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);
+  AVSG_SET(s.counters, 0, sizeof(DevCounters));
+  AVSG_SET(s.err, 0, sizeof(DevErr));
+#undef AVSG_SET
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  h->has_t = false;
+  h->last_t = -1;
+  h->latched = false;
+  h->steps = h->selected = h->host_misses = 0;
+  return AVSG_OK;
+}
+
+}  // namespace
+
+extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const void* host_v,
+                           avsg_handle* out) {
+  if (!out) return AVSG_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !host_k) return AVSG_ERR_INVALID_ARG;
+  const avsg_config c = *cfg;
+  const bool shared = c.kv_shared != 0;
+  const bool no_reuse = (c.flags & AVSG_FLAG_NO_REUSE) != 0;
+  if (c.num_requests < 1 || c.num_kv_heads < 1 || c.q_per_kv < 1 || c.entry_tokens < 1 ||
+      c.entry_tokens > 64 || c.head_dim < 8 || c.v_dim < 8 || c.head_dim % 8 || c.v_dim % 8 ||
+      c.num_entries < 1 || c.num_entries > 0x7FFFFFFF || c.buffer_slots < 1 || c.max_select < 1 ||
+      c.max_tokens_per_step < 1 || c.max_tokens_per_step > kMaxTokens || c.reserved0 || c.reserved1 ||
+      (c.flags & ~AVSG_FLAG_NO_REUSE) || !(c.softmax_scale >= 0.f) || isinf(c.softmax_scale) ||
+      (shared && (c.v_dim != c.head_dim || (host_v && host_v != host_k))) || (!shared && !host_v))
+    return AVSG_ERR_INVALID_ARG;
+  const int64_t U = (int64_t)c.num_requests * c.num_kv_heads;
+  if (U > 65535) return AVSG_ERR_INVALID_ARG;
+  const int64_t max_union = (int64_t)c.max_tokens_per_step * c.max_select;
+  if (!no_reuse && max_union > c.buffer_slots) return AVSG_ERR_CAPACITY;
+  if (max_union > (1 << 24) || (!no_reuse && c.buffer_slots > (1 << 24))) return AVSG_ERR_INVALID_ARG;
+  if (!attention_supported(c.head_dim, c.v_dim, c.q_per_kv, c.kv_shared)) return AVSG_ERR_UNSUPPORTED;
+  const int64_t ek = (int64_t)c.entry_tokens * c.head_dim * 2;
+  const int64_t ev = shared ? 0 : (int64_t)c.entry_tokens * c.v_dim * 2;
+  if ((double)U * max_union * ((ek + ev) / 16) >= 2147483647.0) return AVSG_ERR_INVALID_ARG;
+
+  avsg_handle h = new avsg_handle_s();
+  h->cfg = c;
+  h->no_reuse = no_reuse;
+  h->host_k = host_k;
+  h->host_v = shared ? nullptr : host_v;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) {
+    release(h);
+    return AVSG_ERR_CUDA;
+  }
+  DeviceState& s = h->ds;
+  s.U = (int32_t)U;
+  s.B = no_reuse ? (int32_t)max_union : c.buffer_slots;
+  s.G = c.q_per_kv;
+  s.D = c.head_dim;
+  s.DV = c.v_dim;
+  s.ET = c.entry_tokens;
+  s.L = c.num_entries;
+  s.kv_shared = shared ? 1 : 0;
+  s.ek = ek;
+  s.ev = ev;
+  s.max_union = (int32_t)max_union;
+  s.HS = pow2_at_least(4LL * (no_reuse ? 1 : c.buffer_slots));
+  s.hs_shift = 32 - log2_exact(s.HS);
+  s.MS = pow2_at_least(2 * max_union);
+  s.MS = s.MS < 2 ? 2 : s.MS;
+  s.ms_shift = 32 - log2_exact(s.MS);
+  if (s.hs_shift >= 32) s.hs_shift = 31;
+  if (s.ms_shift >= 32) s.ms_shift = 31;
+  h->tile_rows = attention_rows_per_tile(s.D, s.DV, s.G, s.kv_shared);
+  h->target_ctas = h->num_sms * env_int("AVSG_ATTN_CTAS_PER_SM", 4);
+  h->gather_ctas = h->num_sms * env_int("AVSG_GATHER_CTAS_PER_SM", 4);
+  {
+    int64_t cap = (h->target_ctas + U - 1) / U;
+    const int64_t by_rows = ((int64_t)c.max_select * c.entry_tokens + h->tile_rows - 1) / h->tile_rows;
+    if (cap > by_rows) cap = by_rows;
+    h->splits_cap = (int)(cap < 1 ? 1 : cap);
+  }
+  const float scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / sqrtf((float)c.head_dim);
+  h->scale_log2 = scale * 1.4426950408889634f;
+
+  int rc = map_host(h, host_k, (size_t)(U * c.num_entries * ek), &s.host_k, &h->reg_k);
+  if (rc == AVSG_OK && !shared)
+    rc = map_host(h, host_v, (size_t)(U * c.num_entries * ev), &s.host_v, &h->reg_v);
+  if (shared) s.host_v = s.host_k;
+  if (rc != AVSG_OK) {
+    release(h);
+    return rc;
+  }
+
+  const bool st_arrays = !no_reuse;
+  const size_t ub = st_arrays ? (size_t)U * s.B : 0;
+  Carver cv;
+  cv.take(&s.kbuf, (size_t)U * s.B * ek);
+  cv.take(&s.vbuf, (size_t)U * s.B * ev);
+  cv.take(&s.tag, ub);
+  cv.take(&s.last, ub);
+  cv.take(&s.seen, ub);
+  cv.take(&s.htab, st_arrays ? (size_t)U * s.HS : 0);
+  cv.take(&s.hused, (size_t)U);
+  cv.take(&s.mset, st_arrays ? (size_t)U * s.MS : 0);
+  cv.take(&s.mslot, st_arrays ? (size_t)U * s.MS : 0);
+  cv.take(&s.mlist, (size_t)U * max_union);
+  cv.take(&s.mcount, (size_t)U);
+  cv.take(&s.desc, (size_t)U * max_union);
+  cv.take(&s.desc_count, 1);
+  cv.take(&s.part, (size_t)U * c.max_tokens_per_step * h->splits_cap * s.G * (s.DV + 2));
+  cv.take(&s.part_count, (size_t)U * kMaxTokens);
+  cv.take(&s.counters, 1);
+  cv.take(&s.err, 1);
+  cv.take(&h->slot_scratch, (size_t)U * max_union);
+  cv.take(&h->hit_scratch, (size_t)U * max_union);
+  cv.take(&h->stage_sel, (size_t)U * max_union);
+  cv.take(&h->stage_q, (size_t)U * c.max_tokens_per_step * s.G * s.D);
+  cv.take(&h->stage_out, (size_t)U * c.max_tokens_per_step * s.G * s.DV);
+  h->dev_bytes = (cv.off + kAlign - 1) / kAlign * kAlign;
+  e = cudaMalloc(&h->dev_block, h->dev_bytes);
+  if (e != cudaSuccess) {
+    release(h);
+    return AVSG_ERR_CUDA;
+  }
+  void* b = h->dev_block;
+  rebase(&s.kbuf, b); rebase(&s.vbuf, b); rebase(&s.tag, b); rebase(&s.last, b);
+  rebase(&s.seen, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.mset, b);
+  rebase(&s.mslot, b); rebase(&s.mlist, b); rebase(&s.mcount, b); rebase(&s.desc, b);
+  rebase(&s.desc_count, b); rebase(&s.part, b); rebase(&s.part_count, b);
+  rebase(&s.counters, b); rebase(&s.err, b);
+  rebase(&h->slot_scratch, b); rebase(&h->hit_scratch, b); rebase(&h->stage_sel, b);
+  rebase(&h->stage_q, b); rebase(&h->stage_out, b);
+  if (shared) s.vbuf = s.kbuf;
+
+  rc = init_state(h, nullptr);
+  if (rc == AVSG_OK) {
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) rc = AVSG_ERR_CUDA;
+  }
+  if (rc != AVSG_OK) {
+    release(h);
+    return rc;
+  }
+  *out = h;
+  return AVSG_OK;
+}
+
+extern "C" int avsg_destroy(avsg_handle h) {
+  if (!h) return AVSG_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  release(h);
+  return e == cudaSuccess ? AVSG_OK : AVSG_ERR_CUDA;
+}
+
+namespace {
+
+cudaEvent_t take_event(avsg_handle h) {
+  if (h->ev_used == h->ev_pool.size()) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    h->ev_pool.push_back(e);
+  }
+  return h->ev_pool[h->ev_used++];
+}
+
+// Records an event before kernel `kernel` (when profiling) and returns it.
+struct Timeline {
+  avsg_handle h;
+  cudaStream_t st;
+  cudaEvent_t prev = nullptr;
+  int prev_kernel = -1;
+  void mark(int next_kernel) {
+    if (!h->prof) return;
+    cudaEvent_t e = take_event(h);
+    if (!e) return;
+    cudaEventRecord(e, st);
+    if (prev && prev_kernel >= 0) h->recs.push_back({prev_kernel, prev, e});
+    prev = e;
+    prev_kernel = next_kernel;
+  }
+};
+
+int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32_t* d_sel,
+                 const float* d_q, float* d_out, int32_t* d_slot_map, uint8_t* d_hit,
+                 cudaStream_t st) {
+  const DeviceState& s = h->ds;
+  h->last_stream = st;
+  h->has_t = true;
+  h->last_t = t;
+  h->steps += 1;
+  h->selected += (uint64_t)s.U * n_tok * k;
+  cudaError_t e;
+  if (k == 0) {
+    e = cudaMemsetAsync(d_out, 0, (size_t)s.U * n_tok * s.G * s.DV * sizeof(float), st);
+    return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
+  }
+  int32_t* slot_map = d_slot_map ? d_slot_map : h->slot_scratch;
+  Timeline tl{h, st};
+  if (h->no_reuse) {
+    tl.mark(2);
+    e = launch_gather_all(s, n_tok, k, d_sel, slot_map, d_hit, h->gather_ctas, st);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    h->host_misses += (uint64_t)s.U * n_tok * k;
+  } else {
+    tl.mark(0);
+    e = launch_match(s, t, n_tok, k, d_sel, slot_map, d_hit, st);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    tl.mark(1);
+    e = launch_victims(s, t, n_tok, k, slot_map, st);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    tl.mark(2);
+    e = launch_gather(s, h->gather_ctas, st);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+  }
+  tl.mark(3);
+  AttnLaunch a;
+  a.n_tok = n_tok;
+  a.k = k;
+  a.splits = attn_splits(h, n_tok, k);
+  a.identity_slots = h->no_reuse ? 1 : 0;
+  a.scale_log2 = h->scale_log2;
+  a.q = d_q;
+  a.out = d_out;
+  a.slot_map = slot_map;
+  e = launch_attention(s, a, st);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  tl.mark(-1);
+  return AVSG_OK;
+}
+
+int check_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k) {
+  if (!h) return AVSG_ERR_INVALID_ARG;
+  if (h->latched) return AVSG_ERR_LATCHED;
+  if (n_tok < 1 || n_tok > h->cfg.max_tokens_per_step || k < 0) return AVSG_ERR_INVALID_ARG;
+  if (k > h->cfg.max_select) return AVSG_ERR_CAPACITY;
+  if ((int64_t)n_tok * k > h->ds.max_union) return AVSG_ERR_CAPACITY;
+  if (t < 0 || (h->has_t && t <= h->last_t)) return AVSG_ERR_BAD_STEP;
+  return AVSG_OK;
+}
+
+}  // namespace
+
+extern "C" int avsg_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32_t* d_sel,
+                         const float* d_q, float* d_out, int32_t* d_slot_map, uint8_t* d_hit,
+                         void* stream) {
+  const int rc = check_step(h, t, n_tok, k);
+  if (rc != AVSG_OK) return rc;
+  if (!d_out || (k > 0 && (!d_sel || !d_q))) return AVSG_ERR_INVALID_ARG;
+  return enqueue_step(h, t, n_tok, k, d_sel, d_q, d_out, d_slot_map, d_hit,
+                      static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int avsg_step_host(avsg_handle h, int32_t t, int32_t n_tok, int32_t k,
+                              const int32_t* h_sel, const float* h_q, float* h_out,
+                              int32_t* h_slot_map, uint8_t* h_hit, void* stream) {
+  int rc = check_step(h, t, n_tok, k);
+  if (rc != AVSG_OK) return rc;
+  if (!h_out || (k > 0 && (!h_sel || !h_q))) return AVSG_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const DeviceState& s = h->ds;
+  const size_t n_sel = (size_t)s.U * n_tok * k;
+  const size_t n_q = (size_t)s.U * n_tok * s.G * s.D;
+  const size_t n_out = (size_t)s.U * n_tok * s.G * s.DV;
+  cudaError_t e = cudaSuccess;
+  if (k > 0) {
+    e = cudaMemcpyAsync(h->stage_sel, h_sel, n_sel * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->stage_q, h_q, n_q * 4, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+  }
+  rc = enqueue_step(h, t, n_tok, k, h->stage_sel, h->stage_q, h->stage_out, h->slot_scratch,
+                    h_hit ? h->hit_scratch : nullptr, st);
+  if (rc != AVSG_OK) return rc;
+  e = cudaMemcpyAsync(h_out, h->stage_out, n_out * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && h_slot_map && n_sel)
+    e = cudaMemcpyAsync(h_slot_map, h->slot_scratch, n_sel * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && h_hit && n_sel)
+    e = cudaMemcpyAsync(h_hit, h->hit_scratch, n_sel, cudaMemcpyDeviceToHost, st);
+  return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
+}
+
+extern "C" int avsg_get_stats(avsg_handle h, avsg_stats* out) {
+  if (!h || !out) return AVSG_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  DevCounters c{};
+  DevErr de{};
+  if (e == cudaSuccess) e = cudaMemcpy(&c, h->ds.counters, sizeof(c), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&de, h->ds.err, sizeof(de), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  memset(out, 0, sizeof(*out));
+  out->steps = h->steps;
+  out->selected = h->selected;
+  out->hits = h->no_reuse ? 0 : c.hits;
+  out->misses = h->no_reuse ? h->host_misses : c.misses;
+  out->unique_selected = out->hits + out->misses;
+  out->miss_bytes = out->misses * (uint64_t)(h->ds.ek + h->ds.ev);
+  out->device_error = de.code;
+  out->error_unit = de.code ? de.unit : -1;
+  out->error_position = de.code ? de.pos : -1;
+  if (de.code) h->latched = true;
+  return AVSG_OK;
+}
+
+extern "C" int avsg_get_info(avsg_handle h, avsg_info* out) {
+  if (!h || !out) return AVSG_ERR_INVALID_ARG;
+  memset(out, 0, sizeof(*out));
+  out->device_bytes = h->dev_bytes;
+  out->hash_capacity = h->no_reuse ? 0 : h->ds.HS;
+  out->miss_set_capacity = h->no_reuse ? 0 : h->ds.MS;
+  out->attn_splits = attn_splits(h, 1, h->cfg.max_select);
+  out->gather_ctas = h->gather_ctas;
+  out->num_sms = h->num_sms;
+  out->host_registered = (h->reg_k || h->reg_v) ? 1 : 0;
+  return AVSG_OK;
+}
+
+extern "C" int avsg_read_state(avsg_handle h, int32_t unit, int32_t* tag, int32_t* last_step,
+                               void* k_rows, void* v_rows) {
+  if (!h || unit < 0 || unit >= h->ds.U) return AVSG_ERR_INVALID_ARG;
+  if (h->no_reuse && (tag || last_step)) return AVSG_ERR_INVALID_ARG;
+  const DeviceState& s = h->ds;
+  cudaError_t e = cudaDeviceSynchronize();
+  const size_t ub = (size_t)unit * s.B;
+  if (e == cudaSuccess && tag) e = cudaMemcpy(tag, s.tag + ub, (size_t)s.B * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && last_step)
+    e = cudaMemcpy(last_step, s.last + ub, (size_t)s.B * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && k_rows)
+    e = cudaMemcpy(k_rows, s.kbuf + ub * s.ek, (size_t)s.B * s.ek, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && v_rows && s.ev)
+    e = cudaMemcpy(v_rows, s.vbuf + ub * s.ev, (size_t)s.B * s.ev, cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
+}
+
+extern "C" int avsg_reset(avsg_handle h, void* stream) {
+  if (!h) return AVSG_ERR_INVALID_ARG;
+  return init_state(h, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int avsg_clear_error(avsg_handle h) {
+  if (!h) return AVSG_ERR_INVALID_ARG;
+  const DeviceState& s = h->ds;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (!h->no_reuse) {
+    if (e == cudaSuccess) e = cudaMemset(s.seen, 0, (size_t)s.U * s.B * 4);
+    if (e == cudaSuccess) e = cudaMemset(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
+    if (e == cudaSuccess) e = cudaMemset(s.mcount, 0, (size_t)s.U * 4);
+  }
+  if (e == cudaSuccess) e = cudaMemset(s.desc_count, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);
+  if (e == cudaSuccess) e = cudaMemset(s.err, 0, sizeof(DevErr));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  h->latched = false;
+  return AVSG_OK;
+}
+
+extern "C" int avsg_profile(avsg_handle h, int32_t enable) {
+  if (!h) return AVSG_ERR_INVALID_ARG;
+  h->prof = enable != 0;
+  if (h->prof) {
+    for (int i = 0; i < 4; ++i) {
+      h->prof_ms[i] = 0;
+      h->prof_launches[i] = 0;
+    }
+    h->recs.clear();
+    h->ev_used = 0;
+  }
+  return AVSG_OK;
+}
+
+extern "C" int avsg_profile_read(avsg_handle h, avsg_kernel_times* out) {
+  if (!h || !out) return AVSG_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  for (const auto& r : h->recs) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess && r.kernel >= 0 && r.kernel < 4) {
+      h->prof_ms[r.kernel] += ms;
+      h->prof_launches[r.kernel] += 1;
+    }
+  }
+  h->recs.clear();
+  h->ev_used = 0;
+  for (int i = 0; i < 4; ++i) {
+    out->ms[i] = h->prof_ms[i];
+    out->launches[i] = h->prof_launches[i];
+  }
+  return AVSG_OK;
+}
+
+extern "C" int avsg_host_alloc(size_t bytes, void** out) {
+  if (!out || bytes == 0) return AVSG_ERR_INVALID_ARG;
+  *out = nullptr;
+  cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  return e == cudaSuccess ? AVSG_OK : AVSG_ERR_CUDA;
+}
+
+extern "C" int avsg_host_free(void* p) {
+  if (!p) return AVSG_OK;
+  return cudaFreeHost(p) == cudaSuccess ? AVSG_OK : AVSG_ERR_CUDA;
+}
+
+extern "C" const char* avsg_strerror(int code) {
+  switch (code) {
+    case AVSG_OK: return "ok";
+    case AVSG_ERR_INVALID_ARG: return "invalid argument";
+    case AVSG_ERR_CAPACITY: return "selection larger than the buffer or max_select";
+    case AVSG_ERR_CUDA: return "CUDA runtime error";
+    case AVSG_ERR_BAD_SELECTION: return "selected id out of range or repeated within a token";
+    case AVSG_ERR_TIMEOUT: return "bounded device wait gave up";
+    case AVSG_ERR_BAD_STEP: return "step index not strictly increasing";
+    case AVSG_ERR_UNSUPPORTED: return "no compiled attention kernel for this shape";
+    case AVSG_ERR_LATCHED: return "a device error is pending; call avsg_clear_error";
+    default: return "unknown error";
+  }
+}
+
+extern "C" int avsg_cuda_error(avsg_handle h) { return h ? (int)h->cuda_err : 0; }

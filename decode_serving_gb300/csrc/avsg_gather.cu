@@ -1,0 +1,131 @@
+// avsg_gather: copy the step's missing KV rows from host memory into their
+// reserved buffer slots.
+//
+// AVSG page (arxivdaily 2609.37538, English abstract): only the misses cross
+// the host link ("miss-only transfer"), and the transfers are split evenly
+// across the accelerator's cores instead of by request.  Here the compacted
+// descriptor list is cut into 16-byte chunks (K row chunks, then V row chunks
+// of each miss) and every CTA takes an equal contiguous range of chunks, so a
+// unit with many misses does not leave other SMs idle.  Host memory is mapped
+// pinned memory read directly by the SMs (over NVLink-C2C on GB300) with
+// 16-byte non-coherent loads, several in flight per thread; the buffer rows
+// are written with 16-byte stores that bypass L1.
+#include "avsg_internal.cuh"
+
+namespace avsg {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 8;
+
+__device__ __forceinline__ uint4 load_host16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void store16(void* p, uint4 v) {
+  asm volatile("st.global.cg.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Copies chunks [begin, end) of the list: chunk c of descriptor d = c / cpe.
+template <typename DescFn>
+__device__ __forceinline__ void copy_chunks(const DeviceState& s, uint32_t begin, uint32_t end,
+                                            DescFn desc_of) {
+  const uint32_t cpk = (uint32_t)(s.ek >> 4), cpv = (uint32_t)(s.ev >> 4), cpe = cpk + cpv;
+  for (uint32_t c0 = begin + threadIdx.x; c0 < end; c0 += kThreads * kUnroll) {
+    uint4 v[kUnroll];
+    unsigned char* dst[kUnroll];
+#pragma unroll
+    for (int r = 0; r < kUnroll; ++r) {
+      const uint32_t c = c0 + (uint32_t)(r * kThreads);
+      dst[r] = nullptr;
+      if (c < end) {
+        const uint32_t d = c / cpe, w = c - d * cpe;
+        int unit, id, slot;
+        if (desc_of(d, unit, id, slot)) {
+          const unsigned char* src;
+          if (w < cpk) {
+            src = s.host_k + ((size_t)unit * s.L + id) * s.ek + ((size_t)w << 4);
+            dst[r] = s.kbuf + ((size_t)unit * s.B + slot) * s.ek + ((size_t)w << 4);
+          } else {
+            src = s.host_v + ((size_t)unit * s.L + id) * s.ev + ((size_t)(w - cpk) << 4);
+            dst[r] = s.vbuf + ((size_t)unit * s.B + slot) * s.ev + ((size_t)(w - cpk) << 4);
+          }
+          v[r] = load_host16(src);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kUnroll; ++r)
+      if (dst[r]) store16(dst[r], v[r]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) gather_kernel(DeviceState s) {
+  if (load_err(s.err) != 0) return;  // no barriers below: a per-thread exit is safe
+  const uint32_t n = (uint32_t)*(volatile int32_t*)s.desc_count;
+  const uint32_t cpe = (uint32_t)((s.ek + s.ev) >> 4);
+  const uint32_t total = n * cpe;
+  const uint32_t per = (total + gridDim.x - 1) / gridDim.x;
+  const uint32_t begin = blockIdx.x * per;
+  const uint32_t end = min(total, begin + per);
+  const GatherDesc* desc = s.desc;
+  copy_chunks(s, begin, end, [&](uint32_t d, int& unit, int& id, int& slot) {
+    const int4 g = __ldcg(reinterpret_cast<const int4*>(desc + d));
+    unit = g.x;
+    id = g.y;
+    slot = g.z;
+    return true;
+  });
+}
+
+// No-reuse comparison path: every selected row of every token is copied to
+// staging slot tok * k + j of its unit; ids are range-checked.
+__global__ void __launch_bounds__(kThreads) gather_all_kernel(DeviceState s, int n_tok, int k,
+                                                              const int32_t* __restrict__ sel,
+                                                              int32_t* __restrict__ slot_map,
+                                                              uint8_t* __restrict__ hit) {
+  if (load_err(s.err) != 0) return;
+  const uint32_t per_unit = (uint32_t)(n_tok * k);
+  const uint32_t n = (uint32_t)s.U * per_unit;
+  // Slot map (identity) and hit flags, one entry per thread of the grid.
+  for (uint32_t d = blockIdx.x * kThreads + threadIdx.x; d < n; d += gridDim.x * kThreads) {
+    if (slot_map) slot_map[d] = (int32_t)(d % per_unit);
+    if (hit) hit[d] = 0;
+  }
+  const uint32_t cpe = (uint32_t)((s.ek + s.ev) >> 4);
+  const uint32_t total = n * cpe;
+  const uint32_t per = (total + gridDim.x - 1) / gridDim.x;
+  const uint32_t begin = blockIdx.x * per;
+  const uint32_t end = min(total, begin + per);
+  copy_chunks(s, begin, end, [&](uint32_t d, int& unit, int& id, int& slot) {
+    unit = (int)(d / per_unit);
+    slot = (int)(d - (uint32_t)unit * per_unit);
+    id = __ldg(sel + d);
+    if (id < 0 || (int64_t)id >= s.L) {
+      raise_error(s.err, AVSG_ERR_BAD_SELECTION, unit, slot);
+      return false;
+    }
+    return true;
+  });
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st) {
+  gather_kernel<<<ctas, kThreads, 0, st>>>(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,
+                              int32_t* slot_map, uint8_t* hit, int ctas, cudaStream_t st) {
+  gather_all_kernel<<<ctas, kThreads, 0, st>>>(s, n_tok, k, sel, slot_map, hit);
+  return cudaGetLastError();
+}
+
+}  // namespace avsg

@@ -1,0 +1,101 @@
+// Internal declarations shared by the kernels and the C interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "avsg.h"
+
+namespace avsg {
+
+constexpr int32_t kEmpty = -1;                 // tag / hash key of an empty cell
+constexpr int32_t kTomb = -2;                  // hash key of an erased cell
+constexpr unsigned long long kMissEmpty = ~0ull;
+constexpr int kOrders = 64;                    // reservation classes 0..63
+constexpr int kNotCandidate = 255;
+constexpr int kMaxTokens = 8;
+
+// First device error of a step; later kernels of the step (and later steps)
+// see a non-zero code and return before touching any state.
+struct DevErr {
+  int32_t code, unit, pos, aux;
+};
+
+struct DevCounters {
+  unsigned long long hits, misses;
+};
+
+// One miss to copy: host row `id` of `unit` into buffer slot `slot`.
+struct GatherDesc {
+  int32_t unit, id, slot, pad;
+};
+
+// Everything a kernel needs about a handle: sizes and device pointers.
+struct DeviceState {
+  int32_t U, B, G, D, DV, ET;      // units, slots per unit, q/kv, widths, tokens/entry
+  int64_t L;                       // entries per unit
+  int32_t HS, hs_shift;            // hash capacity (pow2) and 32 - log2(HS)
+  int32_t MS, ms_shift;            // miss-set capacity (pow2) and 32 - log2(MS)
+  int32_t max_union;               // max_tokens_per_step * max_select
+  int32_t kv_shared;
+  int64_t ek, ev;                  // bytes of one entry's K row / V row (ev 0 if shared)
+  const unsigned char* host_k;     // mapped host KV (device-visible pointers)
+  const unsigned char* host_v;
+  unsigned char* kbuf;             // [U][B][ek]
+  unsigned char* vbuf;             // [U][B][ev]
+  int32_t* tag;                    // [U][B] resident id or kEmpty
+  int32_t* last;                   // [U][B] step of last selection, -1 never
+  int32_t* seen;                   // [U][B] token bits of this step's hits; 0 between steps
+  int2* htab;                      // [U][HS] {key, slot}
+  int32_t* hused;                  // [U] non-empty hash cells (live + erased)
+  unsigned long long* mset;        // [U][MS] {id | token bits << 32}, kMissEmpty between steps
+  int32_t* mslot;                  // [U][MS] slot reserved for the miss in that cell
+  int32_t* mlist;                  // [U][max_union] cells of this step's distinct misses
+  int32_t* mcount;                 // [U] distinct misses this step
+  GatherDesc* desc;                // [U * max_union]
+  int32_t* desc_count;             // [1]
+  float* part;                     // split-K partials
+  int32_t* part_count;             // [U][max_tokens] arrival counters, 0 between steps
+  DevCounters* counters;
+  DevErr* err;
+};
+
+__device__ __forceinline__ uint32_t fib_hash(int32_t id, int shift) {
+  // Knuth's multiplicative (Fibonacci) hashing: top bits of id * 2^32/phi.
+  return ((uint32_t)id * 2654435769u) >> shift;
+}
+
+__device__ __forceinline__ int load_err(const DevErr* e) {
+  return *(const volatile int32_t*)&e->code;
+}
+
+__device__ __forceinline__ void raise_error(DevErr* e, int code, int unit, int pos) {
+  if (atomicCAS(&e->code, 0, code) == 0) {
+    e->unit = unit;
+    e->pos = pos;
+  }
+}
+
+// Kernel launchers (one per .cu file).
+cudaError_t launch_match(const DeviceState& s, int t, int n_tok, int k, const int32_t* sel,
+                         int32_t* slot_map, uint8_t* hit, cudaStream_t st);
+size_t victims_smem_bytes(const DeviceState& s);
+cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_t* slot_map,
+                           cudaStream_t st);
+cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
+cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,
+                              int32_t* slot_map, uint8_t* hit, int ctas, cudaStream_t st);
+
+struct AttnLaunch {
+  int n_tok, k, splits;
+  int identity_slots;              // 1: slot of (tok, j) is tok * k + j (no-reuse staging)
+  float scale_log2;                // softmax scale * log2(e)
+  const float* q;
+  float* out;
+  const int32_t* slot_map;
+};
+bool attention_supported(int D, int DV, int G, int kv_shared);
+int attention_rows_per_tile(int D, int DV, int G, int kv_shared);
+cudaError_t launch_attention(const DeviceState& s, const AttnLaunch& a, cudaStream_t st);
+
+}  // namespace avsg

@@ -1,0 +1,155 @@
+// avsg_match: match each selected id against its unit's resident ids.
+//
+// AVSG page (arxivdaily 2609.37538, English abstract): hash matching of the
+// selected tokens against the entries retained in the HBM buffer identifies
+// the reusable slots.  Here every lane of a warp probes one id, so a warp
+// matches 32 ids at once; a probe reads a 16-byte window of two table cells.
+//
+// Grid (ceil(n_tok*k / 256), U), 256 threads.  Per id:
+//   * range check (id in [0, L)), else BAD_SELECTION;
+//   * lookup in the unit's open-addressed table (linear probing, Fibonacci
+//     hash); a hit writes its slot and sets the token's bit in seen[slot]
+//     (a bit already set means the id repeats within one token's list);
+//   * a miss is entered in the per-step miss set (one cell per distinct id,
+//     token bits merged, so a multi-token iteration reserves each id once);
+//     the first token to enter an id appends the cell to the unit's miss list;
+//     the slot map gets -2 - cell until the reservation kernel resolves it.
+// Nothing in the buffer state (tags, last_step, hash table) changes here, so a
+// BAD_SELECTION leaves the state as it was.
+#include "avsg_internal.cuh"
+
+namespace avsg {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, int n_tok, int k,
+                                                         const int32_t* __restrict__ sel,
+                                                         int32_t* __restrict__ slot_map,
+                                                         uint8_t* __restrict__ hit) {
+  (void)t;
+  const int u = blockIdx.y;
+  const int n = n_tok * k;
+  const int pos = blockIdx.x * kThreads + threadIdx.x;
+  __shared__ int s_cnt[2];
+  __shared__ int s_stop;
+  if (blockIdx.x == 0 && u == 0 && threadIdx.x == 0) *s.desc_count = 0;
+  if (threadIdx.x == 0) {
+    s_stop = load_err(s.err);
+    s_cnt[0] = s_cnt[1] = 0;
+  }
+  __syncthreads();
+  if (s_stop) return;  // block-uniform: an earlier step latched an error
+
+  bool uniq_hit = false, uniq_miss = false;
+  int miss_cell = -1;
+  if (pos < n) {
+    const int tok = pos / k;
+    const size_t off = (size_t)u * n + pos;
+    const int32_t id = sel[off];
+    if (id < 0 || (int64_t)id >= s.L) {
+      raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
+      slot_map[off] = -1;
+      if (hit) hit[off] = 0;
+    } else {
+      // Hash lookup: 16-byte windows of two cells, starting at the even cell
+      // at or before the home cell.  A cell before the home cell never holds
+      // this id, and an empty one there does not end the probe.
+      const int2* tab = s.htab + (size_t)u * s.HS;
+      const uint32_t mask = (uint32_t)s.HS - 1u;
+      const uint32_t home = fib_hash(id, s.hs_shift);
+      uint32_t cell = home & ~1u;
+      int slot = -1;
+      bool skip_first = (home & 1u) != 0;
+      for (int probes = 0; probes < s.HS; probes += 2) {
+        const int4 w = __ldcg(reinterpret_cast<const int4*>(tab + (cell & mask)));
+        if (!skip_first) {
+          if (w.x == id) { slot = w.y; break; }
+          if (w.x == kEmpty) break;
+        }
+        if (w.z == id) { slot = w.w; break; }
+        if (w.z == kEmpty) break;
+        skip_first = false;
+        cell += 2;
+      }
+      const unsigned bit = 1u << tok;
+      if (slot >= 0) {
+        const int old = atomicOr(&s.seen[(size_t)u * s.B + slot], (int)bit);
+        if (old & bit) raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
+        uniq_hit = (old == 0);
+        slot_map[off] = slot;
+        if (hit) hit[off] = 1;
+      } else {
+        unsigned long long* ms = s.mset + (size_t)u * s.MS;
+        const uint32_t mmask = (uint32_t)s.MS - 1u;
+        const unsigned long long tokbit = (unsigned long long)bit << 32;
+        uint32_t c = fib_hash(id, s.ms_shift);
+        // Each failed compare-and-swap means another token added its bit to
+        // this cell, so retries are bounded by the token count.
+        for (int iter = 0; iter < s.MS + 2 * kMaxTokens; ++iter) {
+          unsigned long long* p = ms + (c & mmask);
+          unsigned long long w = *(volatile unsigned long long*)p;
+          if (w == kMissEmpty) {
+            const unsigned long long prev = atomicCAS(p, kMissEmpty, tokbit | (uint32_t)id);
+            if (prev == kMissEmpty) {
+              miss_cell = (int)(c & mmask);
+              uniq_miss = true;
+              break;
+            }
+            w = prev;
+          }
+          if ((uint32_t)w == (uint32_t)id) {
+            if (w & tokbit) {
+              raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
+              miss_cell = (int)(c & mmask);
+              break;
+            }
+            const unsigned long long prev = atomicCAS(p, w, w | tokbit);
+            if (prev == w) {
+              miss_cell = (int)(c & mmask);
+              break;
+            }
+            continue;  // lost a race on this cell; read it again
+          }
+          ++c;
+        }
+        if (miss_cell < 0) raise_error(s.err, AVSG_ERR_CAPACITY, u, pos);  // miss set full
+        slot_map[off] = -2 - miss_cell;
+        if (hit) hit[off] = 0;
+      }
+    }
+  }
+
+  // Append first-seen misses to the unit's list: one atomic per warp.
+  const unsigned ball = __ballot_sync(0xffffffffu, uniq_miss);
+  if (ball) {
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    if (lane == __ffs(ball) - 1) base = atomicAdd(&s.mcount[u], __popc(ball));
+    base = __shfl_sync(0xffffffffu, base, __ffs(ball) - 1);
+    if (uniq_miss) s.mlist[(size_t)u * s.max_union + base + __popc(ball & ((1u << lane) - 1u))] = miss_cell;
+  }
+  // Distinct hits and misses of the step.
+  const unsigned hb = __ballot_sync(0xffffffffu, uniq_hit);
+  if ((threadIdx.x & 31) == 0) {
+    if (hb) atomicAdd(&s_cnt[0], __popc(hb));
+    if (ball) atomicAdd(&s_cnt[1], __popc(ball));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (s_cnt[0]) atomicAdd(&s.counters->hits, (unsigned long long)s_cnt[0]);
+    if (s_cnt[1]) atomicAdd(&s.counters->misses, (unsigned long long)s_cnt[1]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_match(const DeviceState& s, int t, int n_tok, int k, const int32_t* sel,
+                         int32_t* slot_map, uint8_t* hit, cudaStream_t st) {
+  const int n = n_tok * k;
+  dim3 grid((unsigned)((n + kThreads - 1) / kThreads), (unsigned)s.U);
+  match_kernel<<<grid, kThreads, 0, st>>>(s, t, n_tok, k, sel, slot_map, hit);
+  return cudaGetLastError();
+}
+
+}  // namespace avsg

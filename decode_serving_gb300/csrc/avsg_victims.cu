@@ -1,0 +1,285 @@
+// avsg_victims: reserve buffer slots for the step's missing ids and commit.
+//
+// Retention policy: bucketed LRU (Spin page, "Unifying Sparse Attention with
+// Hierarchical Memory for Scalable Long-Context LLM Serving", section 2B:
+// recency buckets, about 64, no global sort, eviction decided in parallel on
+// the GPU) combined with the AVSG page's slot reservation for entries that
+// need a transfer (arxivdaily 2609.37538, English abstract).
+//
+// One CTA of 1024 threads per unit.  Slots are put in 64 reservation orders:
+//   order 0      : empty slot;
+//   order 64 - b : occupied, not selected this step, bucket b = min(63, t - last);
+//   excluded     : selected this step (a hit; its last_step becomes t).
+// A slot's rank is the number of candidates in lower orders plus the number
+// of lower-indexed slots in its own order, computed with a per-warp order
+// histogram (warp w owns a contiguous slot range), one exclusive scan over
+// (order, warp), and __match_any_sync within each 32-slot chunk -- no sort of
+// the slots.  The m distinct missing ids are sorted ascending (bitonic sort in
+// shared memory); the i-th takes the slot of rank i.  Then, per miss: erase the
+// evicted id from the hash table, insert the new one, set tag and last_step,
+// append a gather descriptor, and resolve the slot map entries that pointed at
+// the miss-set cell.  The miss set is emptied for the next step.
+#include "avsg_internal.cuh"
+
+namespace avsg {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// Linear-probing erase of a key known to be present.
+__device__ void hash_erase(int2* tab, uint32_t mask, int shift, int32_t key) {
+  uint32_t c = fib_hash(key, shift);
+  for (uint32_t i = 0; i <= mask; ++i, ++c) {
+    int2* p = tab + (c & mask);
+    const int32_t kk = *(volatile int32_t*)&p->x;
+    if (kk == key) {
+      p->x = kTomb;
+      return;
+    }
+    if (kk == kEmpty) return;
+  }
+}
+
+// Linear-probing insert of a key known to be absent; takes the first empty or
+// erased cell on the probe path.  Returns 1 if it consumed an empty cell.
+__device__ int hash_insert(int2* tab, uint32_t mask, int shift, int32_t key, int32_t slot,
+                           DevErr* err, int unit) {
+  uint32_t c = fib_hash(key, shift);
+  for (uint32_t i = 0; i <= 2 * mask + 2 * kThreads; ++i) {
+    int2* p = tab + (c & mask);
+    const int32_t kk = *(volatile int32_t*)&p->x;
+    if (kk == kEmpty || kk == kTomb) {
+      if (atomicCAS(&p->x, kk, key) == kk) {
+        p->y = slot;
+        return kk == kEmpty ? 1 : 0;
+      }
+      continue;  // another insert took this cell; look at it again
+    }
+    ++c;
+  }
+  raise_error(err, AVSG_ERR_CAPACITY, unit, -1);  // unreachable: live keys <= B < HS
+  return 0;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+}  // namespace
+
+namespace {
+
+struct VictimsSmem {
+  size_t keys, victim, wstart, ord, total;
+};
+
+__host__ __device__ inline VictimsSmem victims_layout(int max_union, int B) {
+  int p = 1;
+  while (p < max_union) p <<= 1;
+  VictimsSmem l;
+  l.keys = 0;
+  l.victim = l.keys + sizeof(unsigned long long) * (size_t)p;
+  l.wstart = l.victim + ((sizeof(int32_t) * (size_t)max_union + 15) & ~(size_t)15);
+  l.ord = l.wstart + sizeof(int32_t) * kOrders * kWarps;
+  l.total = l.ord + (((size_t)B + 15) & ~(size_t)15);
+  return l;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int t, int n_tok,
+                                                              int k, int32_t* __restrict__ slot_map) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_stop, s_base, s_used, s_rebuild, s_live;
+  __shared__ int wsum[kWarps];
+  const int u = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const VictimsSmem lay = victims_layout(s.max_union, s.B);
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem + lay.keys);
+  int32_t* victim = reinterpret_cast<int32_t*>(smem + lay.victim);
+  int32_t* wstart = reinterpret_cast<int32_t*>(smem + lay.wstart);  // [order][warp]
+  uint8_t* ord = smem + lay.ord;
+
+  if (tid == 0) {
+    s_stop = load_err(s.err);
+    s_used = 0;
+    s_live = 0;
+  }
+  __syncthreads();
+  if (s_stop) return;
+
+  const int B = s.B;
+  const size_t ub = (size_t)u * B;
+  const int m = s.mcount[u];
+  unsigned long long* ms = s.mset + (size_t)u * s.MS;
+
+  // 1. Distinct missing ids, ascending: key = id << 32 | miss-set cell.
+  const int P = next_pow2(m > 0 ? m : 1);
+  for (int i = tid; i < P; i += kThreads) {
+    unsigned long long key = ~0ull;
+    if (i < m) {
+      const int cell = s.mlist[(size_t)u * s.max_union + i];
+      key = ((unsigned long long)(uint32_t)ms[cell] << 32) | (uint32_t)cell;
+    }
+    keys[i] = key;
+  }
+  for (int i = tid; i < kOrders * kWarps; i += kThreads) wstart[i] = 0;
+  __syncthreads();
+  for (int kk = 2; kk <= P; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < P / 2; i += kThreads) {
+        const int lo = 2 * i - (i & (j - 1));
+        const int hi = lo + j;
+        const bool up = (lo & kk) == 0;
+        const unsigned long long a = keys[lo], b = keys[hi];
+        if ((a > b) == up) {
+          keys[lo] = b;
+          keys[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // 2. Reservation order of every slot; per-warp histogram over orders.
+  const int chunk = ((B + kWarps * 32 - 1) / (kWarps * 32)) * 32;  // slots per warp
+  const int w_begin = warp * chunk, w_end = min(B, w_begin + chunk);
+  for (int base = w_begin; base < w_begin + chunk; base += 32) {
+    const int sl = base + lane;
+    int o = kNotCandidate;
+    if (sl < w_end) {
+      const int sn = s.seen[ub + sl];
+      if (sn) {
+        s.last[ub + sl] = t;  // selected this step: refreshed, never a victim
+        s.seen[ub + sl] = 0;
+      } else if (s.tag[ub + sl] == kEmpty) {
+        o = 0;
+      } else {
+        const int age = max(1, t - s.last[ub + sl]);
+        o = kOrders - min(kOrders - 1, age);
+      }
+      ord[sl] = (uint8_t)o;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, o);
+    if (o != kNotCandidate && lane == __ffs(peers) - 1) wstart[o * kWarps + warp] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // 3. Exclusive scan of wstart in (order, warp) order: 2 values per thread.
+  {
+    const int a = wstart[2 * tid], b = wstart[2 * tid + 1];
+    const int incl = warp_incl_scan(a + b, lane);
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int v = wsum[lane];
+      wsum[lane] = warp_incl_scan(v, lane) - v;
+    }
+    __syncthreads();
+    const int excl = wsum[warp] + incl - (a + b);
+    wstart[2 * tid] = excl;
+    wstart[2 * tid + 1] = excl + a;
+  }
+  __syncthreads();
+
+  // 4. Rank within order by slot index; the first m ranks are the victims.
+  for (int base = w_begin; base < w_begin + chunk; base += 32) {
+    const int sl = base + lane;
+    const int o = sl < w_end ? (int)ord[sl] : kNotCandidate;
+    const unsigned peers = __match_any_sync(0xffffffffu, o);
+    if (o != kNotCandidate) {
+      const int r = wstart[o * kWarps + warp] + __popc(peers & ((1u << lane) - 1u));
+      if (r < m) victim[r] = sl;
+    }
+    __syncwarp();
+    if (o != kNotCandidate && lane == __ffs(peers) - 1) wstart[o * kWarps + warp] += __popc(peers);
+    __syncwarp();
+  }
+  if (tid == 0) s_base = m > 0 ? atomicAdd(s.desc_count, m) : 0;
+  __syncthreads();
+
+  // 5. Commit: erase evicted ids, then insert the new ones.
+  int2* tab = s.htab + (size_t)u * s.HS;
+  const uint32_t hmask = (uint32_t)s.HS - 1u;
+  for (int i = tid; i < m; i += kThreads) {
+    const int32_t old = s.tag[ub + victim[i]];
+    if (old != kEmpty) hash_erase(tab, hmask, s.hs_shift, old);
+  }
+  __syncthreads();
+  int used = 0;
+  for (int i = tid; i < m; i += kThreads) {
+    const unsigned long long key = keys[i];
+    const int32_t id = (int32_t)(key >> 32);
+    const int cell = (int)(uint32_t)key;
+    const int v = victim[i];
+    used += hash_insert(tab, hmask, s.hs_shift, id, v, s.err, u);
+    s.tag[ub + v] = id;
+    s.last[ub + v] = t;
+    s.mslot[(size_t)u * s.MS + cell] = v;
+    ms[cell] = kMissEmpty;
+    s.desc[s_base + i] = GatherDesc{u, id, v, 0};
+  }
+  used = __reduce_add_sync(0xffffffffu, used);
+  if (lane == 0 && used) atomicAdd(&s_used, used);
+  __syncthreads();
+
+  // 6. Resolve slot-map entries of misses (-2 - cell -> reserved slot).
+  const int n = n_tok * k;
+  for (int p = tid; p < n; p += kThreads) {
+    const size_t off = (size_t)u * n + p;
+    const int sm = slot_map[off];
+    if (sm <= -2) slot_map[off] = s.mslot[(size_t)u * s.MS + (-2 - sm)];
+  }
+
+  // 7. Rebuild the table from the tags when erased cells pile up.
+  if (tid == 0) {
+    const int total = s.hused[u] + s_used;
+    s_rebuild = total > s.HS / 2;
+    s.hused[u] = total;
+    s.mcount[u] = 0;
+  }
+  __syncthreads();
+  if (s_rebuild) {
+    for (int i = tid; i < s.HS; i += kThreads) tab[i] = make_int2(kEmpty, kEmpty);
+    __syncthreads();
+    int live = 0;
+    for (int sl = tid; sl < B; sl += kThreads) {
+      const int32_t tg = s.tag[ub + sl];
+      if (tg != kEmpty) {
+        hash_insert(tab, hmask, s.hs_shift, tg, sl, s.err, u);
+        ++live;
+      }
+    }
+    live = __reduce_add_sync(0xffffffffu, live);
+    if (lane == 0 && live) atomicAdd(&s_live, live);
+    __syncthreads();
+    if (tid == 0) s.hused[u] = s_live;
+  }
+}
+
+}  // namespace
+
+size_t victims_smem_bytes(const DeviceState& s) { return victims_layout(s.max_union, s.B).total; }
+
+cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_t* slot_map,
+                           cudaStream_t st) {
+  const size_t smem = victims_smem_bytes(s);
+  cudaError_t e = cudaFuncSetAttribute(victims_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  victims_kernel<<<s.U, kThreads, smem, st>>>(s, t, n_tok, k, slot_map);
+  return cudaGetLastError();
+}
+
+}  // namespace avsg
