@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--slots", type=int, default=0, help="override B (latent sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--skip-no-reuse", action="store_true",
+                    help="skip the no-reuse comparison pass (profiling runs)")
     ap.add_argument("--_oracle", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--_oracle_cost", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--_units", type=int, default=1, help=argparse.SUPPRESS)
@@ -271,11 +273,13 @@ def run_ours(args, rank, world, torch):
     sess.close()
 
     # no-reuse comparison: every selected row crosses the host link each step
-    nr_steps = min(args.steps, 500)
-    sess = make(no_reuse=True)
-    per_nr, _, _, _, _, _ = timed_pass(sess, nr_steps, False)
-    sess.close()
-    res["no_reuse_ms_per_step"] = float(per_nr.sum() / nr_steps)
+    res["no_reuse_ms_per_step"] = None
+    if not args.skip_no_reuse:
+        nr_steps = min(args.steps, 500)
+        sess = make(no_reuse=True)
+        per_nr, _, _, _, _, _ = timed_pass(sess, nr_steps, False)
+        sess.close()
+        res["no_reuse_ms_per_step"] = float(per_nr.sum() / nr_steps)
     res["gen_s"] = gen_s
     res["w"] = w
     res["h2d_peak_gbs"] = pinned_h2d_peak_gbs(torch)
@@ -468,9 +472,10 @@ def report_ours(args, res, world, max_ms, max_e2e_ms) -> dict:
         "match_victims_attention_hbm": {"gbs": hbm_bytes / (hbm_us * 1e-6) / 1e9 if hbm_us else None,
                                         "frac": (hbm_bytes / (hbm_us * 1e-6) / 1e9) / hbm_peak
                                         if hbm_us else None},
-        "no_reuse": {"ms_per_step": res["no_reuse_ms_per_step"],
-                     "steps_per_s": 1e3 / res["no_reuse_ms_per_step"],
-                     "reuse_speedup": res["no_reuse_ms_per_step"] / max_ms},
+        "no_reuse": None if res["no_reuse_ms_per_step"] is None else {
+            "ms_per_step": res["no_reuse_ms_per_step"],
+            "steps_per_s": 1e3 / res["no_reuse_ms_per_step"],
+            "reuse_speedup": res["no_reuse_ms_per_step"] / max_ms},
         "roofline": roof, "kernels": kernels,
         "gpu_launches": 4 * K,
         "clocks": res["clocks"],

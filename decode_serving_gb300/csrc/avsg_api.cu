@@ -133,6 +133,11 @@ int attn_splits(const avsg_handle h, int n_tok, int k) {
   return (int)(s < 1 ? 1 : s);
 }
 
+int env_int_any(const char* name, int dflt) {
+  const char* v = getenv(name);
+  return (v && *v) ? atoi(v) : dflt;
+}
+
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
@@ -141,6 +146,23 @@ int env_int(const char* name, int dflt) {
 }
 
 }  // namespace
+
+namespace avsg {
+
+bool pdl_enabled() {
+  static const int on = env_int_any("AVSG_PDL", 1);
+  return on != 0;
+}
+
+cudaError_t ensure_smem(const void* kernel, size_t bytes, int* done_bytes) {
+  if ((int)bytes <= *done_bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) *done_bytes = (int)bytes;
+  return e;
+}
+
+}  // namespace avsg
 
 namespace {
 
@@ -163,7 +185,7 @@ int init_state(avsg_handle h, cudaStream_t st) {
   }
   AVSG_SET(s.desc_count, 0, 4);
   AVSG_SET(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);
-  AVSG_SET(s.counters, 0, sizeof(DevCounters));
+  AVSG_SET(s.counters, 0, (size_t)s.U * sizeof(DevCounters));
   AVSG_SET(s.err, 0, sizeof(DevErr));
 #undef AVSG_SET
   if (e != cudaSuccess) return fail_cuda(h, e);
@@ -270,7 +292,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.desc_count, 1);
   cv.take(&s.part, (size_t)U * c.max_tokens_per_step * h->splits_cap * s.G * (s.DV + 2));
   cv.take(&s.part_count, (size_t)U * kMaxTokens);
-  cv.take(&s.counters, 1);
+  cv.take(&s.counters, (size_t)U);
   cv.take(&s.err, 1);
   cv.take(&h->slot_scratch, (size_t)U * max_union);
   cv.take(&h->hit_scratch, (size_t)U * max_union);
@@ -442,9 +464,15 @@ extern "C" int avsg_step_host(avsg_handle h, int32_t t, int32_t n_tok, int32_t k
 extern "C" int avsg_get_stats(avsg_handle h, avsg_stats* out) {
   if (!h || !out) return AVSG_ERR_INVALID_ARG;
   cudaError_t e = cudaDeviceSynchronize();
-  DevCounters c{};
+  std::vector<DevCounters> cu((size_t)h->ds.U);
   DevErr de{};
-  if (e == cudaSuccess) e = cudaMemcpy(&c, h->ds.counters, sizeof(c), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(cu.data(), h->ds.counters, cu.size() * sizeof(DevCounters), cudaMemcpyDeviceToHost);
+  DevCounters c{};
+  for (const DevCounters& x : cu) {
+    c.hits += x.hits;
+    c.misses += x.misses;
+  }
   if (e == cudaSuccess) e = cudaMemcpy(&de, h->ds.err, sizeof(de), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return fail_cuda(h, e);
   memset(out, 0, sizeof(*out));

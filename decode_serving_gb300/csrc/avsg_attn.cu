@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(SH::NT) attn_kernel(DeviceState s, AttnLaunch 
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sp = blockIdx.x, u = blockIdx.y, tok = blockIdx.z;
+  griddep_wait();
+  griddep_launch();
   if (tid == 0) s_stop = load_err(s.err);
   if (tid < G) {
     mrun[tid] = -INFINITY;
@@ -324,14 +326,13 @@ __global__ void __launch_bounds__(SH::NT) attn_kernel(DeviceState s, AttnLaunch 
 
 template <class SH>
 cudaError_t run(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
+  static int smem_done = 0;
   const int eps = (a.k + a.splits - 1) / a.splits;
   const size_t smem = SH::REGION0 + SH::QS_BYTES + ((size_t)eps * 4 + 15) / 16 * 16;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<SH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = ensure_smem((const void*)attn_kernel<SH>, smem, &smem_done);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)a.splits, (unsigned)s.U, (unsigned)a.n_tok);
-  attn_kernel<SH><<<grid, SH::NT, smem, st>>>(s, a);
-  return cudaGetLastError();
+  return launch_pdl(attn_kernel<SH>, grid, dim3(SH::NT), smem, st, s, a);
 }
 
 // Compiled shapes: (D, Dv, G, shared).

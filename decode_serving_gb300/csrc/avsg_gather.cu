@@ -67,6 +67,8 @@ __device__ __forceinline__ void copy_chunks(const DeviceState& s, uint32_t begin
 }
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(DeviceState s) {
+  griddep_wait();
+  griddep_launch();
   if (load_err(s.err) != 0) return;  // no barriers below: a per-thread exit is safe
   const uint32_t n = (uint32_t)*(volatile int32_t*)s.desc_count;
   const uint32_t cpe = (uint32_t)((s.ek + s.ev) >> 4);
@@ -90,6 +92,8 @@ __global__ void __launch_bounds__(kThreads) gather_all_kernel(DeviceState s, int
                                                               const int32_t* __restrict__ sel,
                                                               int32_t* __restrict__ slot_map,
                                                               uint8_t* __restrict__ hit) {
+  griddep_wait();
+  griddep_launch();
   if (load_err(s.err) != 0) return;
   const uint32_t per_unit = (uint32_t)(n_tok * k);
   const uint32_t n = (uint32_t)s.U * per_unit;
@@ -118,14 +122,13 @@ __global__ void __launch_bounds__(kThreads) gather_all_kernel(DeviceState s, int
 }  // namespace
 
 cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st) {
-  gather_kernel<<<ctas, kThreads, 0, st>>>(s);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
 }
 
 cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,
                               int32_t* slot_map, uint8_t* hit, int ctas, cudaStream_t st) {
-  gather_all_kernel<<<ctas, kThreads, 0, st>>>(s, n_tok, k, sel, slot_map, hit);
-  return cudaGetLastError();
+  return launch_pdl(gather_all_kernel, dim3(ctas), dim3(kThreads), 0, st, s, n_tok, k, sel,
+                    slot_map, hit);
 }
 
 }  // namespace avsg

@@ -56,13 +56,22 @@ struct DeviceState {
   int32_t* desc_count;             // [1]
   float* part;                     // split-K partials
   int32_t* part_count;             // [U][max_tokens] arrival counters, 0 between steps
-  DevCounters* counters;
+  DevCounters* counters;           // [U] distinct hits / misses, summed over steps
   DevErr* err;
 };
 
 __device__ __forceinline__ uint32_t fib_hash(int32_t id, int shift) {
   // Knuth's multiplicative (Fibonacci) hashing: top bits of id * 2^32/phi.
   return ((uint32_t)id * 2654435769u) >> shift;
+}
+
+// Programmatic dependent launch: a kernel may be scheduled while the previous
+// one in the stream drains; griddep_wait() blocks until that grid has finished
+// and its memory is visible, so everything after it sees the previous kernel's
+// results.  griddep_launch() lets the next kernel start its own prologue.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ int load_err(const DevErr* e) {
@@ -75,6 +84,27 @@ __device__ __forceinline__ void raise_error(DevErr* e, int code, int unit, int p
     e->pos = pos;
   }
 }
+
+// Launch with programmatic stream serialization (see griddep_wait).
+bool pdl_enabled();
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
+// Raises a kernel's dynamic shared memory limit once per size.
+cudaError_t ensure_smem(const void* kernel, size_t bytes, int* done_bytes);
 
 // Kernel launchers (one per .cu file).
 cudaError_t launch_match(const DeviceState& s, int t, int n_tok, int k, const int32_t* sel,

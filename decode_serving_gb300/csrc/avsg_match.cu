@@ -31,17 +31,15 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
   const int u = blockIdx.y;
   const int n = n_tok * k;
   const int pos = blockIdx.x * kThreads + threadIdx.x;
-  __shared__ int s_cnt[2];
   __shared__ int s_stop;
+  griddep_wait();
+  griddep_launch();
   if (blockIdx.x == 0 && u == 0 && threadIdx.x == 0) *s.desc_count = 0;
-  if (threadIdx.x == 0) {
-    s_stop = load_err(s.err);
-    s_cnt[0] = s_cnt[1] = 0;
-  }
+  if (threadIdx.x == 0) s_stop = load_err(s.err);
   __syncthreads();
   if (s_stop) return;  // block-uniform: an earlier step latched an error
 
-  bool uniq_hit = false, uniq_miss = false;
+  bool uniq_miss = false;
   int miss_cell = -1;
   if (pos < n) {
     const int tok = pos / k;
@@ -76,7 +74,6 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
       if (slot >= 0) {
         const int old = atomicOr(&s.seen[(size_t)u * s.B + slot], (int)bit);
         if (old & bit) raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
-        uniq_hit = (old == 0);
         slot_map[off] = slot;
         if (hit) hit[off] = 1;
       } else {
@@ -129,17 +126,6 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
     base = __shfl_sync(0xffffffffu, base, __ffs(ball) - 1);
     if (uniq_miss) s.mlist[(size_t)u * s.max_union + base + __popc(ball & ((1u << lane) - 1u))] = miss_cell;
   }
-  // Distinct hits and misses of the step.
-  const unsigned hb = __ballot_sync(0xffffffffu, uniq_hit);
-  if ((threadIdx.x & 31) == 0) {
-    if (hb) atomicAdd(&s_cnt[0], __popc(hb));
-    if (ball) atomicAdd(&s_cnt[1], __popc(ball));
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    if (s_cnt[0]) atomicAdd(&s.counters->hits, (unsigned long long)s_cnt[0]);
-    if (s_cnt[1]) atomicAdd(&s.counters->misses, (unsigned long long)s_cnt[1]);
-  }
 }
 
 }  // namespace
@@ -148,8 +134,7 @@ cudaError_t launch_match(const DeviceState& s, int t, int n_tok, int k, const in
                          int32_t* slot_map, uint8_t* hit, cudaStream_t st) {
   const int n = n_tok * k;
   dim3 grid((unsigned)((n + kThreads - 1) / kThreads), (unsigned)s.U);
-  match_kernel<<<grid, kThreads, 0, st>>>(s, t, n_tok, k, sel, slot_map, hit);
-  return cudaGetLastError();
+  return launch_pdl(match_kernel, grid, dim3(kThreads), 0, st, s, t, n_tok, k, sel, slot_map, hit);
 }
 
 }  // namespace avsg

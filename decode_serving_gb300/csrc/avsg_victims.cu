@@ -81,39 +81,49 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 
 namespace {
 
+constexpr int kCountRankMax = 2048;  // above this many misses, sort instead of counting
+
 struct VictimsSmem {
-  size_t keys, victim, wstart, ord, total;
+  size_t keys, rank, victim, wstart, ord, total;
 };
 
 __host__ __device__ inline VictimsSmem victims_layout(int max_union, int B) {
   int p = 1;
   while (p < max_union) p <<= 1;
   VictimsSmem l;
+  const size_t mu = ((sizeof(int32_t) * (size_t)max_union + 15) & ~(size_t)15);
   l.keys = 0;
-  l.victim = l.keys + sizeof(unsigned long long) * (size_t)p;
-  l.wstart = l.victim + ((sizeof(int32_t) * (size_t)max_union + 15) & ~(size_t)15);
+  l.rank = l.keys + sizeof(unsigned long long) * (size_t)p;
+  l.victim = l.rank + mu;
+  l.wstart = l.victim + mu;
   l.ord = l.wstart + sizeof(int32_t) * kOrders * kWarps;
   l.total = l.ord + (((size_t)B + 15) & ~(size_t)15);
   return l;
 }
 
+constexpr int kBatch = 8;  // 32-slot chunks whose state one warp loads before using it
+
 __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int t, int n_tok,
                                                               int k, int32_t* __restrict__ slot_map) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int s_stop, s_base, s_used, s_rebuild, s_live;
+  __shared__ int s_stop, s_base, s_used, s_rebuild, s_live, s_hits;
   __shared__ int wsum[kWarps];
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const VictimsSmem lay = victims_layout(s.max_union, s.B);
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem + lay.keys);
+  int32_t* rank = reinterpret_cast<int32_t*>(smem + lay.rank);
   int32_t* victim = reinterpret_cast<int32_t*>(smem + lay.victim);
   int32_t* wstart = reinterpret_cast<int32_t*>(smem + lay.wstart);  // [order][warp]
   uint8_t* ord = smem + lay.ord;
 
+  griddep_wait();
+  griddep_launch();
   if (tid == 0) {
     s_stop = load_err(s.err);
     s_used = 0;
     s_live = 0;
+    s_hits = 0;
   }
   __syncthreads();
   if (s_stop) return;
@@ -123,8 +133,11 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   const int m = s.mcount[u];
   unsigned long long* ms = s.mset + (size_t)u * s.MS;
 
-  // 1. Distinct missing ids, ascending: key = id << 32 | miss-set cell.
-  const int P = next_pow2(m > 0 ? m : 1);
+  // 1. Distinct missing ids (key = id << 32 | miss-set cell) and the rank of
+  //    each in ascending id order: counted directly when there are few,
+  //    otherwise by a bitonic sort.
+  const bool counting = m <= kCountRankMax;
+  const int P = counting ? m : next_pow2(m);
   for (int i = tid; i < P; i += kThreads) {
     unsigned long long key = ~0ull;
     if (i < m) {
@@ -135,45 +148,79 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   }
   for (int i = tid; i < kOrders * kWarps; i += kThreads) wstart[i] = 0;
   __syncthreads();
-  for (int kk = 2; kk <= P; kk <<= 1) {
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < P / 2; i += kThreads) {
-        const int lo = 2 * i - (i & (j - 1));
-        const int hi = lo + j;
-        const bool up = (lo & kk) == 0;
-        const unsigned long long a = keys[lo], b = keys[hi];
-        if ((a > b) == up) {
-          keys[lo] = b;
-          keys[hi] = a;
-        }
-      }
-      __syncthreads();
+  if (counting) {
+    // tpk threads per key, each counting smaller keys over a strided share.
+    int tpk = 1;
+    while (tpk < 32 && tpk * 2 * (m > 0 ? m : 1) <= kThreads) tpk <<= 1;
+    const int per_round = kThreads / tpk;
+    for (int base = 0; base < m; base += per_round) {
+      const int i = base + tid / tpk, part = tid & (tpk - 1);
+      const unsigned long long key = i < m ? keys[i] : ~0ull;
+      int r = 0;
+      if (i < m)
+        for (int j = part; j < m; j += tpk) r += keys[j] < key ? 1 : 0;
+      for (int o = tpk >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+      if (i < m && part == 0) rank[i] = r;
     }
+  } else {
+    for (int kk = 2; kk <= P; kk <<= 1) {
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < P / 2; i += kThreads) {
+          const int lo = 2 * i - (i & (j - 1));
+          const int hi = lo + j;
+          const bool up = (lo & kk) == 0;
+          const unsigned long long a = keys[lo], b = keys[hi];
+          if ((a > b) == up) {
+            keys[lo] = b;
+            keys[hi] = a;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < m; i += kThreads) rank[i] = i;
   }
 
-  // 2. Reservation order of every slot; per-warp histogram over orders.
+  // 2. Reservation order of every slot; per-warp histogram over orders.  Each
+  //    warp owns a contiguous range and loads kBatch chunks of state at once.
   const int chunk = ((B + kWarps * 32 - 1) / (kWarps * 32)) * 32;  // slots per warp
   const int w_begin = warp * chunk, w_end = min(B, w_begin + chunk);
-  for (int base = w_begin; base < w_begin + chunk; base += 32) {
-    const int sl = base + lane;
-    int o = kNotCandidate;
-    if (sl < w_end) {
-      const int sn = s.seen[ub + sl];
-      if (sn) {
+  int hits = 0;
+  for (int base = w_begin; base < w_begin + chunk; base += 32 * kBatch) {
+    int sn[kBatch], tg[kBatch], ls[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int sl = base + b * 32 + lane;
+      const bool in = sl < w_end && base + b * 32 < w_begin + chunk;
+      sn[b] = in ? __ldcg(s.seen + ub + sl) : -1;
+      tg[b] = in ? __ldcg(s.tag + ub + sl) : kEmpty;
+      ls[b] = in ? __ldcg(s.last + ub + sl) : 0;
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (base + b * 32 >= w_begin + chunk) break;  // warp-uniform
+      const int sl = base + b * 32 + lane;
+      int o = kNotCandidate;
+      if (sn[b] > 0) {
         s.last[ub + sl] = t;  // selected this step: refreshed, never a victim
         s.seen[ub + sl] = 0;
-      } else if (s.tag[ub + sl] == kEmpty) {
-        o = 0;
-      } else {
-        const int age = max(1, t - s.last[ub + sl]);
-        o = kOrders - min(kOrders - 1, age);
+        ++hits;
+      } else if (sn[b] == 0) {
+        if (tg[b] == kEmpty) {
+          o = 0;
+        } else {
+          const int age = max(1, t - ls[b]);
+          o = kOrders - min(kOrders - 1, age);
+        }
       }
-      ord[sl] = (uint8_t)o;
+      if (sl < w_end) ord[sl] = (uint8_t)o;
+      const unsigned peers = __match_any_sync(0xffffffffu, o);
+      if (o != kNotCandidate && lane == __ffs(peers) - 1) wstart[o * kWarps + warp] += __popc(peers);
+      __syncwarp();
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, o);
-    if (o != kNotCandidate && lane == __ffs(peers) - 1) wstart[o * kWarps + warp] += __popc(peers);
-    __syncwarp();
   }
+  hits = __reduce_add_sync(0xffffffffu, hits);
+  if (lane == 0 && hits) atomicAdd(&s_hits, hits);
   __syncthreads();
 
   // 3. Exclusive scan of wstart in (order, warp) order: 2 values per thread.
@@ -222,13 +269,14 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     const unsigned long long key = keys[i];
     const int32_t id = (int32_t)(key >> 32);
     const int cell = (int)(uint32_t)key;
-    const int v = victim[i];
+    const int r = rank[i];
+    const int v = victim[r];
     used += hash_insert(tab, hmask, s.hs_shift, id, v, s.err, u);
     s.tag[ub + v] = id;
     s.last[ub + v] = t;
     s.mslot[(size_t)u * s.MS + cell] = v;
     ms[cell] = kMissEmpty;
-    s.desc[s_base + i] = GatherDesc{u, id, v, 0};
+    s.desc[s_base + r] = GatherDesc{u, id, v, 0};
   }
   used = __reduce_add_sync(0xffffffffu, used);
   if (lane == 0 && used) atomicAdd(&s_used, used);
@@ -242,12 +290,14 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     if (sm <= -2) slot_map[off] = s.mslot[(size_t)u * s.MS + (-2 - sm)];
   }
 
-  // 7. Rebuild the table from the tags when erased cells pile up.
+  // 7. Statistics, and a rebuild of the table when erased cells pile up.
   if (tid == 0) {
     const int total = s.hused[u] + s_used;
     s_rebuild = total > s.HS / 2;
     s.hused[u] = total;
     s.mcount[u] = 0;
+    s.counters[u].hits += (unsigned long long)s_hits;
+    s.counters[u].misses += (unsigned long long)m;
   }
   __syncthreads();
   if (s_rebuild) {
@@ -268,6 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   }
 }
 
+int g_victims_smem = 0;
+
 }  // namespace
 
 size_t victims_smem_bytes(const DeviceState& s) { return victims_layout(s.max_union, s.B).total; }
@@ -275,11 +327,9 @@ size_t victims_smem_bytes(const DeviceState& s) { return victims_layout(s.max_un
 cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_t* slot_map,
                            cudaStream_t st) {
   const size_t smem = victims_smem_bytes(s);
-  cudaError_t e = cudaFuncSetAttribute(victims_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = ensure_smem((const void*)victims_kernel, smem, &g_victims_smem);
   if (e != cudaSuccess) return e;
-  victims_kernel<<<s.U, kThreads, smem, st>>>(s, t, n_tok, k, slot_map);
-  return cudaGetLastError();
+  return launch_pdl(victims_kernel, dim3(s.U), dim3(kThreads), smem, st, s, t, n_tok, k, slot_map);
 }
 
 }  // namespace avsg
