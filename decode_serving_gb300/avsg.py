@@ -99,6 +99,8 @@ SIGNATURES = {
     "avsg_host_free": [_P],
     "avsg_strerror": [ctypes.c_int],
     "avsg_cuda_error": [_P],
+    "avsg_attention_noalloc": [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P,
+                               _P, _P, ctypes.c_float, _P],
 }
 
 _lib = None
@@ -202,6 +204,16 @@ def avsg_host_alloc(nbytes: int) -> int:
 
 def avsg_host_free(p: int) -> None:
     _check(load_library().avsg_host_free(p), "avsg_host_free")
+
+
+def avsg_attention_noalloc(num_units, rows_per_unit, q_per_kv, head_dim, v_dim, entry_tokens,
+                           kv_shared, n_tok, k, d_k_rows, d_v_rows, d_index, d_q, d_out,
+                           softmax_scale=0.0, stream=0) -> None:
+    """Attention over caller-held device rows; allocates nothing (see avsg.h)."""
+    _check(load_library().avsg_attention_noalloc(
+        num_units, rows_per_unit, q_per_kv, head_dim, v_dim, entry_tokens, 1 if kv_shared else 0,
+        n_tok, k, d_k_rows, d_v_rows or None, d_index or None, d_q or None, d_out,
+        float(softmax_scale), stream or None), "avsg_attention_noalloc")
 
 
 def avsg_strerror(code: int) -> str:

@@ -202,6 +202,34 @@ int avsg_clear_error(avsg_handle h);
 int avsg_profile(avsg_handle h, int32_t enable);
 int avsg_profile_read(avsg_handle h, avsg_kernel_times* out);
 
+/*
+ * avsg_attention_noalloc -- the attention of avsg_step over rows the caller
+ * already holds on the device, allocating nothing.  The pages have no
+ * counterpart: this exists for callers that cannot call cudaMalloc (code
+ * running inside another framework's memory pool or allocator budget, or a
+ * serving process that must not allocate once it runs).
+ *   d_k_rows   : device bf16 [num_units][rows_per_unit][entry_tokens][head_dim].
+ *   d_v_rows   : device bf16 [num_units][rows_per_unit][entry_tokens][v_dim],
+ *                ignored (may be NULL) when kv_shared (V is the K row).
+ *   d_index    : device int32 [num_units][n_tok][k], row of each selected
+ *                entry, each in [0, rows_per_unit).
+ *   d_q, d_out : as in avsg_step.  softmax_scale 0 selects 1/sqrt(head_dim).
+ * Shapes: those avsg_create accepts for attention; num_units <= 4096
+ * (AVSG_ERR_CAPACITY beyond), n_tok <= 8.
+ * Scratch: a fixed 8 MiB device array inside the library, held by every GPU
+ * that loads it until the process exits.  The first call on a device looks
+ * up that array's address (cudaGetSymbolAddress); make the first call before
+ * any stream capture.  Every call shares the array and clears what must start
+ * at zero; calls that overlap on the GPU race, so serialise them.
+ * An index outside [0, rows_per_unit) makes the call fill d_out with NaN.
+ * Returns after enqueueing on `stream`; host-side errors change nothing.
+ */
+int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, int32_t q_per_kv,
+                           int32_t head_dim, int32_t v_dim, int32_t entry_tokens,
+                           int32_t kv_shared, int32_t n_tok, int32_t k, const void* d_k_rows,
+                           const void* d_v_rows, const int32_t* d_index, const float* d_q,
+                           float* d_out, float softmax_scale, void* stream);
+
 /* Pinned, mapped, portable host memory for the KV cache (cudaHostAlloc). */
 int avsg_host_alloc(size_t bytes, void** out);
 int avsg_host_free(void* p);
