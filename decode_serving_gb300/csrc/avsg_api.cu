@@ -27,6 +27,7 @@ struct avsg_handle_s {
   cudaError_t cuda_err = cudaSuccess;
   uint64_t steps = 0, selected = 0, host_misses = 0;
   float scale_log2 = 0.f;
+  size_t part_floats = 0;
   int32_t* slot_scratch = nullptr;  // [U][max_union] when the caller passes no slot map
   uint8_t* hit_scratch = nullptr;   // [U][max_union]
   int32_t* stage_sel = nullptr;     // avsg_step_host staging
@@ -151,6 +152,11 @@ namespace avsg {
 
 bool pdl_enabled() {
   static const int on = env_int_any("AVSG_PDL", 1);
+  return on != 0;
+}
+
+bool attention_tc_enabled() {
+  static const int on = env_int_any("AVSG_ATTN_TC", 1);
   return on != 0;
 }
 
@@ -290,7 +296,12 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.mcount, (size_t)U);
   cv.take(&s.desc, (size_t)U * max_union);
   cv.take(&s.desc_count, 1);
-  cv.take(&s.part, (size_t)U * c.max_tokens_per_step * h->splits_cap * s.G * (s.DV + 2));
+  {
+    size_t part = (size_t)U * c.max_tokens_per_step * h->splits_cap * s.G * (s.DV + 2);
+    const size_t tc = attention_tc_part_floats((int)U, c.max_tokens_per_step, s.G, s.DV, h->num_sms);
+    h->part_floats = part > tc ? part : tc;
+    cv.take(&s.part, h->part_floats);
+  }
   cv.take(&s.part_count, (size_t)U * kMaxTokens);
   cv.take(&s.counters, (size_t)U);
   cv.take(&s.err, 1);
@@ -396,7 +407,7 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
     if (e != cudaSuccess) return fail_cuda(h, e);
   }
   tl.mark(3);
-  AttnLaunch a;
+  AttnLaunch a{};
   a.n_tok = n_tok;
   a.k = k;
   a.splits = attn_splits(h, n_tok, k);
@@ -405,6 +416,8 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
   a.q = d_q;
   a.out = d_out;
   a.slot_map = slot_map;
+  a.num_sms = h->num_sms;
+  a.part_capacity = h->part_floats;
   e = launch_attention(s, a, st);
   if (e != cudaSuccess) return fail_cuda(h, e);
   tl.mark(-1);

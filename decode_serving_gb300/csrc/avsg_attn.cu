@@ -366,6 +366,9 @@ int attention_rows_per_tile(int D, int DV, int G, int kv_shared) {
 }
 
 cudaError_t launch_attention(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
+  if (attention_tc_enabled() && attention_tc_supported(s.D, s.DV, s.G, s.kv_shared) &&
+      a.num_sms > 0)
+    return launch_attention_tc(s, a, a.num_sms, st);
 #define X(d, dv, g, sh, cw, hgp)                                      \
   if (s.D == d && s.DV == dv && s.G == g && (s.kv_shared != 0) == sh) \
     return run<Shape<d, dv, g, sh, cw, hgp>>(s, a, st);

@@ -1,0 +1,564 @@
+// avsg_attn_tc: split-K decode attention on the tensor cores, for K rows of
+// 64 or 128 values and up to 8 query heads per kv-head.
+//
+// Same operation as avsg_attn.cu (the Attention operation of the Spin page,
+// "Unifying Sparse Attention with Hierarchical Memory for Scalable
+// Long-Context LLM Serving", section 2A, over exactly the rows DSA selected,
+// AVSG page arxivdaily 2609.37538, English abstract), built for GB300:
+//
+// * Rows are staged by the TMA engine: one lane per row issues a bulk copy
+//   (cp.async.bulk, completion counted on an mbarrier) into a padded shared
+//   row, so ldmatrix reads are free of bank conflicts.  Each warp runs its own
+//   3-stage pipeline; waits are bounded and report AVSG_ERR_TIMEOUT.
+// * Scores and the V sum use mma.m16n8k16 (bf16 in, fp32 accumulate) with the
+//   operands swapped: 16 selected rows form M, and the N = 8 columns hold the
+//   G query heads twice -- the bf16 rounding of scale*log2(e)*q (hi) and the
+//   bf16 rounding of what remains (lo).  hi + lo carries q to ~2^-16
+//   relative, so the scores are fp32-accurate without wasting MMA rows on
+//   padding.  P is split the same way for the V sum.
+// * The grid is persistent: 2 CTAs per SM, each taking an equal contiguous
+//   share of all 16-row tiles of all (unit, token) pairs.  A CTA writes one
+//   partial (max, sum, acc) per pair segment it covers; the last CTA to finish
+//   a pair merges its segments.  No CTA waits for another.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "avsg_internal.cuh"
+
+namespace avsg {
+namespace {
+
+constexpr int kWarpsTc = 4;
+constexpr int kThreadsTc = kWarpsTc * 32;
+constexpr int kTileRows = 16;
+constexpr int kStages = 3;
+constexpr int kCtasPerSm = 2;
+constexpr long long kWaitSpins = 1ll << 22;  // bounded mbarrier wait
+
+template <int D_, int G_, bool SHARED_>
+struct TcShape {
+  static constexpr int D = D_, G = G_;
+  static constexpr bool SHARED = SHARED_;
+  static constexpr int PITCH = 2 * D + 16;                    // bytes per staged row
+  static constexpr int NCOL = 2 * G;                          // hi and lo columns
+  static constexpr int NTN = (NCOL + 7) / 8;                  // n-tiles of 8 columns
+  static constexpr int KS = D / 16;                           // k-steps of the score MMA
+  static constexpr int MT = D / 16;                           // m-tiles of the V sum
+  static constexpr int STAGE_BYTES = kTileRows * PITCH * (SHARED ? 1 : 2);
+  static constexpr int PTILE_BYTES = NTN * kTileRows * 16;    // bf16 P tile per warp
+  static constexpr int WARP_BYTES = kStages * STAGE_BYTES + PTILE_BYTES;
+  static constexpr int MERGE_BYTES = kWarpsTc * G * (D + 2) * 4;
+  static constexpr int SMEM = (kWarpsTc * WARP_BYTES > MERGE_BYTES ? kWarpsTc * WARP_BYTES
+                                                                   : MERGE_BYTES) + 128;
+  static_assert(D % 16 == 0 && (G == 1 || G == 2 || G == 4 || G == 8), "unsupported shape");
+  static_assert(WARP_BYTES % 16 == 0, "alignment");
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// Waits for phase `parity` of the barrier to complete; false after the bound.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (long long i = 0; i < kWaitSpins; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16 round-to-nearest of x (hi) and of the remainder x - hi (lo).
+__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+}
+
+__device__ __forceinline__ uint32_t pack2(uint16_t lo_k, uint16_t hi_k) {
+  return (uint32_t)lo_k | ((uint32_t)hi_k << 16);
+}
+
+}  // namespace
+}  // namespace avsg
+
+namespace avsg {
+namespace {
+
+struct TcParams {
+  int n_tok, k, ET;
+  int rows_per_pair, tiles_per_pair;
+  long long tiles;  // all pairs
+  int ctas, max_seg;
+  int identity;
+  float scale_log2;
+  const float* q;
+  float* out;
+  const int32_t* slot_map;
+};
+
+// CTA c covers global tiles [c*T/C, (c+1)*T/C); the CTA holding tile x:
+__device__ __forceinline__ int cta_of_tile(long long x, int C, long long T) {
+  return (int)(((x + 1) * C - 1) / T);
+}
+
+template <class SH>
+__global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcParams p) {
+  constexpr int D = SH::D, G = SH::G, NTN = SH::NTN, KS = SH::KS, MT = SH::MT;
+  constexpr int PITCH = SH::PITCH;
+  constexpr int NH = G == 1 ? 1 : 2;              // heads per thread
+  constexpr int OWNERS = G >= 2 ? G / 2 : 1;      // lanes c < OWNERS own their heads
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+  __shared__ __align__(8) unsigned long long bars[kWarpsTc][kStages];
+  __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G];
+  __shared__ int s_stop, s_last;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  griddep_wait();
+  griddep_launch();
+  if (tid == 0) s_stop = load_err(s.err);
+  __syncthreads();
+  if (s_stop) return;
+
+  unsigned char* wbase = smem + warp * SH::WARP_BYTES;
+  unsigned char* ptile = wbase + kStages * SH::STAGE_BYTES;
+  const uint32_t bar0 = smem_u32(&bars[warp][0]);
+  // Zero the warp's staging once: rows past the end of a partial tile then
+  // always hold finite values (zeros or earlier rows), which P = 0 cancels.
+  for (int i = lane; i < SH::WARP_BYTES / 16; i += 32)
+    reinterpret_cast<uint4*>(wbase)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(bar0 + 8 * st, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+
+  uint32_t phase = 0;    // bit st: parity of the next completion of stage st
+  uint32_t pending = 0;  // bit st: a copy into stage st is in flight
+  bool failed = false;
+  const int head_base = G == 1 ? 0 : 2 * (c % OWNERS);
+  const bool owner = c < OWNERS;
+
+  const long long T = p.tiles;
+  const int C = p.ctas;
+  const long long t_begin = (long long)blockIdx.x * T / C;
+  const long long t_end = (long long)(blockIdx.x + 1) * T / C;
+  for (long long t = t_begin; t < t_end;) {
+    const int pair = (int)(t / p.tiles_per_pair);
+    const long long pair_t0 = (long long)pair * p.tiles_per_pair;
+    const int ta = (int)(t - pair_t0);
+    const int tb = (int)(min(t_end, pair_t0 + p.tiles_per_pair) - pair_t0);
+    t = pair_t0 + tb;
+    const int u = pair / p.n_tok, tok = pair - u * p.n_tok;
+
+    // q as MMA B fragments: column n < G is hi(q_n), G <= n < 2G is lo(q_{n-G}).
+    uint32_t qb[KS][NTN][2];
+    {
+      const float* qg = p.q + (size_t)pair * G * D;
+#pragma unroll
+      for (int nt = 0; nt < NTN; ++nt) {
+        const int col = g + 8 * nt;
+        const int head = col < G ? col : col - G;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint16_t e[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int d = 16 * ks + 2 * c + (i & 1) + 8 * (i >> 1);
+            uint16_t hi = 0, lo = 0;
+            if (col < 2 * G) split_bf16(__ldg(qg + head * D + d) * p.scale_log2, hi, lo);
+            e[i] = col < G ? hi : lo;
+          }
+          qb[ks][nt][0] = pack2(e[0], e[1]);
+          qb[ks][nt][1] = pack2(e[2], e[3]);
+        }
+      }
+    }
+
+    float m[NH], l[NH];
+    float acc[MT][NTN][4];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.f;
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
+
+    // This warp's tiles of the segment: ta + warp, ta + warp + 4, ...
+    const int n_my = tb - ta - warp > 0 ? (tb - ta - warp + kWarpsTc - 1) / kWarpsTc : 0;
+    auto issue = [&](int i, int st) {
+      const int ti = ta + warp + i * kWarpsTc;
+      const int row0 = ti * kTileRows;
+      const int nrows = min(kTileRows, p.rows_per_pair - row0);
+      const uint32_t bar = bar0 + 8 * st;
+      unsigned char* kst = wbase + st * SH::STAGE_BYTES;
+      unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
+      if (lane == 0) mbar_expect_tx(bar, (uint32_t)nrows * (SH::SHARED ? 2 * D : 4 * D));
+      __syncwarp();
+      const int r = lane & 15;
+      const bool is_v = lane >= 16;
+      if (r < nrows && !(SH::SHARED && is_v)) {
+        const int row = row0 + r;
+        const int ent = p.ET == 1 ? row : row / p.ET;
+        const int sub = row - ent * p.ET;
+        const int slot = p.identity ? tok * p.k + ent : __ldg(p.slot_map + (size_t)pair * p.k + ent);
+        const size_t srow = ((size_t)u * s.B + slot) * p.ET + sub;
+        const unsigned char* src = (is_v ? s.vbuf : s.kbuf) + srow * (2 * D);
+        bulk_copy(smem_u32((is_v ? vst : kst) + r * PITCH), src, 2 * D, bar);
+      }
+      pending |= 1u << st;
+    };
+
+    const int pro = n_my < kStages ? n_my : kStages;
+    for (int i = 0; i < pro; ++i) issue(i, i);
+    for (int i = 0; i < n_my && !failed; ++i) {
+      const int st = i % kStages;
+      const uint32_t bar = bar0 + 8 * st;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar, (phase >> st) & 1u))) {
+        failed = true;
+        raise_error(s.err, AVSG_ERR_TIMEOUT, u, -1);
+        break;
+      }
+      phase ^= 1u << st;
+      pending &= ~(1u << st);
+      const int ti = ta + warp + i * kWarpsTc;
+      const int nrows = min(kTileRows, p.rows_per_pair - ti * kTileRows);
+      const unsigned char* kst = wbase + st * SH::STAGE_BYTES;
+      const unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
+      const uint32_t kaddr = smem_u32(kst), vaddr = smem_u32(vst);
+
+      // scores^T (16 rows x 8 columns per n-tile)
+      float sc[NTN][4];
+#pragma unroll
+      for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) sc[nt][i2] = 0.f;
+      {
+        const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int acol = (lane >> 4) * 8;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kaddr + arow * PITCH + (16 * ks + acol) * 2, a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NTN; ++nt) mma_bf16(sc[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
+        }
+      }
+      // hi + lo -> full scores sv[row half][head j] for rows g and g + 8
+      float sv[2][2];
+      if (G == 8) {
+        sv[0][0] = sc[0][0] + sc[NTN - 1][0];
+        sv[0][1] = sc[0][1] + sc[NTN - 1][1];
+        sv[1][0] = sc[0][2] + sc[NTN - 1][2];
+        sv[1][1] = sc[0][3] + sc[NTN - 1][3];
+      } else if (G == 1) {
+        sv[0][0] = sc[0][0] + sc[0][1];
+        sv[1][0] = sc[0][2] + sc[0][3];
+        sv[0][1] = sv[1][1] = -INFINITY;
+      } else {
+        const int xm = G / 2;  // lane distance from a hi column pair to its lo pair
+        sv[0][0] = sc[0][0] + __shfl_xor_sync(0xffffffffu, sc[0][0], xm);
+        sv[0][1] = sc[0][1] + __shfl_xor_sync(0xffffffffu, sc[0][1], xm);
+        sv[1][0] = sc[0][2] + __shfl_xor_sync(0xffffffffu, sc[0][2], xm);
+        sv[1][1] = sc[0][3] + __shfl_xor_sync(0xffffffffu, sc[0][3], xm);
+      }
+      if (g >= nrows) sv[0][0] = sv[0][1] = -INFINITY;
+      if (g + 8 >= nrows) sv[1][0] = sv[1][1] = -INFINITY;
+
+      // online softmax per head over the 16 rows (lanes with equal c)
+      float pv[2][2], alpha[2] = {1.f, 1.f};
+#pragma unroll
+      for (int j = 0; j < NH; ++j) {
+        float mx = fmaxf(sv[0][j], sv[1][j]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(m[j], mx);
+        float p0 = 0.f, p1 = 0.f;
+        if (m_new != -INFINITY) {
+          alpha[j] = exp2f(m[j] - m_new);
+          p0 = exp2f(sv[0][j] - m_new);
+          p1 = exp2f(sv[1][j] - m_new);
+        }
+        float sum = p0 + p1;
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+        l[j] = l[j] * alpha[j] + sum;
+        m[j] = m_new;
+        pv[0][j] = p0;
+        pv[1][j] = p1;
+      }
+      if (NH == 1) alpha[1] = alpha[0];
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NTN; ++nt) {
+            acc[mt][nt][0] *= alpha[0];
+            acc[mt][nt][1] *= alpha[1];
+            acc[mt][nt][2] *= alpha[0];
+            acc[mt][nt][3] *= alpha[1];
+          }
+      }
+
+      // P^T tile in shared memory (rows x [hi columns | lo columns]) -> B fragments
+      if (owner) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int rr = g + 8 * h;
+          uint16_t hi0, lo0, hi1 = 0, lo1 = 0;
+          split_bf16(pv[h][0], hi0, lo0);
+          if (NH == 2) split_bf16(pv[h][1], hi1, lo1);
+          if (G == 1) {
+            *reinterpret_cast<uint32_t*>(ptile + rr * 16) = pack2(hi0, lo0);
+          } else {
+            const int chi = head_base, clo = G + head_base;
+            *reinterpret_cast<uint32_t*>(ptile + (chi >> 3) * 256 + rr * 16 + (chi & 7) * 2) =
+                pack2(hi0, hi1);
+            *reinterpret_cast<uint32_t*>(ptile + (clo >> 3) * 256 + rr * 16 + (clo & 7) * 2) =
+                pack2(lo0, lo1);
+          }
+        }
+      }
+      __syncwarp();
+      uint32_t pb[NTN][2];
+#pragma unroll
+      for (int nt = 0; nt < NTN; ++nt)
+        ldsm_x2_t(smem_u32(ptile + nt * 256 + (lane & 15) * 16), pb[nt][0], pb[nt][1]);
+
+      // O^T += V^T P^T
+      {
+        const int vrow = (lane & 7) + ((lane >> 4) << 3);
+        const int vcol = ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vaddr + vrow * PITCH + (16 * mt + vcol) * 2, a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NTN; ++nt) mma_bf16(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        }
+      }
+      __syncwarp();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (i + kStages < n_my) issue(i + kStages, st);
+    }
+    if (failed) {  // let the copies still in flight land before the memory is reused
+      for (int st = 0; st < kStages; ++st)
+        if (pending & (1u << st)) {
+          mbar_wait(bar0 + 8 * st, (phase >> st) & 1u);
+          phase ^= 1u << st;
+        }
+      pending = 0;
+    }
+
+    // Per-warp result -> shared memory, then merge the 4 warps.
+    __syncthreads();  // every warp is done with its staging (reused below)
+    float* mo = reinterpret_cast<float*>(smem);  // [warp][G][D]
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int dv = 16 * mt + g + 8 * (i >> 1);
+        float v;
+        int head;
+        if (G == 8) {
+          v = acc[mt][0][i] + acc[mt][NTN - 1][i];
+          head = 2 * c + (i & 1);
+        } else if (G == 1) {
+          v = (i & 1) ? 0.f : acc[mt][0][i] + acc[mt][0][i + 1];
+          head = 0;
+        } else {
+          v = acc[mt][0][i] + __shfl_xor_sync(0xffffffffu, acc[mt][0][i], G / 2);
+          head = head_base + (i & 1);
+        }
+        if (owner && (G != 1 || (i & 1) == 0)) mo[(warp * G + head) * D + dv] = v;
+      }
+    if (owner && g == 0) {
+#pragma unroll
+      for (int j = 0; j < NH; ++j) {
+        s_m[warp][head_base + j] = m[j];
+        s_l[warp][head_base + j] = l[j];
+      }
+    }
+    __syncthreads();
+
+    const int first = cta_of_tile(pair_t0, C, T);
+    const int last = cta_of_tile(pair_t0 + p.tiles_per_pair - 1, C, T);
+    const int nseg = last - first + 1;
+    float* out = p.out + (size_t)pair * G * D;
+    const size_t stride = (size_t)G * (D + 2);
+    float* pbase = s.part + (size_t)pair * p.max_seg * stride;
+    float* pp = pbase + (size_t)(blockIdx.x - first) * stride;
+    for (int o = tid; o < G * D; o += kThreadsTc) {
+      const int head = o / D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarpsTc; ++w) M = fmaxf(M, s_m[w][head]);
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarpsTc; ++w) {
+          const float e = exp2f(s_m[w][head] - M);
+          L = fmaf(s_l[w][head], e, L);
+          O = fmaf(mo[(w * G) * D + o], e, O);
+        }
+      }
+      if (nseg == 1) {
+        out[o] = L > 0.f ? O / L : 0.f;
+      } else {
+        pp[2 * G + o] = O;
+        if (o % D == 0) {
+          pp[head] = M;
+          pp[G + head] = L;
+        }
+      }
+    }
+    if (nseg > 1) {
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        const int prev = atomicAdd(&s.part_count[u * kMaxTokens + tok], 1);
+        s_last = prev == nseg - 1;
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        for (int o = tid; o < G * D; o += kThreadsTc) {
+          const int head = o / D;
+          float M = -INFINITY;
+          for (int q2 = 0; q2 < nseg; ++q2) M = fmaxf(M, __ldcg(pbase + q2 * stride + head));
+          float L = 0.f, O = 0.f;
+          if (M != -INFINITY)
+            for (int q2 = 0; q2 < nseg; ++q2) {
+              const float e = exp2f(__ldcg(pbase + q2 * stride + head) - M);
+              L = fmaf(__ldcg(pbase + q2 * stride + G + head), e, L);
+              O = fmaf(__ldcg(pbase + q2 * stride + 2 * G + o), e, O);
+            }
+          out[o] = L > 0.f ? O / L : 0.f;
+        }
+        if (tid == 0) s.part_count[u * kMaxTokens + tok] = 0;
+      }
+    }
+    __syncthreads();  // the merge area is staging again for the next segment
+  }
+}
+
+template <class SH>
+cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaStream_t st) {
+  static int smem_done = 0;
+  TcParams p;
+  p.n_tok = a.n_tok;
+  p.k = a.k;
+  p.ET = s.ET;
+  p.rows_per_pair = a.k * s.ET;
+  p.tiles_per_pair = (p.rows_per_pair + kTileRows - 1) / kTileRows;
+  const long long pairs = (long long)s.U * a.n_tok;
+  p.tiles = pairs * p.tiles_per_pair;
+  long long C = (long long)num_sms * kCtasPerSm;
+  if (C > p.tiles) C = p.tiles;
+  const size_t stride = (size_t)SH::G * (SH::D + 2);
+  for (;;) {
+    const long long per = p.tiles / C;  // fewest tiles a CTA gets
+    p.max_seg = (int)((p.tiles_per_pair + per - 1) / per + 1);
+    if ((size_t)pairs * p.max_seg * stride <= (size_t)a.part_capacity || C == 1) break;
+    C = C * 3 / 4 > 0 ? C * 3 / 4 : 1;
+  }
+  p.ctas = (int)C;
+  p.identity = a.identity_slots;
+  p.scale_log2 = a.scale_log2;
+  p.q = a.q;
+  p.out = a.out;
+  p.slot_map = a.slot_map;
+  cudaError_t e = ensure_smem((const void*)attn_tc_kernel<SH>, SH::SMEM, &smem_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_tc_kernel<SH>, dim3(p.ctas), dim3(kThreadsTc), SH::SMEM, st, s, p);
+}
+
+}  // namespace
+
+bool attention_tc_supported(int D, int DV, int G, int kv_shared) {
+  (void)kv_shared;
+  return D == DV && (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sms) {
+  // pairs * max_seg <= T / floor(T / C) + 2 * pairs <= 2 * C + 2 * pairs (see run_tc)
+  const size_t pairs = (size_t)U * max_tokens;
+  return (2 * (size_t)num_sms * kCtasPerSm + 2 * pairs) * (size_t)G * (DV + 2);
+}
+
+cudaError_t launch_attention_tc(const DeviceState& s, const AttnLaunch& a, int num_sms,
+                                cudaStream_t st) {
+#define X(d, g, sh)                                                         \
+  if (s.D == d && s.G == g && (s.kv_shared != 0) == sh)                     \
+    return run_tc<TcShape<d, g, sh>>(s, a, num_sms, st);
+  X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
+  X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
+  X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)
+  X(64, 1, true) X(64, 2, true) X(64, 4, true) X(64, 8, true)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace avsg

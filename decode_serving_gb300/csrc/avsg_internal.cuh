@@ -123,9 +123,17 @@ struct AttnLaunch {
   const float* q;
   float* out;
   const int32_t* slot_map;
+  int num_sms;                     // SMs of the device (persistent grid size)
+  size_t part_capacity;            // floats available at DeviceState::part
 };
 bool attention_supported(int D, int DV, int G, int kv_shared);
 int attention_rows_per_tile(int D, int DV, int G, int kv_shared);
 cudaError_t launch_attention(const DeviceState& s, const AttnLaunch& a, cudaStream_t st);
+// Tensor-core attention (avsg_attn_tc.cu): K rows of 64 or 128, G <= 8, Dv == D.
+bool attention_tc_supported(int D, int DV, int G, int kv_shared);
+size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sms);
+cudaError_t launch_attention_tc(const DeviceState& s, const AttnLaunch& a, int num_sms,
+                                cudaStream_t st);
+bool attention_tc_enabled();
 
 }  // namespace avsg

@@ -143,7 +143,7 @@ extern "C" int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, 
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    AttnLaunch a;
+    AttnLaunch a{};
     a.n_tok = n_tok;
     a.k = k;
     a.splits = (int)splits;
@@ -152,6 +152,8 @@ extern "C" int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, 
     a.q = d_q;
     a.out = d_out;
     a.slot_map = d_index;
+    a.num_sms = sms;
+    a.part_capacity = (kScratchBytes - kPartOffset) / sizeof(float);
     e = launch_attention(s, a, st);
   }
   if (e == cudaSuccess) {
