@@ -6,10 +6,12 @@
 // Long-Context LLM Serving", section 2A, over exactly the rows DSA selected,
 // AVSG page arxivdaily 2609.37538, English abstract), built for GB300:
 //
-// * Rows are staged by the TMA engine: one lane per row issues a bulk copy
-//   (cp.async.bulk, completion counted on an mbarrier) into a padded shared
-//   row, so ldmatrix reads are free of bank conflicts.  Each warp runs its own
-//   3-stage pipeline; waits are bounded and report AVSG_ERR_TIMEOUT.
+// * Rows are gathered into padded shared rows (so ldmatrix reads are free of
+//   bank conflicts) with 16-byte cp.async: one warp instruction moves a whole
+//   256-byte row (2 for 128-byte rows), slot ids are fetched a tile ahead, and
+//   each warp runs its own 3-stage pipeline closed by cp.async.wait_group.
+//   (Per-row TMA bulk copies were measured first: at ~40 cycles per 256-byte
+//   request the TMA engine capped the kernel at ~1.9 TB/s.)
 // * Scores and the V sum use mma.m16n8k16 (bf16 in, fp32 accumulate) with the
 //   operands swapped: 16 selected rows form M, and the N = 8 columns hold the
 //   G query heads twice -- the bf16 rounding of scale*log2(e)*q (hi) and the
@@ -33,7 +35,6 @@ constexpr int kThreadsTc = kWarpsTc * 32;
 constexpr int kTileRows = 16;
 constexpr int kStages = 3;
 constexpr int kCtasPerSm = 2;
-constexpr long long kWaitSpins = 1ll << 22;  // bounded mbarrier wait
 
 template <int D_, int G_, bool SHARED_>
 struct TcShape {
@@ -58,37 +59,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src)
                : "memory");
 }
-
-// Waits for phase `parity` of the barrier to complete; false after the bound.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kWaitSpins; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -162,7 +140,6 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
   constexpr int OWNERS = G >= 2 ? G / 2 : 1;      // lanes c < OWNERS own their heads
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
-  __shared__ __align__(8) unsigned long long bars[kWarpsTc][kStages];
   __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G];
   __shared__ int s_stop, s_last;
 
@@ -176,21 +153,11 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
 
   unsigned char* wbase = smem + warp * SH::WARP_BYTES;
   unsigned char* ptile = wbase + kStages * SH::STAGE_BYTES;
-  const uint32_t bar0 = smem_u32(&bars[warp][0]);
   // Zero the warp's staging once: rows past the end of a partial tile then
   // always hold finite values (zeros or earlier rows), which P = 0 cancels.
   for (int i = lane; i < SH::WARP_BYTES / 16; i += 32)
     reinterpret_cast<uint4*>(wbase)[i] = make_uint4(0u, 0u, 0u, 0u);
-  if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(bar0 + 8 * st, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncwarp();
-
-  uint32_t phase = 0;    // bit st: parity of the next completion of stage st
-  uint32_t pending = 0;  // bit st: a copy into stage st is in flight
-  bool failed = false;
   const int head_base = G == 1 ? 0 : 2 * (c % OWNERS);
   const bool owner = c < OWNERS;
 
@@ -246,41 +213,40 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
 
     // This warp's tiles of the segment: ta + warp, ta + warp + 4, ...
     const int n_my = tb - ta - warp > 0 ? (tb - ta - warp + kWarpsTc - 1) / kWarpsTc : 0;
-    auto issue = [&](int i, int st) {
-      const int ti = ta + warp + i * kWarpsTc;
-      const int row0 = ti * kTileRows;
-      const int nrows = min(kTileRows, p.rows_per_pair - row0);
-      const uint32_t bar = bar0 + 8 * st;
+    // Buffer row of row (lane & 15) of this warp's i-th tile, or -1.
+    auto row_index = [&](int i) -> long long {
+      const int row = (ta + warp + i * kWarpsTc) * kTileRows + (lane & 15);
+      if (i >= n_my || row >= p.rows_per_pair) return -1;
+      const int ent = p.ET == 1 ? row : row / p.ET;
+      const int sub = row - ent * p.ET;
+      const int slot = p.identity ? tok * p.k + ent : __ldg(p.slot_map + (size_t)pair * p.k + ent);
+      return ((long long)u * s.B + slot) * p.ET + sub;
+    };
+    constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
+    constexpr int RPI = 32 / CPR;    // rows per warp instruction
+    auto issue = [&](long long myrow, int st) {
       unsigned char* kst = wbase + st * SH::STAGE_BYTES;
       unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
-      if (lane == 0) mbar_expect_tx(bar, (uint32_t)nrows * (SH::SHARED ? 2 * D : 4 * D));
-      __syncwarp();
-      const int r = lane & 15;
-      const bool is_v = lane >= 16;
-      if (r < nrows && !(SH::SHARED && is_v)) {
-        const int row = row0 + r;
-        const int ent = p.ET == 1 ? row : row / p.ET;
-        const int sub = row - ent * p.ET;
-        const int slot = p.identity ? tok * p.k + ent : __ldg(p.slot_map + (size_t)pair * p.k + ent);
-        const size_t srow = ((size_t)u * s.B + slot) * p.ET + sub;
-        const unsigned char* src = (is_v ? s.vbuf : s.kbuf) + srow * (2 * D);
-        bulk_copy(smem_u32((is_v ? vst : kst) + r * PITCH), src, 2 * D, bar);
+      const int ch = lane % CPR, rsub = lane / CPR;
+#pragma unroll
+      for (int it = 0; it < kTileRows / RPI; ++it) {
+        const int r = it * RPI + rsub;
+        const long long srow = __shfl_sync(0xffffffffu, myrow, r);
+        if (srow >= 0) {
+          cp_async16(kst + r * PITCH + ch * 16, s.kbuf + srow * (2 * D) + ch * 16);
+          if (!SH::SHARED) cp_async16(vst + r * PITCH + ch * 16, s.vbuf + srow * (2 * D) + ch * 16);
+        }
       }
-      pending |= 1u << st;
+      cp_async_commit();  // one group per tile (empty past the end) keeps the count uniform
     };
 
-    const int pro = n_my < kStages ? n_my : kStages;
-    for (int i = 0; i < pro; ++i) issue(i, i);
-    for (int i = 0; i < n_my && !failed; ++i) {
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) issue(row_index(i), i);
+    long long next_row = row_index(kStages);
+    for (int i = 0; i < n_my; ++i) {
       const int st = i % kStages;
-      const uint32_t bar = bar0 + 8 * st;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar, (phase >> st) & 1u))) {
-        failed = true;
-        raise_error(s.err, AVSG_ERR_TIMEOUT, u, -1);
-        break;
-      }
-      phase ^= 1u << st;
-      pending &= ~(1u << st);
+      cp_async_wait<kStages - 1>();
+      __syncwarp();
       const int ti = ta + warp + i * kWarpsTc;
       const int nrows = min(kTileRows, p.rows_per_pair - ti * kTileRows);
       const unsigned char* kst = wbase + st * SH::STAGE_BYTES;
@@ -288,11 +254,11 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
       const uint32_t kaddr = smem_u32(kst), vaddr = smem_u32(vst);
 
       // scores^T (16 rows x 8 columns per n-tile)
-      float sc[NTN][4];
+      float sc[NTN][4], sc2[NTN][4];  // two chains: even and odd k-steps
 #pragma unroll
       for (int nt = 0; nt < NTN; ++nt)
 #pragma unroll
-        for (int i2 = 0; i2 < 4; ++i2) sc[nt][i2] = 0.f;
+        for (int i2 = 0; i2 < 4; ++i2) sc[nt][i2] = sc2[nt][i2] = 0.f;
       {
         const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
         const int acol = (lane >> 4) * 8;
@@ -301,8 +267,13 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
           uint32_t a0, a1, a2, a3;
           ldsm_x4(kaddr + arow * PITCH + (16 * ks + acol) * 2, a0, a1, a2, a3);
 #pragma unroll
-          for (int nt = 0; nt < NTN; ++nt) mma_bf16(sc[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
+          for (int nt = 0; nt < NTN; ++nt)
+            mma_bf16((ks & 1) ? sc2[nt] : sc[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
         }
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+          for (int i2 = 0; i2 < 4; ++i2) sc[nt][i2] += sc2[nt][i2];
       }
       // hi + lo -> full scores sv[row half][head j] for rows g and g + 8
       float sv[2][2];
@@ -399,18 +370,11 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
           for (int nt = 0; nt < NTN; ++nt) mma_bf16(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
         }
       }
-      __syncwarp();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      if (i + kStages < n_my) issue(i + kStages, st);
+      __syncwarp();  // every lane has read stage st
+      issue(next_row, st);
+      next_row = row_index(i + kStages + 1);
     }
-    if (failed) {  // let the copies still in flight land before the memory is reused
-      for (int st = 0; st < kStages; ++st)
-        if (pending & (1u << st)) {
-          mbar_wait(bar0 + 8 * st, (phase >> st) & 1u);
-          phase ^= 1u << st;
-        }
-      pending = 0;
-    }
+    cp_async_wait<0>();
 
     // Per-warp result -> shared memory, then merge the 4 warps.
     __syncthreads();  // every warp is done with its staging (reused below)
