@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
       const int slot = p.identity ? tok * p.k + ent : __ldg(p.slot_map + (size_t)pair * p.k + ent);
       return ((long long)u * s.B + slot) * p.ET + sub;
     };
+    long long next_row;
     constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;    // rows per warp instruction
     auto issue = [&](long long myrow, int st) {
@@ -240,9 +241,14 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
       cp_async_commit();  // one group per tile (empty past the end) keeps the count uniform
     };
 
+    {
+      long long first_rows[kStages + 1];  // slot loads issued together, then the copies
 #pragma unroll
-    for (int i = 0; i < kStages; ++i) issue(row_index(i), i);
-    long long next_row = row_index(kStages);
+      for (int i = 0; i <= kStages; ++i) first_rows[i] = row_index(i);
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) issue(first_rows[i], i);
+      next_row = first_rows[kStages];
+    }
     for (int i = 0; i < n_my; ++i) {
       const int st = i % kStages;
       cp_async_wait<kStages - 1>();
@@ -448,18 +454,29 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
       __syncthreads();
       if (s_last) {
         __threadfence();
+        // Weight of each segment per head, once, in shared memory (the
+        // staging area is free here); then every output is a sum of
+        // independent loads.
+        float* wseg = reinterpret_cast<float*>(smem);  // [nseg][G]
+        if (tid < G) {
+          float M = -INFINITY, L = 0.f;
+          for (int q2 = 0; q2 < nseg; ++q2) M = fmaxf(M, __ldcg(pbase + q2 * stride + tid));
+          for (int q2 = 0; q2 < nseg; ++q2) {
+            const float e = M == -INFINITY ? 0.f : exp2f(__ldcg(pbase + q2 * stride + tid) - M);
+            wseg[q2 * G + tid] = e;
+            L = fmaf(__ldcg(pbase + q2 * stride + G + tid), e, L);
+          }
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          for (int q2 = 0; q2 < nseg; ++q2) wseg[q2 * G + tid] *= inv;
+        }
+        __syncthreads();
         for (int o = tid; o < G * D; o += kThreadsTc) {
           const int head = o / D;
-          float M = -INFINITY;
-          for (int q2 = 0; q2 < nseg; ++q2) M = fmaxf(M, __ldcg(pbase + q2 * stride + head));
-          float L = 0.f, O = 0.f;
-          if (M != -INFINITY)
-            for (int q2 = 0; q2 < nseg; ++q2) {
-              const float e = exp2f(__ldcg(pbase + q2 * stride + head) - M);
-              L = fmaf(__ldcg(pbase + q2 * stride + G + head), e, L);
-              O = fmaf(__ldcg(pbase + q2 * stride + 2 * G + o), e, O);
-            }
-          out[o] = L > 0.f ? O / L : 0.f;
+          float O = 0.f;
+#pragma unroll 8
+          for (int q2 = 0; q2 < nseg; ++q2)
+            O = fmaf(__ldcg(pbase + q2 * stride + 2 * G + o), wseg[q2 * G + head], O);
+          out[o] = O;
         }
         if (tid == 0) s.part_count[u * kMaxTokens + tok] = 0;
       }
