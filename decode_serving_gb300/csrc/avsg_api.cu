@@ -161,10 +161,12 @@ bool attention_tc_enabled() {
 }
 
 cudaError_t ensure_smem(const void* kernel, size_t bytes, int* done_bytes) {
-  if ((int)bytes <= *done_bytes) return cudaSuccess;
-  const cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) *done_bytes = (int)bytes;
+  if (*done_bytes > 0 && (int)bytes <= *done_bytes - 1) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess && bytes > 0)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) *done_bytes = (int)bytes + 1;  // +1: 0 bytes also counts as done
   return e;
 }
 

@@ -122,6 +122,9 @@ __global__ void __launch_bounds__(kThreads) gather_all_kernel(DeviceState s, int
 }  // namespace
 
 cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st) {
+  static int attr_done = 0;
+  const cudaError_t e = ensure_smem((const void*)gather_kernel, 0, &attr_done);
+  if (e != cudaSuccess) return e;
   return launch_pdl(gather_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
 }
 

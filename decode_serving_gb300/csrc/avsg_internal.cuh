@@ -103,7 +103,9 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
 }
 
-// Raises a kernel's dynamic shared memory limit once per size.
+// Raises a kernel's dynamic shared memory limit once per size, and asks for
+// the largest shared-memory carveout so consecutive kernels of a step keep
+// one L1/shared split.
 cudaError_t ensure_smem(const void* kernel, size_t bytes, int* done_bytes);
 
 // Kernel launchers (one per .cu file).

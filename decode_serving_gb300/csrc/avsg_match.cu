@@ -134,6 +134,9 @@ cudaError_t launch_match(const DeviceState& s, int t, int n_tok, int k, const in
                          int32_t* slot_map, uint8_t* hit, cudaStream_t st) {
   const int n = n_tok * k;
   dim3 grid((unsigned)((n + kThreads - 1) / kThreads), (unsigned)s.U);
+  static int attr_done = 0;
+  const cudaError_t e = ensure_smem((const void*)match_kernel, 0, &attr_done);
+  if (e != cudaSuccess) return e;
   return launch_pdl(match_kernel, grid, dim3(kThreads), 0, st, s, t, n_tok, k, sel, slot_map, hit);
 }
 
