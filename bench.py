@@ -431,7 +431,7 @@ def report_ours(args, res, world, max_ms, max_e2e_ms) -> dict:
     w = res["w"]
     K = args.steps
     sel_step = w.units * w.tokens_per_step * w.k
-    value = world * sel_step * 1e3 / max_ms
+    value = whole_job_value(w, world, max_ms)
     hbm_peak, peak_kind = measured_peaks()
     ab = algorithmic_bytes(w, res["hits"], res["misses"], K)
     traffic = ncu_traffic()
@@ -498,6 +498,22 @@ def report_ours(args, res, world, max_ms, max_e2e_ms) -> dict:
     return line
 
 
+def slowest_rank(torch, ms_per_step, e2e_ms, world, device):
+    """Step time of the slowest rank (max over ranks); e2e likewise (None stays None)."""
+    t = torch.tensor([ms_per_step, e2e_ms if e2e_ms is not None else 0.0], dtype=torch.float64,
+                     device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t[0]), (float(t[1]) if e2e_ms is not None else None)
+
+
+def whole_job_value(w, world, max_ms) -> float:
+    """Selected entries of all ranks per second: every rank runs its own copy of
+    the batch (units shard across GPUs with no exchange), so a step of the job
+    is `world` batches in the slowest rank's step time."""
+    return world * w.units * w.tokens_per_step * w.k * 1e3 / max_ms
+
+
 def main():
     args = parse()
     if args._oracle_cost:
@@ -524,11 +540,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     res = run_ours(args, rank, world, torch)
-    ms = torch.tensor([res["ms_per_step"], res.get("e2e_ms", 0.0)], dtype=torch.float64,
-                      device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(ms, op=torch.distributed.ReduceOp.MAX)
-    max_ms, max_e2e = float(ms[0]), (float(ms[1]) if "e2e_ms" in res else None)
+    max_ms, max_e2e = slowest_rank(torch, res["ms_per_step"], res.get("e2e_ms"), world, "cuda")
     if rank == 0:
         line = report_ours(args, res, world, max_ms, max_e2e)
         if world == 1 and not args.no_cpu_baseline:
