@@ -75,11 +75,15 @@ class avsg_info(ctypes.Structure):
     ]
 
 
+AVSG_NUM_KERNELS = 6
+
+
 class avsg_kernel_times(ctypes.Structure):
-    _fields_ = [("ms", ctypes.c_double * 4), ("launches", ctypes.c_uint64 * 4)]
+    _fields_ = [("ms", ctypes.c_double * AVSG_NUM_KERNELS),
+                ("launches", ctypes.c_uint64 * AVSG_NUM_KERNELS)]
 
 
-KERNEL_NAMES = ("match", "victims", "gather", "attention")
+KERNEL_NAMES = ("match", "victims", "gather", "attention", "attention_miss", "commit")
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32

@@ -42,8 +42,12 @@ struct avsg_handle_s {
     cudaEvent_t a, b;
   };
   std::vector<Rec> recs;
-  double prof_ms[4] = {0, 0, 0, 0};
-  uint64_t prof_launches[4] = {0, 0, 0, 0};
+  double prof_ms[AVSG_NUM_KERNELS] = {};
+  uint64_t prof_launches[AVSG_NUM_KERNELS] = {};
+  // side stream: the miss gather and the table commit run there while the
+  // caller's stream runs attention over the hit rows
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_commit = nullptr;
 };
 
 namespace {
@@ -117,6 +121,9 @@ int map_host(avsg_handle h, const void* p, size_t bytes, const unsigned char** d
 void release(avsg_handle h) {
   if (!h) return;
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
+  for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_commit})
+    if (e) cudaEventDestroy(e);
+  if (h->side) cudaStreamDestroy(h->side);
   if (h->dev_block) cudaFree(h->dev_block);
   if (h->reg_k && h->host_k) cudaHostUnregister(const_cast<void*>(h->host_k));
   if (h->reg_v && h->host_v) cudaHostUnregister(const_cast<void*>(h->host_v));
@@ -157,6 +164,11 @@ bool pdl_enabled() {
 
 bool attention_tc_enabled() {
   static const int on = env_int_any("AVSG_ATTN_TC", 1);
+  return on != 0;
+}
+
+bool overlap_enabled() {
+  static const int on = env_int_any("AVSG_OVERLAP", 1);
   return on != 0;
 }
 
@@ -298,6 +310,10 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.mcount, (size_t)U);
   cv.take(&s.desc, (size_t)U * max_union);
   cv.take(&s.desc_count, 1);
+  cv.take(&s.dbase, (size_t)U);
+  cv.take(&s.dcount, (size_t)U);
+  cv.take(&s.order, (size_t)U * max_union);
+  cv.take(&s.nhit, (size_t)U * kMaxTokens);
   {
     size_t part = (size_t)U * c.max_tokens_per_step * h->splits_cap * s.G * (s.DV + 2);
     const size_t tc = attention_tc_part_floats((int)U, c.max_tokens_per_step, s.G, s.DV, h->num_sms);
@@ -322,12 +338,21 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   rebase(&s.kbuf, b); rebase(&s.vbuf, b); rebase(&s.tag, b); rebase(&s.last, b);
   rebase(&s.seen, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.mset, b);
   rebase(&s.mslot, b); rebase(&s.mlist, b); rebase(&s.mcount, b); rebase(&s.desc, b);
-  rebase(&s.desc_count, b); rebase(&s.part, b); rebase(&s.part_count, b);
+  rebase(&s.desc_count, b); rebase(&s.part, b);
+  rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&s.order, b); rebase(&s.nhit, b); rebase(&s.part_count, b);
   rebase(&s.counters, b); rebase(&s.err, b);
   rebase(&h->slot_scratch, b); rebase(&h->hit_scratch, b); rebase(&h->stage_sel, b);
   rebase(&h->stage_q, b); rebase(&h->stage_out, b);
   if (shared) s.vbuf = s.kbuf;
 
+  e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_gather, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_commit, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    release(h);
+    return AVSG_ERR_CUDA;
+  }
   rc = init_state(h, nullptr);
   if (rc == AVSG_OK) {
     e = cudaDeviceSynchronize();
@@ -359,20 +384,25 @@ cudaEvent_t take_event(avsg_handle h) {
   return h->ev_pool[h->ev_used++];
 }
 
-// Records an event before kernel `kernel` (when profiling) and returns it.
-struct Timeline {
+// Per-kernel CUDA events (when profiling): begin(kernel, stream) before a
+// launch, end() after it, on the stream the kernel runs on.
+struct Prof {
   avsg_handle h;
-  cudaStream_t st;
-  cudaEvent_t prev = nullptr;
-  int prev_kernel = -1;
-  void mark(int next_kernel) {
+  cudaEvent_t a = nullptr;
+  int kernel = -1;
+  void begin(int k, cudaStream_t st) {
     if (!h->prof) return;
-    cudaEvent_t e = take_event(h);
-    if (!e) return;
-    cudaEventRecord(e, st);
-    if (prev && prev_kernel >= 0) h->recs.push_back({prev_kernel, prev, e});
-    prev = e;
-    prev_kernel = next_kernel;
+    a = take_event(h);
+    kernel = k;
+    if (a) cudaEventRecord(a, st);
+  }
+  void end(cudaStream_t st) {
+    if (!h->prof || !a) return;
+    cudaEvent_t b = take_event(h);
+    if (!b) return;
+    cudaEventRecord(b, st);
+    h->recs.push_back({kernel, a, b});
+    a = nullptr;
   }
 };
 
@@ -391,24 +421,6 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
     return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
   }
   int32_t* slot_map = d_slot_map ? d_slot_map : h->slot_scratch;
-  Timeline tl{h, st};
-  if (h->no_reuse) {
-    tl.mark(2);
-    e = launch_gather_all(s, n_tok, k, d_sel, slot_map, d_hit, h->gather_ctas, st);
-    if (e != cudaSuccess) return fail_cuda(h, e);
-    h->host_misses += (uint64_t)s.U * n_tok * k;
-  } else {
-    tl.mark(0);
-    e = launch_match(s, t, n_tok, k, d_sel, slot_map, d_hit, st);
-    if (e != cudaSuccess) return fail_cuda(h, e);
-    tl.mark(1);
-    e = launch_victims(s, t, n_tok, k, slot_map, st);
-    if (e != cudaSuccess) return fail_cuda(h, e);
-    tl.mark(2);
-    e = launch_gather(s, h->gather_ctas, st);
-    if (e != cudaSuccess) return fail_cuda(h, e);
-  }
-  tl.mark(3);
   AttnLaunch a{};
   a.n_tok = n_tok;
   a.k = k;
@@ -420,9 +432,54 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
   a.slot_map = slot_map;
   a.num_sms = h->num_sms;
   a.part_capacity = h->part_floats;
-  e = launch_attention(s, a, st);
+  Prof pf{h};
+#define AVSG_RUN(kernel_index, stream, call) \
+  do {                                       \
+    pf.begin(kernel_index, stream);          \
+    e = (call);                              \
+    if (e != cudaSuccess) return fail_cuda(h, e); \
+    pf.end(stream);                          \
+  } while (0)
+  if (h->no_reuse) {
+    AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather_all(s, n_tok, k, d_sel, slot_map, d_hit, h->gather_ctas, st));
+    h->host_misses += (uint64_t)s.U * n_tok * k;
+    AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(s, a, st));
+    return AVSG_OK;
+  }
+  // Two attention passes (hit rows beside the gather, then miss rows) when
+  // the tensor-core kernel serves this shape and the partials fit.
+  const int pairs = s.U * n_tok;
+  const int resident = 2 * h->num_sms;
+  const int splits_h = resident / pairs > 0 ? resident / pairs : 1;
+  const int splits_m = splits_h / 4 > 0 ? splits_h / 4 : 1;
+  const bool overlap =
+      overlap_enabled() && attention_tc_enabled() &&
+      attention_tc_supported(s.D, s.DV, s.G, s.kv_shared) &&
+      (size_t)pairs * (splits_h + splits_m) * s.G * (s.DV + 2) <= h->part_floats;
+  AVSG_RUN(AVSG_KERNEL_MATCH, st, launch_match(s, t, n_tok, k, d_sel, slot_map, d_hit, st));
+  AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(s, t, n_tok, k, slot_map, overlap ? 1 : 0, st));
+  if (!overlap) {
+    AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(s, h->gather_ctas, st));
+    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(s, st));
+    AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(s, a, st));
+    return AVSG_OK;
+  }
+  e = cudaEventRecord(h->ev_fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  tl.mark(-1);
+  AVSG_RUN(AVSG_KERNEL_GATHER, h->side, launch_gather(s, h->gather_ctas, h->side));
+  e = cudaEventRecord(h->ev_gather, h->side);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_COMMIT, h->side, launch_commit(s, h->side));
+  e = cudaEventRecord(h->ev_commit, h->side);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(s, a, 0, splits_h, splits_m, st));
+  e = cudaStreamWaitEvent(st, h->ev_gather, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, st, launch_attention_tc_pass(s, a, 1, splits_h, splits_m, st));
+  e = cudaStreamWaitEvent(st, h->ev_commit, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+#undef AVSG_RUN
   return AVSG_OK;
 }
 
@@ -561,7 +618,7 @@ extern "C" int avsg_profile(avsg_handle h, int32_t enable) {
   if (!h) return AVSG_ERR_INVALID_ARG;
   h->prof = enable != 0;
   if (h->prof) {
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < AVSG_NUM_KERNELS; ++i) {
       h->prof_ms[i] = 0;
       h->prof_launches[i] = 0;
     }
@@ -577,14 +634,15 @@ extern "C" int avsg_profile_read(avsg_handle h, avsg_kernel_times* out) {
   if (e != cudaSuccess) return fail_cuda(h, e);
   for (const auto& r : h->recs) {
     float ms = 0.f;
-    if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess && r.kernel >= 0 && r.kernel < 4) {
+    if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess && r.kernel >= 0 &&
+        r.kernel < AVSG_NUM_KERNELS) {
       h->prof_ms[r.kernel] += ms;
       h->prof_launches[r.kernel] += 1;
     }
   }
   h->recs.clear();
   h->ev_used = 0;
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < AVSG_NUM_KERNELS; ++i) {
     out->ms[i] = h->prof_ms[i];
     out->launches[i] = h->prof_launches[i];
   }

@@ -18,10 +18,15 @@
 //   bf16 rounding of what remains (lo).  hi + lo carries q to ~2^-16
 //   relative, so the scores are fp32-accurate without wasting MMA rows on
 //   padding.  P is split the same way for the V sum.
-// * The grid is persistent: 2 CTAs per SM, each taking an equal contiguous
-//   share of all 16-row tiles of all (unit, token) pairs.  A CTA writes one
-//   partial (max, sum, acc) per pair segment it covers; the last CTA to finish
-//   a pair merges its segments.  No CTA waits for another.
+// * Single pass (attn_tc_kernel): a persistent grid of 2 CTAs per SM, each
+//   taking an equal contiguous share of all 16-row tiles of all (unit, token)
+//   pairs; a CTA writes one partial (max, sum, acc) per pair segment it
+//   covers and the last CTA to finish a pair merges its segments.
+// * Two passes (attn_tc_pass_kernel): over the hit-first slot lists the
+//   reservation kernel writes -- pass 0 covers the rows that were already
+//   resident and can run while the gather copies the misses in; pass 1 covers
+//   the missed rows and merges both passes.
+// No CTA waits for another.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -117,14 +122,24 @@ namespace {
 
 struct TcParams {
   int n_tok, k, ET;
-  int rows_per_pair, tiles_per_pair;
-  long long tiles;  // all pairs
-  int ctas, max_seg;
-  int identity;
+  int identity;                 // slot of entry e of (unit, token) is token * k + e
   float scale_log2;
   const float* q;
   float* out;
-  const int32_t* slot_map;
+  const int32_t* slots;         // [pairs][k] slot of each listed entry
+  // persistent single pass
+  int rows_per_pair, tiles_per_pair;
+  long long tiles;              // all pairs
+  int ctas, max_seg;
+  // two passes (hits, then misses)
+  int splits_h, splits_m;
+};
+
+struct SegArgs {
+  int pair, u, tok;
+  int ent_base;                 // first listed entry of the range
+  int rows;                     // rows of the range (entries * ET)
+  int ta, tb;                   // this CTA's tiles [ta, tb) of the range
 };
 
 // CTA c covers global tiles [c*T/C, (c+1)*T/C); the CTA holding tile x:
@@ -132,366 +147,465 @@ __device__ __forceinline__ int cta_of_tile(long long x, int C, long long T) {
   return (int)(((x + 1) * C - 1) / T);
 }
 
+// Zeroes the CTA's staging once: rows past the end of a partial tile then
+// always hold finite values (zeros or earlier rows), which P = 0 cancels.
 template <class SH>
-__global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcParams p) {
+__device__ __forceinline__ void tc_zero_staging(unsigned char* smem) {
+  for (int i = threadIdx.x; i < kWarpsTc * SH::WARP_BYTES / 16; i += kThreadsTc)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+}
+
+// One segment: this CTA's tiles [ta, tb) of one (unit, token) row range.
+// Every warp runs its own 3-stage pipeline over tiles ta + warp, ta + warp + 4,
+// ...; the four warps are then merged and the CTA's result is left in shared
+// memory: cm[h], cl[h] (max and sum of exp2 per head) and co[h * D + d]
+// (unnormalised output).  All threads of the CTA call it.
+template <class SH>
+__device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArgs& a,
+                           unsigned char* smem, float* cm, float* cl, float* co,
+                           float (*s_m)[SH::G], float (*s_l)[SH::G]) {
   constexpr int D = SH::D, G = SH::G, NTN = SH::NTN, KS = SH::KS, MT = SH::MT;
   constexpr int PITCH = SH::PITCH;
   constexpr int NH = G == 1 ? 1 : 2;              // heads per thread
   constexpr int OWNERS = G >= 2 ? G / 2 : 1;      // lanes c < OWNERS own their heads
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
-  __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G];
-  __shared__ int s_stop, s_last;
-
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
+  const int head_base = G == 1 ? 0 : 2 * (c % OWNERS);
+  const bool owner = c < OWNERS;
+  unsigned char* wbase = smem + warp * SH::WARP_BYTES;
+  unsigned char* ptile = wbase + kStages * SH::STAGE_BYTES;
+  const int pair = a.pair, u = a.u, tok = a.tok;
+
+  // q as MMA B fragments: column n < G is hi(q_n), G <= n < 2G is lo(q_{n-G}).
+  uint32_t qb[KS][NTN][2];
+  {
+    const float* qg = p.q + (size_t)pair * G * D;
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) {
+      const int col = g + 8 * nt;
+      const int head = col < G ? col : col - G;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint16_t e[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int d = 16 * ks + 2 * c + (i & 1) + 8 * (i >> 1);
+          uint16_t hi = 0, lo = 0;
+          if (col < 2 * G) split_bf16(__ldg(qg + head * D + d) * p.scale_log2, hi, lo);
+          e[i] = col < G ? hi : lo;
+        }
+        qb[ks][nt][0] = pack2(e[0], e[1]);
+        qb[ks][nt][1] = pack2(e[2], e[3]);
+      }
+    }
+  }
+
+  float m[NH], l[NH];
+  float acc[MT][NTN][4];
+#pragma unroll
+  for (int j = 0; j < NH; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+  }
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
+
+  const int n_my = a.tb - a.ta - warp > 0 ? (a.tb - a.ta - warp + kWarpsTc - 1) / kWarpsTc : 0;
+  // Buffer row of row (lane & 15) of this warp's i-th tile, or -1.
+  auto row_index = [&](int i) -> long long {
+    const int row = (a.ta + warp + i * kWarpsTc) * kTileRows + (lane & 15);
+    if (i >= n_my || row >= a.rows) return -1;
+    const int ent = a.ent_base + (p.ET == 1 ? row : row / p.ET);
+    const int sub = row - (ent - a.ent_base) * p.ET;
+    const int slot = p.identity ? tok * p.k + ent : __ldg(p.slots + (size_t)pair * p.k + ent);
+    return ((long long)u * s.B + slot) * p.ET + sub;
+  };
+  constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
+  constexpr int RPI = 32 / CPR;    // rows per warp instruction
+  auto issue = [&](long long myrow, int st) {
+    unsigned char* kst = wbase + st * SH::STAGE_BYTES;
+    unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
+    const int ch = lane % CPR, rsub = lane / CPR;
+#pragma unroll
+    for (int it = 0; it < kTileRows / RPI; ++it) {
+      const int r = it * RPI + rsub;
+      const long long srow = __shfl_sync(0xffffffffu, myrow, r);
+      if (srow >= 0) {
+        cp_async16(kst + r * PITCH + ch * 16, s.kbuf + srow * (2 * D) + ch * 16);
+        if (!SH::SHARED) cp_async16(vst + r * PITCH + ch * 16, s.vbuf + srow * (2 * D) + ch * 16);
+      }
+    }
+    cp_async_commit();  // one group per tile (empty past the end) keeps the count uniform
+  };
+
+  long long next_row;
+  {
+    long long first_rows[kStages + 1];  // slot loads issued together, then the copies
+#pragma unroll
+    for (int i = 0; i <= kStages; ++i) first_rows[i] = row_index(i);
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) issue(first_rows[i], i);
+    next_row = first_rows[kStages];
+  }
+  for (int i = 0; i < n_my; ++i) {
+    const int st = i % kStages;
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const int ti = a.ta + warp + i * kWarpsTc;
+    const int nrows = min(kTileRows, a.rows - ti * kTileRows);
+    const unsigned char* kst = wbase + st * SH::STAGE_BYTES;
+    const unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
+    const uint32_t kaddr = smem_u32(kst), vaddr = smem_u32(vst);
+
+    // scores^T (16 rows x 8 columns per n-tile), two chains: even and odd k-steps
+    float sc[NTN][4], sc2[NTN][4];
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+      for (int i2 = 0; i2 < 4; ++i2) sc[nt][i2] = sc2[nt][i2] = 0.f;
+    {
+      const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int acol = (lane >> 4) * 8;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kaddr + arow * PITCH + (16 * ks + acol) * 2, a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt)
+          mma_bf16((ks & 1) ? sc2[nt] : sc[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) sc[nt][i2] += sc2[nt][i2];
+    }
+    // hi + lo -> full scores sv[row half][head j] for rows g and g + 8
+    float sv[2][2];
+    if (G == 8) {
+      sv[0][0] = sc[0][0] + sc[NTN - 1][0];
+      sv[0][1] = sc[0][1] + sc[NTN - 1][1];
+      sv[1][0] = sc[0][2] + sc[NTN - 1][2];
+      sv[1][1] = sc[0][3] + sc[NTN - 1][3];
+    } else if (G == 1) {
+      sv[0][0] = sc[0][0] + sc[0][1];
+      sv[1][0] = sc[0][2] + sc[0][3];
+      sv[0][1] = sv[1][1] = -INFINITY;
+    } else {
+      const int xm = G / 2;  // lane distance from a hi column pair to its lo pair
+      sv[0][0] = sc[0][0] + __shfl_xor_sync(0xffffffffu, sc[0][0], xm);
+      sv[0][1] = sc[0][1] + __shfl_xor_sync(0xffffffffu, sc[0][1], xm);
+      sv[1][0] = sc[0][2] + __shfl_xor_sync(0xffffffffu, sc[0][2], xm);
+      sv[1][1] = sc[0][3] + __shfl_xor_sync(0xffffffffu, sc[0][3], xm);
+    }
+    if (g >= nrows) sv[0][0] = sv[0][1] = -INFINITY;
+    if (g + 8 >= nrows) sv[1][0] = sv[1][1] = -INFINITY;
+
+    // online softmax per head over the 16 rows (lanes with equal c)
+    float pv[2][2], alpha[2] = {1.f, 1.f};
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+      float mx = fmaxf(sv[0][j], sv[1][j]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m[j], mx);
+      float p0 = 0.f, p1 = 0.f;
+      if (m_new != -INFINITY) {
+        alpha[j] = exp2f(m[j] - m_new);
+        p0 = exp2f(sv[0][j] - m_new);
+        p1 = exp2f(sv[1][j] - m_new);
+      }
+      float sum = p0 + p1;
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+      l[j] = l[j] * alpha[j] + sum;
+      m[j] = m_new;
+      pv[0][j] = p0;
+      pv[1][j] = p1;
+    }
+    if (NH == 1) alpha[1] = alpha[0];
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+          acc[mt][nt][0] *= alpha[0];
+          acc[mt][nt][1] *= alpha[1];
+          acc[mt][nt][2] *= alpha[0];
+          acc[mt][nt][3] *= alpha[1];
+        }
+    }
+
+    // P^T tile in shared memory (rows x [hi columns | lo columns]) -> B fragments
+    if (owner) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rr = g + 8 * h;
+        uint16_t hi0, lo0, hi1 = 0, lo1 = 0;
+        split_bf16(pv[h][0], hi0, lo0);
+        if (NH == 2) split_bf16(pv[h][1], hi1, lo1);
+        if (G == 1) {
+          *reinterpret_cast<uint32_t*>(ptile + rr * 16) = pack2(hi0, lo0);
+        } else {
+          const int chi = head_base, clo = G + head_base;
+          *reinterpret_cast<uint32_t*>(ptile + (chi >> 3) * 256 + rr * 16 + (chi & 7) * 2) =
+              pack2(hi0, hi1);
+          *reinterpret_cast<uint32_t*>(ptile + (clo >> 3) * 256 + rr * 16 + (clo & 7) * 2) =
+              pack2(lo0, lo1);
+        }
+      }
+    }
+    __syncwarp();
+    uint32_t pb[NTN][2];
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt)
+      ldsm_x2_t(smem_u32(ptile + nt * 256 + (lane & 15) * 16), pb[nt][0], pb[nt][1]);
+
+    // O^T += V^T P^T
+    {
+      const int vrow = (lane & 7) + ((lane >> 4) << 3);
+      const int vcol = ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vaddr + vrow * PITCH + (16 * mt + vcol) * 2, a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) mma_bf16(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+      }
+    }
+    __syncwarp();  // every lane has read stage st
+    issue(next_row, st);
+    next_row = row_index(i + kStages + 1);
+  }
+  cp_async_wait<0>();
+
+  // Per-warp result -> shared memory, then merge the 4 warps.
+  __syncthreads();  // every warp is done with its staging (reused below)
+  float* mo = reinterpret_cast<float*>(smem);  // [warp][G][D]
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int dv = 16 * mt + g + 8 * (i >> 1);
+      float v;
+      int head;
+      if (G == 8) {
+        v = acc[mt][0][i] + acc[mt][NTN - 1][i];
+        head = 2 * c + (i & 1);
+      } else if (G == 1) {
+        v = (i & 1) ? 0.f : acc[mt][0][i] + acc[mt][0][i + 1];
+        head = 0;
+      } else {
+        v = acc[mt][0][i] + __shfl_xor_sync(0xffffffffu, acc[mt][0][i], G / 2);
+        head = head_base + (i & 1);
+      }
+      if (owner && (G != 1 || (i & 1) == 0)) mo[(warp * G + head) * D + dv] = v;
+    }
+  if (owner && g == 0) {
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+      s_m[warp][head_base + j] = m[j];
+      s_l[warp][head_base + j] = l[j];
+    }
+  }
+  __syncthreads();
+  if (tid < G) {
+    float M = -INFINITY, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarpsTc; ++w) M = fmaxf(M, s_m[w][tid]);
+    if (M != -INFINITY)
+#pragma unroll
+      for (int w = 0; w < kWarpsTc; ++w) L = fmaf(s_l[w][tid], exp2f(s_m[w][tid] - M), L);
+    cm[tid] = M;
+    cl[tid] = L;
+  }
+  __syncthreads();
+  for (int o = tid; o < G * D; o += kThreadsTc) {
+    const int head = o / D;
+    const float M = cm[head];
+    float O = 0.f;
+    if (M != -INFINITY)
+#pragma unroll
+      for (int w = 0; w < kWarpsTc; ++w) O = fmaf(mo[(w * G) * D + o], exp2f(s_m[w][head] - M), O);
+    co[o] = O;
+  }
+  __syncthreads();
+}
+
+// Writes this CTA's segment result as partial `idx` of a pair.
+template <int G, int D>
+__device__ __forceinline__ void tc_write_partial(float* pp, const float* cm, const float* cl,
+                                                 const float* co) {
+  for (int o = threadIdx.x; o < G * D; o += kThreadsTc) pp[2 * G + o] = co[o];
+  if (threadIdx.x < G) {
+    pp[threadIdx.x] = cm[threadIdx.x];
+    pp[G + threadIdx.x] = cl[threadIdx.x];
+  }
+}
+
+// Merges nseg partials of a pair into its output (run by one CTA).
+template <int G, int D>
+__device__ void tc_merge_partials(const float* pbase, int nseg, float* out, float* wseg) {
+  const size_t stride = (size_t)G * (D + 2);
+  const int tid = threadIdx.x;
+  if (tid < G) {  // weight of every partial per head, normalised
+    float M = -INFINITY, L = 0.f;
+    for (int q2 = 0; q2 < nseg; ++q2) M = fmaxf(M, __ldcg(pbase + q2 * stride + tid));
+    for (int q2 = 0; q2 < nseg; ++q2) {
+      const float e = M == -INFINITY ? 0.f : exp2f(__ldcg(pbase + q2 * stride + tid) - M);
+      wseg[q2 * G + tid] = e;
+      L = fmaf(__ldcg(pbase + q2 * stride + G + tid), e, L);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int q2 = 0; q2 < nseg; ++q2) wseg[q2 * G + tid] *= inv;
+  }
+  __syncthreads();
+  for (int o = tid; o < G * D; o += kThreadsTc) {
+    const int head = o / D;
+    float O = 0.f;
+#pragma unroll 8
+    for (int q2 = 0; q2 < nseg; ++q2)
+      O = fmaf(__ldcg(pbase + q2 * stride + 2 * G + o), wseg[q2 * G + head], O);
+    out[o] = O;
+  }
+}
+
+// Single pass, persistent: 2 CTAs per SM, each an equal share of all tiles.
+template <class SH>
+__global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcParams p) {
+  constexpr int D = SH::D, G = SH::G;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+  __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G], cm[G], cl[G];
+  __shared__ int s_stop, s_last;
+  const int tid = threadIdx.x;
   griddep_wait();
   griddep_launch();
   if (tid == 0) s_stop = load_err(s.err);
   __syncthreads();
   if (s_stop) return;
-
-  unsigned char* wbase = smem + warp * SH::WARP_BYTES;
-  unsigned char* ptile = wbase + kStages * SH::STAGE_BYTES;
-  // Zero the warp's staging once: rows past the end of a partial tile then
-  // always hold finite values (zeros or earlier rows), which P = 0 cancels.
-  for (int i = lane; i < SH::WARP_BYTES / 16; i += 32)
-    reinterpret_cast<uint4*>(wbase)[i] = make_uint4(0u, 0u, 0u, 0u);
-  __syncwarp();
-  const int head_base = G == 1 ? 0 : 2 * (c % OWNERS);
-  const bool owner = c < OWNERS;
+  tc_zero_staging<SH>(smem);
+  float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
 
   const long long T = p.tiles;
   const int C = p.ctas;
   const long long t_begin = (long long)blockIdx.x * T / C;
   const long long t_end = (long long)(blockIdx.x + 1) * T / C;
+  const size_t stride = (size_t)G * (D + 2);
   for (long long t = t_begin; t < t_end;) {
     const int pair = (int)(t / p.tiles_per_pair);
     const long long pair_t0 = (long long)pair * p.tiles_per_pair;
-    const int ta = (int)(t - pair_t0);
-    const int tb = (int)(min(t_end, pair_t0 + p.tiles_per_pair) - pair_t0);
-    t = pair_t0 + tb;
-    const int u = pair / p.n_tok, tok = pair - u * p.n_tok;
-
-    // q as MMA B fragments: column n < G is hi(q_n), G <= n < 2G is lo(q_{n-G}).
-    uint32_t qb[KS][NTN][2];
-    {
-      const float* qg = p.q + (size_t)pair * G * D;
-#pragma unroll
-      for (int nt = 0; nt < NTN; ++nt) {
-        const int col = g + 8 * nt;
-        const int head = col < G ? col : col - G;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint16_t e[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int d = 16 * ks + 2 * c + (i & 1) + 8 * (i >> 1);
-            uint16_t hi = 0, lo = 0;
-            if (col < 2 * G) split_bf16(__ldg(qg + head * D + d) * p.scale_log2, hi, lo);
-            e[i] = col < G ? hi : lo;
-          }
-          qb[ks][nt][0] = pack2(e[0], e[1]);
-          qb[ks][nt][1] = pack2(e[2], e[3]);
-        }
-      }
-    }
-
-    float m[NH], l[NH];
-    float acc[MT][NTN][4];
-#pragma unroll
-    for (int j = 0; j < NH; ++j) {
-      m[j] = -INFINITY;
-      l[j] = 0.f;
-    }
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NTN; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
-
-    // This warp's tiles of the segment: ta + warp, ta + warp + 4, ...
-    const int n_my = tb - ta - warp > 0 ? (tb - ta - warp + kWarpsTc - 1) / kWarpsTc : 0;
-    // Buffer row of row (lane & 15) of this warp's i-th tile, or -1.
-    auto row_index = [&](int i) -> long long {
-      const int row = (ta + warp + i * kWarpsTc) * kTileRows + (lane & 15);
-      if (i >= n_my || row >= p.rows_per_pair) return -1;
-      const int ent = p.ET == 1 ? row : row / p.ET;
-      const int sub = row - ent * p.ET;
-      const int slot = p.identity ? tok * p.k + ent : __ldg(p.slot_map + (size_t)pair * p.k + ent);
-      return ((long long)u * s.B + slot) * p.ET + sub;
-    };
-    long long next_row;
-    constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
-    constexpr int RPI = 32 / CPR;    // rows per warp instruction
-    auto issue = [&](long long myrow, int st) {
-      unsigned char* kst = wbase + st * SH::STAGE_BYTES;
-      unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
-      const int ch = lane % CPR, rsub = lane / CPR;
-#pragma unroll
-      for (int it = 0; it < kTileRows / RPI; ++it) {
-        const int r = it * RPI + rsub;
-        const long long srow = __shfl_sync(0xffffffffu, myrow, r);
-        if (srow >= 0) {
-          cp_async16(kst + r * PITCH + ch * 16, s.kbuf + srow * (2 * D) + ch * 16);
-          if (!SH::SHARED) cp_async16(vst + r * PITCH + ch * 16, s.vbuf + srow * (2 * D) + ch * 16);
-        }
-      }
-      cp_async_commit();  // one group per tile (empty past the end) keeps the count uniform
-    };
-
-    {
-      long long first_rows[kStages + 1];  // slot loads issued together, then the copies
-#pragma unroll
-      for (int i = 0; i <= kStages; ++i) first_rows[i] = row_index(i);
-#pragma unroll
-      for (int i = 0; i < kStages; ++i) issue(first_rows[i], i);
-      next_row = first_rows[kStages];
-    }
-    for (int i = 0; i < n_my; ++i) {
-      const int st = i % kStages;
-      cp_async_wait<kStages - 1>();
-      __syncwarp();
-      const int ti = ta + warp + i * kWarpsTc;
-      const int nrows = min(kTileRows, p.rows_per_pair - ti * kTileRows);
-      const unsigned char* kst = wbase + st * SH::STAGE_BYTES;
-      const unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
-      const uint32_t kaddr = smem_u32(kst), vaddr = smem_u32(vst);
-
-      // scores^T (16 rows x 8 columns per n-tile)
-      float sc[NTN][4], sc2[NTN][4];  // two chains: even and odd k-steps
-#pragma unroll
-      for (int nt = 0; nt < NTN; ++nt)
-#pragma unroll
-        for (int i2 = 0; i2 < 4; ++i2) sc[nt][i2] = sc2[nt][i2] = 0.f;
-      {
-        const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int acol = (lane >> 4) * 8;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(kaddr + arow * PITCH + (16 * ks + acol) * 2, a0, a1, a2, a3);
-#pragma unroll
-          for (int nt = 0; nt < NTN; ++nt)
-            mma_bf16((ks & 1) ? sc2[nt] : sc[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < NTN; ++nt)
-#pragma unroll
-          for (int i2 = 0; i2 < 4; ++i2) sc[nt][i2] += sc2[nt][i2];
-      }
-      // hi + lo -> full scores sv[row half][head j] for rows g and g + 8
-      float sv[2][2];
-      if (G == 8) {
-        sv[0][0] = sc[0][0] + sc[NTN - 1][0];
-        sv[0][1] = sc[0][1] + sc[NTN - 1][1];
-        sv[1][0] = sc[0][2] + sc[NTN - 1][2];
-        sv[1][1] = sc[0][3] + sc[NTN - 1][3];
-      } else if (G == 1) {
-        sv[0][0] = sc[0][0] + sc[0][1];
-        sv[1][0] = sc[0][2] + sc[0][3];
-        sv[0][1] = sv[1][1] = -INFINITY;
-      } else {
-        const int xm = G / 2;  // lane distance from a hi column pair to its lo pair
-        sv[0][0] = sc[0][0] + __shfl_xor_sync(0xffffffffu, sc[0][0], xm);
-        sv[0][1] = sc[0][1] + __shfl_xor_sync(0xffffffffu, sc[0][1], xm);
-        sv[1][0] = sc[0][2] + __shfl_xor_sync(0xffffffffu, sc[0][2], xm);
-        sv[1][1] = sc[0][3] + __shfl_xor_sync(0xffffffffu, sc[0][3], xm);
-      }
-      if (g >= nrows) sv[0][0] = sv[0][1] = -INFINITY;
-      if (g + 8 >= nrows) sv[1][0] = sv[1][1] = -INFINITY;
-
-      // online softmax per head over the 16 rows (lanes with equal c)
-      float pv[2][2], alpha[2] = {1.f, 1.f};
-#pragma unroll
-      for (int j = 0; j < NH; ++j) {
-        float mx = fmaxf(sv[0][j], sv[1][j]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m[j], mx);
-        float p0 = 0.f, p1 = 0.f;
-        if (m_new != -INFINITY) {
-          alpha[j] = exp2f(m[j] - m_new);
-          p0 = exp2f(sv[0][j] - m_new);
-          p1 = exp2f(sv[1][j] - m_new);
-        }
-        float sum = p0 + p1;
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-        l[j] = l[j] * alpha[j] + sum;
-        m[j] = m_new;
-        pv[0][j] = p0;
-        pv[1][j] = p1;
-      }
-      if (NH == 1) alpha[1] = alpha[0];
-      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < NTN; ++nt) {
-            acc[mt][nt][0] *= alpha[0];
-            acc[mt][nt][1] *= alpha[1];
-            acc[mt][nt][2] *= alpha[0];
-            acc[mt][nt][3] *= alpha[1];
-          }
-      }
-
-      // P^T tile in shared memory (rows x [hi columns | lo columns]) -> B fragments
-      if (owner) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int rr = g + 8 * h;
-          uint16_t hi0, lo0, hi1 = 0, lo1 = 0;
-          split_bf16(pv[h][0], hi0, lo0);
-          if (NH == 2) split_bf16(pv[h][1], hi1, lo1);
-          if (G == 1) {
-            *reinterpret_cast<uint32_t*>(ptile + rr * 16) = pack2(hi0, lo0);
-          } else {
-            const int chi = head_base, clo = G + head_base;
-            *reinterpret_cast<uint32_t*>(ptile + (chi >> 3) * 256 + rr * 16 + (chi & 7) * 2) =
-                pack2(hi0, hi1);
-            *reinterpret_cast<uint32_t*>(ptile + (clo >> 3) * 256 + rr * 16 + (clo & 7) * 2) =
-                pack2(lo0, lo1);
-          }
-        }
-      }
-      __syncwarp();
-      uint32_t pb[NTN][2];
-#pragma unroll
-      for (int nt = 0; nt < NTN; ++nt)
-        ldsm_x2_t(smem_u32(ptile + nt * 256 + (lane & 15) * 16), pb[nt][0], pb[nt][1]);
-
-      // O^T += V^T P^T
-      {
-        const int vrow = (lane & 7) + ((lane >> 4) << 3);
-        const int vcol = ((lane >> 3) & 1) * 8;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vaddr + vrow * PITCH + (16 * mt + vcol) * 2, a0, a1, a2, a3);
-#pragma unroll
-          for (int nt = 0; nt < NTN; ++nt) mma_bf16(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
-        }
-      }
-      __syncwarp();  // every lane has read stage st
-      issue(next_row, st);
-      next_row = row_index(i + kStages + 1);
-    }
-    cp_async_wait<0>();
-
-    // Per-warp result -> shared memory, then merge the 4 warps.
-    __syncthreads();  // every warp is done with its staging (reused below)
-    float* mo = reinterpret_cast<float*>(smem);  // [warp][G][D]
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int dv = 16 * mt + g + 8 * (i >> 1);
-        float v;
-        int head;
-        if (G == 8) {
-          v = acc[mt][0][i] + acc[mt][NTN - 1][i];
-          head = 2 * c + (i & 1);
-        } else if (G == 1) {
-          v = (i & 1) ? 0.f : acc[mt][0][i] + acc[mt][0][i + 1];
-          head = 0;
-        } else {
-          v = acc[mt][0][i] + __shfl_xor_sync(0xffffffffu, acc[mt][0][i], G / 2);
-          head = head_base + (i & 1);
-        }
-        if (owner && (G != 1 || (i & 1) == 0)) mo[(warp * G + head) * D + dv] = v;
-      }
-    if (owner && g == 0) {
-#pragma unroll
-      for (int j = 0; j < NH; ++j) {
-        s_m[warp][head_base + j] = m[j];
-        s_l[warp][head_base + j] = l[j];
-      }
-    }
-    __syncthreads();
+    SegArgs a;
+    a.pair = pair;
+    a.u = pair / p.n_tok;
+    a.tok = pair - a.u * p.n_tok;
+    a.ent_base = 0;
+    a.rows = p.rows_per_pair;
+    a.ta = (int)(t - pair_t0);
+    a.tb = (int)(min(t_end, pair_t0 + p.tiles_per_pair) - pair_t0);
+    t = pair_t0 + a.tb;
+    tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
 
     const int first = cta_of_tile(pair_t0, C, T);
     const int last = cta_of_tile(pair_t0 + p.tiles_per_pair - 1, C, T);
     const int nseg = last - first + 1;
     float* out = p.out + (size_t)pair * G * D;
-    const size_t stride = (size_t)G * (D + 2);
-    float* pbase = s.part + (size_t)pair * p.max_seg * stride;
-    float* pp = pbase + (size_t)(blockIdx.x - first) * stride;
-    for (int o = tid; o < G * D; o += kThreadsTc) {
-      const int head = o / D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarpsTc; ++w) M = fmaxf(M, s_m[w][head]);
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarpsTc; ++w) {
-          const float e = exp2f(s_m[w][head] - M);
-          L = fmaf(s_l[w][head], e, L);
-          O = fmaf(mo[(w * G) * D + o], e, O);
-        }
+    if (nseg == 1) {
+      for (int o = tid; o < G * D; o += kThreadsTc) {
+        const float L = cl[o / D];
+        out[o] = L > 0.f ? co[o] / L : 0.f;
       }
-      if (nseg == 1) {
-        out[o] = L > 0.f ? O / L : 0.f;
-      } else {
-        pp[2 * G + o] = O;
-        if (o % D == 0) {
-          pp[head] = M;
-          pp[G + head] = L;
-        }
-      }
-    }
-    if (nseg > 1) {
+    } else {
+      float* pbase = s.part + (size_t)pair * p.max_seg * stride;
+      tc_write_partial<G, D>(pbase + (size_t)(blockIdx.x - first) * stride, cm, cl, co);
       __threadfence();
       __syncthreads();
-      if (tid == 0) {
-        const int prev = atomicAdd(&s.part_count[u * kMaxTokens + tok], 1);
-        s_last = prev == nseg - 1;
-      }
+      if (tid == 0) s_last = atomicAdd(&s.part_count[a.u * kMaxTokens + a.tok], 1) == nseg - 1;
       __syncthreads();
       if (s_last) {
         __threadfence();
-        // Weight of each segment per head, once, in shared memory (the
-        // staging area is free here); then every output is a sum of
-        // independent loads.
-        float* wseg = reinterpret_cast<float*>(smem);  // [nseg][G]
-        if (tid < G) {
-          float M = -INFINITY, L = 0.f;
-          for (int q2 = 0; q2 < nseg; ++q2) M = fmaxf(M, __ldcg(pbase + q2 * stride + tid));
-          for (int q2 = 0; q2 < nseg; ++q2) {
-            const float e = M == -INFINITY ? 0.f : exp2f(__ldcg(pbase + q2 * stride + tid) - M);
-            wseg[q2 * G + tid] = e;
-            L = fmaf(__ldcg(pbase + q2 * stride + G + tid), e, L);
-          }
-          const float inv = L > 0.f ? 1.f / L : 0.f;
-          for (int q2 = 0; q2 < nseg; ++q2) wseg[q2 * G + tid] *= inv;
-        }
-        __syncthreads();
-        for (int o = tid; o < G * D; o += kThreadsTc) {
-          const int head = o / D;
-          float O = 0.f;
-#pragma unroll 8
-          for (int q2 = 0; q2 < nseg; ++q2)
-            O = fmaf(__ldcg(pbase + q2 * stride + 2 * G + o), wseg[q2 * G + head], O);
-          out[o] = O;
-        }
-        if (tid == 0) s.part_count[u * kMaxTokens + tok] = 0;
+        tc_merge_partials<G, D>(pbase, nseg, out, co + G * D);
+        if (tid == 0) s.part_count[a.u * kMaxTokens + a.tok] = 0;
       }
     }
     __syncthreads();  // the merge area is staging again for the next segment
   }
 }
 
+// Two passes over the hit-first slot lists: pass 0 over each (unit, token)'s
+// hit rows (it may run while the misses are still being copied in), pass 1
+// over its miss rows; the last pass-1 CTA of a pair merges both passes.
 template <class SH>
-cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaStream_t st) {
-  static int smem_done = 0;
-  TcParams p;
+__global__ void __launch_bounds__(kThreadsTc) attn_tc_pass_kernel(DeviceState s, TcParams p,
+                                                                  int pass) {
+  constexpr int D = SH::D, G = SH::G;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+  __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G], cm[G], cl[G];
+  __shared__ int s_stop, s_last;
+  const int tid = threadIdx.x;
+  griddep_wait();
+  griddep_launch();
+  if (tid == 0) s_stop = load_err(s.err);
+  __syncthreads();
+  if (s_stop) return;
+  tc_zero_staging<SH>(smem);
+  float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
+
+  const int sp = blockIdx.x, pair = blockIdx.y;
+  SegArgs a;
+  a.pair = pair;
+  a.u = pair / p.n_tok;
+  a.tok = pair - a.u * p.n_tok;
+  const int nh = s.nhit[a.u * kMaxTokens + a.tok];
+  a.ent_base = pass ? nh : 0;
+  a.rows = (pass ? p.k - nh : nh) * p.ET;
+  const int tiles = (a.rows + kTileRows - 1) / kTileRows;
+  const int S = pass ? p.splits_m : p.splits_h;
+  a.ta = (int)((long long)sp * tiles / S);
+  a.tb = (int)((long long)(sp + 1) * tiles / S);
+  tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
+
+  const int nseg = p.splits_h + p.splits_m;
+  const size_t stride = (size_t)G * (D + 2);
+  float* pbase = s.part + (size_t)pair * nseg * stride;
+  tc_write_partial<G, D>(pbase + (size_t)(pass ? p.splits_h + sp : sp) * stride, cm, cl, co);
+  if (!pass) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&s.part_count[a.u * kMaxTokens + a.tok], 1) == p.splits_m - 1;
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    tc_merge_partials<G, D>(pbase, nseg, p.out + (size_t)pair * G * D, co + G * D);
+    if (tid == 0) s.part_count[a.u * kMaxTokens + a.tok] = 0;
+  }
+}
+
+template <class SH>
+TcParams tc_params(const DeviceState& s, const AttnLaunch& a) {
+  TcParams p{};
   p.n_tok = a.n_tok;
   p.k = a.k;
   p.ET = s.ET;
+  p.identity = a.identity_slots;
+  p.scale_log2 = a.scale_log2;
+  p.q = a.q;
+  p.out = a.out;
+  return p;
+}
+
+template <class SH>
+cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaStream_t st) {
+  static int smem_done = 0;
+  TcParams p = tc_params<SH>(s, a);
+  p.slots = a.slot_map;
   p.rows_per_pair = a.k * s.ET;
   p.tiles_per_pair = (p.rows_per_pair + kTileRows - 1) / kTileRows;
   const long long pairs = (long long)s.U * a.n_tok;
@@ -502,18 +616,28 @@ cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaS
   for (;;) {
     const long long per = p.tiles / C;  // fewest tiles a CTA gets
     p.max_seg = (int)((p.tiles_per_pair + per - 1) / per + 1);
-    if ((size_t)pairs * p.max_seg * stride <= (size_t)a.part_capacity || C == 1) break;
+    if ((size_t)pairs * p.max_seg * stride <= a.part_capacity || C == 1) break;
     C = C * 3 / 4 > 0 ? C * 3 / 4 : 1;
   }
   p.ctas = (int)C;
-  p.identity = a.identity_slots;
-  p.scale_log2 = a.scale_log2;
-  p.q = a.q;
-  p.out = a.out;
-  p.slot_map = a.slot_map;
   cudaError_t e = ensure_smem((const void*)attn_tc_kernel<SH>, SH::SMEM, &smem_done);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_tc_kernel<SH>, dim3(p.ctas), dim3(kThreadsTc), SH::SMEM, st, s, p);
+}
+
+template <class SH>
+cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int splits_h,
+                        int splits_m, cudaStream_t st) {
+  static int smem_done = 0;
+  TcParams p = tc_params<SH>(s, a);
+  p.slots = s.order;
+  p.identity = 0;
+  p.splits_h = splits_h;
+  p.splits_m = splits_m;
+  cudaError_t e = ensure_smem((const void*)attn_tc_pass_kernel<SH>, SH::SMEM, &smem_done);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)(pass ? splits_m : splits_h), (unsigned)(s.U * a.n_tok));
+  return launch_pdl(attn_tc_pass_kernel<SH>, grid, dim3(kThreadsTc), SH::SMEM, st, s, p, pass);
 }
 
 }  // namespace
@@ -527,6 +651,19 @@ size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sm
   // pairs * max_seg <= T / floor(T / C) + 2 * pairs <= 2 * C + 2 * pairs (see run_tc)
   const size_t pairs = (size_t)U * max_tokens;
   return (2 * (size_t)num_sms * kCtasPerSm + 2 * pairs) * (size_t)G * (DV + 2);
+}
+
+cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
+                                     int splits_h, int splits_m, cudaStream_t st) {
+#define X(d, g, sh)                                                         \
+  if (s.D == d && s.G == g && (s.kv_shared != 0) == sh)                     \
+    return run_tc_pass<TcShape<d, g, sh>>(s, a, pass, splits_h, splits_m, st);
+  X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
+  X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
+  X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)
+  X(64, 1, true) X(64, 2, true) X(64, 4, true) X(64, 8, true)
+#undef X
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attention_tc(const DeviceState& s, const AttnLaunch& a, int num_sms,

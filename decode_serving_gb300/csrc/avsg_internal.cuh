@@ -25,9 +25,10 @@ struct DevCounters {
   unsigned long long hits, misses;
 };
 
-// One miss to copy: host row `id` of `unit` into buffer slot `slot`.
+// One miss to copy: host row `id` of `unit` into buffer slot `slot`, which
+// held `old_id` (kEmpty if none) before this step.
 struct GatherDesc {
-  int32_t unit, id, slot, pad;
+  int32_t unit, id, slot, old_id;
 };
 
 // Everything a kernel needs about a handle: sizes and device pointers.
@@ -54,6 +55,10 @@ struct DeviceState {
   int32_t* mcount;                 // [U] distinct misses this step
   GatherDesc* desc;                // [U * max_union]
   int32_t* desc_count;             // [1]
+  int32_t* dbase;                  // [U] first descriptor of the unit this step
+  int32_t* dcount;                 // [U] descriptors of the unit this step
+  int32_t* order;                  // [U][n_tok][k] selected slots, hits first
+  int32_t* nhit;                   // [U][kMaxTokens] entries that were hits, per token
   float* part;                     // split-K partials
   int32_t* part_count;             // [U][max_tokens] arrival counters, 0 between steps
   DevCounters* counters;           // [U] distinct hits / misses, summed over steps
@@ -113,7 +118,11 @@ cudaError_t launch_match(const DeviceState& s, int t, int n_tok, int k, const in
                          int32_t* slot_map, uint8_t* hit, cudaStream_t st);
 size_t victims_smem_bytes(const DeviceState& s);
 cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_t* slot_map,
-                           cudaStream_t st);
+                           int hits_first, cudaStream_t st);
+// Hash-table update of a step (erase evicted ids, insert new ones, rebuild):
+// needed only by the next step's match, so it may run beside the gather and
+// the attention.
+cudaError_t launch_commit(const DeviceState& s, cudaStream_t st);
 cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
 cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,
                               int32_t* slot_map, uint8_t* hit, int ctas, cudaStream_t st);
@@ -136,6 +145,9 @@ bool attention_tc_supported(int D, int DV, int G, int kv_shared);
 size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sms);
 cudaError_t launch_attention_tc(const DeviceState& s, const AttnLaunch& a, int num_sms,
                                 cudaStream_t st);
+// pass 0: hit rows of every (unit, token); pass 1: miss rows, then the merge.
+cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
+                                     int splits_h, int splits_m, cudaStream_t st);
 bool attention_tc_enabled();
 
 }  // namespace avsg

@@ -1,5 +1,8 @@
 // avsg_victims: reserve buffer slots for the step's missing ids and commit.
 //
+// (The hash-table update of the step, commit_kernel below, runs separately:
+// only the next step's match needs it.)
+//
 // Retention policy: bucketed LRU (Spin page, "Unifying Sparse Attention with
 // Hierarchical Memory for Scalable Long-Context LLM Serving", section 2B:
 // recency buckets, about 64, no global sort, eviction decided in parallel on
@@ -104,9 +107,10 @@ __host__ __device__ inline VictimsSmem victims_layout(int max_union, int B) {
 constexpr int kBatch = 8;  // 32-slot chunks whose state one warp loads before using it
 
 __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int t, int n_tok,
-                                                              int k, int32_t* __restrict__ slot_map) {
+                                                              int k, int32_t* __restrict__ slot_map,
+                                                              int hits_first) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int s_stop, s_base, s_used, s_rebuild, s_live, s_hits;
+  __shared__ int s_stop, s_base, s_hits, s_run[2];
   __shared__ int wsum[kWarps];
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -121,8 +125,6 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   griddep_launch();
   if (tid == 0) {
     s_stop = load_err(s.err);
-    s_used = 0;
-    s_live = 0;
     s_hits = 0;
   }
   __syncthreads();
@@ -256,51 +258,126 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   if (tid == 0) s_base = m > 0 ? atomicAdd(s.desc_count, m) : 0;
   __syncthreads();
 
-  // 5. Commit: erase evicted ids, then insert the new ones.
-  int2* tab = s.htab + (size_t)u * s.HS;
-  const uint32_t hmask = (uint32_t)s.HS - 1u;
-  for (int i = tid; i < m; i += kThreads) {
-    const int32_t old = s.tag[ub + victim[i]];
-    if (old != kEmpty) hash_erase(tab, hmask, s.hs_shift, old);
-  }
-  __syncthreads();
-  int used = 0;
+  // 5. Reserve: new tags and last_step, gather descriptors (with the evicted
+  //    id, for the hash-table update that runs later), miss-set cells freed.
   for (int i = tid; i < m; i += kThreads) {
     const unsigned long long key = keys[i];
     const int32_t id = (int32_t)(key >> 32);
     const int cell = (int)(uint32_t)key;
     const int r = rank[i];
     const int v = victim[r];
-    used += hash_insert(tab, hmask, s.hs_shift, id, v, s.err, u);
+    const int32_t old = s.tag[ub + v];
     s.tag[ub + v] = id;
     s.last[ub + v] = t;
     s.mslot[(size_t)u * s.MS + cell] = v;
     ms[cell] = kMissEmpty;
-    s.desc[s_base + r] = GatherDesc{u, id, v, 0};
+    s.desc[s_base + r] = GatherDesc{u, id, v, old};
+  }
+  __syncthreads();
+
+  // 6. Resolve slot-map entries of misses (-2 - cell -> reserved slot); with
+  //    hits_first, also list each token's slots hits first (misses from the
+  //    back) and count its hits.
+  const int n = n_tok * k;
+  if (!hits_first) {
+    for (int p = tid; p < n; p += kThreads) {
+      const size_t off = (size_t)u * n + p;
+      const int sm = slot_map[off];
+      if (sm <= -2) slot_map[off] = s.mslot[(size_t)u * s.MS + (-2 - sm)];
+    }
+  } else {
+    for (int j = 0; j < n_tok; ++j) {
+      if (tid == 0) s_run[0] = s_run[1] = 0;
+      __syncthreads();
+      const size_t row0 = (size_t)u * n + (size_t)j * k;
+      for (int c0 = 0; c0 < k; c0 += kThreads) {
+        const int p = c0 + tid;
+        int sm = 0;
+        bool is_hit = false;
+        if (p < k) {
+          sm = slot_map[row0 + p];
+          is_hit = sm >= 0;
+          if (!is_hit) {
+            sm = s.mslot[(size_t)u * s.MS + (-2 - sm)];
+            slot_map[row0 + p] = sm;
+          }
+        }
+        const unsigned hb = __ballot_sync(0xffffffffu, p < k && is_hit);
+        const unsigned mb = __ballot_sync(0xffffffffu, p < k && !is_hit);
+        if (lane == 0) wsum[warp] = (__popc(hb) << 16) | __popc(mb);
+        __syncthreads();
+        int before = 0;  // packed (hits << 16 | misses) of lower warps in this chunk
+        for (int w2 = 0; w2 < warp; ++w2) before += wsum[w2];
+        const int run_h = s_run[0], run_m = s_run[1];
+        const unsigned lt = (1u << lane) - 1u;
+        if (p < k) {
+          const int idx = is_hit ? run_h + (before >> 16) + __popc(hb & lt)
+                                 : k - 1 - (run_m + (before & 0xFFFF) + __popc(mb & lt));
+          s.order[row0 + idx] = sm;
+        }
+        __syncthreads();
+        if (tid == kThreads - 1) {
+          const int tot = before + wsum[warp];
+          s_run[0] = run_h + (tot >> 16);
+          s_run[1] = run_m + (tot & 0xFFFF);
+        }
+        __syncthreads();
+      }
+      if (tid == 0) s.nhit[u * kMaxTokens + j] = s_run[0];
+      __syncthreads();
+    }
+  }
+
+  // 7. Statistics and this step's descriptor range (for the table update).
+  if (tid == 0) {
+    s.mcount[u] = 0;
+    s.dbase[u] = s_base;
+    s.dcount[u] = m;
+    s.counters[u].hits += (unsigned long long)s_hits;
+    s.counters[u].misses += (unsigned long long)m;
+  }
+}
+
+// Hash-table update of one unit: erase the ids this step evicted, insert the
+// ids it loaded, rebuild from the tags when erased cells pile up.
+__global__ void __launch_bounds__(kThreads, 1) commit_kernel(DeviceState s) {
+  __shared__ int s_stop, s_used, s_rebuild, s_live;
+  const int u = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  griddep_wait();
+  griddep_launch();
+  if (tid == 0) {
+    s_stop = load_err(s.err);
+    s_used = 0;
+    s_live = 0;
+  }
+  __syncthreads();
+  if (s_stop) return;
+  const int m = s.dcount[u], base = s.dbase[u];
+  int2* tab = s.htab + (size_t)u * s.HS;
+  const uint32_t hmask = (uint32_t)s.HS - 1u;
+  for (int i = tid; i < m; i += kThreads) {
+    const int32_t old = s.desc[base + i].old_id;
+    if (old != kEmpty) hash_erase(tab, hmask, s.hs_shift, old);
+  }
+  __syncthreads();
+  int used = 0;
+  for (int i = tid; i < m; i += kThreads) {
+    const GatherDesc d = s.desc[base + i];
+    used += hash_insert(tab, hmask, s.hs_shift, d.id, d.slot, s.err, u);
   }
   used = __reduce_add_sync(0xffffffffu, used);
   if (lane == 0 && used) atomicAdd(&s_used, used);
   __syncthreads();
-
-  // 6. Resolve slot-map entries of misses (-2 - cell -> reserved slot).
-  const int n = n_tok * k;
-  for (int p = tid; p < n; p += kThreads) {
-    const size_t off = (size_t)u * n + p;
-    const int sm = slot_map[off];
-    if (sm <= -2) slot_map[off] = s.mslot[(size_t)u * s.MS + (-2 - sm)];
-  }
-
-  // 7. Statistics, and a rebuild of the table when erased cells pile up.
   if (tid == 0) {
     const int total = s.hused[u] + s_used;
     s_rebuild = total > s.HS / 2;
     s.hused[u] = total;
-    s.mcount[u] = 0;
-    s.counters[u].hits += (unsigned long long)s_hits;
-    s.counters[u].misses += (unsigned long long)m;
   }
   __syncthreads();
   if (s_rebuild) {
+    const int B = s.B;
+    const size_t ub = (size_t)u * B;
     for (int i = tid; i < s.HS; i += kThreads) tab[i] = make_int2(kEmpty, kEmpty);
     __syncthreads();
     int live = 0;
@@ -325,11 +402,19 @@ int g_victims_smem = 0;
 size_t victims_smem_bytes(const DeviceState& s) { return victims_layout(s.max_union, s.B).total; }
 
 cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_t* slot_map,
-                           cudaStream_t st) {
+                           int hits_first, cudaStream_t st) {
   const size_t smem = victims_smem_bytes(s);
   cudaError_t e = ensure_smem((const void*)victims_kernel, smem, &g_victims_smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(victims_kernel, dim3(s.U), dim3(kThreads), smem, st, s, t, n_tok, k, slot_map);
+  return launch_pdl(victims_kernel, dim3(s.U), dim3(kThreads), smem, st, s, t, n_tok, k, slot_map,
+                    hits_first);
+}
+
+cudaError_t launch_commit(const DeviceState& s, cudaStream_t st) {
+  static int attr_done = 0;
+  const cudaError_t e = ensure_smem((const void*)commit_kernel, 0, &attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(commit_kernel, dim3(s.U), dim3(kThreads), 0, st, s);
 }
 
 }  // namespace avsg

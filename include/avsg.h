@@ -16,6 +16,11 @@
  * Multi-token prediction: with n_tok > 1 query tokens per step, one shared
  * reservation covers the union of the tokens' selections (same abstract).
  *
+ * Within a step the copy of the misses (bound by the host link) overlaps the
+ * attention over the selected rows that were already resident: the library
+ * runs the gather and the hash-table update on an internal stream, forked
+ * from and joined back into the caller's stream with events.
+ *
  * Reservation order (the pages give no formula; this is the reading the
  * library implements): empty slots first, by ascending slot index; then the
  * slots not selected in this step, by bucket min(63, t - last_step) from 63
@@ -106,12 +111,20 @@ typedef struct avsg_info {
 
 /*
  * Per-kernel device time (ms), accumulated over the steps enqueued while
- * profiling was on (CUDA events on the caller's stream between kernels).
- * Index: 0 match, 1 reservation, 2 gather, 3 attention.  launches[i] counts them.
+ * profiling was on: CUDA events recorded just before and after each kernel on
+ * the stream it runs on (the events themselves keep consecutive kernels from
+ * overlapping their launches).  launches[i] counts the timed launches.
  */
+#define AVSG_KERNEL_MATCH 0
+#define AVSG_KERNEL_RESERVE 1
+#define AVSG_KERNEL_GATHER 2
+#define AVSG_KERNEL_ATTENTION 3      /* single pass, or the pass over hit rows */
+#define AVSG_KERNEL_ATTENTION_MISS 4 /* pass over miss rows and the merge */
+#define AVSG_KERNEL_COMMIT 5         /* hash-table update */
+#define AVSG_NUM_KERNELS 6
 typedef struct avsg_kernel_times {
-  double ms[4];
-  uint64_t launches[4];
+  double ms[AVSG_NUM_KERNELS];
+  uint64_t launches[AVSG_NUM_KERNELS];
 } avsg_kernel_times;
 
 /*
