@@ -496,7 +496,7 @@ def report_ours(args, res, world, max_ms, max_e2e_ms) -> dict:
         "kernel_timing": ("second pass over the same steps with library CUDA events between "
                           "kernels (defeats launch overlap); that pass's ms_per_step: "
                           f"{res['ms_per_step_profiled']:.4f}"),
-        "gpu_launches": res["launches_per_step"] * K,
+        "gpu_launches": int(round(res["launches_per_step"] * K)),
         "clocks": res["clocks"],
     }
     if max_e2e_ms is not None:
