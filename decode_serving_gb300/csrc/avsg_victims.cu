@@ -1,7 +1,4 @@
-// avsg_victims: reserve buffer slots for the step's missing ids and commit.
-//
-// (The hash-table update of the step, commit_kernel below, runs separately:
-// only the next step's match needs it.)
+// avsg_victims: reserve buffer slots for the step's missing ids.
 //
 // Retention policy: bucketed LRU (Spin page, "Unifying Sparse Attention with
 // Hierarchical Memory for Scalable Long-Context LLM Serving", section 2B:
@@ -14,14 +11,18 @@
 //   order 64 - b : occupied, not selected this step, bucket b = min(63, t - last);
 //   excluded     : selected this step (a hit; its last_step becomes t).
 // A slot's rank is the number of candidates in lower orders plus the number
-// of lower-indexed slots in its own order, computed with a per-warp order
-// histogram (warp w owns a contiguous slot range), one exclusive scan over
-// (order, warp), and __match_any_sync within each 32-slot chunk -- no sort of
-// the slots.  The m distinct missing ids are sorted ascending (bitonic sort in
-// shared memory); the i-th takes the slot of rank i.  Then, per miss: erase the
-// evicted id from the hash table, insert the new one, set tag and last_step,
-// append a gather descriptor, and resolve the slot map entries that pointed at
-// the miss-set cell.  The miss set is emptied for the next step.
+// of lower-indexed slots in its own order: a per-warp order histogram (warp w
+// owns a contiguous slot range), one exclusive scan over (order, warp), and,
+// only for the orders that can hold one of the m victims, an in-order ballot
+// count within each 32-slot chunk -- no sort of the slots.  The m distinct
+// missing ids are ranked in ascending id order (counting, or a bitonic sort
+// for very many); the i-th takes the slot of rank i: its tag and last_step are
+// set, a gather descriptor (with the evicted id) is appended, the slot map
+// entries that pointed at its miss-set cell are resolved, and, for the
+// two-pass attention, each token's slots are listed hits first.
+//
+// The hash-table update of the step (commit_kernel below) runs separately:
+// only the next step's match needs it.
 #include "avsg_internal.cuh"
 
 namespace avsg {
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
                                                               int k, int32_t* __restrict__ slot_map,
                                                               int hits_first) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int s_stop, s_base, s_hits, s_run[2];
+  __shared__ int s_stop, s_base, s_hits, s_omax, s_tot;
   __shared__ int wsum[kWarps];
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -183,8 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     for (int i = tid; i < m; i += kThreads) rank[i] = i;
   }
 
-  // 2. Reservation order of every slot; per-warp histogram over orders.  Each
-  //    warp owns a contiguous range and loads kBatch chunks of state at once.
+  // 2. Reservation order of every slot; per-warp histogram over orders (each
+  //    warp owns a contiguous slot range and a private row of counters, so
+  //    plain shared-memory atomics need no ordering).
   const int chunk = ((B + kWarps * 32 - 1) / (kWarps * 32)) * 32;  // slots per warp
   const int w_begin = warp * chunk, w_end = min(B, w_begin + chunk);
   int hits = 0;
@@ -200,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
-      if (base + b * 32 >= w_begin + chunk) break;  // warp-uniform
       const int sl = base + b * 32 + lane;
+      if (sl >= w_end || base + b * 32 >= w_begin + chunk) continue;
       int o = kNotCandidate;
       if (sn[b] > 0) {
         s.last[ub + sl] = t;  // selected this step: refreshed, never a victim
@@ -214,11 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
           const int age = max(1, t - ls[b]);
           o = kOrders - min(kOrders - 1, age);
         }
+        atomicAdd(&wstart[o * kWarps + warp], 1);
       }
-      if (sl < w_end) ord[sl] = (uint8_t)o;
-      const unsigned peers = __match_any_sync(0xffffffffu, o);
-      if (o != kNotCandidate && lane == __ffs(peers) - 1) wstart[o * kWarps + warp] += __popc(peers);
-      __syncwarp();
+      ord[sl] = (uint8_t)o;
     }
   }
   hits = __reduce_add_sync(0xffffffffu, hits);
@@ -226,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   __syncthreads();
 
   // 3. Exclusive scan of wstart in (order, warp) order: 2 values per thread.
+  //    The last order whose start is below m bounds the orders that can hold
+  //    a victim (o_max).
   {
     const int a = wstart[2 * tid], b = wstart[2 * tid + 1];
     const int incl = warp_incl_scan(a + b, lane);
@@ -240,20 +242,35 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     wstart[2 * tid] = excl;
     wstart[2 * tid + 1] = excl + a;
   }
+  if (tid == 0) s_omax = -1;
   __syncthreads();
+  if (tid < kOrders && wstart[tid * kWarps] < m) atomicMax(&s_omax, tid);
+  __syncthreads();
+  const int o_max = s_omax;
 
-  // 4. Rank within order by slot index; the first m ranks are the victims.
-  for (int base = w_begin; base < w_begin + chunk; base += 32) {
-    const int sl = base + lane;
-    const int o = sl < w_end ? (int)ord[sl] : kNotCandidate;
-    const unsigned peers = __match_any_sync(0xffffffffu, o);
-    if (o != kNotCandidate) {
-      const int r = wstart[o * kWarps + warp] + __popc(peers & ((1u << lane) - 1u));
-      if (r < m) victim[r] = sl;
+  // 4. Rank within order by slot index, only for orders <= o_max; the first
+  //    m ranks are the victims.  Lanes of a chunk are grouped by order with a
+  //    ballot per distinct order present (usually one or two).
+  if (o_max >= 0) {
+    for (int base = w_begin; base < w_begin + chunk; base += 32) {
+      const int sl = base + lane;
+      const int o = sl < w_end ? (int)ord[sl] : kNotCandidate;
+      unsigned todo = __ballot_sync(0xffffffffu, o <= o_max);
+      while (todo) {
+        const int leader = __ffs(todo) - 1;
+        const int ol = __shfl_sync(0xffffffffu, o, leader);
+        const unsigned peers = __ballot_sync(0xffffffffu, o == ol && o <= o_max);
+        const int start = wstart[ol * kWarps + warp];
+        if (o == ol) {
+          const int r = start + __popc(peers & ((1u << lane) - 1u));
+          if (r < m) victim[r] = sl;
+        }
+        __syncwarp();
+        if (lane == leader) wstart[ol * kWarps + warp] = start + __popc(peers);
+        __syncwarp();
+        todo &= ~peers;
+      }
     }
-    __syncwarp();
-    if (o != kNotCandidate && lane == __ffs(peers) - 1) wstart[o * kWarps + warp] += __popc(peers);
-    __syncwarp();
   }
   if (tid == 0) s_base = m > 0 ? atomicAdd(s.desc_count, m) : 0;
   __syncthreads();
@@ -277,55 +294,62 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
 
   // 6. Resolve slot-map entries of misses (-2 - cell -> reserved slot); with
   //    hits_first, also list each token's slots hits first (misses from the
-  //    back) and count its hits.
+  //    back) and count its hits.  Each thread owns a contiguous run of
+  //    positions and issues all its loads before using them; one block scan
+  //    of packed (hits << 16 | misses) counts places both lists.
   const int n = n_tok * k;
-  if (!hits_first) {
-    for (int p = tid; p < n; p += kThreads) {
-      const size_t off = (size_t)u * n + p;
-      const int sm = slot_map[off];
-      if (sm <= -2) slot_map[off] = s.mslot[(size_t)u * s.MS + (-2 - sm)];
-    }
-  } else {
-    for (int j = 0; j < n_tok; ++j) {
-      if (tid == 0) s_run[0] = s_run[1] = 0;
-      __syncthreads();
-      const size_t row0 = (size_t)u * n + (size_t)j * k;
-      for (int c0 = 0; c0 < k; c0 += kThreads) {
-        const int p = c0 + tid;
-        int sm = 0;
-        bool is_hit = false;
-        if (p < k) {
-          sm = slot_map[row0 + p];
-          is_hit = sm >= 0;
-          if (!is_hit) {
-            sm = s.mslot[(size_t)u * s.MS + (-2 - sm)];
-            slot_map[row0 + p] = sm;
-          }
+  constexpr int kRun = 8;  // positions per thread per round
+  for (int j = 0; j < n_tok; ++j) {
+    const size_t row0 = (size_t)u * n + (size_t)j * k;
+    int run_h = 0, run_m = 0;
+    for (int c0 = 0; c0 < k; c0 += kThreads * kRun) {
+      const int p0 = c0 + tid * kRun;
+      int sm[kRun];
+#pragma unroll
+      for (int e = 0; e < kRun; ++e) sm[e] = p0 + e < k ? slot_map[row0 + p0 + e] : 0;
+      unsigned hitbits = 0;
+      int nh = 0, nm = 0;
+#pragma unroll
+      for (int e = 0; e < kRun; ++e) {
+        if (p0 + e >= k) continue;
+        if (sm[e] <= -2) {
+          sm[e] = s.mslot[(size_t)u * s.MS + (-2 - sm[e])];
+          slot_map[row0 + p0 + e] = sm[e];
+          ++nm;
+        } else {
+          hitbits |= 1u << e;
+          ++nh;
         }
-        const unsigned hb = __ballot_sync(0xffffffffu, p < k && is_hit);
-        const unsigned mb = __ballot_sync(0xffffffffu, p < k && !is_hit);
-        if (lane == 0) wsum[warp] = (__popc(hb) << 16) | __popc(mb);
-        __syncthreads();
-        int before = 0;  // packed (hits << 16 | misses) of lower warps in this chunk
-        for (int w2 = 0; w2 < warp; ++w2) before += wsum[w2];
-        const int run_h = s_run[0], run_m = s_run[1];
-        const unsigned lt = (1u << lane) - 1u;
-        if (p < k) {
-          const int idx = is_hit ? run_h + (before >> 16) + __popc(hb & lt)
-                                 : k - 1 - (run_m + (before & 0xFFFF) + __popc(mb & lt));
-          s.order[row0 + idx] = sm;
-        }
-        __syncthreads();
-        if (tid == kThreads - 1) {
-          const int tot = before + wsum[warp];
-          s_run[0] = run_h + (tot >> 16);
-          s_run[1] = run_m + (tot & 0xFFFF);
-        }
-        __syncthreads();
       }
-      if (tid == 0) s.nhit[u * kMaxTokens + j] = s_run[0];
-      __syncthreads();
+      if (hits_first) {
+        const int packed = (nh << 16) | nm;
+        const int incl = warp_incl_scan(packed, lane);
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+          const int v = wsum[lane];
+          const int vi = warp_incl_scan(v, lane);
+          wsum[lane] = vi - v;
+          if (lane == 31) s_tot = vi;
+        }
+        __syncthreads();
+        const int before = wsum[warp] + incl - packed;
+        int h = run_h + (before >> 16), mm = run_m + (before & 0xFFFF);
+#pragma unroll
+        for (int e = 0; e < kRun; ++e) {
+          if (p0 + e >= k) continue;
+          if ((hitbits >> e) & 1u)
+            s.order[row0 + h++] = sm[e];
+          else
+            s.order[row0 + (k - 1 - mm++)] = sm[e];
+        }
+        const int tot = s_tot;
+        run_h += tot >> 16;
+        run_m += tot & 0xFFFF;
+        __syncthreads();  // wsum and s_tot are reused by the next round
+      }
     }
+    if (hits_first && tid == 0) s.nhit[u * kMaxTokens + j] = run_h;
   }
 
   // 7. Statistics and this step's descriptor range (for the table update).
