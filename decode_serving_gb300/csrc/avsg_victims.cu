@@ -136,6 +136,23 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   const int m = s.mcount[u];
   unsigned long long* ms = s.mset + (size_t)u * s.MS;
 
+  // The slot state of the first kBatch chunks is loaded now, so that its
+  // latency overlaps phase 1's dependent loads.
+  const int chunk = ((B + kWarps * 32 - 1) / (kWarps * 32)) * 32;  // slots per warp
+  const int w_begin = warp * chunk, w_end = min(B, w_begin + chunk);
+  int sn[kBatch], tg[kBatch], ls[kBatch];
+  auto load_batch = [&](int base) {
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int sl = base + b * 32 + lane;
+      const bool in = sl < w_end && base + b * 32 < w_begin + chunk;
+      sn[b] = in ? __ldcg(s.seen + ub + sl) : -1;
+      tg[b] = in ? __ldcg(s.tag + ub + sl) : kEmpty;
+      ls[b] = in ? __ldcg(s.last + ub + sl) : 0;
+    }
+  };
+  load_batch(w_begin);
+
   // 1. Distinct missing ids (key = id << 32 | miss-set cell) and the rank of
   //    each in ascending id order: counted directly when there are few,
   //    otherwise by a bitonic sort.
@@ -187,19 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   // 2. Reservation order of every slot; per-warp histogram over orders (each
   //    warp owns a contiguous slot range and a private row of counters, so
   //    plain shared-memory atomics need no ordering).
-  const int chunk = ((B + kWarps * 32 - 1) / (kWarps * 32)) * 32;  // slots per warp
-  const int w_begin = warp * chunk, w_end = min(B, w_begin + chunk);
   int hits = 0;
   for (int base = w_begin; base < w_begin + chunk; base += 32 * kBatch) {
-    int sn[kBatch], tg[kBatch], ls[kBatch];
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int sl = base + b * 32 + lane;
-      const bool in = sl < w_end && base + b * 32 < w_begin + chunk;
-      sn[b] = in ? __ldcg(s.seen + ub + sl) : -1;
-      tg[b] = in ? __ldcg(s.tag + ub + sl) : kEmpty;
-      ls[b] = in ? __ldcg(s.last + ub + sl) : 0;
-    }
+    if (base != w_begin) load_batch(base);
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int sl = base + b * 32 + lane;
@@ -294,27 +301,30 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
 
   // 6. Resolve slot-map entries of misses (-2 - cell -> reserved slot); with
   //    hits_first, also list each token's slots hits first (misses from the
-  //    back) and count its hits.  Each thread owns a contiguous run of
-  //    positions and issues all its loads before using them; one block scan
+  //    back) and count its hits.  Thread t takes positions t, t + 1024, ...
+  //    of a round (coalesced), issues all its loads first, and one block scan
   //    of packed (hits << 16 | misses) counts places both lists.
   const int n = n_tok * k;
-  constexpr int kRun = 8;  // positions per thread per round
+  constexpr int kRun = 4;  // positions per thread per round
   for (int j = 0; j < n_tok; ++j) {
     const size_t row0 = (size_t)u * n + (size_t)j * k;
     int run_h = 0, run_m = 0;
     for (int c0 = 0; c0 < k; c0 += kThreads * kRun) {
-      const int p0 = c0 + tid * kRun;
       int sm[kRun];
 #pragma unroll
-      for (int e = 0; e < kRun; ++e) sm[e] = p0 + e < k ? slot_map[row0 + p0 + e] : 0;
+      for (int e = 0; e < kRun; ++e) {
+        const int p = c0 + e * kThreads + tid;
+        sm[e] = p < k ? slot_map[row0 + p] : 0;
+      }
       unsigned hitbits = 0;
       int nh = 0, nm = 0;
 #pragma unroll
       for (int e = 0; e < kRun; ++e) {
-        if (p0 + e >= k) continue;
+        const int p = c0 + e * kThreads + tid;
+        if (p >= k) continue;
         if (sm[e] <= -2) {
           sm[e] = s.mslot[(size_t)u * s.MS + (-2 - sm[e])];
-          slot_map[row0 + p0 + e] = sm[e];
+          slot_map[row0 + p] = sm[e];
           ++nm;
         } else {
           hitbits |= 1u << e;
@@ -337,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
         int h = run_h + (before >> 16), mm = run_m + (before & 0xFFFF);
 #pragma unroll
         for (int e = 0; e < kRun; ++e) {
-          if (p0 + e >= k) continue;
+          if (c0 + e * kThreads + tid >= k) continue;
           if ((hitbits >> e) & 1u)
             s.order[row0 + h++] = sm[e];
           else
