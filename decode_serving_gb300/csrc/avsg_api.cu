@@ -201,7 +201,6 @@ int init_state(avsg_handle h, cudaStream_t st) {
     AVSG_SET(s.htab, 0xFF, (size_t)s.U * s.HS * sizeof(int2));
     AVSG_SET(s.hused, 0, (size_t)s.U * 4);
     AVSG_SET(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
-    AVSG_SET(s.mcount, 0, (size_t)s.U * 4);
   }
   AVSG_SET(s.desc_count, 0, 4);
   AVSG_SET(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);
@@ -306,8 +305,6 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.hused, (size_t)U);
   cv.take(&s.mset, st_arrays ? (size_t)U * s.MS : 0);
   cv.take(&s.mslot, st_arrays ? (size_t)U * s.MS : 0);
-  cv.take(&s.mlist, (size_t)U * max_union);
-  cv.take(&s.mcount, (size_t)U);
   cv.take(&s.desc, (size_t)U * max_union);
   cv.take(&s.desc_count, 1);
   cv.take(&s.dbase, (size_t)U);
@@ -337,7 +334,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   void* b = h->dev_block;
   rebase(&s.kbuf, b); rebase(&s.vbuf, b); rebase(&s.tag, b); rebase(&s.last, b);
   rebase(&s.seen, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.mset, b);
-  rebase(&s.mslot, b); rebase(&s.mlist, b); rebase(&s.mcount, b); rebase(&s.desc, b);
+  rebase(&s.mslot, b); rebase(&s.desc, b);
   rebase(&s.desc_count, b); rebase(&s.part, b);
   rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&s.order, b); rebase(&s.nhit, b); rebase(&s.part_count, b);
   rebase(&s.counters, b); rebase(&s.err, b);
@@ -603,7 +600,6 @@ extern "C" int avsg_clear_error(avsg_handle h) {
   if (!h->no_reuse) {
     if (e == cudaSuccess) e = cudaMemset(s.seen, 0, (size_t)s.U * s.B * 4);
     if (e == cudaSuccess) e = cudaMemset(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
-    if (e == cudaSuccess) e = cudaMemset(s.mcount, 0, (size_t)s.U * 4);
   }
   if (e == cudaSuccess) e = cudaMemset(s.desc_count, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);

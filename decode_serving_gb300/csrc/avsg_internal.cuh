@@ -51,8 +51,6 @@ struct DeviceState {
   int32_t* hused;                  // [U] non-empty hash cells (live + erased)
   unsigned long long* mset;        // [U][MS] {id | token bits << 32}, kMissEmpty between steps
   int32_t* mslot;                  // [U][MS] slot reserved for the miss in that cell
-  int32_t* mlist;                  // [U][max_union] cells of this step's distinct misses
-  int32_t* mcount;                 // [U] distinct misses this step
   GatherDesc* desc;                // [U * max_union]
   int32_t* desc_count;             // [1]
   int32_t* dbase;                  // [U] first descriptor of the unit this step

@@ -11,9 +11,9 @@
 //     hash); a hit writes its slot and sets the token's bit in seen[slot]
 //     (a bit already set means the id repeats within one token's list);
 //   * a miss is entered in the per-step miss set (one cell per distinct id,
-//     token bits merged, so a multi-token iteration reserves each id once);
-//     the first token to enter an id appends the cell to the unit's miss list;
-//     the slot map gets -2 - cell until the reservation kernel resolves it.
+//     claimed or extended with one compare-and-swap; token bits merged, so a
+//     multi-token iteration reserves each id once); the slot map gets
+//     -2 - cell until the reservation kernel resolves it.
 // Nothing in the buffer state (tags, last_step, hash table) changes here, so a
 // BAD_SELECTION leaves the state as it was.
 #include "avsg_internal.cuh"
@@ -39,7 +39,6 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
   __syncthreads();
   if (s_stop) return;  // block-uniform: an earlier step latched an error
 
-  bool uniq_miss = false;
   int miss_cell = -1;
   if (pos < n) {
     const int tok = pos / k;
@@ -81,33 +80,31 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
         const uint32_t mmask = (uint32_t)s.MS - 1u;
         const unsigned long long tokbit = (unsigned long long)bit << 32;
         uint32_t c = fib_hash(id, s.ms_shift);
-        // Each failed compare-and-swap means another token added its bit to
-        // this cell, so retries are bounded by the token count.
+        unsigned long long expect = kMissEmpty;  // first try: claim an empty cell
+        // Each failed compare-and-swap on the id's own cell means another
+        // token added its bit, so retries are bounded by the token count.
         for (int iter = 0; iter < s.MS + 2 * kMaxTokens; ++iter) {
           unsigned long long* p = ms + (c & mmask);
-          unsigned long long w = *(volatile unsigned long long*)p;
-          if (w == kMissEmpty) {
-            const unsigned long long prev = atomicCAS(p, kMissEmpty, tokbit | (uint32_t)id);
-            if (prev == kMissEmpty) {
-              miss_cell = (int)(c & mmask);
-              uniq_miss = true;
-              break;
-            }
-            w = prev;
+          const unsigned long long want = expect == kMissEmpty ? (tokbit | (uint32_t)id) : (expect | tokbit);
+          const unsigned long long prev = atomicCAS(p, expect, want);
+          if (prev == expect) {
+            miss_cell = (int)(c & mmask);
+            break;
           }
-          if ((uint32_t)w == (uint32_t)id) {
-            if (w & tokbit) {
+          if ((uint32_t)prev == (uint32_t)id) {  // this id's cell, claimed by another token
+            if (prev & tokbit) {
               raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
               miss_cell = (int)(c & mmask);
               break;
             }
-            const unsigned long long prev = atomicCAS(p, w, w | tokbit);
-            if (prev == w) {
-              miss_cell = (int)(c & mmask);
-              break;
-            }
-            continue;  // lost a race on this cell; read it again
+            expect = prev;  // add this token's bit
+            continue;
           }
+          if (prev == kMissEmpty) {  // lost an empty cell to another id? it is now taken; retry it
+            expect = kMissEmpty;
+            continue;
+          }
+          expect = kMissEmpty;  // another id's cell: probe on
           ++c;
         }
         if (miss_cell < 0) raise_error(s.err, AVSG_ERR_CAPACITY, u, pos);  // miss set full
@@ -117,15 +114,6 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
     }
   }
 
-  // Append first-seen misses to the unit's list: one atomic per warp.
-  const unsigned ball = __ballot_sync(0xffffffffu, uniq_miss);
-  if (ball) {
-    const int lane = threadIdx.x & 31;
-    int base = 0;
-    if (lane == __ffs(ball) - 1) base = atomicAdd(&s.mcount[u], __popc(ball));
-    base = __shfl_sync(0xffffffffu, base, __ffs(ball) - 1);
-    if (uniq_miss) s.mlist[(size_t)u * s.max_union + base + __popc(ball & ((1u << lane) - 1u))] = miss_cell;
-  }
 }
 
 }  // namespace

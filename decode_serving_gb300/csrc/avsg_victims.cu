@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
                                                               int k, int32_t* __restrict__ slot_map,
                                                               int hits_first) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int s_stop, s_base, s_hits, s_omax, s_tot;
+  __shared__ int s_stop, s_base, s_hits, s_omax, s_tot, s_m;
   __shared__ int wsum[kWarps];
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -133,7 +133,6 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
 
   const int B = s.B;
   const size_t ub = (size_t)u * B;
-  const int m = s.mcount[u];
   unsigned long long* ms = s.mset + (size_t)u * s.MS;
 
   // The slot state of the first kBatch chunks is loaded now, so that its
@@ -153,19 +152,29 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   };
   load_batch(w_begin);
 
-  // 1. Distinct missing ids (key = id << 32 | miss-set cell) and the rank of
-  //    each in ascending id order: counted directly when there are few,
-  //    otherwise by a bitonic sort.
+  // 1. Distinct missing ids: every claimed cell of the unit's miss set, as
+  //    key = id << 32 | cell (one coalesced pass, compacted by ballots), and
+  //    the rank of each in ascending id order: counted directly when there
+  //    are few, otherwise by a bitonic sort.
+  if (tid == 0) s_m = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < s.MS; c0 += kThreads) {
+    const int cell = c0 + tid;
+    const unsigned long long w = cell < s.MS ? __ldcg(ms + cell) : kMissEmpty;
+    const bool used = w != kMissEmpty;
+    const unsigned bal = __ballot_sync(0xffffffffu, used);
+    int wbase = 0;
+    if (lane == 0 && bal) wbase = atomicAdd(&s_m, __popc(bal));
+    wbase = __shfl_sync(0xffffffffu, wbase, 0);
+    if (used)
+      keys[wbase + __popc(bal & ((1u << lane) - 1u))] =
+          ((unsigned long long)(uint32_t)w << 32) | (uint32_t)cell;
+  }
+  __syncthreads();
+  const int m = s_m;
   const bool counting = m <= kCountRankMax;
   const int P = counting ? m : next_pow2(m);
-  for (int i = tid; i < P; i += kThreads) {
-    unsigned long long key = ~0ull;
-    if (i < m) {
-      const int cell = s.mlist[(size_t)u * s.max_union + i];
-      key = ((unsigned long long)(uint32_t)ms[cell] << 32) | (uint32_t)cell;
-    }
-    keys[i] = key;
-  }
+  for (int i = m + tid; i < P; i += kThreads) keys[i] = ~0ull;
   for (int i = tid; i < kOrders * kWarps; i += kThreads) wstart[i] = 0;
   __syncthreads();
   if (counting) {
@@ -364,7 +373,6 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
 
   // 7. Statistics and this step's descriptor range (for the table update).
   if (tid == 0) {
-    s.mcount[u] = 0;
     s.dbase[u] = s_base;
     s.dcount[u] = m;
     s.counters[u].hits += (unsigned long long)s_hits;
