@@ -31,19 +31,18 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
   const int u = blockIdx.y;
   const int n = n_tok * k;
   const int pos = blockIdx.x * kThreads + threadIdx.x;
-  __shared__ int s_stop;
   griddep_wait();
   griddep_launch();
   if (blockIdx.x == 0 && u == 0 && threadIdx.x == 0) *s.desc_count = 0;
-  if (threadIdx.x == 0) s_stop = load_err(s.err);
-  __syncthreads();
-  if (s_stop) return;  // block-uniform: an earlier step latched an error
-
+  // The error word and the id are loaded together (no block barrier in
+  // between); a latched error from an earlier step ends the thread.
+  const int stop = load_err(s.err);
   int miss_cell = -1;
   if (pos < n) {
     const int tok = pos / k;
     const size_t off = (size_t)u * n + pos;
     const int32_t id = sel[off];
+    if (stop) return;
     if (id < 0 || (int64_t)id >= s.L) {
       raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
       slot_map[off] = -1;

@@ -158,9 +158,19 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   //    are few, otherwise by a bitonic sort.
   if (tid == 0) s_m = 0;
   __syncthreads();
-  for (int c0 = 0; c0 < s.MS; c0 += kThreads) {
-    const int cell = c0 + tid;
-    const unsigned long long w = cell < s.MS ? __ldcg(ms + cell) : kMissEmpty;
+  constexpr int kCellsAhead = 4;  // miss-set cells a thread loads before compacting
+  for (int c0 = 0; c0 < s.MS; c0 += kThreads * kCellsAhead) {
+    unsigned long long wv[kCellsAhead];
+#pragma unroll
+    for (int e = 0; e < kCellsAhead; ++e) {
+      const int cell = c0 + e * kThreads + tid;
+      wv[e] = cell < s.MS ? __ldcg(ms + cell) : kMissEmpty;
+    }
+#pragma unroll
+    for (int e = 0; e < kCellsAhead; ++e) {
+    if (c0 + e * kThreads >= s.MS) break;  // warp-uniform
+    const int cell = c0 + e * kThreads + tid;
+    const unsigned long long w = wv[e];
     const bool used = w != kMissEmpty;
     const unsigned bal = __ballot_sync(0xffffffffu, used);
     int wbase = 0;
@@ -169,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     if (used)
       keys[wbase + __popc(bal & ((1u << lane) - 1u))] =
           ((unsigned long long)(uint32_t)w << 32) | (uint32_t)cell;
+    }
   }
   __syncthreads();
   const int m = s_m;
