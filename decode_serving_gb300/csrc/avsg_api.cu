@@ -265,7 +265,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   s.ek = ek;
   s.ev = ev;
   s.max_union = (int32_t)max_union;
-  s.HS = pow2_at_least(4LL * (no_reuse ? 1 : c.buffer_slots));
+  s.HS = pow2_at_least(8LL * (no_reuse ? 1 : c.buffer_slots));
   s.hs_shift = 32 - log2_exact(s.HS);
   s.MS = pow2_at_least(2 * max_union);
   s.MS = s.MS < 2 ? 2 : s.MS;

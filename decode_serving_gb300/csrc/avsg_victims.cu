@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) commit_kernel(DeviceState s) {
   __syncthreads();
   if (tid == 0) {
     const int total = s.hused[u] + s_used;
-    s_rebuild = total > s.HS / 2;
+    s_rebuild = total > s.HS / 4;
     s.hused[u] = total;
   }
   __syncthreads();
