@@ -47,7 +47,8 @@ struct avsg_handle_s {
   // side stream: the miss gather and the table commit run there while the
   // caller's stream runs attention over the hit rows
   cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_commit = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_fork2 = nullptr, ev_gather = nullptr, ev_commit = nullptr;
+  bool staged = false;  // staging area allocated: the two-pass pipeline is available
 };
 
 namespace {
@@ -121,7 +122,7 @@ int map_host(avsg_handle h, const void* p, size_t bytes, const unsigned char** d
 void release(avsg_handle h) {
   if (!h) return;
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
-  for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_commit})
+  for (cudaEvent_t e : {h->ev_fork, h->ev_fork2, h->ev_gather, h->ev_commit})
     if (e) cudaEventDestroy(e);
   if (h->side) cudaStreamDestroy(h->side);
   if (h->dev_block) cudaFree(h->dev_block);
@@ -298,6 +299,10 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   Carver cv;
   cv.take(&s.kbuf, (size_t)U * s.B * ek);
   cv.take(&s.vbuf, (size_t)U * s.B * ev);
+  // staging rows for the two-pass pipeline (one per miss-set cell)
+  h->staged = !no_reuse && attention_tc_supported(s.D, s.DV, s.G, s.kv_shared);
+  cv.take(&s.kstage, h->staged ? (size_t)U * s.MS * ek : 0);
+  cv.take(&s.vstage, h->staged ? (size_t)U * s.MS * ev : 0);
   cv.take(&s.tag, ub);
   cv.take(&s.last, ub);
   cv.take(&s.seen, ub);
@@ -333,6 +338,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   }
   void* b = h->dev_block;
   rebase(&s.kbuf, b); rebase(&s.vbuf, b); rebase(&s.tag, b); rebase(&s.last, b);
+  rebase(&s.kstage, b); rebase(&s.vstage, b);
   rebase(&s.seen, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.mset, b);
   rebase(&s.mslot, b); rebase(&s.desc, b);
   rebase(&s.desc_count, b); rebase(&s.part, b);
@@ -340,10 +346,14 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   rebase(&s.counters, b); rebase(&s.err, b);
   rebase(&h->slot_scratch, b); rebase(&h->hit_scratch, b); rebase(&h->stage_sel, b);
   rebase(&h->stage_q, b); rebase(&h->stage_out, b);
-  if (shared) s.vbuf = s.kbuf;
+  if (shared) {
+    s.vbuf = s.kbuf;
+    s.vstage = s.kstage;
+  }
 
   e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork2, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_gather, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_commit, cudaEventDisableTiming);
   if (e != cudaSuccess) {
@@ -443,37 +453,48 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
     AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(s, a, st));
     return AVSG_OK;
   }
-  // Two attention passes (hit rows beside the gather, then miss rows) when
-  // the tensor-core kernel serves this shape and the partials fit.
+  // Two-pass pipeline (the tensor-core shapes): right after match, the
+  // missed rows are copied from host into a staging area on the side stream
+  // while the reservation and the attention over hit rows run here; the
+  // attention over miss rows reads the staged rows; the side stream then
+  // places them into their reserved slots and updates the hash table.
   const int pairs = s.U * n_tok;
   const int resident = 2 * h->num_sms;
   const int splits_h = resident / pairs > 0 ? resident / pairs : 1;
-  const int splits_m = splits_h / 4 > 0 ? splits_h / 4 : 1;
+  const int splits_m = splits_h;
   const bool overlap =
-      overlap_enabled() && attention_tc_enabled() &&
-      attention_tc_supported(s.D, s.DV, s.G, s.kv_shared) &&
+      h->staged && overlap_enabled() && attention_tc_enabled() &&
       (size_t)pairs * (splits_h + splits_m) * s.G * (s.DV + 2) <= h->part_floats;
   AVSG_RUN(AVSG_KERNEL_MATCH, st, launch_match(s, t, n_tok, k, d_sel, slot_map, d_hit, st));
-  AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(s, t, n_tok, k, slot_map, overlap ? 1 : 0, st));
   if (!overlap) {
+    AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(s, t, n_tok, k, slot_map, 0, st));
     AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(s, h->gather_ctas, st));
-    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(s, st));
+    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(s, 0, st));
     AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(s, a, st));
     return AVSG_OK;
   }
   e = cudaEventRecord(h->ev_fork, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_GATHER, h->side, launch_gather(s, h->gather_ctas, h->side));
+  AVSG_RUN(AVSG_KERNEL_GATHER, h->side, launch_gather_stage(s, h->gather_ctas, h->side));
   e = cudaEventRecord(h->ev_gather, h->side);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_COMMIT, h->side, launch_commit(s, h->side));
+  AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(s, t, n_tok, k, slot_map, 1, st));
+  e = cudaEventRecord(h->ev_fork2, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork2, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_COMMIT, h->side, launch_commit(s, 1, h->side));
   e = cudaEventRecord(h->ev_commit, h->side);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(s, a, 0, splits_h, splits_m, st));
   e = cudaStreamWaitEvent(st, h->ev_gather, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, st, launch_attention_tc_pass(s, a, 1, splits_h, splits_m, st));
+  DeviceState staged = s;  // miss rows are read from the staging area, by cell
+  staged.kbuf = s.kstage;
+  staged.vbuf = s.vstage;
+  staged.B = s.MS;
+  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, st,
+           launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, st));
   e = cudaStreamWaitEvent(st, h->ev_commit, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
 #undef AVSG_RUN

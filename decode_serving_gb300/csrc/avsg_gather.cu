@@ -86,6 +86,65 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(DeviceState s) {
   });
 }
 
+// Staged gather: runs right after match, before any slot is reserved.  Each
+// CTA takes an equal contiguous range of all units' miss-set cells (hashing
+// spreads the claimed cells evenly); a warp reads 32 cells, and for every
+// claimed one copies host row `id` of that unit into the staging area at the
+// cell, 32 lanes per row and several rows in flight per lane.
+__global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
+  __shared__ long long s_cell[kThreads / 32][32];  // claimed cells of a warp's chunk
+  __shared__ int s_id[kThreads / 32][32];
+  griddep_wait();
+  griddep_launch();
+  if (load_err(s.err) != 0) return;  // no block barriers below: a per-thread exit is safe
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = kThreads / 32;
+  const long long ncell = (long long)s.U * s.MS;
+  const long long c_begin = blockIdx.x * ncell / gridDim.x;
+  const long long c_end = (blockIdx.x + 1) * ncell / gridDim.x;
+  const uint32_t cpk = (uint32_t)(s.ek >> 4), cpv = (uint32_t)(s.ev >> 4), cpe = cpk + cpv;
+  for (long long c0 = c_begin + warp * 32; c0 < c_end; c0 += nwarp * 32) {
+    const long long cell = c0 + lane;
+    const unsigned long long w = cell < c_end ? __ldcg(s.mset + cell) : kMissEmpty;
+    const bool claimed = w != kMissEmpty;
+    const unsigned bal = __ballot_sync(0xffffffffu, claimed);
+    if (claimed) {
+      const int r = __popc(bal & ((1u << lane) - 1u));
+      s_cell[warp][r] = cell;
+      s_id[warp][r] = (int)(uint32_t)w;
+    }
+    __syncwarp();
+    const uint32_t items = (uint32_t)__popc(bal) * cpe;  // (row, 16-byte chunk) pairs
+    for (uint32_t it0 = lane; it0 < items; it0 += 32 * kUnroll) {
+      uint4 v[kUnroll];
+      unsigned char* dst[kUnroll];
+#pragma unroll
+      for (int q = 0; q < kUnroll; ++q) {
+        const uint32_t it = it0 + 32u * q;
+        dst[q] = nullptr;
+        if (it < items) {
+          const uint32_t r = it / cpe, j = it - r * cpe;
+          const long long cg = s_cell[warp][r];
+          const long long unit = cg / s.MS;
+          const long long hrow = unit * s.L + s_id[warp][r];
+          const unsigned char* src;
+          if (j < cpk) {
+            src = s.host_k + hrow * s.ek + ((size_t)j << 4);
+            dst[q] = s.kstage + cg * s.ek + ((size_t)j << 4);
+          } else {
+            src = s.host_v + hrow * s.ev + ((size_t)(j - cpk) << 4);
+            dst[q] = s.vstage + cg * s.ev + ((size_t)(j - cpk) << 4);
+          }
+          v[q] = load_host16(src);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kUnroll; ++q)
+        if (dst[q]) store16(dst[q], v[q]);
+    }
+    __syncwarp();  // the list is rewritten by the next chunk
+  }
+}
+
 // No-reuse comparison path: every selected row of every token is copied to
 // staging slot tok * k + j of its unit; ids are range-checked.
 __global__ void __launch_bounds__(kThreads) gather_all_kernel(DeviceState s, int n_tok, int k,
@@ -126,6 +185,13 @@ cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st) {
   const cudaError_t e = ensure_smem((const void*)gather_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
   return launch_pdl(gather_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
+}
+
+cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st) {
+  static int attr_done = 0;
+  const cudaError_t e = ensure_smem((const void*)gather_stage_kernel, 0, &attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(gather_stage_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
 }
 
 cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,

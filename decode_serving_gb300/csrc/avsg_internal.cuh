@@ -26,9 +26,10 @@ struct DevCounters {
 };
 
 // One miss to copy: host row `id` of `unit` into buffer slot `slot`, which
-// held `old_id` (kEmpty if none) before this step.
+// held `old_id` (kEmpty if none) before this step; `cell` is the id's
+// miss-set cell (and its row in the staging area).
 struct GatherDesc {
-  int32_t unit, id, slot, old_id;
+  int32_t unit, id, slot, old_id, cell, pad0, pad1, pad2;
 };
 
 // Everything a kernel needs about a handle: sizes and device pointers.
@@ -44,6 +45,8 @@ struct DeviceState {
   const unsigned char* host_v;
   unsigned char* kbuf;             // [U][B][ek]
   unsigned char* vbuf;             // [U][B][ev]
+  unsigned char* kstage;           // [U][MS][ek] missed rows by miss-set cell (staged gather)
+  unsigned char* vstage;           // [U][MS][ev]
   int32_t* tag;                    // [U][B] resident id or kEmpty
   int32_t* last;                   // [U][B] step of last selection, -1 never
   int32_t* seen;                   // [U][B] token bits of this step's hits; 0 between steps
@@ -120,8 +123,13 @@ cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_
 // Hash-table update of a step (erase evicted ids, insert new ones, rebuild):
 // needed only by the next step's match, so it may run beside the gather and
 // the attention.
-cudaError_t launch_commit(const DeviceState& s, cudaStream_t st);
+// With place != 0 it first copies the staged rows into their slots; it always
+// empties the step's miss-set cells.
+cudaError_t launch_commit(const DeviceState& s, int place, cudaStream_t st);
 cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
+// Staged gather: right after match, the host row of every claimed miss-set
+// cell is copied to kstage/vstage at that cell (no slot needed yet).
+cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st);
 cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,
                               int32_t* slot_map, uint8_t* hit, int ctas, cudaStream_t st);
 

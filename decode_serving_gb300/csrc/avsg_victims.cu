@@ -22,7 +22,8 @@
 // two-pass attention, each token's slots are listed hits first.
 //
 // The hash-table update of the step (commit_kernel below) runs separately:
-// only the next step's match needs it.
+// only the next step's match needs it.  It also moves staged rows into their
+// slots and empties the miss set.
 #include "avsg_internal.cuh"
 
 namespace avsg {
@@ -314,8 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     s.tag[ub + v] = id;
     s.last[ub + v] = t;
     s.mslot[(size_t)u * s.MS + cell] = v;
-    ms[cell] = kMissEmpty;
-    s.desc[s_base + r] = GatherDesc{u, id, v, old};
+    s.desc[s_base + r] = GatherDesc{u, id, v, old, cell, 0, 0, 0};
   }
   __syncthreads();
 
@@ -343,8 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
         const int p = c0 + e * kThreads + tid;
         if (p >= k) continue;
         if (sm[e] <= -2) {
-          sm[e] = s.mslot[(size_t)u * s.MS + (-2 - sm[e])];
-          slot_map[row0 + p] = sm[e];
+          const int cell = -2 - sm[e];
+          slot_map[row0 + p] = s.mslot[(size_t)u * s.MS + cell];
+          sm[e] = cell;  // the miss pass reads the staged row of this cell
           ++nm;
         } else {
           hitbits |= 1u << e;
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
 
 // Hash-table update of one unit: erase the ids this step evicted, insert the
 // ids it loaded, rebuild from the tags when erased cells pile up.
-__global__ void __launch_bounds__(kThreads, 1) commit_kernel(DeviceState s) {
+__global__ void __launch_bounds__(kThreads, 1) commit_kernel(DeviceState s, int place) {
   __shared__ int s_stop, s_used, s_rebuild, s_live;
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -407,11 +408,27 @@ __global__ void __launch_bounds__(kThreads, 1) commit_kernel(DeviceState s) {
   __syncthreads();
   if (s_stop) return;
   const int m = s.dcount[u], base = s.dbase[u];
+  if (place) {  // staged rows -> their slots, 16 bytes per thread per step
+    const int cpk = (int)(s.ek >> 4), cpv = (int)(s.ev >> 4), cpe = cpk + cpv;
+    for (int c = tid; c < m * cpe; c += kThreads) {
+      const int i = c / cpe, w = c - i * cpe;
+      const GatherDesc d = s.desc[base + i];
+      const size_t srow = (size_t)u * s.MS + d.cell, drow = (size_t)u * s.B + d.slot;
+      if (w < cpk)
+        reinterpret_cast<uint4*>(s.kbuf + drow * s.ek)[w] =
+            __ldcg(reinterpret_cast<const uint4*>(s.kstage + srow * s.ek) + w);
+      else
+        reinterpret_cast<uint4*>(s.vbuf + drow * s.ev)[w - cpk] =
+            __ldcg(reinterpret_cast<const uint4*>(s.vstage + srow * s.ev) + (w - cpk));
+    }
+  }
+  unsigned long long* ms = s.mset + (size_t)u * s.MS;
   int2* tab = s.htab + (size_t)u * s.HS;
   const uint32_t hmask = (uint32_t)s.HS - 1u;
   for (int i = tid; i < m; i += kThreads) {
-    const int32_t old = s.desc[base + i].old_id;
-    if (old != kEmpty) hash_erase(tab, hmask, s.hs_shift, old);
+    const GatherDesc d = s.desc[base + i];
+    ms[d.cell] = kMissEmpty;  // the miss set starts the next step empty
+    if (d.old_id != kEmpty) hash_erase(tab, hmask, s.hs_shift, d.old_id);
   }
   __syncthreads();
   int used = 0;
@@ -463,11 +480,11 @@ cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_
                     hits_first);
 }
 
-cudaError_t launch_commit(const DeviceState& s, cudaStream_t st) {
+cudaError_t launch_commit(const DeviceState& s, int place, cudaStream_t st) {
   static int attr_done = 0;
   const cudaError_t e = ensure_smem((const void*)commit_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(commit_kernel, dim3(s.U), dim3(kThreads), 0, st, s);
+  return launch_pdl(commit_kernel, dim3(s.U), dim3(kThreads), 0, st, s, place);
 }
 
 }  // namespace avsg
