@@ -249,6 +249,7 @@ def run_ours(args, rank, world, torch):
     hits, misses = st1.hits - st0.hits, st1.misses - st0.misses
     uniq = hits + misses
     res = {"launches_per_step": sum(n for _, n in prof.values()) / max(1, args.steps),
+           "host_us_per_step": 1e6 * wall / args.steps,
            "per_step_ms": per, "ms_per_step": ms_step, "wall_s": wall, "prof": prof,
            "ms_per_step_profiled": float(per_prof.sum() / args.steps),
            "clocks": clocks, "hits": hits, "misses": misses, "unique": uniq,
@@ -478,6 +479,7 @@ def report_ours(args, res, world, max_ms, max_e2e_ms) -> dict:
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 K/V, fp32 accumulate",
         "data": "synthetic (seeded generator)", "config": describe(w),
         "steps_per_s": 1e3 / max_ms,
+        "host_wall_us_per_step": res["host_us_per_step"],
         "step_latency_ms": {"median": float(np.median(per)), "p99": float(np.percentile(per, 99))},
         "hit_rate": {"timed_steps": res["hits"] / max(1, res["unique"]),
                      "all_steps": res["hit_rate_all"]},

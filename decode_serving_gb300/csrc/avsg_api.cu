@@ -46,9 +46,12 @@ struct avsg_handle_s {
   uint64_t prof_launches[AVSG_NUM_KERNELS] = {};
   // side stream: the miss gather and the table commit run there while the
   // caller's stream runs attention over the hit rows
-  cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_fork2 = nullptr, ev_gather = nullptr, ev_commit = nullptr;
+  cudaStream_t side = nullptr, side2 = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_reserve = nullptr, ev_commit = nullptr,
+              ev_place = nullptr;
   bool staged = false;  // staging area allocated: the two-pass pipeline is available
+  unsigned long long* mset_base = nullptr;  // two miss sets, [2][U][MS]
+  uint64_t parity = 0;
 };
 
 namespace {
@@ -122,9 +125,10 @@ int map_host(avsg_handle h, const void* p, size_t bytes, const unsigned char** d
 void release(avsg_handle h) {
   if (!h) return;
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
-  for (cudaEvent_t e : {h->ev_fork, h->ev_fork2, h->ev_gather, h->ev_commit})
+  for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_reserve, h->ev_commit, h->ev_place})
     if (e) cudaEventDestroy(e);
   if (h->side) cudaStreamDestroy(h->side);
+  if (h->side2) cudaStreamDestroy(h->side2);
   if (h->dev_block) cudaFree(h->dev_block);
   if (h->reg_k && h->host_k) cudaHostUnregister(const_cast<void*>(h->host_k));
   if (h->reg_v && h->host_v) cudaHostUnregister(const_cast<void*>(h->host_v));
@@ -201,7 +205,7 @@ int init_state(avsg_handle h, cudaStream_t st) {
     AVSG_SET(s.seen, 0, ub * 4);
     AVSG_SET(s.htab, 0xFF, (size_t)s.U * s.HS * sizeof(int2));
     AVSG_SET(s.hused, 0, (size_t)s.U * 4);
-    AVSG_SET(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
+    AVSG_SET(h->mset_base, 0xFF, 2 * (size_t)s.U * s.MS * 8);
   }
   AVSG_SET(s.desc_count, 0, 4);
   AVSG_SET(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);
@@ -308,18 +312,27 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.seen, ub);
   cv.take(&s.htab, st_arrays ? (size_t)U * s.HS : 0);
   cv.take(&s.hused, (size_t)U);
-  cv.take(&s.mset, st_arrays ? (size_t)U * s.MS : 0);
+  cv.take(&h->mset_base, st_arrays ? 2 * (size_t)U * s.MS : 0);
+  cv.take(&s.hslot, (size_t)U * max_union);
   cv.take(&s.mslot, st_arrays ? (size_t)U * s.MS : 0);
   cv.take(&s.desc, (size_t)U * max_union);
   cv.take(&s.desc_count, 1);
   cv.take(&s.dbase, (size_t)U);
   cv.take(&s.dcount, (size_t)U);
-  cv.take(&s.order, (size_t)U * max_union);
-  cv.take(&s.nhit, (size_t)U * kMaxTokens);
+
   {
     size_t part = (size_t)U * c.max_tokens_per_step * h->splits_cap * s.G * (s.DV + 2);
     const size_t tc = attention_tc_part_floats((int)U, c.max_tokens_per_step, s.G, s.DV, h->num_sms);
+    size_t two = 0;  // two-pass attention: pairs * (hit splits + miss splits)
+    for (int nt = 1; nt <= c.max_tokens_per_step; ++nt) {
+      const int pairs = (int)U * nt;
+      const int sh = 2 * h->num_sms / pairs > 0 ? 2 * h->num_sms / pairs : 1;
+      const int sm = sh > (s.MS + kMissListMax - 1) / kMissListMax ? sh : (s.MS + kMissListMax - 1) / kMissListMax;
+      const size_t need = (size_t)pairs * (sh + sm) * s.G * (s.DV + 2);
+      two = need > two ? need : two;
+    }
     h->part_floats = part > tc ? part : tc;
+    h->part_floats = h->part_floats > two ? h->part_floats : two;
     cv.take(&s.part, h->part_floats);
   }
   cv.take(&s.part_count, (size_t)U * kMaxTokens);
@@ -342,7 +355,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   rebase(&s.seen, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.mset, b);
   rebase(&s.mslot, b); rebase(&s.desc, b);
   rebase(&s.desc_count, b); rebase(&s.part, b);
-  rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&s.order, b); rebase(&s.nhit, b); rebase(&s.part_count, b);
+  rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&h->mset_base, b); rebase(&s.hslot, b);
+  s.mset = h->mset_base; rebase(&s.part_count, b);
   rebase(&s.counters, b); rebase(&s.err, b);
   rebase(&h->slot_scratch, b); rebase(&h->hit_scratch, b); rebase(&h->stage_sel, b);
   rebase(&h->stage_q, b); rebase(&h->stage_out, b);
@@ -352,10 +366,9 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   }
 
   e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork2, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_gather, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_commit, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side2, cudaStreamNonBlocking);
+  for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_gather, &h->ev_reserve, &h->ev_commit, &h->ev_place})
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     release(h);
     return AVSG_ERR_CUDA;
@@ -453,49 +466,66 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
     AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(s, a, st));
     return AVSG_OK;
   }
-  // Two-pass pipeline (the tensor-core shapes): right after match, the
-  // missed rows are copied from host into a staging area on the side stream
-  // while the reservation and the attention over hit rows run here; the
-  // attention over miss rows reads the staged rows; the side stream then
-  // places them into their reserved slots and updates the hash table.
+  // Two-pass pipeline (the tensor-core shapes).  After match, three
+  // streams run side by side:
+  //   caller's stream: attention over the hit rows (their slots are known);
+  //   side stream:     the missed rows, host -> staging area (host link);
+  //   side stream 2:   the reservation, then the hash-table update.
+  // The attention over the missed rows (read from staging) follows the
+  // gather and the reservation; the staged rows are then placed into their
+  // slots, and the other step's miss set is emptied, on the side stream.
+  // The two miss sets alternate by step.
   const int pairs = s.U * n_tok;
   const int resident = 2 * h->num_sms;
   const int splits_h = resident / pairs > 0 ? resident / pairs : 1;
-  const int splits_m = splits_h;
+  const int min_m = (s.MS + kMissListMax - 1) / kMissListMax;
+  const int splits_m = splits_h > min_m ? splits_h : min_m;
   const bool overlap =
       h->staged && overlap_enabled() && attention_tc_enabled() &&
       (size_t)pairs * (splits_h + splits_m) * s.G * (s.DV + 2) <= h->part_floats;
-  AVSG_RUN(AVSG_KERNEL_MATCH, st, launch_match(s, t, n_tok, k, d_sel, slot_map, d_hit, st));
+  DeviceState sc = s;
+  const size_t set_cells = (size_t)s.U * s.MS;
+  sc.mset = h->mset_base + (h->parity & 1) * set_cells;  // the set that is empty now
+  AVSG_RUN(AVSG_KERNEL_MATCH, st, launch_match(sc, t, n_tok, k, d_sel, slot_map, d_hit, st));
   if (!overlap) {
-    AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(s, t, n_tok, k, slot_map, 0, st));
-    AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(s, h->gather_ctas, st));
-    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(s, 0, st));
-    AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(s, a, st));
-    return AVSG_OK;
+    AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(sc, t, n_tok, k, slot_map, st));
+    AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(sc, h->gather_ctas, st));
+    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(sc, st));
+    AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(sc, a, st));
+    e = cudaMemsetAsync(sc.mset, 0xFF, set_cells * 8, st);  // the miss set starts empty
+    return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
   }
+  h->parity += 1;
   e = cudaEventRecord(h->ev_fork, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side2, h->ev_fork, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_GATHER, h->side, launch_gather_stage(s, h->gather_ctas, h->side));
+  AVSG_RUN(AVSG_KERNEL_GATHER, h->side, launch_gather_stage(sc, h->gather_ctas, h->side));
   e = cudaEventRecord(h->ev_gather, h->side);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(s, t, n_tok, k, slot_map, 1, st));
-  e = cudaEventRecord(h->ev_fork2, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork2, 0);
+  AVSG_RUN(AVSG_KERNEL_RESERVE, h->side2, launch_victims(sc, t, n_tok, k, slot_map, h->side2));
+  e = cudaEventRecord(h->ev_reserve, h->side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_COMMIT, h->side, launch_commit(s, 1, h->side));
-  e = cudaEventRecord(h->ev_commit, h->side);
+  AVSG_RUN(AVSG_KERNEL_COMMIT, h->side2, launch_commit(sc, h->side2));
+  e = cudaEventRecord(h->ev_commit, h->side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(s, a, 0, splits_h, splits_m, st));
+  AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, splits_h, splits_m, st));
   e = cudaStreamWaitEvent(st, h->ev_gather, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_reserve, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  DeviceState staged = s;  // miss rows are read from the staging area, by cell
+  DeviceState staged = sc;  // miss rows are read from the staging area, by cell
   staged.kbuf = s.kstage;
   staged.vbuf = s.vstage;
   staged.B = s.MS;
   AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, st,
            launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, st));
-  e = cudaStreamWaitEvent(st, h->ev_commit, 0);
+  e = cudaStreamWaitEvent(h->side, h->ev_reserve, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_PLACE, h->side, launch_place(sc, h->gather_ctas, h->side));
+  e = cudaMemsetAsync(h->mset_base + ((h->parity & 1) * set_cells), 0xFF, set_cells * 8, h->side);
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_place, h->side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_place, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_commit, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
 #undef AVSG_RUN
   return AVSG_OK;
@@ -620,7 +650,7 @@ extern "C" int avsg_clear_error(avsg_handle h) {
   cudaError_t e = cudaDeviceSynchronize();
   if (!h->no_reuse) {
     if (e == cudaSuccess) e = cudaMemset(s.seen, 0, (size_t)s.U * s.B * 4);
-    if (e == cudaSuccess) e = cudaMemset(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
+    if (e == cudaSuccess) e = cudaMemset(h->mset_base, 0xFF, 2 * (size_t)s.U * s.MS * 8);
   }
   if (e == cudaSuccess) e = cudaMemset(s.desc_count, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);

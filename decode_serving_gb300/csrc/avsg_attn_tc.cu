@@ -22,10 +22,11 @@
 //   taking an equal contiguous share of all 16-row tiles of all (unit, token)
 //   pairs; a CTA writes one partial (max, sum, acc) per pair segment it
 //   covers and the last CTA to finish a pair merges its segments.
-// * Two passes (attn_tc_pass_kernel): over the hit-first slot lists the
-//   reservation kernel writes -- pass 0 covers the rows that were already
-//   resident and can run while the gather copies the misses in; pass 1 covers
-//   the missed rows and merges both passes.
+// * Two passes (attn_tc_pass_kernel): pass 0 covers the selected rows that
+//   were already resident (the hit slots match wrote; misses are masked) and
+//   runs beside the gather and the reservation; pass 1 covers the missed rows,
+//   read from the staging area by miss-set cell (each CTA scans a share of the
+//   unit's cells for the ones its token selected), and merges both passes.
 // No CTA waits for another.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -40,6 +41,8 @@ constexpr int kThreadsTc = kWarpsTc * 32;
 constexpr int kTileRows = 16;
 constexpr int kStages = 3;
 constexpr int kCtasPerSm = 2;
+constexpr int kListMax = kMissListMax;
+constexpr int kListPerThread = kListMax / kThreadsTc;
 
 template <int D_, int G_, bool SHARED_>
 struct TcShape {
@@ -140,6 +143,7 @@ struct SegArgs {
   int ent_base;                 // first listed entry of the range
   int rows;                     // rows of the range (entries * ET)
   int ta, tb;                   // this CTA's tiles [ta, tb) of the range
+  const int32_t* list;          // when set: slot of entry e is list[e] (shared memory)
 };
 
 // CTA c covers global tiles [c*T/C, (c+1)*T/C); the CTA holding tile x:
@@ -222,12 +226,18 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
     if (i >= n_my || row >= a.rows) return -1;
     const int ent = a.ent_base + (p.ET == 1 ? row : row / p.ET);
     const int sub = row - (ent - a.ent_base) * p.ET;
-    const int slot = p.identity ? tok * p.k + ent : __ldg(p.slots + (size_t)pair * p.k + ent);
+    const int slot = a.list ? a.list[ent]
+                   : p.identity ? tok * p.k + ent
+                                : __ldg(p.slots + (size_t)pair * p.k + ent);
+    if (slot < 0) return -1;  // not a row of this pass (a miss in the pass over hit rows)
     return ((long long)u * s.B + slot) * p.ET + sub;
   };
   constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
   constexpr int RPI = 32 / CPR;    // rows per warp instruction
+  unsigned long long vmasks = 0;  // 16 bits per stage: which rows of the staged tile are real
   auto issue = [&](long long myrow, int st) {
+    const unsigned long long vm = __ballot_sync(0xffffffffu, myrow >= 0) & 0xFFFFu;
+    vmasks = (vmasks & ~(0xFFFFull << (16 * st))) | (vm << (16 * st));
     unsigned char* kst = wbase + st * SH::STAGE_BYTES;
     unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
     const int ch = lane % CPR, rsub = lane / CPR;
@@ -256,8 +266,7 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
     const int st = i % kStages;
     cp_async_wait<kStages - 1>();
     __syncwarp();
-    const int ti = a.ta + warp + i * kWarpsTc;
-    const int nrows = min(kTileRows, a.rows - ti * kTileRows);
+    const unsigned vmask = (unsigned)(vmasks >> (16 * st)) & 0xFFFFu;
     const unsigned char* kst = wbase + st * SH::STAGE_BYTES;
     const unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
     const uint32_t kaddr = smem_u32(kst), vaddr = smem_u32(vst);
@@ -302,8 +311,8 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
       sv[1][0] = sc[0][2] + __shfl_xor_sync(0xffffffffu, sc[0][2], xm);
       sv[1][1] = sc[0][3] + __shfl_xor_sync(0xffffffffu, sc[0][3], xm);
     }
-    if (g >= nrows) sv[0][0] = sv[0][1] = -INFINITY;
-    if (g + 8 >= nrows) sv[1][0] = sv[1][1] = -INFINITY;
+    if (!((vmask >> g) & 1u)) sv[0][0] = sv[0][1] = -INFINITY;
+    if (!((vmask >> (g + 8)) & 1u)) sv[1][0] = sv[1][1] = -INFINITY;
 
     // online softmax per head over the 16 rows (lanes with equal c)
     float pv[2][2], alpha[2] = {1.f, 1.f};
@@ -506,6 +515,7 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
     a.u = pair / p.n_tok;
     a.tok = pair - a.u * p.n_tok;
     a.ent_base = 0;
+    a.list = nullptr;
     a.rows = p.rows_per_pair;
     a.ta = (int)(t - pair_t0);
     a.tb = (int)(min(t_end, pair_t0 + p.tiles_per_pair) - pair_t0);
@@ -548,7 +558,7 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_pass_kernel(DeviceState s,
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
   __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G], cm[G], cl[G];
-  __shared__ int s_stop, s_last;
+  __shared__ int s_stop, s_last, s_wcnt[kWarpsTc];
   const int tid = threadIdx.x;
   griddep_wait();
   griddep_launch();
@@ -559,17 +569,48 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_pass_kernel(DeviceState s,
   float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
 
   const int sp = blockIdx.x, pair = blockIdx.y;
+  const int lane = tid & 31, warp = tid >> 5;
   SegArgs a;
   a.pair = pair;
   a.u = pair / p.n_tok;
   a.tok = pair - a.u * p.n_tok;
-  const int nh = s.nhit[a.u * kMaxTokens + a.tok];
-  a.ent_base = pass ? nh : 0;
-  a.rows = (pass ? p.k - nh : nh) * p.ET;
-  const int tiles = (a.rows + kTileRows - 1) / kTileRows;
-  const int S = pass ? p.splits_m : p.splits_h;
-  a.ta = (int)((long long)sp * tiles / S);
-  a.tb = (int)((long long)(sp + 1) * tiles / S);
+  a.ent_base = 0;
+  a.list = nullptr;
+  if (pass == 0) {  // every selected position; misses masked (their hit slot is -1)
+    a.rows = p.k * p.ET;
+    const int tiles = (a.rows + kTileRows - 1) / kTileRows;
+    a.ta = (int)((long long)sp * tiles / p.splits_h);
+    a.tb = (int)((long long)(sp + 1) * tiles / p.splits_h);
+  } else {  // this CTA's share of the unit's miss-set cells that carry the token
+    int32_t* list = reinterpret_cast<int32_t*>(smem + kWarpsTc * SH::WARP_BYTES);
+    const int c_lo = (int)((long long)sp * s.MS / p.splits_m);
+    const int c_hi = (int)((long long)(sp + 1) * s.MS / p.splits_m);
+    const unsigned long long* msu = s.mset + (size_t)a.u * s.MS;
+    const unsigned long long tokbit = 1ull << (32 + a.tok);
+    bool take[kListPerThread];
+#pragma unroll
+    for (int e = 0; e < kListPerThread; ++e) {
+      const int cell = c_lo + e * kThreadsTc + tid;
+      const unsigned long long w = cell < c_hi ? __ldcg(msu + cell) : kMissEmpty;
+      take[e] = w != kMissEmpty && (w & tokbit);
+    }
+    int nlist = 0;
+#pragma unroll
+    for (int e = 0; e < kListPerThread; ++e) {  // in cell order, deterministic
+      const unsigned bal = __ballot_sync(0xffffffffu, take[e]);
+      if (lane == 0) s_wcnt[warp] = __popc(bal);
+      __syncthreads();
+      int before = nlist;
+      for (int w2 = 0; w2 < warp; ++w2) before += s_wcnt[w2];
+      if (take[e]) list[before + __popc(bal & ((1u << lane) - 1u))] = c_lo + e * kThreadsTc + tid;
+      for (int w2 = 0; w2 < kWarpsTc; ++w2) nlist += s_wcnt[w2];
+      __syncthreads();
+    }
+    a.list = list;
+    a.rows = nlist * p.ET;
+    a.ta = 0;
+    a.tb = (a.rows + kTileRows - 1) / kTileRows;
+  }
   tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
 
   const int nseg = p.splits_h + p.splits_m;
@@ -630,14 +671,15 @@ cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int
                         int splits_m, cudaStream_t st) {
   static int smem_done = 0;
   TcParams p = tc_params<SH>(s, a);
-  p.slots = s.order;
+  p.slots = s.hslot;
   p.identity = 0;
   p.splits_h = splits_h;
   p.splits_m = splits_m;
-  cudaError_t e = ensure_smem((const void*)attn_tc_pass_kernel<SH>, SH::SMEM, &smem_done);
+  const size_t smem = SH::SMEM + kListMax * sizeof(int32_t);
+  cudaError_t e = ensure_smem((const void*)attn_tc_pass_kernel<SH>, smem, &smem_done);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(pass ? splits_m : splits_h), (unsigned)(s.U * a.n_tok));
-  return launch_pdl(attn_tc_pass_kernel<SH>, grid, dim3(kThreadsTc), SH::SMEM, st, s, p, pass);
+  return launch_pdl(attn_tc_pass_kernel<SH>, grid, dim3(kThreadsTc), smem, st, s, p, pass);
 }
 
 }  // namespace

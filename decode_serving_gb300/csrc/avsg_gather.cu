@@ -145,6 +145,43 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
   }
 }
 
+// Place: every miss's staged row (by miss-set cell) into its reserved buffer
+// slot, an equal share of the 16-byte chunks per CTA (device to device).
+__global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s) {
+  griddep_wait();
+  griddep_launch();
+  if (load_err(s.err) != 0) return;
+  const uint32_t n = (uint32_t)*(volatile int32_t*)s.desc_count;
+  const uint32_t cpk = (uint32_t)(s.ek >> 4), cpv = (uint32_t)(s.ev >> 4), cpe = cpk + cpv;
+  const uint32_t total = n * cpe;
+  const uint32_t per = (total + gridDim.x - 1) / gridDim.x;
+  const uint32_t begin = blockIdx.x * per, end = min(total, begin + per);
+  for (uint32_t c0 = begin + threadIdx.x; c0 < end; c0 += kThreads * kUnroll) {
+    uint4 v[kUnroll];
+    uint4* dst[kUnroll];
+#pragma unroll
+    for (int r = 0; r < kUnroll; ++r) {
+      const uint32_t c = c0 + (uint32_t)(r * kThreads);
+      dst[r] = nullptr;
+      if (c < end) {
+        const uint32_t d = c / cpe, w = c - d * cpe;
+        const GatherDesc g = s.desc[d];
+        const size_t srow = (size_t)g.unit * s.MS + g.cell, drow = (size_t)g.unit * s.B + g.slot;
+        if (w < cpk) {
+          v[r] = __ldcg(reinterpret_cast<const uint4*>(s.kstage + srow * s.ek) + w);
+          dst[r] = reinterpret_cast<uint4*>(s.kbuf + drow * s.ek) + w;
+        } else {
+          v[r] = __ldcg(reinterpret_cast<const uint4*>(s.vstage + srow * s.ev) + (w - cpk));
+          dst[r] = reinterpret_cast<uint4*>(s.vbuf + drow * s.ev) + (w - cpk);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kUnroll; ++r)
+      if (dst[r]) *dst[r] = v[r];
+  }
+}
+
 // No-reuse comparison path: every selected row of every token is copied to
 // staging slot tok * k + j of its unit; ids are range-checked.
 __global__ void __launch_bounds__(kThreads) gather_all_kernel(DeviceState s, int n_tok, int k,
@@ -192,6 +229,13 @@ cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st)
   const cudaError_t e = ensure_smem((const void*)gather_stage_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
   return launch_pdl(gather_stage_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
+}
+
+cudaError_t launch_place(const DeviceState& s, int ctas, cudaStream_t st) {
+  static int attr_done = 0;
+  const cudaError_t e = ensure_smem((const void*)place_kernel, 0, &attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(place_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
 }
 
 cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,

@@ -14,6 +14,7 @@ constexpr unsigned long long kMissEmpty = ~0ull;
 constexpr int kOrders = 64;                    // reservation classes 0..63
 constexpr int kNotCandidate = 255;
 constexpr int kMaxTokens = 8;
+constexpr int kMissListMax = 1024;             // miss-set cells one miss-pass CTA scans
 
 // First device error of a step; later kernels of the step (and later steps)
 // see a non-zero code and return before touching any state.
@@ -52,14 +53,14 @@ struct DeviceState {
   int32_t* seen;                   // [U][B] token bits of this step's hits; 0 between steps
   int2* htab;                      // [U][HS] {key, slot}
   int32_t* hused;                  // [U] non-empty hash cells (live + erased)
-  unsigned long long* mset;        // [U][MS] {id | token bits << 32}, kMissEmpty between steps
+  unsigned long long* mset;        // [U][MS] {id | token bits << 32}: this step's miss set
+                                   // (two sets alternate by step; each is empty when its step starts)
+  int32_t* hslot;                  // [U][n_tok][k] slot of each selected id if it was a hit, else -1
   int32_t* mslot;                  // [U][MS] slot reserved for the miss in that cell
   GatherDesc* desc;                // [U * max_union]
   int32_t* desc_count;             // [1]
   int32_t* dbase;                  // [U] first descriptor of the unit this step
   int32_t* dcount;                 // [U] descriptors of the unit this step
-  int32_t* order;                  // [U][n_tok][k] selected slots, hits first
-  int32_t* nhit;                   // [U][kMaxTokens] entries that were hits, per token
   float* part;                     // split-K partials
   int32_t* part_count;             // [U][max_tokens] arrival counters, 0 between steps
   DevCounters* counters;           // [U] distinct hits / misses, summed over steps
@@ -119,17 +120,17 @@ cudaError_t launch_match(const DeviceState& s, int t, int n_tok, int k, const in
                          int32_t* slot_map, uint8_t* hit, cudaStream_t st);
 size_t victims_smem_bytes(const DeviceState& s);
 cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_t* slot_map,
-                           int hits_first, cudaStream_t st);
+                           cudaStream_t st);
 // Hash-table update of a step (erase evicted ids, insert new ones, rebuild):
 // needed only by the next step's match, so it may run beside the gather and
 // the attention.
-// With place != 0 it first copies the staged rows into their slots; it always
-// empties the step's miss-set cells.
-cudaError_t launch_commit(const DeviceState& s, int place, cudaStream_t st);
+cudaError_t launch_commit(const DeviceState& s, cudaStream_t st);
 cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
 // Staged gather: right after match, the host row of every claimed miss-set
 // cell is copied to kstage/vstage at that cell (no slot needed yet).
 cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st);
+// Staged rows -> their reserved slots (after the gather and the reservation).
+cudaError_t launch_place(const DeviceState& s, int ctas, cudaStream_t st);
 cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,
                               int32_t* slot_map, uint8_t* hit, int ctas, cudaStream_t st);
 

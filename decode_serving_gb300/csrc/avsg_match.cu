@@ -8,8 +8,10 @@
 // Grid (ceil(n_tok*k / 256), U), 256 threads.  Per id:
 //   * range check (id in [0, L)), else BAD_SELECTION;
 //   * lookup in the unit's open-addressed table (linear probing, Fibonacci
-//     hash); a hit writes its slot and sets the token's bit in seen[slot]
-//     (a bit already set means the id repeats within one token's list);
+//     hash); a hit writes its slot (slot map and the internal hit-slot list
+//     the attention over hit rows reads) and sets the token's bit in
+//     seen[slot] (a bit already set means the id repeats within one token's
+//     list);
 //   * a miss is entered in the per-step miss set (one cell per distinct id,
 //     claimed or extended with one compare-and-swap; token bits merged, so a
 //     multi-token iteration reserves each id once); the slot map gets
@@ -73,6 +75,7 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
         const int old = atomicOr(&s.seen[(size_t)u * s.B + slot], (int)bit);
         if (old & bit) raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
         slot_map[off] = slot;
+        s.hslot[off] = slot;
         if (hit) hit[off] = 1;
       } else {
         unsigned long long* ms = s.mset + (size_t)u * s.MS;
@@ -108,6 +111,7 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
         }
         if (miss_cell < 0) raise_error(s.err, AVSG_ERR_CAPACITY, u, pos);  // miss set full
         slot_map[off] = -2 - miss_cell;
+        s.hslot[off] = -1;
         if (hit) hit[off] = 0;
       }
     }

@@ -22,8 +22,7 @@
 // two-pass attention, each token's slots are listed hits first.
 //
 // The hash-table update of the step (commit_kernel below) runs separately:
-// only the next step's match needs it.  It also moves staged rows into their
-// slots and empties the miss set.
+// only the next step's match needs it.
 #include "avsg_internal.cuh"
 
 namespace avsg {
@@ -109,10 +108,9 @@ __host__ __device__ inline VictimsSmem victims_layout(int max_union, int B) {
 constexpr int kBatch = 8;  // 32-slot chunks whose state one warp loads before using it
 
 __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int t, int n_tok,
-                                                              int k, int32_t* __restrict__ slot_map,
-                                                              int hits_first) {
+                                                              int k, int32_t* __restrict__ slot_map) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int s_stop, s_base, s_hits, s_omax, s_tot, s_m;
+  __shared__ int s_stop, s_base, s_hits, s_omax, s_m;
   __shared__ int wsum[kWarps];
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -319,68 +317,24 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   }
   __syncthreads();
 
-  // 6. Resolve slot-map entries of misses (-2 - cell -> reserved slot); with
-  //    hits_first, also list each token's slots hits first (misses from the
-  //    back) and count its hits.  Thread t takes positions t, t + 1024, ...
-  //    of a round (coalesced), issues all its loads first, and one block scan
-  //    of packed (hits << 16 | misses) counts places both lists.
+  // 6. Resolve slot-map entries of misses (-2 - cell -> reserved slot).
+  //    Thread t takes positions t, t + 1024, ... (coalesced) and issues its
+  //    loads before using them.
   const int n = n_tok * k;
-  constexpr int kRun = 4;  // positions per thread per round
-  for (int j = 0; j < n_tok; ++j) {
-    const size_t row0 = (size_t)u * n + (size_t)j * k;
-    int run_h = 0, run_m = 0;
-    for (int c0 = 0; c0 < k; c0 += kThreads * kRun) {
-      int sm[kRun];
+  constexpr int kRun = 4;
+  for (int c0 = 0; c0 < n; c0 += kThreads * kRun) {
+    int sm[kRun];
 #pragma unroll
-      for (int e = 0; e < kRun; ++e) {
-        const int p = c0 + e * kThreads + tid;
-        sm[e] = p < k ? slot_map[row0 + p] : 0;
-      }
-      unsigned hitbits = 0;
-      int nh = 0, nm = 0;
-#pragma unroll
-      for (int e = 0; e < kRun; ++e) {
-        const int p = c0 + e * kThreads + tid;
-        if (p >= k) continue;
-        if (sm[e] <= -2) {
-          const int cell = -2 - sm[e];
-          slot_map[row0 + p] = s.mslot[(size_t)u * s.MS + cell];
-          sm[e] = cell;  // the miss pass reads the staged row of this cell
-          ++nm;
-        } else {
-          hitbits |= 1u << e;
-          ++nh;
-        }
-      }
-      if (hits_first) {
-        const int packed = (nh << 16) | nm;
-        const int incl = warp_incl_scan(packed, lane);
-        if (lane == 31) wsum[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-          const int v = wsum[lane];
-          const int vi = warp_incl_scan(v, lane);
-          wsum[lane] = vi - v;
-          if (lane == 31) s_tot = vi;
-        }
-        __syncthreads();
-        const int before = wsum[warp] + incl - packed;
-        int h = run_h + (before >> 16), mm = run_m + (before & 0xFFFF);
-#pragma unroll
-        for (int e = 0; e < kRun; ++e) {
-          if (c0 + e * kThreads + tid >= k) continue;
-          if ((hitbits >> e) & 1u)
-            s.order[row0 + h++] = sm[e];
-          else
-            s.order[row0 + (k - 1 - mm++)] = sm[e];
-        }
-        const int tot = s_tot;
-        run_h += tot >> 16;
-        run_m += tot & 0xFFFF;
-        __syncthreads();  // wsum and s_tot are reused by the next round
-      }
+    for (int e = 0; e < kRun; ++e) {
+      const int p = c0 + e * kThreads + tid;
+      sm[e] = p < n ? slot_map[(size_t)u * n + p] : 0;
     }
-    if (hits_first && tid == 0) s.nhit[u * kMaxTokens + j] = run_h;
+#pragma unroll
+    for (int e = 0; e < kRun; ++e) {
+      const int p = c0 + e * kThreads + tid;
+      if (p < n && sm[e] <= -2)
+        slot_map[(size_t)u * n + p] = s.mslot[(size_t)u * s.MS + (-2 - sm[e])];
+    }
   }
 
   // 7. Statistics and this step's descriptor range (for the table update).
@@ -394,7 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
 
 // Hash-table update of one unit: erase the ids this step evicted, insert the
 // ids it loaded, rebuild from the tags when erased cells pile up.
-__global__ void __launch_bounds__(kThreads, 1) commit_kernel(DeviceState s, int place) {
+constexpr int kCommitThreads = 256;  // small CTAs: they share SMs with the attention
+
+__global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
   __shared__ int s_stop, s_used, s_rebuild, s_live;
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -408,31 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1) commit_kernel(DeviceState s, int 
   __syncthreads();
   if (s_stop) return;
   const int m = s.dcount[u], base = s.dbase[u];
-  if (place) {  // staged rows -> their slots, 16 bytes per thread per step
-    const int cpk = (int)(s.ek >> 4), cpv = (int)(s.ev >> 4), cpe = cpk + cpv;
-    for (int c = tid; c < m * cpe; c += kThreads) {
-      const int i = c / cpe, w = c - i * cpe;
-      const GatherDesc d = s.desc[base + i];
-      const size_t srow = (size_t)u * s.MS + d.cell, drow = (size_t)u * s.B + d.slot;
-      if (w < cpk)
-        reinterpret_cast<uint4*>(s.kbuf + drow * s.ek)[w] =
-            __ldcg(reinterpret_cast<const uint4*>(s.kstage + srow * s.ek) + w);
-      else
-        reinterpret_cast<uint4*>(s.vbuf + drow * s.ev)[w - cpk] =
-            __ldcg(reinterpret_cast<const uint4*>(s.vstage + srow * s.ev) + (w - cpk));
-    }
-  }
-  unsigned long long* ms = s.mset + (size_t)u * s.MS;
   int2* tab = s.htab + (size_t)u * s.HS;
   const uint32_t hmask = (uint32_t)s.HS - 1u;
-  for (int i = tid; i < m; i += kThreads) {
-    const GatherDesc d = s.desc[base + i];
-    ms[d.cell] = kMissEmpty;  // the miss set starts the next step empty
-    if (d.old_id != kEmpty) hash_erase(tab, hmask, s.hs_shift, d.old_id);
+  for (int i = tid; i < m; i += kCommitThreads) {
+    const int32_t old = s.desc[base + i].old_id;
+    if (old != kEmpty) hash_erase(tab, hmask, s.hs_shift, old);
   }
   __syncthreads();
   int used = 0;
-  for (int i = tid; i < m; i += kThreads) {
+  for (int i = tid; i < m; i += kCommitThreads) {
     const GatherDesc d = s.desc[base + i];
     used += hash_insert(tab, hmask, s.hs_shift, d.id, d.slot, s.err, u);
   }
@@ -448,10 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1) commit_kernel(DeviceState s, int 
   if (s_rebuild) {
     const int B = s.B;
     const size_t ub = (size_t)u * B;
-    for (int i = tid; i < s.HS; i += kThreads) tab[i] = make_int2(kEmpty, kEmpty);
+    for (int i = tid; i < s.HS; i += kCommitThreads) tab[i] = make_int2(kEmpty, kEmpty);
     __syncthreads();
     int live = 0;
-    for (int sl = tid; sl < B; sl += kThreads) {
+    for (int sl = tid; sl < B; sl += kCommitThreads) {
       const int32_t tg = s.tag[ub + sl];
       if (tg != kEmpty) {
         hash_insert(tab, hmask, s.hs_shift, tg, sl, s.err, u);
@@ -472,19 +412,18 @@ int g_victims_smem = 0;
 size_t victims_smem_bytes(const DeviceState& s) { return victims_layout(s.max_union, s.B).total; }
 
 cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_t* slot_map,
-                           int hits_first, cudaStream_t st) {
+                           cudaStream_t st) {
   const size_t smem = victims_smem_bytes(s);
   cudaError_t e = ensure_smem((const void*)victims_kernel, smem, &g_victims_smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(victims_kernel, dim3(s.U), dim3(kThreads), smem, st, s, t, n_tok, k, slot_map,
-                    hits_first);
+  return launch_pdl(victims_kernel, dim3(s.U), dim3(kThreads), smem, st, s, t, n_tok, k, slot_map);
 }
 
-cudaError_t launch_commit(const DeviceState& s, int place, cudaStream_t st) {
+cudaError_t launch_commit(const DeviceState& s, cudaStream_t st) {
   static int attr_done = 0;
   const cudaError_t e = ensure_smem((const void*)commit_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(commit_kernel, dim3(s.U), dim3(kThreads), 0, st, s, place);
+  return launch_pdl(commit_kernel, dim3(s.U), dim3(kCommitThreads), 0, st, s);
 }
 
 }  // namespace avsg

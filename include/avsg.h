@@ -17,9 +17,10 @@
  * reservation covers the union of the tokens' selections (same abstract).
  *
  * Within a step the copy of the misses (bound by the host link) overlaps the
- * attention over the selected rows that were already resident: the library
- * runs the gather and the hash-table update on an internal stream, forked
- * from and joined back into the caller's stream with events.
+ * reservation and the attention over the selected rows that were already
+ * resident: the library runs the gather (into a staging area), the
+ * reservation and the hash-table update on two internal streams, forked from
+ * and joined back into the caller's stream with events.
  *
  * Reservation order (the pages give no formula; this is the reading the
  * library implements): empty slots first, by ascending slot index; then the
@@ -121,7 +122,8 @@ typedef struct avsg_info {
 #define AVSG_KERNEL_ATTENTION 3      /* single pass, or the pass over hit rows */
 #define AVSG_KERNEL_ATTENTION_MISS 4 /* pass over miss rows and the merge */
 #define AVSG_KERNEL_COMMIT 5         /* hash-table update */
-#define AVSG_NUM_KERNELS 6
+#define AVSG_KERNEL_PLACE 6          /* staged missed rows into their slots */
+#define AVSG_NUM_KERNELS 7
 typedef struct avsg_kernel_times {
   double ms[AVSG_NUM_KERNELS];
   uint64_t launches[AVSG_NUM_KERNELS];
