@@ -75,7 +75,7 @@ class avsg_info(ctypes.Structure):
     ]
 
 
-AVSG_NUM_KERNELS = 7
+AVSG_NUM_KERNELS = 6
 
 
 class avsg_kernel_times(ctypes.Structure):
@@ -83,7 +83,7 @@ class avsg_kernel_times(ctypes.Structure):
                 ("launches", ctypes.c_uint64 * AVSG_NUM_KERNELS)]
 
 
-KERNEL_NAMES = ("match", "victims", "gather", "attention", "attention_miss", "commit", "place")
+KERNEL_NAMES = ("match", "victims", "gather", "attention", "attention_miss", "commit")
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32

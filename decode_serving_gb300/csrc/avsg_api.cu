@@ -14,6 +14,8 @@ struct avsg_handle_s {
   avsg_config cfg{};
   DeviceState ds{};
   int device = 0, num_sms = 0, gather_ctas = 0, splits_cap = 0, target_ctas = 0, tile_rows = 0;
+  int stage_ctas = 0;  // CTAs of the staged gather (it shares the GPU with the reservation)
+  int miss_splits = 1;
   void* dev_block = nullptr;
   size_t dev_bytes = 0;
   const void* host_k = nullptr;
@@ -48,10 +50,25 @@ struct avsg_handle_s {
   // caller's stream runs attention over the hit rows
   cudaStream_t side = nullptr, side2 = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_reserve = nullptr, ev_commit = nullptr,
-              ev_place = nullptr;
+              ev_place = nullptr;  // ev_place: the side stream's last work of the step
   bool staged = false;  // staging area allocated: the two-pass pipeline is available
+  bool overlap = false;  // steps run the two-pass pipeline
   unsigned long long* mset_base = nullptr;  // two miss sets, [2][U][MS]
   uint64_t parity = 0;
+  // Captured steps: one CUDA graph per (tokens, k, miss set), re-pointed at
+  // each step by updating its first kernel node (see StepIO).
+  struct StepGraph {
+    int n_tok = 0, k = 0, par = 0;
+    DeviceState sc{};           // the state the first kernel was captured with
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    cudaGraphNode_t first = nullptr;
+    cudaKernelNodeParams kp{};  // function and launch shape of the first node
+    uint64_t used = 0;
+  };
+  std::vector<StepGraph> graphs;
+  uint64_t graph_clock = 0;
+  cudaStream_t cap = nullptr;  // capture origin
 };
 
 namespace {
@@ -124,6 +141,11 @@ int map_host(avsg_handle h, const void* p, size_t bytes, const unsigned char** d
 
 void release(avsg_handle h) {
   if (!h) return;
+  for (auto& g : h->graphs) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+  }
+  if (h->cap) cudaStreamDestroy(h->cap);
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
   for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_reserve, h->ev_commit, h->ev_place})
     if (e) cudaEventDestroy(e);
@@ -133,6 +155,22 @@ void release(avsg_handle h) {
   if (h->reg_k && h->host_k) cudaHostUnregister(const_cast<void*>(h->host_k));
   if (h->reg_v && h->host_v) cudaHostUnregister(const_cast<void*>(h->host_v));
   delete h;
+}
+
+// CTAs per (unit, token) of the two attention passes: the hit pass fills
+// about two CTAs per SM; the miss pass scans at most kMissScanMax miss-set
+// cells per CTA (and at least AVSG_MISS_SPLITS CTAs); together they stay
+// within what one merge takes.
+void two_pass_splits(const avsg_handle h, int n_tok, int* splits_h, int* splits_m) {
+  const DeviceState& s = h->ds;
+  const int pairs = s.U * n_tok;
+  int sm = s.MS > kMissScanMax ? s.MS / kMissScanMax : 1;
+  while (sm < h->miss_splits && s.MS / sm > 2) sm *= 2;
+  int sh = 2 * h->num_sms / pairs > 0 ? 2 * h->num_sms / pairs : 1;
+  const int cap = attention_tc_max_segments(s.D, s.G, s.kv_shared);
+  if (sh + sm > cap) sh = cap - sm > 1 ? cap - sm : 1;
+  *splits_h = sh;
+  *splits_m = sm;
 }
 
 // Splits of a (unit, token)'s entries over CTAs: about target_ctas CTAs in all,
@@ -174,6 +212,11 @@ bool attention_tc_enabled() {
 
 bool overlap_enabled() {
   static const int on = env_int_any("AVSG_OVERLAP", 1);
+  return on != 0;
+}
+
+bool graphs_enabled() {
+  static const int on = env_int_any("AVSG_GRAPH", 1);
   return on != 0;
 }
 
@@ -280,6 +323,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   h->tile_rows = attention_rows_per_tile(s.D, s.DV, s.G, s.kv_shared);
   h->target_ctas = h->num_sms * env_int("AVSG_ATTN_CTAS_PER_SM", 4);
   h->gather_ctas = h->num_sms * env_int("AVSG_GATHER_CTAS_PER_SM", 4);
+  h->stage_ctas = env_int("AVSG_STAGE_CTAS", h->num_sms * 2 / 5);
+  h->miss_splits = env_int("AVSG_MISS_SPLITS", 2);  // at least this many miss-pass CTAs per pair
   {
     int64_t cap = (h->target_ctas + U - 1) / U;
     const int64_t by_rows = ((int64_t)c.max_select * c.entry_tokens + h->tile_rows - 1) / h->tile_rows;
@@ -317,6 +362,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.mslot, st_arrays ? (size_t)U * s.MS : 0);
   cv.take(&s.desc, (size_t)U * max_union);
   cv.take(&s.desc_count, 1);
+  cv.take(&s.io, 1);
   cv.take(&s.dbase, (size_t)U);
   cv.take(&s.dcount, (size_t)U);
 
@@ -326,13 +372,14 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     size_t two = 0;  // two-pass attention: pairs * (hit splits + miss splits)
     for (int nt = 1; nt <= c.max_tokens_per_step; ++nt) {
       const int pairs = (int)U * nt;
-      const int sh = 2 * h->num_sms / pairs > 0 ? 2 * h->num_sms / pairs : 1;
-      const int sm = sh > (s.MS + kMissListMax - 1) / kMissListMax ? sh : (s.MS + kMissListMax - 1) / kMissListMax;
+      int sh = 0, sm = 0;
+      two_pass_splits(h, nt, &sh, &sm);
       const size_t need = (size_t)pairs * (sh + sm) * s.G * (s.DV + 2);
       two = need > two ? need : two;
     }
     h->part_floats = part > tc ? part : tc;
     h->part_floats = h->part_floats > two ? h->part_floats : two;
+    h->overlap = h->staged && overlap_enabled() && attention_tc_enabled();
     cv.take(&s.part, h->part_floats);
   }
   cv.take(&s.part_count, (size_t)U * kMaxTokens);
@@ -352,7 +399,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   void* b = h->dev_block;
   rebase(&s.kbuf, b); rebase(&s.vbuf, b); rebase(&s.tag, b); rebase(&s.last, b);
   rebase(&s.kstage, b); rebase(&s.vstage, b);
-  rebase(&s.seen, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.mset, b);
+  rebase(&s.seen, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.io, b);
   rebase(&s.mslot, b); rebase(&s.desc, b);
   rebase(&s.desc_count, b); rebase(&s.part, b);
   rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&h->mset_base, b); rebase(&s.hslot, b);
@@ -365,8 +412,15 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     s.vstage = s.kstage;
   }
 
-  e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side2, cudaStreamNonBlocking);
+  // The side streams get the highest priority: when match ends, the CTAs of
+  // the gather and the reservation are placed before those of the attention.
+  int prio_low = 0, prio_high = 0;
+  e = cudaDeviceGetStreamPriorityRange(&prio_low, &prio_high);
+  if (e == cudaSuccess)
+    e = cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, prio_high);
+  if (e == cudaSuccess)
+    e = cudaStreamCreateWithPriority(&h->side2, cudaStreamNonBlocking, prio_high);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking);
   for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_gather, &h->ev_reserve, &h->ev_commit, &h->ev_place})
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
@@ -426,6 +480,162 @@ struct Prof {
   }
 };
 
+// Enqueues the kernels of one step on st (and the side streams, forked from
+// and joined back into st).  par selects the miss set the step fills; the
+// step's pointers come in v.  With first != null (capture), returns the
+// graph node of the first kernel there.
+int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& v,
+                cudaStream_t st, DeviceState* sc_out, cudaGraphNode_t* first) {
+  const DeviceState& s = h->ds;
+  cudaError_t e;
+  AttnLaunch a{};
+  a.n_tok = n_tok;
+  a.k = k;
+  a.splits = attn_splits(h, n_tok, k);
+  a.identity_slots = h->no_reuse ? 1 : 0;
+  a.scale_log2 = h->scale_log2;
+  a.q = v.q;
+  a.out = v.out;
+  a.slot_map = v.slot_map;
+  a.io = s.io;
+  a.num_sms = h->num_sms;
+  a.part_capacity = h->part_floats;
+  Prof pf{h};
+#define AVSG_RUN(kernel_index, stream, call) \
+  do {                                       \
+    pf.begin(kernel_index, stream);          \
+    e = (call);                              \
+    if (e != cudaSuccess) return fail_cuda(h, e); \
+    pf.end(stream);                          \
+  } while (0)
+  // The graph node of the kernel just captured on st.
+  auto take_first = [&]() -> cudaError_t {
+    if (!first) return cudaSuccess;
+    cudaStreamCaptureStatus cs;
+    const cudaGraphNode_t* deps = nullptr;
+    size_t nd = 0;
+    cudaError_t ce = cudaStreamGetCaptureInfo(st, &cs, nullptr, nullptr, &deps, nullptr, &nd);
+    if (ce == cudaSuccess && (cs != cudaStreamCaptureStatusActive || nd != 1))
+      ce = cudaErrorStreamCaptureInvalidated;
+    if (ce == cudaSuccess) *first = deps[0];
+    return ce;
+  };
+  DeviceState sc = s;
+  const size_t set_cells = (size_t)s.U * s.MS;
+  sc.mset = h->mset_base + (size_t)par * set_cells;
+  if (sc_out) *sc_out = sc;
+  if (h->no_reuse) {
+    AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather_all(sc, v, n_tok, k, h->gather_ctas, st));
+    e = take_first();
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(sc, a, st));
+    return AVSG_OK;
+  }
+  AVSG_RUN(AVSG_KERNEL_MATCH, st, launch_match(sc, v, n_tok, k, st));
+  e = take_first();
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  if (!h->overlap) {
+    AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(sc, n_tok, k, st));
+    AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(sc, h->gather_ctas, st));
+    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(sc, st));
+    AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(sc, a, st));
+    e = cudaMemsetAsync(sc.mset, 0xFF, set_cells * 8, st);  // the miss set starts empty
+    return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
+  }
+  // Two-pass pipeline (the tensor-core shapes).  After match, three
+  // streams run side by side:
+  //   st:     attention over the hit rows (their slots are known);
+  //   side:   the missed rows, host -> staging area (host link), then the
+  //           other miss set (the previous step's) is emptied;
+  //   side2:  the reservation, then the hash-table update.
+  // The attention over the missed rows (read from staging) follows the
+  // gather and the reservation, and stores each staged row into its slot.
+  int splits_h = 0, splits_m = 0;
+  two_pass_splits(h, n_tok, &splits_h, &splits_m);
+  e = cudaEventRecord(h->ev_fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side2, h->ev_fork, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_GATHER, h->side, launch_gather_stage(sc, h->stage_ctas, h->side));
+  e = cudaEventRecord(h->ev_gather, h->side);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_RESERVE, h->side2, launch_victims(sc, n_tok, k, h->side2));
+  e = cudaEventRecord(h->ev_reserve, h->side2);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_COMMIT, h->side2, launch_commit(sc, h->side2));
+  e = cudaEventRecord(h->ev_commit, h->side2);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  e = cudaMemsetAsync(h->mset_base + (size_t)(par ^ 1) * set_cells, 0xFF, set_cells * 8, h->side);
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_place, h->side);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_ATTENTION, st,
+           launch_attention_tc_pass(sc, a, 0, splits_h, splits_m, nullptr, st));
+  e = cudaStreamWaitEvent(st, h->ev_gather, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_reserve, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  DeviceState staged = sc;  // miss rows are read from the staging area, by cell
+  staged.kbuf = s.kstage;
+  staged.vbuf = s.vstage;
+  staged.B = s.MS;
+  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, st,
+           launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, &sc, st));
+  e = cudaStreamWaitEvent(st, h->ev_place, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_commit, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+#undef AVSG_RUN
+  return AVSG_OK;
+}
+
+constexpr size_t kMaxGraphs = 16;
+
+// The captured step for (n_tok, k, par), captured now if it is not cached
+// (the least recently used one is dropped beyond kMaxGraphs).
+int step_graph(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& v,
+               avsg_handle_s::StepGraph** out) {
+  h->graph_clock += 1;
+  for (auto& g : h->graphs)
+    if (g.n_tok == n_tok && g.k == k && g.par == par) {
+      g.used = h->graph_clock;
+      *out = &g;
+      return AVSG_OK;
+    }
+  if (h->graphs.size() >= kMaxGraphs) {
+    size_t lru = 0;
+    for (size_t i = 1; i < h->graphs.size(); ++i)
+      if (h->graphs[i].used < h->graphs[lru].used) lru = i;
+    cudaGraphExecDestroy(h->graphs[lru].exec);
+    cudaGraphDestroy(h->graphs[lru].graph);
+    h->graphs.erase(h->graphs.begin() + (long)lru);
+  }
+  avsg_handle_s::StepGraph g;
+  g.n_tok = n_tok;
+  g.k = k;
+  g.par = par;
+  cudaError_t e = cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  const int rc = enqueue_dag(h, n_tok, k, par, v, h->cap, &g.sc, &g.first);
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(h->cap, &graph);
+  if (rc != AVSG_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (e == cudaSuccess) e = cudaGraphKernelNodeGetParams(g.first, &g.kp);
+  if (e == cudaSuccess)
+    e = cudaGraphInstantiateWithFlags(&g.exec, graph, cudaGraphInstantiateFlagUseNodePriority);
+  if (e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    return fail_cuda(h, e);
+  }
+  g.graph = graph;
+  g.kp.kernelParams = nullptr;
+  g.kp.extra = nullptr;
+  g.used = h->graph_clock;
+  h->graphs.push_back(g);
+  *out = &h->graphs.back();
+  return AVSG_OK;
+}
+
 int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32_t* d_sel,
                  const float* d_q, float* d_out, int32_t* d_slot_map, uint8_t* d_hit,
                  cudaStream_t st) {
@@ -440,95 +650,31 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
     e = cudaMemsetAsync(d_out, 0, (size_t)s.U * n_tok * s.G * s.DV * sizeof(float), st);
     return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
   }
-  int32_t* slot_map = d_slot_map ? d_slot_map : h->slot_scratch;
-  AttnLaunch a{};
-  a.n_tok = n_tok;
-  a.k = k;
-  a.splits = attn_splits(h, n_tok, k);
-  a.identity_slots = h->no_reuse ? 1 : 0;
-  a.scale_log2 = h->scale_log2;
-  a.q = d_q;
-  a.out = d_out;
-  a.slot_map = slot_map;
-  a.num_sms = h->num_sms;
-  a.part_capacity = h->part_floats;
-  Prof pf{h};
-#define AVSG_RUN(kernel_index, stream, call) \
-  do {                                       \
-    pf.begin(kernel_index, stream);          \
-    e = (call);                              \
-    if (e != cudaSuccess) return fail_cuda(h, e); \
-    pf.end(stream);                          \
-  } while (0)
-  if (h->no_reuse) {
-    AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather_all(s, n_tok, k, d_sel, slot_map, d_hit, h->gather_ctas, st));
-    h->host_misses += (uint64_t)s.U * n_tok * k;
-    AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(s, a, st));
-    return AVSG_OK;
-  }
-  // Two-pass pipeline (the tensor-core shapes).  After match, three
-  // streams run side by side:
-  //   caller's stream: attention over the hit rows (their slots are known);
-  //   side stream:     the missed rows, host -> staging area (host link);
-  //   side stream 2:   the reservation, then the hash-table update.
-  // The attention over the missed rows (read from staging) follows the
-  // gather and the reservation; the staged rows are then placed into their
-  // slots, and the other step's miss set is emptied, on the side stream.
-  // The two miss sets alternate by step.
-  const int pairs = s.U * n_tok;
-  const int resident = 2 * h->num_sms;
-  const int splits_h = resident / pairs > 0 ? resident / pairs : 1;
-  const int min_m = (s.MS + kMissListMax - 1) / kMissListMax;
-  const int splits_m = splits_h > min_m ? splits_h : min_m;
-  const bool overlap =
-      h->staged && overlap_enabled() && attention_tc_enabled() &&
-      (size_t)pairs * (splits_h + splits_m) * s.G * (s.DV + 2) <= h->part_floats;
-  DeviceState sc = s;
-  const size_t set_cells = (size_t)s.U * s.MS;
-  sc.mset = h->mset_base + (h->parity & 1) * set_cells;  // the set that is empty now
-  AVSG_RUN(AVSG_KERNEL_MATCH, st, launch_match(sc, t, n_tok, k, d_sel, slot_map, d_hit, st));
-  if (!overlap) {
-    AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(sc, t, n_tok, k, slot_map, st));
-    AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(sc, h->gather_ctas, st));
-    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(sc, st));
-    AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(sc, a, st));
-    e = cudaMemsetAsync(sc.mset, 0xFF, set_cells * 8, st);  // the miss set starts empty
-    return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
-  }
-  h->parity += 1;
-  e = cudaEventRecord(h->ev_fork, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side2, h->ev_fork, 0);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_GATHER, h->side, launch_gather_stage(sc, h->gather_ctas, h->side));
-  e = cudaEventRecord(h->ev_gather, h->side);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_RESERVE, h->side2, launch_victims(sc, t, n_tok, k, slot_map, h->side2));
-  e = cudaEventRecord(h->ev_reserve, h->side2);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_COMMIT, h->side2, launch_commit(sc, h->side2));
-  e = cudaEventRecord(h->ev_commit, h->side2);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, splits_h, splits_m, st));
-  e = cudaStreamWaitEvent(st, h->ev_gather, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_reserve, 0);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  DeviceState staged = sc;  // miss rows are read from the staging area, by cell
-  staged.kbuf = s.kstage;
-  staged.vbuf = s.vstage;
-  staged.B = s.MS;
-  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, st,
-           launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, st));
-  e = cudaStreamWaitEvent(h->side, h->ev_reserve, 0);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_PLACE, h->side, launch_place(sc, h->gather_ctas, h->side));
-  e = cudaMemsetAsync(h->mset_base + ((h->parity & 1) * set_cells), 0xFF, set_cells * 8, h->side);
-  if (e == cudaSuccess) e = cudaEventRecord(h->ev_place, h->side);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_place, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_commit, 0);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-#undef AVSG_RUN
-  return AVSG_OK;
+  if (h->no_reuse) h->host_misses += (uint64_t)s.U * n_tok * k;
+  StepIO v{};
+  v.sel = d_sel;
+  v.q = d_q;
+  v.out = d_out;
+  v.slot_map = d_slot_map ? d_slot_map : h->slot_scratch;
+  v.hit = d_hit;
+  v.t = t;
+  // The two-pass pipeline alternates miss sets (each step empties the
+  // other); the serial order empties its one set at the end of the step.
+  const int par = h->overlap && !h->no_reuse ? (int)(h->parity & 1) : 0;
+  if (h->overlap && !h->no_reuse) h->parity += 1;
+  if (h->prof || !graphs_enabled())
+    return enqueue_dag(h, n_tok, k, par, v, st, nullptr, nullptr);
+  avsg_handle_s::StepGraph* g = nullptr;
+  const int rc = step_graph(h, n_tok, k, par, v, &g);
+  if (rc != AVSG_OK) return rc;
+  DeviceState sc = g->sc;
+  int32_t nt = n_tok, kk = k;
+  void* args[] = {&sc, &v, &nt, &kk};  // (DeviceState, StepIO, n_tok, k): match or gather_all
+  cudaKernelNodeParams kp = g->kp;
+  kp.kernelParams = args;
+  e = cudaGraphExecKernelNodeSetParams(g->exec, g->first, &kp);
+  if (e == cudaSuccess) e = cudaGraphLaunch(g->exec, st);
+  return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
 }
 
 int check_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k) {

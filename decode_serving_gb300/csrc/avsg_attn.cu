@@ -102,6 +102,12 @@ __global__ void __launch_bounds__(SH::NT) attn_kernel(DeviceState s, AttnLaunch 
   const int sp = blockIdx.x, u = blockIdx.y, tok = blockIdx.z;
   griddep_wait();
   griddep_launch();
+  if (a.io) {  // this step's q, out and slot map
+    const StepIO io = load_io(a.io);
+    a.q = io.q;
+    a.out = io.out;
+    a.slot_map = io.slot_map;
+  }
   if (tid == 0) s_stop = load_err(s.err);
   if (tid < G) {
     mrun[tid] = -INFINITY;

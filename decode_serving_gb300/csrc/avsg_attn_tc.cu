@@ -41,8 +41,9 @@ constexpr int kThreadsTc = kWarpsTc * 32;
 constexpr int kTileRows = 16;
 constexpr int kStages = 3;
 constexpr int kCtasPerSm = 2;
-constexpr int kListMax = kMissListMax;
-constexpr int kListPerThread = kListMax / kThreadsTc;
+constexpr int kScanMax = kMissScanMax;          // miss-set cells one miss-pass CTA scans
+constexpr int32_t kPlaceBit = (int32_t)0x80000000;
+constexpr int32_t kCellMask = 0x7FFFFFFF;
 
 template <int D_, int G_, bool SHARED_>
 struct TcShape {
@@ -61,6 +62,10 @@ struct TcShape {
                                                                    : MERGE_BYTES) + 128;
   static_assert(D % 16 == 0 && (G == 1 || G == 2 || G == 4 || G == 8), "unsupported shape");
   static_assert(WARP_BYTES % 16 == 0, "alignment");
+  // Most partials one merge takes: the four warps' outputs, the CTA's own
+  // and 2 floats per partial and head must fit in the warps' staging.
+  static constexpr int MAX_SEG = (kWarpsTc * WARP_BYTES / 4 - (kWarpsTc + 1) * G * D) / (2 * G);
+  static_assert(MAX_SEG >= 16, "merge scratch");
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -130,6 +135,13 @@ struct TcParams {
   const float* q;
   float* out;
   const int32_t* slots;         // [pairs][k] slot of each listed entry
+  const StepIO* io;             // when set, q and out (and slots, single pass) come from here
+  // miss pass: rows are read from the staging area and also stored into
+  // their reserved slots: place_k/place_v rows (unit * place_B + slot) * ET + sub
+  unsigned char* place_k;
+  unsigned char* place_v;
+  int place_B;
+  const int32_t* mslot;         // [U][MS] reserved slot of each miss-set cell
   // persistent single pass
   int rows_per_pair, tiles_per_pair;
   long long tiles;              // all pairs
@@ -143,7 +155,8 @@ struct SegArgs {
   int ent_base;                 // first listed entry of the range
   int rows;                     // rows of the range (entries * ET)
   int ta, tb;                   // this CTA's tiles [ta, tb) of the range
-  const int32_t* list;          // when set: slot of entry e is list[e] (shared memory)
+  const int32_t* list;          // when set: entry e is list[e] & kCellMask (shared memory);
+                                // bit 31 set: this pass stores the row into its slot
 };
 
 // CTA c covers global tiles [c*T/C, (c+1)*T/C); the CTA holding tile x:
@@ -226,7 +239,7 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
     if (i >= n_my || row >= a.rows) return -1;
     const int ent = a.ent_base + (p.ET == 1 ? row : row / p.ET);
     const int sub = row - (ent - a.ent_base) * p.ET;
-    const int slot = a.list ? a.list[ent]
+    const int slot = a.list ? (a.list[ent] & kCellMask)
                    : p.identity ? tok * p.k + ent
                                 : __ldg(p.slots + (size_t)pair * p.k + ent);
     if (slot < 0) return -1;  // not a row of this pass (a miss in the pass over hit rows)
@@ -235,6 +248,23 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
   constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
   constexpr int RPI = 32 / CPR;    // rows per warp instruction
   unsigned long long vmasks = 0;  // 16 bits per stage: which rows of the staged tile are real
+  // Miss pass: for row (lane & 15) of the next three tiles (in order), the
+  // reserved slot (loaded when the tile is issued, used after it is
+  // consumed) and the row's sub-index, or -1 when this pass does not store it.
+  const bool place = p.place_k != nullptr;
+  int pslot[kStages], psub[kStages];
+#pragma unroll
+  for (int i = 0; i < kStages; ++i) pslot[i] = psub[i] = -1;
+  auto place_info = [&](int i, int& slot, int& sub) {
+    slot = sub = -1;
+    const int row = (a.ta + warp + i * kWarpsTc) * kTileRows + (lane & 15);
+    if (!place || i >= n_my || row >= a.rows) return;
+    const int ent = a.ent_base + (p.ET == 1 ? row : row / p.ET);
+    const int e = a.list[ent];
+    if (!(e & kPlaceBit)) return;
+    slot = __ldcg(p.mslot + (size_t)u * s.MS + (e & kCellMask));
+    sub = row - (ent - a.ent_base) * p.ET;
+  };
   auto issue = [&](long long myrow, int st) {
     const unsigned long long vm = __ballot_sync(0xffffffffu, myrow >= 0) & 0xFFFFu;
     vmasks = (vmasks & ~(0xFFFFull << (16 * st))) | (vm << (16 * st));
@@ -261,6 +291,9 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
 #pragma unroll
     for (int i = 0; i < kStages; ++i) issue(first_rows[i], i);
     next_row = first_rows[kStages];
+    if (place)
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) place_info(i, pslot[i], psub[i]);
   }
   for (int i = 0; i < n_my; ++i) {
     const int st = i % kStages;
@@ -388,6 +421,30 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
         for (int nt = 0; nt < NTN; ++nt) mma_bf16(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
       }
     }
+    if (place) {  // the tile's rows that this pass owns -> their reserved slots
+      const long long drow =
+          (pslot[0] >= 0 && psub[0] >= 0) ? ((long long)u * p.place_B + pslot[0]) * p.ET + psub[0] : -1;
+      const int ch = lane % CPR, rsub = lane / CPR;
+#pragma unroll
+      for (int it = 0; it < kTileRows / RPI; ++it) {
+        const int r = it * RPI + rsub;
+        const long long dr = __shfl_sync(0xffffffffu, drow, r);
+        if (dr >= 0) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(kst + r * PITCH + ch * 16);
+          *reinterpret_cast<uint4*>(p.place_k + dr * (2 * D) + ch * 16) = kv;
+          if (!SH::SHARED) {
+            const uint4 vv = *reinterpret_cast<const uint4*>(vst + r * PITCH + ch * 16);
+            *reinterpret_cast<uint4*>(p.place_v + dr * (2 * D) + ch * 16) = vv;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j + 1 < kStages; ++j) {
+        pslot[j] = pslot[j + 1];
+        psub[j] = psub[j + 1];
+      }
+      place_info(i + kStages, pslot[kStages - 1], psub[kStages - 1]);
+    }
     __syncwarp();  // every lane has read stage st
     issue(next_row, st);
     next_row = row_index(i + kStages + 1);
@@ -458,30 +515,60 @@ __device__ __forceinline__ void tc_write_partial(float* pp, const float* cm, con
   }
 }
 
-// Merges nseg partials of a pair into its output (run by one CTA).
+// Merges nseg partials of a pair into its output (run by one CTA).  Every
+// partial's (m, l) is loaded at once; the weighted sum of the output rows
+// then takes one round of loads per four partials.  wseg: 2 * nseg * G floats
+// of shared memory.
 template <int G, int D>
 __device__ void tc_merge_partials(const float* pbase, int nseg, float* out, float* wseg) {
+  constexpr int R = (G * D + kThreadsTc - 1) / kThreadsTc;  // outputs per thread
+  constexpr int QB = 4;                                     // partials per round of loads
   const size_t stride = (size_t)G * (D + 2);
   const int tid = threadIdx.x;
-  if (tid < G) {  // weight of every partial per head, normalised
-    float M = -INFINITY, L = 0.f;
-    for (int q2 = 0; q2 < nseg; ++q2) M = fmaxf(M, __ldcg(pbase + q2 * stride + tid));
-    for (int q2 = 0; q2 < nseg; ++q2) {
-      const float e = M == -INFINITY ? 0.f : exp2f(__ldcg(pbase + q2 * stride + tid) - M);
-      wseg[q2 * G + tid] = e;
-      L = fmaf(__ldcg(pbase + q2 * stride + G + tid), e, L);
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int q2 = 0; q2 < nseg; ++q2) wseg[q2 * G + tid] *= inv;
+  float* wm = wseg;             // [nseg][G]: m, then the normalised weight
+  float* wl = wseg + nseg * G;  // [nseg][G]: l
+  for (int i = tid; i < nseg * G; i += kThreadsTc) {
+    const int q2 = i / G, h = i - q2 * G;
+    wm[i] = __ldcg(pbase + q2 * stride + h);
+    wl[i] = __ldcg(pbase + q2 * stride + G + h);
   }
   __syncthreads();
-  for (int o = tid; o < G * D; o += kThreadsTc) {
-    const int head = o / D;
-    float O = 0.f;
-#pragma unroll 8
-    for (int q2 = 0; q2 < nseg; ++q2)
-      O = fmaf(__ldcg(pbase + q2 * stride + 2 * G + o), wseg[q2 * G + head], O);
-    out[o] = O;
+  if (tid < G) {
+    float M = -INFINITY, L = 0.f;
+    for (int q2 = 0; q2 < nseg; ++q2) M = fmaxf(M, wm[q2 * G + tid]);
+    for (int q2 = 0; q2 < nseg; ++q2) {
+      const float e = M == -INFINITY ? 0.f : exp2f(wm[q2 * G + tid] - M);
+      wm[q2 * G + tid] = e;
+      L = fmaf(wl[q2 * G + tid], e, L);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int q2 = 0; q2 < nseg; ++q2) wm[q2 * G + tid] *= inv;
+  }
+  __syncthreads();
+  float O[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) O[r] = 0.f;
+  for (int q0 = 0; q0 < nseg; q0 += QB) {
+    float v[QB][R];
+#pragma unroll
+    for (int j = 0; j < QB; ++j)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int o = tid + r * kThreadsTc;
+        v[j][r] = (q0 + j < nseg && o < G * D) ? __ldcg(pbase + (q0 + j) * stride + 2 * G + o) : 0.f;
+      }
+#pragma unroll
+    for (int j = 0; j < QB; ++j)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int o = tid + r * kThreadsTc;
+        if (q0 + j < nseg && o < G * D) O[r] = fmaf(v[j][r], wm[(q0 + j) * G + o / D], O[r]);
+      }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int o = tid + r * kThreadsTc;
+    if (o < G * D) out[o] = O[r];
   }
 }
 
@@ -496,6 +583,12 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
   const int tid = threadIdx.x;
   griddep_wait();
   griddep_launch();
+  if (p.io) {  // this step's q, out and slot map
+    const StepIO io = load_io(p.io);
+    p.q = io.q;
+    p.out = io.out;
+    p.slots = io.slot_map;
+  }
   if (tid == 0) s_stop = load_err(s.err);
   __syncthreads();
   if (s_stop) return;
@@ -548,84 +641,159 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
   }
 }
 
-// Two passes over the hit-first slot lists: pass 0 over each (unit, token)'s
-// hit rows (it may run while the misses are still being copied in), pass 1
-// over its miss rows; the last pass-1 CTA of a pair merges both passes.
+// Hit pass: every selected position of a (unit, token), with the hit slots
+// that match wrote (a miss has slot -1 and is masked); runs while the missed
+// rows are still crossing the host link.  CTA (sp, pair) takes an equal
+// share of the pair's tiles and writes partial sp of the pair.
 template <class SH>
-__global__ void __launch_bounds__(kThreadsTc) attn_tc_pass_kernel(DeviceState s, TcParams p,
-                                                                  int pass) {
+__global__ void __launch_bounds__(kThreadsTc) attn_tc_hits_kernel(DeviceState s, TcParams p) {
   constexpr int D = SH::D, G = SH::G;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
   __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G], cm[G], cl[G];
-  __shared__ int s_stop, s_last, s_wcnt[kWarpsTc];
+  __shared__ int s_stop;
   const int tid = threadIdx.x;
   griddep_wait();
   griddep_launch();
+  if (p.io) {  // this step's q and out (slots: the hit slots of match)
+    const StepIO io = load_io(p.io);
+    p.q = io.q;
+    p.out = io.out;
+  }
   if (tid == 0) s_stop = load_err(s.err);
-  __syncthreads();
+  tc_zero_staging<SH>(smem);  // (its barrier also publishes s_stop)
   if (s_stop) return;
-  tc_zero_staging<SH>(smem);
   float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
 
   const int sp = blockIdx.x, pair = blockIdx.y;
-  const int lane = tid & 31, warp = tid >> 5;
   SegArgs a;
   a.pair = pair;
   a.u = pair / p.n_tok;
   a.tok = pair - a.u * p.n_tok;
   a.ent_base = 0;
   a.list = nullptr;
-  if (pass == 0) {  // every selected position; misses masked (their hit slot is -1)
-    a.rows = p.k * p.ET;
-    const int tiles = (a.rows + kTileRows - 1) / kTileRows;
-    a.ta = (int)((long long)sp * tiles / p.splits_h);
-    a.tb = (int)((long long)(sp + 1) * tiles / p.splits_h);
-  } else {  // this CTA's share of the unit's miss-set cells that carry the token
-    int32_t* list = reinterpret_cast<int32_t*>(smem + kWarpsTc * SH::WARP_BYTES);
-    const int c_lo = (int)((long long)sp * s.MS / p.splits_m);
-    const int c_hi = (int)((long long)(sp + 1) * s.MS / p.splits_m);
-    const unsigned long long* msu = s.mset + (size_t)a.u * s.MS;
-    const unsigned long long tokbit = 1ull << (32 + a.tok);
-    bool take[kListPerThread];
-#pragma unroll
-    for (int e = 0; e < kListPerThread; ++e) {
-      const int cell = c_lo + e * kThreadsTc + tid;
-      const unsigned long long w = cell < c_hi ? __ldcg(msu + cell) : kMissEmpty;
-      take[e] = w != kMissEmpty && (w & tokbit);
-    }
-    int nlist = 0;
-#pragma unroll
-    for (int e = 0; e < kListPerThread; ++e) {  // in cell order, deterministic
-      const unsigned bal = __ballot_sync(0xffffffffu, take[e]);
-      if (lane == 0) s_wcnt[warp] = __popc(bal);
-      __syncthreads();
-      int before = nlist;
-      for (int w2 = 0; w2 < warp; ++w2) before += s_wcnt[w2];
-      if (take[e]) list[before + __popc(bal & ((1u << lane) - 1u))] = c_lo + e * kThreadsTc + tid;
-      for (int w2 = 0; w2 < kWarpsTc; ++w2) nlist += s_wcnt[w2];
-      __syncthreads();
-    }
-    a.list = list;
-    a.rows = nlist * p.ET;
-    a.ta = 0;
-    a.tb = (a.rows + kTileRows - 1) / kTileRows;
+  a.rows = p.k * p.ET;
+  const int tiles = (a.rows + kTileRows - 1) / kTileRows;
+  a.ta = (int)((long long)sp * tiles / p.splits_h);
+  a.tb = (int)((long long)(sp + 1) * tiles / p.splits_h);
+  tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
+  const size_t stride = (size_t)G * (D + 2);
+  float* pbase = s.part + (size_t)pair * (p.splits_h + p.splits_m) * stride;
+  tc_write_partial<G, D>(pbase + (size_t)sp * stride, cm, cl, co);
+}
+
+// Miss pass: CTA (sp, pair) copies its range of the unit's miss set into
+// shared memory (one round of 16-byte async copies), lists the claimed cells
+// that carry this token (a fixed order: by thread, then by stride), attends
+// over their rows in the staging area, and stores every row whose lowest
+// token is this one into its reserved slot.  With one CTA per pair it then
+// merges its result with the hit pass's partials and writes the output;
+// otherwise the last CTA of the pair does.  `s` is the staged view of the
+// state: kbuf/vbuf are the staging rows and B the miss-set capacity.
+template <class SH>
+__global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s, TcParams p) {
+  constexpr int D = SH::D, G = SH::G;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+  int32_t* list = reinterpret_cast<int32_t*>(smem + kWarpsTc * SH::WARP_BYTES);  // [kScanMax]
+  unsigned long long* cells = reinterpret_cast<unsigned long long*>(list + kScanMax);
+  __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G], cm[G], cl[G];
+  __shared__ int s_stop, s_last, s_wsum[kWarpsTc];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sp = blockIdx.x, pair = blockIdx.y;
+  const int u = pair / p.n_tok, tok = pair - u * p.n_tok;
+  const int span = s.MS / p.splits_m;  // both powers of two, span <= kScanMax
+  const int c_lo = sp * span;
+  griddep_wait();
+  griddep_launch();
+  {
+    const unsigned long long* src = s.mset + (size_t)u * s.MS + c_lo;
+    for (int i = tid; i < span / 2; i += kThreadsTc) cp_async16(cells + 2 * i, src + 2 * i);
+    cp_async_commit();
   }
+  if (p.io) {
+    const StepIO io = load_io(p.io);
+    p.q = io.q;
+    p.out = io.out;
+  }
+  if (tid == 0) s_stop = load_err(s.err);
+  tc_zero_staging<SH>(smem);
+  cp_async_wait<0>();
+  __syncthreads();
+  if (s_stop) return;
+
+  // cells tid, tid + 128, ... of the range: those carrying this token, in a
+  // fixed order (thread, then stride); bit 31 marks the lowest token of a cell
+  const unsigned long long tokbit = 1ull << (32 + tok);
+  const unsigned long long below = (tokbit - 1ull) & ~0xFFFFFFFFull;  // lower tokens' bits
+  int cnt = 0;
+  for (int c0 = tid; c0 < span; c0 += 8 * kThreadsTc) {
+    unsigned long long w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + j * kThreadsTc;
+      w[j] = c < span ? cells[c] : kMissEmpty;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cnt += (w[j] != kMissEmpty && (w[j] & tokbit)) ? 1 : 0;
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int base = incl - cnt, nlist = 0;
+#pragma unroll
+  for (int w2 = 0; w2 < kWarpsTc; ++w2) {
+    base += w2 < warp ? s_wsum[w2] : 0;
+    nlist += s_wsum[w2];
+  }
+  for (int c0 = tid; c0 < span; c0 += 8 * kThreadsTc) {
+    unsigned long long w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + j * kThreadsTc;
+      w[j] = c < span ? cells[c] : kMissEmpty;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (w[j] != kMissEmpty && (w[j] & tokbit))
+        list[base++] = (c_lo + c0 + j * kThreadsTc) | ((w[j] & below) ? 0 : kPlaceBit);
+  }
+  __syncthreads();
+
+  float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
+  SegArgs a;
+  a.pair = pair;
+  a.u = u;
+  a.tok = tok;
+  a.ent_base = 0;
+  a.list = list;
+  a.rows = nlist * p.ET;
+  a.ta = 0;
+  a.tb = (a.rows + kTileRows - 1) / kTileRows;
   tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
 
   const int nseg = p.splits_h + p.splits_m;
   const size_t stride = (size_t)G * (D + 2);
   float* pbase = s.part + (size_t)pair * nseg * stride;
-  tc_write_partial<G, D>(pbase + (size_t)(pass ? p.splits_h + sp : sp) * stride, cm, cl, co);
-  if (!pass) return;
+  tc_write_partial<G, D>(pbase + (size_t)(p.splits_h + sp) * stride, cm, cl, co);
+  if (p.splits_m == 1) {  // the hit pass has finished: merge now
+    __syncthreads();
+    tc_merge_partials<G, D>(pbase, nseg, p.out + (size_t)pair * G * D, co + G * D);
+    return;
+  }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&s.part_count[a.u * kMaxTokens + a.tok], 1) == p.splits_m - 1;
+  if (tid == 0) s_last = atomicAdd(&s.part_count[u * kMaxTokens + tok], 1) == p.splits_m - 1;
   __syncthreads();
   if (s_last) {
     __threadfence();
     tc_merge_partials<G, D>(pbase, nseg, p.out + (size_t)pair * G * D, co + G * D);
-    if (tid == 0) s.part_count[a.u * kMaxTokens + a.tok] = 0;
+    if (tid == 0) s.part_count[u * kMaxTokens + tok] = 0;
   }
 }
 
@@ -639,6 +807,7 @@ TcParams tc_params(const DeviceState& s, const AttnLaunch& a) {
   p.scale_log2 = a.scale_log2;
   p.q = a.q;
   p.out = a.out;
+  p.io = a.io;
   return p;
 }
 
@@ -657,7 +826,9 @@ cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaS
   for (;;) {
     const long long per = p.tiles / C;  // fewest tiles a CTA gets
     p.max_seg = (int)((p.tiles_per_pair + per - 1) / per + 1);
-    if ((size_t)pairs * p.max_seg * stride <= a.part_capacity || C == 1) break;
+    if (((size_t)pairs * p.max_seg * stride <= a.part_capacity && p.max_seg <= SH::MAX_SEG) ||
+        C == 1)
+      break;
     C = C * 3 / 4 > 0 ? C * 3 / 4 : 1;
   }
   p.ctas = (int)C;
@@ -668,21 +839,46 @@ cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaS
 
 template <class SH>
 cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int splits_h,
-                        int splits_m, cudaStream_t st) {
-  static int smem_done = 0;
+                        int splits_m, const DeviceState* placed, cudaStream_t st) {
+  static int smem_hits = 0, smem_miss = 0;
   TcParams p = tc_params<SH>(s, a);
   p.slots = s.hslot;
   p.identity = 0;
   p.splits_h = splits_h;
   p.splits_m = splits_m;
-  const size_t smem = SH::SMEM + kListMax * sizeof(int32_t);
-  cudaError_t e = ensure_smem((const void*)attn_tc_pass_kernel<SH>, smem, &smem_done);
-  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(pass ? splits_m : splits_h), (unsigned)(s.U * a.n_tok));
-  return launch_pdl(attn_tc_pass_kernel<SH>, grid, dim3(kThreadsTc), smem, st, s, p, pass);
+  if (pass == 0) {
+    cudaError_t e = ensure_smem((const void*)attn_tc_hits_kernel<SH>, SH::SMEM, &smem_hits);
+    if (e != cudaSuccess) return e;
+    // Not launched early: its CTAs would take every SM while match runs,
+    // ahead of the reservation and the gather on the other streams.
+    return launch_ex(false, attn_tc_hits_kernel<SH>, grid, dim3(kThreadsTc), SH::SMEM, st, s, p);
+  }
+  if (s.MS % splits_m != 0 || s.MS / splits_m > kScanMax || (s.MS / splits_m) % 2 != 0 ||
+      splits_h + splits_m > SH::MAX_SEG)
+    return cudaErrorInvalidValue;
+  p.place_k = placed->kbuf;
+  p.place_v = placed->vbuf;
+  p.place_B = placed->B;
+  p.mslot = placed->mslot;
+  const size_t smem = SH::SMEM + (size_t)kScanMax * (sizeof(int32_t) + sizeof(unsigned long long));
+  cudaError_t e = ensure_smem((const void*)attn_tc_miss_kernel<SH>, smem, &smem_miss);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_tc_miss_kernel<SH>, grid, dim3(kThreadsTc), smem, st, s, p);
 }
 
 }  // namespace
+
+int attention_tc_max_segments(int D, int G, int kv_shared) {
+#define X(d, g, sh) \
+  if (D == d && G == g && (kv_shared != 0) == sh) return TcShape<d, g, sh>::MAX_SEG;
+  X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
+  X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
+  X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)
+  X(64, 1, true) X(64, 2, true) X(64, 4, true) X(64, 8, true)
+#undef X
+  return 0;
+}
 
 bool attention_tc_supported(int D, int DV, int G, int kv_shared) {
   (void)kv_shared;
@@ -696,10 +892,11 @@ size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sm
 }
 
 cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
-                                     int splits_h, int splits_m, cudaStream_t st) {
+                                     int splits_h, int splits_m, const DeviceState* placed,
+                                     cudaStream_t st) {
 #define X(d, g, sh)                                                         \
   if (s.D == d && s.G == g && (s.kv_shared != 0) == sh)                     \
-    return run_tc_pass<TcShape<d, g, sh>>(s, a, pass, splits_h, splits_m, st);
+    return run_tc_pass<TcShape<d, g, sh>>(s, a, pass, splits_h, splits_m, placed, st);
   X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
   X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
   X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)

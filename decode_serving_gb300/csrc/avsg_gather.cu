@@ -88,44 +88,66 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(DeviceState s) {
 
 // Staged gather: runs right after match, before any slot is reserved.  Each
 // CTA takes an equal contiguous range of all units' miss-set cells (hashing
-// spreads the claimed cells evenly); a warp reads 32 cells, and for every
-// claimed one copies host row `id` of that unit into the staging area at the
-// cell, 32 lanes per row and several rows in flight per lane.
+// spreads the claimed cells evenly) and walks it in rounds of kStageCells:
+// the claimed cells of a round are compacted into a shared list, then the
+// whole CTA copies the listed host rows into the staging area at their
+// cells, consecutive threads on consecutive 16-byte chunks of a row and
+// kUnroll chunks in flight per thread.  Few CTAs keep the host link busy, so
+// the reservation kernel finds free SMs beside this one.
+constexpr int kStageCells = 4096;
+constexpr int kStageWarps = kThreads / 32;
+
 __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
-  __shared__ long long s_cell[kThreads / 32][32];  // claimed cells of a warp's chunk
-  __shared__ int s_id[kThreads / 32][32];
+  __shared__ uint32_t s_off[kStageCells];  // claimed cells of the round (offset in the round)
+  __shared__ int32_t s_id[kStageCells];
+  __shared__ int s_n;
   griddep_wait();
   griddep_launch();
-  if (load_err(s.err) != 0) return;  // no block barriers below: a per-thread exit is safe
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = kThreads / 32;
+  if (load_err(s.err) != 0) return;  // uniform over the CTA
+  const int lane = threadIdx.x & 31;
   const long long ncell = (long long)s.U * s.MS;
   const long long c_begin = blockIdx.x * ncell / gridDim.x;
   const long long c_end = (blockIdx.x + 1) * ncell / gridDim.x;
   const uint32_t cpk = (uint32_t)(s.ek >> 4), cpv = (uint32_t)(s.ev >> 4), cpe = cpk + cpv;
-  for (long long c0 = c_begin + warp * 32; c0 < c_end; c0 += nwarp * 32) {
-    const long long cell = c0 + lane;
-    const unsigned long long w = cell < c_end ? __ldcg(s.mset + cell) : kMissEmpty;
-    const bool claimed = w != kMissEmpty;
-    const unsigned bal = __ballot_sync(0xffffffffu, claimed);
-    if (claimed) {
-      const int r = __popc(bal & ((1u << lane) - 1u));
-      s_cell[warp][r] = cell;
-      s_id[warp][r] = (int)(uint32_t)w;
+  for (long long r0 = c_begin; r0 < c_end; r0 += kStageCells) {
+    if (threadIdx.x == 0) s_n = 0;
+    __syncthreads();
+    const int span = (int)min((long long)kStageCells, c_end - r0);
+    constexpr int kPer = kStageCells / kThreads;
+    unsigned long long w[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int off = e * kThreads + (int)threadIdx.x;
+      w[e] = off < span ? __ldcg(s.mset + r0 + off) : kMissEmpty;
     }
-    __syncwarp();
-    const uint32_t items = (uint32_t)__popc(bal) * cpe;  // (row, 16-byte chunk) pairs
-    for (uint32_t it0 = lane; it0 < items; it0 += 32 * kUnroll) {
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const bool claimed = w[e] != kMissEmpty;
+      const unsigned bal = __ballot_sync(0xffffffffu, claimed);
+      if (bal == 0u) continue;  // uniform over the warp
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&s_n, __popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (claimed) {
+        const int r = base + __popc(bal & ((1u << lane) - 1u));
+        s_off[r] = (uint32_t)(e * kThreads + (int)threadIdx.x);
+        s_id[r] = (int32_t)(uint32_t)w[e];
+      }
+    }
+    __syncthreads();
+    const uint32_t items = (uint32_t)s_n * cpe;  // (row, 16-byte chunk) pairs
+    for (uint32_t it0 = threadIdx.x; it0 < items; it0 += kThreads * kUnroll) {
       uint4 v[kUnroll];
       unsigned char* dst[kUnroll];
 #pragma unroll
       for (int q = 0; q < kUnroll; ++q) {
-        const uint32_t it = it0 + 32u * q;
+        const uint32_t it = it0 + (uint32_t)(q * kThreads);
         dst[q] = nullptr;
         if (it < items) {
           const uint32_t r = it / cpe, j = it - r * cpe;
-          const long long cg = s_cell[warp][r];
+          const long long cg = r0 + s_off[r];
           const long long unit = cg / s.MS;
-          const long long hrow = unit * s.L + s_id[warp][r];
+          const long long hrow = unit * s.L + s_id[r];
           const unsigned char* src;
           if (j < cpk) {
             src = s.host_k + hrow * s.ek + ((size_t)j << 4);
@@ -141,55 +163,20 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
       for (int q = 0; q < kUnroll; ++q)
         if (dst[q]) store16(dst[q], v[q]);
     }
-    __syncwarp();  // the list is rewritten by the next chunk
-  }
-}
-
-// Place: every miss's staged row (by miss-set cell) into its reserved buffer
-// slot, an equal share of the 16-byte chunks per CTA (device to device).
-__global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s) {
-  griddep_wait();
-  griddep_launch();
-  if (load_err(s.err) != 0) return;
-  const uint32_t n = (uint32_t)*(volatile int32_t*)s.desc_count;
-  const uint32_t cpk = (uint32_t)(s.ek >> 4), cpv = (uint32_t)(s.ev >> 4), cpe = cpk + cpv;
-  const uint32_t total = n * cpe;
-  const uint32_t per = (total + gridDim.x - 1) / gridDim.x;
-  const uint32_t begin = blockIdx.x * per, end = min(total, begin + per);
-  for (uint32_t c0 = begin + threadIdx.x; c0 < end; c0 += kThreads * kUnroll) {
-    uint4 v[kUnroll];
-    uint4* dst[kUnroll];
-#pragma unroll
-    for (int r = 0; r < kUnroll; ++r) {
-      const uint32_t c = c0 + (uint32_t)(r * kThreads);
-      dst[r] = nullptr;
-      if (c < end) {
-        const uint32_t d = c / cpe, w = c - d * cpe;
-        const GatherDesc g = s.desc[d];
-        const size_t srow = (size_t)g.unit * s.MS + g.cell, drow = (size_t)g.unit * s.B + g.slot;
-        if (w < cpk) {
-          v[r] = __ldcg(reinterpret_cast<const uint4*>(s.kstage + srow * s.ek) + w);
-          dst[r] = reinterpret_cast<uint4*>(s.kbuf + drow * s.ek) + w;
-        } else {
-          v[r] = __ldcg(reinterpret_cast<const uint4*>(s.vstage + srow * s.ev) + (w - cpk));
-          dst[r] = reinterpret_cast<uint4*>(s.vbuf + drow * s.ev) + (w - cpk);
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kUnroll; ++r)
-      if (dst[r]) *dst[r] = v[r];
+    __syncthreads();  // the list is rewritten by the next round
   }
 }
 
 // No-reuse comparison path: every selected row of every token is copied to
 // staging slot tok * k + j of its unit; ids are range-checked.
-__global__ void __launch_bounds__(kThreads) gather_all_kernel(DeviceState s, int n_tok, int k,
-                                                              const int32_t* __restrict__ sel,
-                                                              int32_t* __restrict__ slot_map,
-                                                              uint8_t* __restrict__ hit) {
+__global__ void __launch_bounds__(kThreads) gather_all_kernel(DeviceState s, StepIO v, int n_tok,
+                                                              int k) {
+  const int32_t* __restrict__ sel = v.sel;
+  int32_t* __restrict__ slot_map = v.slot_map;
+  uint8_t* __restrict__ hit = v.hit;
   griddep_wait();
   griddep_launch();
+  if (blockIdx.x == 0 && threadIdx.x == 0) *s.io = v;  // for the attention after this kernel
   if (load_err(s.err) != 0) return;
   const uint32_t per_unit = (uint32_t)(n_tok * k);
   const uint32_t n = (uint32_t)s.U * per_unit;
@@ -231,17 +218,12 @@ cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st)
   return launch_pdl(gather_stage_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
 }
 
-cudaError_t launch_place(const DeviceState& s, int ctas, cudaStream_t st) {
-  static int attr_done = 0;
-  const cudaError_t e = ensure_smem((const void*)place_kernel, 0, &attr_done);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(place_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
-}
 
-cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,
-                              int32_t* slot_map, uint8_t* hit, int ctas, cudaStream_t st) {
-  return launch_pdl(gather_all_kernel, dim3(ctas), dim3(kThreads), 0, st, s, n_tok, k, sel,
-                    slot_map, hit);
+static_assert(kStageCells % kThreads == 0, "a round is whole passes of the CTA");
+
+cudaError_t launch_gather_all(const DeviceState& s, const StepIO& v, int n_tok, int k, int ctas,
+                              cudaStream_t st) {
+  return launch_pdl(gather_all_kernel, dim3(ctas), dim3(kThreads), 0, st, s, v, n_tok, k);
 }
 
 }  // namespace avsg

@@ -14,7 +14,7 @@ constexpr unsigned long long kMissEmpty = ~0ull;
 constexpr int kOrders = 64;                    // reservation classes 0..63
 constexpr int kNotCandidate = 255;
 constexpr int kMaxTokens = 8;
-constexpr int kMissListMax = 1024;             // miss-set cells one miss-pass CTA scans
+constexpr int kMissScanMax = 4096;             // miss-set cells one miss-pass CTA scans
 
 // First device error of a step; later kernels of the step (and later steps)
 // see a non-zero code and return before touching any state.
@@ -34,6 +34,20 @@ struct GatherDesc {
 };
 
 // Everything a kernel needs about a handle: sizes and device pointers.
+// Per-step inputs and outputs.  The step's first kernel receives them by
+// value and stores them at DeviceState::io; the kernels after it read them
+// there (after their grid-dependency wait).  A step captured as a CUDA graph
+// is thus re-pointed by updating the parameters of one kernel node.
+struct StepIO {
+  const int32_t* sel;
+  const float* q;
+  float* out;
+  int32_t* slot_map;
+  uint8_t* hit;
+  int32_t t;
+  int32_t pad;
+};
+
 struct DeviceState {
   int32_t U, B, G, D, DV, ET;      // units, slots per unit, q/kv, widths, tokens/entry
   int64_t L;                       // entries per unit
@@ -41,6 +55,7 @@ struct DeviceState {
   int32_t MS, ms_shift;            // miss-set capacity (pow2) and 32 - log2(MS)
   int32_t max_union;               // max_tokens_per_step * max_select
   int32_t kv_shared;
+  StepIO* io;                      // this step's inputs and outputs (see StepIO)
   int64_t ek, ev;                  // bytes of one entry's K row / V row (ev 0 if shared)
   const unsigned char* host_k;     // mapped host KV (device-visible pointers)
   const unsigned char* host_v;
@@ -85,6 +100,20 @@ __device__ __forceinline__ int load_err(const DevErr* e) {
   return *(const volatile int32_t*)&e->code;
 }
 
+// This step's StepIO, written by the step's first kernel (L2 loads: it was
+// written by another grid).
+__device__ __forceinline__ StepIO load_io(const StepIO* p) {
+  static_assert(sizeof(StepIO) % 8 == 0, "StepIO is loaded as 8-byte words");
+  union {
+    StepIO v;
+    unsigned long long w[sizeof(StepIO) / 8];
+  } u;
+  const unsigned long long* src = reinterpret_cast<const unsigned long long*>(p);
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(StepIO) / 8); ++i) u.w[i] = __ldcg(src + i);
+  return u.v;
+}
+
 __device__ __forceinline__ void raise_error(DevErr* e, int code, int unit, int pos) {
   if (atomicCAS(&e->code, 0, code) == 0) {
     e->unit = unit;
@@ -95,8 +124,8 @@ __device__ __forceinline__ void raise_error(DevErr* e, int code, int unit, int p
 // Launch with programmatic stream serialization (see griddep_wait).
 bool pdl_enabled();
 template <typename... Params, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t st, Args... args) {
+cudaError_t launch_ex(bool pdl, void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t st, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -104,10 +133,15 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl && pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  return launch_ex(true, kernel, grid, block, smem, st, args...);
 }
 
 // Raises a kernel's dynamic shared memory limit once per size, and asks for
@@ -116,11 +150,9 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 cudaError_t ensure_smem(const void* kernel, size_t bytes, int* done_bytes);
 
 // Kernel launchers (one per .cu file).
-cudaError_t launch_match(const DeviceState& s, int t, int n_tok, int k, const int32_t* sel,
-                         int32_t* slot_map, uint8_t* hit, cudaStream_t st);
+cudaError_t launch_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st);
 size_t victims_smem_bytes(const DeviceState& s);
-cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_t* slot_map,
-                           cudaStream_t st);
+cudaError_t launch_victims(const DeviceState& s, int n_tok, int k, cudaStream_t st);
 // Hash-table update of a step (erase evicted ids, insert new ones, rebuild):
 // needed only by the next step's match, so it may run beside the gather and
 // the attention.
@@ -129,10 +161,8 @@ cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
 // Staged gather: right after match, the host row of every claimed miss-set
 // cell is copied to kstage/vstage at that cell (no slot needed yet).
 cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st);
-// Staged rows -> their reserved slots (after the gather and the reservation).
-cudaError_t launch_place(const DeviceState& s, int ctas, cudaStream_t st);
-cudaError_t launch_gather_all(const DeviceState& s, int n_tok, int k, const int32_t* sel,
-                              int32_t* slot_map, uint8_t* hit, int ctas, cudaStream_t st);
+cudaError_t launch_gather_all(const DeviceState& s, const StepIO& v, int n_tok, int k, int ctas,
+                              cudaStream_t st);
 
 struct AttnLaunch {
   int n_tok, k, splits;
@@ -141,6 +171,7 @@ struct AttnLaunch {
   const float* q;
   float* out;
   const int32_t* slot_map;
+  const StepIO* io;                // when set, q, out and slot_map are read from here
   int num_sms;                     // SMs of the device (persistent grid size)
   size_t part_capacity;            // floats available at DeviceState::part
 };
@@ -152,9 +183,15 @@ bool attention_tc_supported(int D, int DV, int G, int kv_shared);
 size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sms);
 cudaError_t launch_attention_tc(const DeviceState& s, const AttnLaunch& a, int num_sms,
                                 cudaStream_t st);
-// pass 0: hit rows of every (unit, token); pass 1: miss rows, then the merge.
+// pass 0: hit rows of every (unit, token), splits_h CTAs per pair.  pass 1:
+// miss rows from the staging area (s is the staged view), splits_m CTAs per
+// pair (MS / splits_m <= kMissScanMax), each staged row also stored into its
+// reserved slot of `placed` (the real state); then the merge.
 cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
-                                     int splits_h, int splits_m, cudaStream_t st);
+                                     int splits_h, int splits_m, const DeviceState* placed,
+                                     cudaStream_t st);
+// Most partials (hit + miss splits) one pair's merge takes.
+int attention_tc_max_segments(int D, int G, int kv_shared);
 bool attention_tc_enabled();
 
 }  // namespace avsg

@@ -25,17 +25,20 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, int n_tok, int k,
-                                                         const int32_t* __restrict__ sel,
-                                                         int32_t* __restrict__ slot_map,
-                                                         uint8_t* __restrict__ hit) {
-  (void)t;
+__global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v, int n_tok,
+                                                         int k) {
+  const int32_t* __restrict__ sel = v.sel;
+  int32_t* __restrict__ slot_map = v.slot_map;
+  uint8_t* __restrict__ hit = v.hit;
   const int u = blockIdx.y;
   const int n = n_tok * k;
   const int pos = blockIdx.x * kThreads + threadIdx.x;
   griddep_wait();
   griddep_launch();
-  if (blockIdx.x == 0 && u == 0 && threadIdx.x == 0) *s.desc_count = 0;
+  if (blockIdx.x == 0 && u == 0 && threadIdx.x == 0) {
+    *s.desc_count = 0;
+    *s.io = v;  // for the kernels after this one
+  }
   // The error word and the id are loaded together (no block barrier in
   // between); a latched error from an earlier step ends the thread.
   const int stop = load_err(s.err);
@@ -121,14 +124,13 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, int t, i
 
 }  // namespace
 
-cudaError_t launch_match(const DeviceState& s, int t, int n_tok, int k, const int32_t* sel,
-                         int32_t* slot_map, uint8_t* hit, cudaStream_t st) {
+cudaError_t launch_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st) {
   const int n = n_tok * k;
   dim3 grid((unsigned)((n + kThreads - 1) / kThreads), (unsigned)s.U);
   static int attr_done = 0;
   const cudaError_t e = ensure_smem((const void*)match_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(match_kernel, grid, dim3(kThreads), 0, st, s, t, n_tok, k, sel, slot_map, hit);
+  return launch_pdl(match_kernel, grid, dim3(kThreads), 0, st, s, v, n_tok, k);
 }
 
 }  // namespace avsg

@@ -107,8 +107,8 @@ __host__ __device__ inline VictimsSmem victims_layout(int max_union, int B) {
 
 constexpr int kBatch = 8;  // 32-slot chunks whose state one warp loads before using it
 
-__global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int t, int n_tok,
-                                                              int k, int32_t* __restrict__ slot_map) {
+__global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int n_tok,
+                                                              int k) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int s_stop, s_base, s_hits, s_omax, s_m;
   __shared__ int wsum[kWarps];
@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
 
   griddep_wait();
   griddep_launch();
+  const StepIO io = load_io(s.io);
+  const int t = io.t;
+  int32_t* __restrict__ slot_map = io.slot_map;
   if (tid == 0) {
     s_stop = load_err(s.err);
     s_hits = 0;
@@ -411,12 +414,11 @@ int g_victims_smem = 0;
 
 size_t victims_smem_bytes(const DeviceState& s) { return victims_layout(s.max_union, s.B).total; }
 
-cudaError_t launch_victims(const DeviceState& s, int t, int n_tok, int k, int32_t* slot_map,
-                           cudaStream_t st) {
+cudaError_t launch_victims(const DeviceState& s, int n_tok, int k, cudaStream_t st) {
   const size_t smem = victims_smem_bytes(s);
   cudaError_t e = ensure_smem((const void*)victims_kernel, smem, &g_victims_smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(victims_kernel, dim3(s.U), dim3(kThreads), smem, st, s, t, n_tok, k, slot_map);
+  return launch_pdl(victims_kernel, dim3(s.U), dim3(kThreads), smem, st, s, n_tok, k);
 }
 
 cudaError_t launch_commit(const DeviceState& s, cudaStream_t st) {
