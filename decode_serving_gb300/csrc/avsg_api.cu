@@ -49,16 +49,13 @@ struct avsg_handle_s {
   // side stream: the miss gather and the table commit run there while the
   // caller's stream runs attention over the hit rows
   cudaStream_t side = nullptr, side2 = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_reserve = nullptr, ev_commit = nullptr,
-              ev_place = nullptr;  // ev_place: the side stream's last work of the step
+  cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_reserve = nullptr, ev_commit = nullptr;
   bool staged = false;  // staging area allocated: the two-pass pipeline is available
   bool overlap = false;  // steps run the two-pass pipeline
-  unsigned long long* mset_base = nullptr;  // two miss sets, [2][U][MS]
-  uint64_t parity = 0;
-  // Captured steps: one CUDA graph per (tokens, k, miss set), re-pointed at
-  // each step by updating its first kernel node (see StepIO).
+  // Captured steps: one CUDA graph per (tokens, k), re-pointed at each step
+  // by updating its first kernel node (see StepIO).
   struct StepGraph {
-    int n_tok = 0, k = 0, par = 0;
+    int n_tok = 0, k = 0;
     DeviceState sc{};           // the state the first kernel was captured with
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
@@ -147,7 +144,7 @@ void release(avsg_handle h) {
   }
   if (h->cap) cudaStreamDestroy(h->cap);
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
-  for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_reserve, h->ev_commit, h->ev_place})
+  for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_reserve, h->ev_commit})
     if (e) cudaEventDestroy(e);
   if (h->side) cudaStreamDestroy(h->side);
   if (h->side2) cudaStreamDestroy(h->side2);
@@ -245,10 +242,10 @@ int init_state(avsg_handle h, cudaStream_t st) {
   if (!h->no_reuse) {
     AVSG_SET(s.tag, 0xFF, ub * 4);
     AVSG_SET(s.last, 0xFF, ub * 4);
-    AVSG_SET(s.seen, 0, ub * 4);
+    AVSG_SET(s.hitbits, 0, (size_t)s.U * s.HT * s.HW * 4);
     AVSG_SET(s.htab, 0xFF, (size_t)s.U * s.HS * sizeof(int2));
     AVSG_SET(s.hused, 0, (size_t)s.U * 4);
-    AVSG_SET(h->mset_base, 0xFF, 2 * (size_t)s.U * s.MS * 8);
+    AVSG_SET(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
   }
   AVSG_SET(s.desc_count, 0, 4);
   AVSG_SET(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);
@@ -285,6 +282,11 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   const int64_t max_union = (int64_t)c.max_tokens_per_step * c.max_select;
   if (!no_reuse && max_union > c.buffer_slots) return AVSG_ERR_CAPACITY;
   if (max_union > (1 << 24) || (!no_reuse && c.buffer_slots > (1 << 24))) return AVSG_ERR_INVALID_ARG;
+  // match keeps a step's miss set and hit bitmaps in one CTA's shared memory
+  if (!no_reuse && (max_union > (int64_t)kMatchCluster * kMatchThreads * kMatchPerThread ||
+                    match_smem_bytes(pow2_at_least(2 * max_union), c.max_tokens_per_step,
+                                     (c.buffer_slots + 31) / 32) > kMatchSmemMax))
+    return AVSG_ERR_CAPACITY;
   if (!attention_supported(c.head_dim, c.v_dim, c.q_per_kv, c.kv_shared)) return AVSG_ERR_UNSUPPORTED;
   const int64_t ek = (int64_t)c.entry_tokens * c.head_dim * 2;
   const int64_t ev = shared ? 0 : (int64_t)c.entry_tokens * c.v_dim * 2;
@@ -315,7 +317,10 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   s.max_union = (int32_t)max_union;
   s.HS = pow2_at_least(8LL * (no_reuse ? 1 : c.buffer_slots));
   s.hs_shift = 32 - log2_exact(s.HS);
+  s.HW = (s.B + 31) / 32;
+  s.HT = c.max_tokens_per_step;
   s.MS = pow2_at_least(2 * max_union);
+  if (s.MS < 2 * kMatchCluster) s.MS = 2 * kMatchCluster;  // every match CTA holds two cells or more
   s.MS = s.MS < 2 ? 2 : s.MS;
   s.ms_shift = 32 - log2_exact(s.MS);
   if (s.hs_shift >= 32) s.hs_shift = 31;
@@ -354,10 +359,10 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.vstage, h->staged ? (size_t)U * s.MS * ev : 0);
   cv.take(&s.tag, ub);
   cv.take(&s.last, ub);
-  cv.take(&s.seen, ub);
+  cv.take(&s.hitbits, st_arrays ? (size_t)U * s.HT * s.HW : 0);
   cv.take(&s.htab, st_arrays ? (size_t)U * s.HS : 0);
   cv.take(&s.hused, (size_t)U);
-  cv.take(&h->mset_base, st_arrays ? 2 * (size_t)U * s.MS : 0);
+  cv.take(&s.mset, st_arrays ? (size_t)U * s.MS : 0);
   cv.take(&s.hslot, (size_t)U * max_union);
   cv.take(&s.mslot, st_arrays ? (size_t)U * s.MS : 0);
   cv.take(&s.desc, (size_t)U * max_union);
@@ -399,11 +404,11 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   void* b = h->dev_block;
   rebase(&s.kbuf, b); rebase(&s.vbuf, b); rebase(&s.tag, b); rebase(&s.last, b);
   rebase(&s.kstage, b); rebase(&s.vstage, b);
-  rebase(&s.seen, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.io, b);
+  rebase(&s.hitbits, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.io, b);
   rebase(&s.mslot, b); rebase(&s.desc, b);
   rebase(&s.desc_count, b); rebase(&s.part, b);
-  rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&h->mset_base, b); rebase(&s.hslot, b);
-  s.mset = h->mset_base; rebase(&s.part_count, b);
+  rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&s.mset, b); rebase(&s.hslot, b);
+  rebase(&s.part_count, b);
   rebase(&s.counters, b); rebase(&s.err, b);
   rebase(&h->slot_scratch, b); rebase(&h->hit_scratch, b); rebase(&h->stage_sel, b);
   rebase(&h->stage_q, b); rebase(&h->stage_out, b);
@@ -421,7 +426,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   if (e == cudaSuccess)
     e = cudaStreamCreateWithPriority(&h->side2, cudaStreamNonBlocking, prio_high);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking);
-  for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_gather, &h->ev_reserve, &h->ev_commit, &h->ev_place})
+  for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_gather, &h->ev_reserve, &h->ev_commit})
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     release(h);
@@ -481,11 +486,10 @@ struct Prof {
 };
 
 // Enqueues the kernels of one step on st (and the side streams, forked from
-// and joined back into st).  par selects the miss set the step fills; the
-// step's pointers come in v.  With first != null (capture), returns the
-// graph node of the first kernel there.
-int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& v,
-                cudaStream_t st, DeviceState* sc_out, cudaGraphNode_t* first) {
+// and joined back into st); the step's pointers come in v.  With first !=
+// null (capture), returns the graph node of the first kernel there.
+int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaStream_t st,
+                DeviceState* sc_out, cudaGraphNode_t* first) {
   const DeviceState& s = h->ds;
   cudaError_t e;
   AttnLaunch a{};
@@ -520,9 +524,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& 
     if (ce == cudaSuccess) *first = deps[0];
     return ce;
   };
-  DeviceState sc = s;
-  const size_t set_cells = (size_t)s.U * s.MS;
-  sc.mset = h->mset_base + (size_t)par * set_cells;
+  const DeviceState& sc = s;
   if (sc_out) *sc_out = sc;
   if (h->no_reuse) {
     AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather_all(sc, v, n_tok, k, h->gather_ctas, st));
@@ -539,14 +541,12 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& 
     AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(sc, h->gather_ctas, st));
     AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(sc, st));
     AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(sc, a, st));
-    e = cudaMemsetAsync(sc.mset, 0xFF, set_cells * 8, st);  // the miss set starts empty
-    return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
+    return AVSG_OK;
   }
   // Two-pass pipeline (the tensor-core shapes).  After match, three
   // streams run side by side:
   //   st:     attention over the hit rows (their slots are known);
-  //   side:   the missed rows, host -> staging area (host link), then the
-  //           other miss set (the previous step's) is emptied;
+  //   side:   the missed rows, host -> staging area (host link);
   //   side2:  the reservation, then the hash-table update.
   // The attention over the missed rows (read from staging) follows the
   // gather and the reservation, and stores each staged row into its slot.
@@ -565,9 +565,6 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& 
   AVSG_RUN(AVSG_KERNEL_COMMIT, h->side2, launch_commit(sc, h->side2));
   e = cudaEventRecord(h->ev_commit, h->side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  e = cudaMemsetAsync(h->mset_base + (size_t)(par ^ 1) * set_cells, 0xFF, set_cells * 8, h->side);
-  if (e == cudaSuccess) e = cudaEventRecord(h->ev_place, h->side);
-  if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_ATTENTION, st,
            launch_attention_tc_pass(sc, a, 0, splits_h, splits_m, nullptr, st));
   e = cudaStreamWaitEvent(st, h->ev_gather, 0);
@@ -579,8 +576,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& 
   staged.B = s.MS;
   AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, st,
            launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, &sc, st));
-  e = cudaStreamWaitEvent(st, h->ev_place, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_commit, 0);
+  e = cudaStreamWaitEvent(st, h->ev_commit, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
 #undef AVSG_RUN
   return AVSG_OK;
@@ -588,13 +584,13 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& 
 
 constexpr size_t kMaxGraphs = 16;
 
-// The captured step for (n_tok, k, par), captured now if it is not cached
-// (the least recently used one is dropped beyond kMaxGraphs).
-int step_graph(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& v,
+// The captured step for (n_tok, k), captured now if it is not cached (the
+// least recently used one is dropped beyond kMaxGraphs).
+int step_graph(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v,
                avsg_handle_s::StepGraph** out) {
   h->graph_clock += 1;
   for (auto& g : h->graphs)
-    if (g.n_tok == n_tok && g.k == k && g.par == par) {
+    if (g.n_tok == n_tok && g.k == k) {
       g.used = h->graph_clock;
       *out = &g;
       return AVSG_OK;
@@ -610,10 +606,9 @@ int step_graph(avsg_handle h, int32_t n_tok, int32_t k, int par, const StepIO& v
   avsg_handle_s::StepGraph g;
   g.n_tok = n_tok;
   g.k = k;
-  g.par = par;
   cudaError_t e = cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeRelaxed);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  const int rc = enqueue_dag(h, n_tok, k, par, v, h->cap, &g.sc, &g.first);
+  const int rc = enqueue_dag(h, n_tok, k, v, h->cap, &g.sc, &g.first);
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(h->cap, &graph);
   if (rc != AVSG_OK) {
@@ -658,14 +653,9 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
   v.slot_map = d_slot_map ? d_slot_map : h->slot_scratch;
   v.hit = d_hit;
   v.t = t;
-  // The two-pass pipeline alternates miss sets (each step empties the
-  // other); the serial order empties its one set at the end of the step.
-  const int par = h->overlap && !h->no_reuse ? (int)(h->parity & 1) : 0;
-  if (h->overlap && !h->no_reuse) h->parity += 1;
-  if (h->prof || !graphs_enabled())
-    return enqueue_dag(h, n_tok, k, par, v, st, nullptr, nullptr);
+  if (h->prof || !graphs_enabled()) return enqueue_dag(h, n_tok, k, v, st, nullptr, nullptr);
   avsg_handle_s::StepGraph* g = nullptr;
-  const int rc = step_graph(h, n_tok, k, par, v, &g);
+  const int rc = step_graph(h, n_tok, k, v, &g);
   if (rc != AVSG_OK) return rc;
   DeviceState sc = g->sc;
   int32_t nt = n_tok, kk = k;
@@ -795,8 +785,8 @@ extern "C" int avsg_clear_error(avsg_handle h) {
   const DeviceState& s = h->ds;
   cudaError_t e = cudaDeviceSynchronize();
   if (!h->no_reuse) {
-    if (e == cudaSuccess) e = cudaMemset(s.seen, 0, (size_t)s.U * s.B * 4);
-    if (e == cudaSuccess) e = cudaMemset(h->mset_base, 0xFF, 2 * (size_t)s.U * s.MS * 8);
+    if (e == cudaSuccess) e = cudaMemset(s.hitbits, 0, (size_t)s.U * s.HT * s.HW * 4);
+    if (e == cudaSuccess) e = cudaMemset(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
   }
   if (e == cudaSuccess) e = cudaMemset(s.desc_count, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);

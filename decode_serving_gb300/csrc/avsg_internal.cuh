@@ -15,6 +15,10 @@ constexpr int kOrders = 64;                    // reservation classes 0..63
 constexpr int kNotCandidate = 255;
 constexpr int kMaxTokens = 8;
 constexpr int kMissScanMax = 4096;             // miss-set cells one miss-pass CTA scans
+constexpr int kMatchCluster = 8;               // match: one cluster of CTAs per unit
+constexpr int kMatchThreads = 256;             // threads per match CTA
+constexpr int kMatchPerThread = 4;             // selected ids per match thread (n_tok * k <= 8192)
+constexpr size_t kMatchSmemMax = 200 * 1024;   // match's part of the miss set + hit bitmaps
 
 // First device error of a step; later kernels of the step (and later steps)
 // see a non-zero code and return before touching any state.
@@ -54,6 +58,7 @@ struct DeviceState {
   int32_t HS, hs_shift;            // hash capacity (pow2) and 32 - log2(HS)
   int32_t MS, ms_shift;            // miss-set capacity (pow2) and 32 - log2(MS)
   int32_t max_union;               // max_tokens_per_step * max_select
+  int32_t HW, HT;                  // hit bitmaps: 32-slot words per token, token rows per unit
   int32_t kv_shared;
   StepIO* io;                      // this step's inputs and outputs (see StepIO)
   int64_t ek, ev;                  // bytes of one entry's K row / V row (ev 0 if shared)
@@ -65,7 +70,7 @@ struct DeviceState {
   unsigned char* vstage;           // [U][MS][ev]
   int32_t* tag;                    // [U][B] resident id or kEmpty
   int32_t* last;                   // [U][B] step of last selection, -1 never
-  int32_t* seen;                   // [U][B] token bits of this step's hits; 0 between steps
+  uint32_t* hitbits;               // [U][HT][HW] this step's hit slots per token (written by match)
   int2* htab;                      // [U][HS] {key, slot}
   int32_t* hused;                  // [U] non-empty hash cells (live + erased)
   unsigned long long* mset;        // [U][MS] {id | token bits << 32}: this step's miss set
@@ -150,6 +155,8 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 cudaError_t ensure_smem(const void* kernel, size_t bytes, int* done_bytes);
 
 // Kernel launchers (one per .cu file).
+// Shared memory of match: the miss set (MS cells) and n_tok hit bitmaps.
+size_t match_smem_bytes(int MS, int n_tok, int HW);
 cudaError_t launch_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st);
 size_t victims_smem_bytes(const DeviceState& s);
 cudaError_t launch_victims(const DeviceState& s, int n_tok, int k, cudaStream_t st);

@@ -2,135 +2,213 @@
 //
 // AVSG page (arxivdaily 2609.37538, English abstract): hash matching of the
 // selected tokens against the entries retained in the HBM buffer identifies
-// the reusable slots.  Here every lane of a warp probes one id, so a warp
-// matches 32 ids at once; a probe reads a 16-byte window of two table cells.
+// the reusable slots.
 //
-// Grid (ceil(n_tok*k / 256), U), 256 threads.  Per id:
+// A cluster of kMatchCluster CTAs per unit; the unit's miss set (cells in
+// contiguous blocks) and hit bitmaps (32-slot words dealt round-robin) are
+// spread over the cluster's shared memories and updated with atomics on
+// distributed shared memory.  A thread takes every (kMatchCluster * 256)-th
+// position of the unit's n_tok * k selected ids (at most kMatchPerThread),
+// loads all of them and then all of their first hash windows before it
+// resolves any.  Per id:
 //   * range check (id in [0, L)), else BAD_SELECTION;
 //   * lookup in the unit's open-addressed table (linear probing, Fibonacci
-//     hash); a hit writes its slot (slot map and the internal hit-slot list
-//     the attention over hit rows reads) and sets the token's bit in
-//     seen[slot] (a bit already set means the id repeats within one token's
-//     list);
-//   * a miss is entered in the per-step miss set (one cell per distinct id,
+//     hash; a probe reads a 16-byte window of two cells);
+//   * a hit writes its slot (slot map and the hit-slot list the attention
+//     over hit rows reads) and sets the slot's bit in the token's hit bitmap
+//     (a bit already set means the id repeats within one token's list);
+//   * a miss is entered in the step's miss set (one cell per distinct id,
 //     claimed or extended with one compare-and-swap; token bits merged, so a
 //     multi-token iteration reserves each id once); the slot map gets
 //     -2 - cell until the reservation kernel resolves it.
-// Nothing in the buffer state (tags, last_step, hash table) changes here, so a
-// BAD_SELECTION leaves the state as it was.
+// The miss set and the hit bitmaps are then written out whole (coalesced),
+// so neither needs clearing between steps.  Nothing in the buffer state
+// (tags, last_step, hash table) changes here, so a BAD_SELECTION leaves the
+// state as it was.
+#include <cooperative_groups.h>
+
 #include "avsg_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace avsg {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = kMatchThreads;
+constexpr int kC = kMatchCluster;
 
 __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v, int n_tok,
                                                          int k) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int MSL = s.MS / kC;              // miss-set cells held by each CTA
+  const int HWL = (s.HW + kC - 1) / kC;   // bitmap words per token held by each CTA
+  unsigned long long* lset = reinterpret_cast<unsigned long long*>(smem);  // [MSL]
+  uint32_t* lbits = reinterpret_cast<uint32_t*>(lset + MSL);               // [n_tok][HWL]
+  __shared__ int s_stop;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int u = blockIdx.x / kC, tid = threadIdx.x;
   const int32_t* __restrict__ sel = v.sel;
   int32_t* __restrict__ slot_map = v.slot_map;
   uint8_t* __restrict__ hit = v.hit;
-  const int u = blockIdx.y;
   const int n = n_tok * k;
-  const int pos = blockIdx.x * kThreads + threadIdx.x;
+  const int HW = s.HW;
+  // shared memory is private: cleared before the wait on the previous kernel
+  for (int i = tid; i < MSL; i += kThreads) lset[i] = kMissEmpty;
+  for (int i = tid; i < n_tok * HWL; i += kThreads) lbits[i] = 0u;
+  cl.sync();  // every CTA's part is cleared before any CTA updates it
   griddep_wait();
   griddep_launch();
-  if (blockIdx.x == 0 && u == 0 && threadIdx.x == 0) {
+  if (u == 0 && rank == 0 && tid == 0) {
     *s.desc_count = 0;
     *s.io = v;  // for the kernels after this one
   }
-  // The error word and the id are loaded together (no block barrier in
-  // between); a latched error from an earlier step ends the thread.
-  const int stop = load_err(s.err);
-  int miss_cell = -1;
-  if (pos < n) {
+  if (tid == 0) s_stop = load_err(s.err);  // a latched error from an earlier step
+  const size_t ubase = (size_t)u * n;
+  const int first = rank * kThreads + tid;
+  int32_t id[kMatchPerThread];
+#pragma unroll
+  for (int j = 0; j < kMatchPerThread; ++j) {
+    const int pos = first + j * kC * kThreads;
+    id[j] = pos < n ? __ldcg(sel + ubase + pos) : kEmpty;
+  }
+  __syncthreads();
+  const bool stop = s_stop != 0;  // uniform over the cluster's work below
+
+  const int2* tab = s.htab + (size_t)u * s.HS;
+  const uint32_t mask = (uint32_t)s.HS - 1u;
+  int4 win[kMatchPerThread];
+#pragma unroll
+  for (int j = 0; j < kMatchPerThread; ++j) {
+    const bool valid = !stop && first + j * kC * kThreads < n && id[j] >= 0 && (int64_t)id[j] < s.L;
+    win[j] = valid ? __ldcg(reinterpret_cast<const int4*>(tab + (fib_hash(id[j], s.hs_shift) & ~1u)))
+                   : make_int4(kEmpty, -1, kEmpty, -1);
+  }
+#pragma unroll
+  for (int j = 0; j < kMatchPerThread; ++j) {
+    const int pos = first + j * kC * kThreads;
+    if (stop || pos >= n) continue;
+    const size_t off = ubase + pos;
     const int tok = pos / k;
-    const size_t off = (size_t)u * n + pos;
-    const int32_t id = sel[off];
-    if (stop) return;
-    if (id < 0 || (int64_t)id >= s.L) {
+    const int32_t x = id[j];
+    if (x < 0 || (int64_t)x >= s.L) {
       raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
       slot_map[off] = -1;
+      s.hslot[off] = -1;
       if (hit) hit[off] = 0;
-    } else {
-      // Hash lookup: 16-byte windows of two cells, starting at the even cell
-      // at or before the home cell.  A cell before the home cell never holds
-      // this id, and an empty one there does not end the probe.
-      const int2* tab = s.htab + (size_t)u * s.HS;
-      const uint32_t mask = (uint32_t)s.HS - 1u;
-      const uint32_t home = fib_hash(id, s.hs_shift);
-      uint32_t cell = home & ~1u;
-      int slot = -1;
-      bool skip_first = (home & 1u) != 0;
-      for (int probes = 0; probes < s.HS; probes += 2) {
-        const int4 w = __ldcg(reinterpret_cast<const int4*>(tab + (cell & mask)));
-        if (!skip_first) {
-          if (w.x == id) { slot = w.y; break; }
-          if (w.x == kEmpty) break;
-        }
-        if (w.z == id) { slot = w.w; break; }
-        if (w.z == kEmpty) break;
-        skip_first = false;
-        cell += 2;
+      continue;
+    }
+    // Windows of two cells, starting at the even cell at or before the home
+    // cell: a cell before the home cell never holds this id, and an empty
+    // one there does not end the probe.
+    const uint32_t home = fib_hash(x, s.hs_shift);
+    uint32_t cell = home & ~1u;
+    bool skip_first = (home & 1u) != 0;
+    int4 w = win[j];
+    int slot = -1;
+    for (int probes = 0; probes < s.HS; probes += 2) {
+      if (probes) w = __ldcg(reinterpret_cast<const int4*>(tab + (cell & mask)));
+      if (!skip_first) {
+        if (w.x == x) { slot = w.y; break; }
+        if (w.x == kEmpty) break;
       }
-      const unsigned bit = 1u << tok;
-      if (slot >= 0) {
-        const int old = atomicOr(&s.seen[(size_t)u * s.B + slot], (int)bit);
-        if (old & bit) raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
-        slot_map[off] = slot;
-        s.hslot[off] = slot;
-        if (hit) hit[off] = 1;
-      } else {
-        unsigned long long* ms = s.mset + (size_t)u * s.MS;
-        const uint32_t mmask = (uint32_t)s.MS - 1u;
-        const unsigned long long tokbit = (unsigned long long)bit << 32;
-        uint32_t c = fib_hash(id, s.ms_shift);
-        unsigned long long expect = kMissEmpty;  // first try: claim an empty cell
-        // Each failed compare-and-swap on the id's own cell means another
-        // token added its bit, so retries are bounded by the token count.
-        for (int iter = 0; iter < s.MS + 2 * kMaxTokens; ++iter) {
-          unsigned long long* p = ms + (c & mmask);
-          const unsigned long long want = expect == kMissEmpty ? (tokbit | (uint32_t)id) : (expect | tokbit);
-          const unsigned long long prev = atomicCAS(p, expect, want);
-          if (prev == expect) {
-            miss_cell = (int)(c & mmask);
+      if (w.z == x) { slot = w.w; break; }
+      if (w.z == kEmpty) break;
+      skip_first = false;
+      cell += 2;
+    }
+    if (slot >= 0) {
+      const int word = slot >> 5;
+      uint32_t* bits = cl.map_shared_rank(lbits, (unsigned)(word % kC));
+      const uint32_t b = 1u << (slot & 31);
+      const uint32_t old = atomicOr(&bits[tok * HWL + word / kC], b);
+      if (old & b) raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
+      slot_map[off] = slot;
+      s.hslot[off] = slot;
+      if (hit) hit[off] = 1;
+    } else {
+      const uint32_t mmask = (uint32_t)s.MS - 1u;
+      const unsigned long long tokbit = 1ull << (32 + tok);
+      uint32_t c = fib_hash(x, s.ms_shift);
+      unsigned long long expect = kMissEmpty;  // first try: claim an empty cell
+      int miss_cell = -1;
+      // A failed compare-and-swap on the id's own cell means another token
+      // added its bit, so retries are bounded by the token count.
+      for (int iter = 0; iter < s.MS + 2 * kMaxTokens; ++iter) {
+        const int mc = (int)(c & mmask);
+        unsigned long long* cellp = cl.map_shared_rank(lset, (unsigned)(mc / MSL)) + (mc % MSL);
+        const unsigned long long want =
+            expect == kMissEmpty ? (tokbit | (uint32_t)x) : (expect | tokbit);
+        const unsigned long long prev = atomicCAS(cellp, expect, want);
+        if (prev == expect) {
+          miss_cell = mc;
+          break;
+        }
+        if ((uint32_t)prev == (uint32_t)x) {  // this id's cell, claimed by another token
+          if (prev & tokbit) {
+            raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
+            miss_cell = mc;
             break;
           }
-          if ((uint32_t)prev == (uint32_t)id) {  // this id's cell, claimed by another token
-            if (prev & tokbit) {
-              raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
-              miss_cell = (int)(c & mmask);
-              break;
-            }
-            expect = prev;  // add this token's bit
-            continue;
-          }
-          if (prev == kMissEmpty) {  // lost an empty cell to another id? it is now taken; retry it
-            expect = kMissEmpty;
-            continue;
-          }
-          expect = kMissEmpty;  // another id's cell: probe on
-          ++c;
+          expect = prev;  // add this token's bit
+          continue;
         }
-        if (miss_cell < 0) raise_error(s.err, AVSG_ERR_CAPACITY, u, pos);  // miss set full
-        slot_map[off] = -2 - miss_cell;
-        s.hslot[off] = -1;
-        if (hit) hit[off] = 0;
+        if (prev == kMissEmpty) {  // an empty cell after all: try it again
+          expect = kMissEmpty;
+          continue;
+        }
+        expect = kMissEmpty;  // another id's cell: probe on
+        ++c;
       }
+      if (miss_cell < 0) raise_error(s.err, AVSG_ERR_CAPACITY, u, pos);  // miss set full
+      slot_map[off] = -2 - miss_cell;
+      s.hslot[off] = -1;
+      if (hit) hit[off] = 0;
     }
   }
-
+  cl.sync();  // every update of this CTA's part is done (and no CTA exits early)
+  if (stop) return;
+  // This CTA's part of the step's miss set and hit bitmaps.
+  unsigned long long* gset = s.mset + (size_t)u * s.MS + (size_t)rank * MSL;
+  for (int i = tid; i < MSL; i += kThreads) gset[i] = lset[i];
+  uint32_t* gbits = s.hitbits + (size_t)u * s.HT * HW;
+  for (int i = tid; i < n_tok * HWL; i += kThreads) {
+    const int t2 = i / HWL, wl = i - t2 * HWL, word = wl * kC + rank;
+    if (word < HW) gbits[t2 * HW + word] = lbits[i];
+  }
 }
 
 }  // namespace
 
+size_t match_smem_bytes(int MS, int n_tok, int HW) {
+  return (size_t)(MS / kMatchCluster) * sizeof(unsigned long long) +
+         (size_t)n_tok * ((HW + kMatchCluster - 1) / kMatchCluster) * sizeof(uint32_t);
+}
+
 cudaError_t launch_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st) {
-  const int n = n_tok * k;
-  dim3 grid((unsigned)((n + kThreads - 1) / kThreads), (unsigned)s.U);
+  if ((int64_t)n_tok * k > (int64_t)kMatchCluster * kMatchThreads * kMatchPerThread ||
+      s.MS < 2 * kMatchCluster || n_tok > s.HT)
+    return cudaErrorInvalidValue;
+  const size_t smem = match_smem_bytes(s.MS, n_tok, s.HW);
   static int attr_done = 0;
-  const cudaError_t e = ensure_smem((const void*)match_kernel, 0, &attr_done);
+  const cudaError_t e = ensure_smem((const void*)match_kernel, match_smem_bytes(s.MS, s.HT, s.HW),
+                                    &attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(match_kernel, grid, dim3(kThreads), 0, st, s, v, n_tok, k);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(s.U * kMatchCluster));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kMatchCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, match_kernel, s, v, n_tok, k);
 }
 
 }  // namespace avsg

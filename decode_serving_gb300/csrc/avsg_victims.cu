@@ -106,6 +106,7 @@ __host__ __device__ inline VictimsSmem victims_layout(int max_union, int B) {
 }
 
 constexpr int kBatch = 8;  // 32-slot chunks whose state one warp loads before using it
+static_assert(kBatch == 8, "the hit-word loads map lane & 7 to a chunk, lane >> 3 to a token");
 
 __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int n_tok,
                                                               int k) {
@@ -142,14 +143,38 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   const int chunk = ((B + kWarps * 32 - 1) / (kWarps * 32)) * 32;  // slots per warp
   const int w_begin = warp * chunk, w_end = min(B, w_begin + chunk);
   int sn[kBatch], tg[kBatch], ls[kBatch];
+  // Hit bitmap words of a batch: lane (b = lane & 7, t = lane >> 3) loads
+  // chunk b's word of tokens t and t + 4 (chunks start at multiples of 32).
+  uint32_t hw0 = 0u, hw1 = 0u;
   auto load_batch = [&](int base) {
+    {
+      const int b = lane & 7, t2 = lane >> 3;
+      const int sl0 = base + b * 32;
+      const bool inb = b < kBatch && sl0 < w_end && sl0 < w_begin + chunk;
+      const uint32_t* hb = s.hitbits + (size_t)u * s.HT * s.HW + (sl0 >> 5);
+      hw0 = (inb && t2 < n_tok) ? __ldcg(hb + (size_t)t2 * s.HW) : 0u;
+      hw1 = (inb && t2 + 4 < n_tok) ? __ldcg(hb + (size_t)(t2 + 4) * s.HW) : 0u;
+    }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int sl = base + b * 32 + lane;
       const bool in = sl < w_end && base + b * 32 < w_begin + chunk;
-      sn[b] = in ? __ldcg(s.seen + ub + sl) : -1;
       tg[b] = in ? __ldcg(s.tag + ub + sl) : kEmpty;
       ls[b] = in ? __ldcg(s.last + ub + sl) : 0;
+    }
+  };
+  // sn[b]: 1 if this lane's slot of chunk b is selected this step, 0 if not,
+  // -1 past the warp's range (all lanes take part).
+  auto batch_hits = [&](int base) {
+    uint32_t x = hw0 | hw1;
+    x |= __shfl_xor_sync(0xffffffffu, x, 8);
+    x |= __shfl_xor_sync(0xffffffffu, x, 16);
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const uint32_t word = __shfl_sync(0xffffffffu, x, b);
+      const int sl = base + b * 32 + lane;
+      const bool in = sl < w_end && base + b * 32 < w_begin + chunk;
+      sn[b] = in ? (int)((word >> lane) & 1u) : -1;
     }
   };
   load_batch(w_begin);
@@ -229,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   int hits = 0;
   for (int base = w_begin; base < w_begin + chunk; base += 32 * kBatch) {
     if (base != w_begin) load_batch(base);
+    batch_hits(base);
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int sl = base + b * 32 + lane;
@@ -236,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
       int o = kNotCandidate;
       if (sn[b] > 0) {
         s.last[ub + sl] = t;  // selected this step: refreshed, never a victim
-        s.seen[ub + sl] = 0;
         ++hits;
       } else if (sn[b] == 0) {
         if (tg[b] == kEmpty) {

@@ -80,6 +80,8 @@ def _cfg(**kw):
     (dict(kv_shared=True, v_dim=64), -1),
     (dict(max_select=300), -2),                       # k larger than the buffer
     (dict(max_tokens_per_step=3, max_select=100), -2),
+    # a step's miss set (2 * 8 * 2048 cells, rounded up) exceeds match's shared memory
+    (dict(max_tokens_per_step=8, max_select=2048, buffer_slots=16384, num_entries=1 << 20), -2),
     (dict(q_per_kv=3), -7),                           # no attention kernel for G=3
     (dict(head_dim=96, v_dim=96), -7),
 ])
