@@ -148,22 +148,22 @@ def pinned_h2d_peak_gbs(torch) -> float:
 def algorithmic_bytes(w, hits, misses, steps) -> dict:
     """Bytes each kernel must move per launch (averaged over the timed steps).
 
-    attention: slot id + K row + V row per selected entry, plus q and out;
+    attention: slot id + K row + V row per selected entry, plus q and out
+           (both passes together);
     match: id (4) + one 16-byte probe window + slot map (4) + hit flag (1)
-           per selected id, + 4 per distinct hit (seen bit) + 8 per distinct
-           miss (miss-set cell);
-    victims: tag, last_step and seen (12 bytes) per slot, + 40 per miss
-           (sorted key, tag/last/slot writes, descriptor, slot map fix-up);
+           per selected id, + 8 per distinct miss (miss-set cell) + the hit
+           bitmaps (1 bit per slot);
+    victims: tag and last_step (8 bytes) per slot + the hit bitmaps, + 40 per
+           miss (sorted key, tag/last/slot writes, descriptor, slot map fix-up);
     gather: one entry (K + V) per miss, read over the host link and written
            to HBM (host-link bytes are the read half)."""
     U, n_tok, k = w.units, w.tokens_per_step, w.k
     sel = U * n_tok * k
     hits_ps, miss_ps = hits / steps, misses / steps
-    rows = U * n_tok * k * w.entry_tokens
-    attn = sel * 4 + rows * (w.head_dim * 2 + (0 if w.kv_shared else w.v_dim * 2)) \
-        + U * n_tok * w.q_per_kv * (w.head_dim + w.v_dim) * 4
-    match = sel * (4 + 16 + 4 + 1) + hits_ps * 4 + miss_ps * 8
-    victims = U * w.slots * 12 + miss_ps * 40
+    row_b = w.entry_k_bytes + w.entry_v_bytes
+    attn = sel * 4 + sel * row_b + U * n_tok * w.q_per_kv * (w.head_dim + w.v_dim) * 4
+    match = sel * (4 + 16 + 4 + 1) + miss_ps * 8 + U * n_tok * w.slots / 8
+    victims = U * w.slots * 8 + U * n_tok * w.slots / 8 + miss_ps * 40
     gather_host = miss_ps * w.entry_bytes
     commit = miss_ps * 40   # descriptor, evicted-id probe window, new-id probe window
     return {"attention": attn, "match": match, "victims": victims, "gather": 2 * gather_host,

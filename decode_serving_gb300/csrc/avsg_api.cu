@@ -161,7 +161,8 @@ void release(avsg_handle h) {
 void two_pass_splits(const avsg_handle h, int n_tok, int* splits_h, int* splits_m) {
   const DeviceState& s = h->ds;
   const int pairs = s.U * n_tok;
-  int sm = s.MS > kMissScanMax ? s.MS / kMissScanMax : 1;
+  const int scan = attention_tc_scan_max(s.D, s.G, s.kv_shared);
+  int sm = scan > 0 && s.MS > scan ? s.MS / scan : 1;
   while (sm < h->miss_splits && s.MS / sm > 2) sm *= 2;
   int sh = 2 * h->num_sms / pairs > 0 ? 2 * h->num_sms / pairs : 1;
   const int cap = attention_tc_max_segments(s.D, s.G, s.kv_shared);
@@ -329,7 +330,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   h->target_ctas = h->num_sms * env_int("AVSG_ATTN_CTAS_PER_SM", 4);
   h->gather_ctas = h->num_sms * env_int("AVSG_GATHER_CTAS_PER_SM", 4);
   h->stage_ctas = env_int("AVSG_STAGE_CTAS", h->num_sms * 2 / 5);
-  h->miss_splits = env_int("AVSG_MISS_SPLITS", 2);  // at least this many miss-pass CTAs per pair
+  h->miss_splits = env_int("AVSG_MISS_SPLITS", 1);  // at least this many miss-pass CTAs per pair
   {
     int64_t cap = (h->target_ctas + U - 1) / U;
     const int64_t by_rows = ((int64_t)c.max_select * c.entry_tokens + h->tile_rows - 1) / h->tile_rows;
@@ -368,6 +369,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.desc, (size_t)U * max_union);
   cv.take(&s.desc_count, 1);
   cv.take(&s.io, 1);
+  cv.take(&s.qbuf, st_arrays ? (size_t)U * c.max_tokens_per_step * s.G * s.D : 0);
   cv.take(&s.dbase, (size_t)U);
   cv.take(&s.dcount, (size_t)U);
 
@@ -404,7 +406,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   void* b = h->dev_block;
   rebase(&s.kbuf, b); rebase(&s.vbuf, b); rebase(&s.tag, b); rebase(&s.last, b);
   rebase(&s.kstage, b); rebase(&s.vstage, b);
-  rebase(&s.hitbits, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.io, b);
+  rebase(&s.hitbits, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.io, b); rebase(&s.qbuf, b);
   rebase(&s.mslot, b); rebase(&s.desc, b);
   rebase(&s.desc_count, b); rebase(&s.part, b);
   rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&s.mset, b); rebase(&s.hslot, b);
@@ -498,7 +500,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   a.splits = attn_splits(h, n_tok, k);
   a.identity_slots = h->no_reuse ? 1 : 0;
   a.scale_log2 = h->scale_log2;
-  a.q = v.q;
+  a.q = h->no_reuse ? nullptr : s.qbuf;  // match copies q (no-reuse: read through io)
   a.out = v.out;
   a.slot_map = v.slot_map;
   a.io = s.io;

@@ -102,9 +102,9 @@ __global__ void __launch_bounds__(SH::NT) attn_kernel(DeviceState s, AttnLaunch 
   const int sp = blockIdx.x, u = blockIdx.y, tok = blockIdx.z;
   griddep_wait();
   griddep_launch();
-  if (a.io) {  // this step's q, out and slot map
+  if (a.io) {  // this step's out and slot map (and q when it is not copied)
     const StepIO io = load_io(a.io);
-    a.q = io.q;
+    if (!a.q) a.q = io.q;
     a.out = io.out;
     a.slot_map = io.slot_map;
   }

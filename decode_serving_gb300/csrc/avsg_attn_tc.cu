@@ -45,6 +45,12 @@ constexpr int kScanMax = kMissScanMax;          // miss-set cells one miss-pass 
 constexpr int32_t kPlaceBit = (int32_t)0x80000000;
 constexpr int32_t kCellMask = 0x7FFFFFFF;
 
+constexpr int pow2_floor_capped(int x, int cap) {
+  int q = 1;
+  while (q * 2 <= x && q * 2 <= cap) q *= 2;
+  return q;
+}
+
 template <int D_, int G_, bool SHARED_>
 struct TcShape {
   static constexpr int D = D_, G = G_;
@@ -65,6 +71,9 @@ struct TcShape {
   // Most partials one merge takes: the four warps' outputs, the CTA's own
   // and 2 floats per partial and head must fit in the warps' staging.
   static constexpr int MAX_SEG = (kWarpsTc * WARP_BYTES / 4 - (kWarpsTc + 1) * G * D) / (2 * G);
+  // Most miss-set cells one miss-pass CTA scans: they are staged in the tile
+  // staging (8 bytes each); a power of two, at most kScanMax.
+  static constexpr int SCAN_MAX = pow2_floor_capped(kWarpsTc * WARP_BYTES / 8, kScanMax);
   static_assert(MAX_SEG >= 16, "merge scratch");
 };
 
@@ -157,20 +166,12 @@ struct SegArgs {
   int ta, tb;                   // this CTA's tiles [ta, tb) of the range
   const int32_t* list;          // when set: entry e is list[e] & kCellMask (shared memory);
                                 // bit 31 set: this pass stores the row into its slot
+  const float* qs;              // when set: the pair's q [G][D] in shared memory
 };
 
 // CTA c covers global tiles [c*T/C, (c+1)*T/C); the CTA holding tile x:
 __device__ __forceinline__ int cta_of_tile(long long x, int C, long long T) {
   return (int)(((x + 1) * C - 1) / T);
-}
-
-// Zeroes the CTA's staging once: rows past the end of a partial tile then
-// always hold finite values (zeros or earlier rows), which P = 0 cancels.
-template <class SH>
-__device__ __forceinline__ void tc_zero_staging(unsigned char* smem) {
-  for (int i = threadIdx.x; i < kWarpsTc * SH::WARP_BYTES / 16; i += kThreadsTc)
-    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
-  __syncthreads();
 }
 
 // One segment: this CTA's tiles [ta, tb) of one (unit, token) row range.
@@ -194,27 +195,23 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
   unsigned char* ptile = wbase + kStages * SH::STAGE_BYTES;
   const int pair = a.pair, u = a.u, tok = a.tok;
 
-  // q as MMA B fragments: column n < G is hi(q_n), G <= n < 2G is lo(q_{n-G}).
-  uint32_t qb[KS][NTN][2];
+  // q of this lane's fragment columns: loaded now, turned into MMA B
+  // fragments after the first row copies are issued (the two round trips
+  // overlap).  Column n < G is hi(q_n), G <= n < 2G is lo(q_{n-G}).
+  float qf[KS][NTN][4];
   {
-    const float* qg = p.q + (size_t)pair * G * D;
+    const float* qg = a.qs ? a.qs : p.q + (size_t)pair * G * D;
 #pragma unroll
     for (int nt = 0; nt < NTN; ++nt) {
       const int col = g + 8 * nt;
       const int head = col < G ? col : col - G;
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint16_t e[4];
+      for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int d = 16 * ks + 2 * c + (i & 1) + 8 * (i >> 1);
-          uint16_t hi = 0, lo = 0;
-          if (col < 2 * G) split_bf16(__ldg(qg + head * D + d) * p.scale_log2, hi, lo);
-          e[i] = col < G ? hi : lo;
+          qf[ks][nt][i] = col >= 2 * G ? 0.f : a.qs ? qg[head * D + d] : __ldg(qg + head * D + d);
         }
-        qb[ks][nt][0] = pack2(e[0], e[1]);
-        qb[ks][nt][1] = pack2(e[2], e[3]);
-      }
     }
   }
 
@@ -278,6 +275,9 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
       if (srow >= 0) {
         cp_async16(kst + r * PITCH + ch * 16, s.kbuf + srow * (2 * D) + ch * 16);
         if (!SH::SHARED) cp_async16(vst + r * PITCH + ch * 16, s.vbuf + srow * (2 * D) + ch * 16);
+      } else {  // no row: zeros (finite values, which P = 0 cancels)
+        *reinterpret_cast<uint4*>(kst + r * PITCH + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+        if (!SH::SHARED) *reinterpret_cast<uint4*>(vst + r * PITCH + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     cp_async_commit();  // one group per tile (empty past the end) keeps the count uniform
@@ -294,6 +294,23 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
     if (place)
 #pragma unroll
       for (int i = 0; i < kStages; ++i) place_info(i, pslot[i], psub[i]);
+  }
+  uint32_t qb[KS][NTN][2];
+#pragma unroll
+  for (int nt = 0; nt < NTN; ++nt) {
+    const int col = g + 8 * nt;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint16_t e[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint16_t hi = 0, lo = 0;
+        if (col < 2 * G) split_bf16(qf[ks][nt][i] * p.scale_log2, hi, lo);
+        e[i] = col < G ? hi : lo;
+      }
+      qb[ks][nt][0] = pack2(e[0], e[1]);
+      qb[ks][nt][1] = pack2(e[2], e[3]);
+    }
   }
   for (int i = 0; i < n_my; ++i) {
     const int st = i % kStages;
@@ -516,13 +533,13 @@ __device__ __forceinline__ void tc_write_partial(float* pp, const float* cm, con
 }
 
 // Merges nseg partials of a pair into its output (run by one CTA).  Every
-// partial's (m, l) is loaded at once; the weighted sum of the output rows
-// then takes one round of loads per four partials.  wseg: 2 * nseg * G floats
-// of shared memory.
+// partial's (m, l) and the first QB partials' output rows are loaded at once;
+// later partials take one more round of loads per QB.  wseg: 2 * nseg * G
+// floats of shared memory.
 template <int G, int D>
 __device__ void tc_merge_partials(const float* pbase, int nseg, float* out, float* wseg) {
   constexpr int R = (G * D + kThreadsTc - 1) / kThreadsTc;  // outputs per thread
-  constexpr int QB = 4;                                     // partials per round of loads
+  constexpr int QB = 8;                                     // partials per round of loads
   const size_t stride = (size_t)G * (D + 2);
   const int tid = threadIdx.x;
   float* wm = wseg;             // [nseg][G]: m, then the normalised weight
@@ -532,6 +549,17 @@ __device__ void tc_merge_partials(const float* pbase, int nseg, float* out, floa
     wm[i] = __ldcg(pbase + q2 * stride + h);
     wl[i] = __ldcg(pbase + q2 * stride + G + h);
   }
+  float v[QB][R];
+  auto load_round = [&](int q0) {
+#pragma unroll
+    for (int j = 0; j < QB; ++j)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int o = tid + r * kThreadsTc;
+        v[j][r] = (q0 + j < nseg && o < G * D) ? __ldcg(pbase + (q0 + j) * stride + 2 * G + o) : 0.f;
+      }
+  };
+  load_round(0);
   __syncthreads();
   if (tid < G) {
     float M = -INFINITY, L = 0.f;
@@ -549,14 +577,7 @@ __device__ void tc_merge_partials(const float* pbase, int nseg, float* out, floa
 #pragma unroll
   for (int r = 0; r < R; ++r) O[r] = 0.f;
   for (int q0 = 0; q0 < nseg; q0 += QB) {
-    float v[QB][R];
-#pragma unroll
-    for (int j = 0; j < QB; ++j)
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int o = tid + r * kThreadsTc;
-        v[j][r] = (q0 + j < nseg && o < G * D) ? __ldcg(pbase + (q0 + j) * stride + 2 * G + o) : 0.f;
-      }
+    if (q0) load_round(q0);
 #pragma unroll
     for (int j = 0; j < QB; ++j)
 #pragma unroll
@@ -583,16 +604,15 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
   const int tid = threadIdx.x;
   griddep_wait();
   griddep_launch();
-  if (p.io) {  // this step's q, out and slot map
+  if (p.io) {  // this step's out and slot map (and q when it is not copied)
     const StepIO io = load_io(p.io);
-    p.q = io.q;
+    if (!p.q) p.q = io.q;
     p.out = io.out;
     p.slots = io.slot_map;
   }
   if (tid == 0) s_stop = load_err(s.err);
   __syncthreads();
   if (s_stop) return;
-  tc_zero_staging<SH>(smem);
   float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
 
   const long long T = p.tiles;
@@ -609,6 +629,7 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
     a.tok = pair - a.u * p.n_tok;
     a.ent_base = 0;
     a.list = nullptr;
+    a.qs = nullptr;
     a.rows = p.rows_per_pair;
     a.ta = (int)(t - pair_t0);
     a.tb = (int)(min(t_end, pair_t0 + p.tiles_per_pair) - pair_t0);
@@ -651,27 +672,28 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_hits_kernel(DeviceState s,
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
   __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G], cm[G], cl[G];
+  __shared__ __align__(16) float s_q[G * D];
   __shared__ int s_stop;
   const int tid = threadIdx.x;
+  const int sp = blockIdx.x, pair = blockIdx.y;
   griddep_wait();
   griddep_launch();
-  if (p.io) {  // this step's q and out (slots: the hit slots of match)
-    const StepIO io = load_io(p.io);
-    p.q = io.q;
-    p.out = io.out;
-  }
+  // q (the copy match made) -> shared memory, in flight while the rest starts
+  for (int i = tid; i < G * D / 4; i += kThreadsTc) cp_async16(s_q + 4 * i, p.q + (size_t)pair * G * D + 4 * i);
+  cp_async_commit();
   if (tid == 0) s_stop = load_err(s.err);
-  tc_zero_staging<SH>(smem);  // (its barrier also publishes s_stop)
+  cp_async_wait<0>();
+  __syncthreads();
   if (s_stop) return;
   float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
 
-  const int sp = blockIdx.x, pair = blockIdx.y;
   SegArgs a;
   a.pair = pair;
   a.u = pair / p.n_tok;
   a.tok = pair - a.u * p.n_tok;
   a.ent_base = 0;
   a.list = nullptr;
+  a.qs = s_q;
   a.rows = p.k * p.ET;
   const int tiles = (a.rows + kTileRows - 1) / kTileRows;
   a.ta = (int)((long long)sp * tiles / p.splits_h);
@@ -695,29 +717,28 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
   constexpr int D = SH::D, G = SH::G;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
-  int32_t* list = reinterpret_cast<int32_t*>(smem + kWarpsTc * SH::WARP_BYTES);  // [kScanMax]
-  unsigned long long* cells = reinterpret_cast<unsigned long long*>(list + kScanMax);
+  // The range's cells are staged in the warps' tile staging (free until the
+  // first tile is issued); the list follows the staging.
+  unsigned long long* cells = reinterpret_cast<unsigned long long*>(smem);           // [span]
+  int32_t* list = reinterpret_cast<int32_t*>(smem + kWarpsTc * SH::WARP_BYTES);       // [span]
   __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G], cm[G], cl[G];
+  __shared__ __align__(16) float s_q[G * D];
   __shared__ int s_stop, s_last, s_wsum[kWarpsTc];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sp = blockIdx.x, pair = blockIdx.y;
   const int u = pair / p.n_tok, tok = pair - u * p.n_tok;
-  const int span = s.MS / p.splits_m;  // both powers of two, span <= kScanMax
+  const int span = s.MS / p.splits_m;  // both powers of two, span <= SH::SCAN_MAX
   const int c_lo = sp * span;
   griddep_wait();
   griddep_launch();
-  {
+  {  // the range of the miss set, and q (the copy match made), in one group
     const unsigned long long* src = s.mset + (size_t)u * s.MS + c_lo;
     for (int i = tid; i < span / 2; i += kThreadsTc) cp_async16(cells + 2 * i, src + 2 * i);
+    for (int i = tid; i < G * D / 4; i += kThreadsTc) cp_async16(s_q + 4 * i, p.q + (size_t)pair * G * D + 4 * i);
     cp_async_commit();
   }
-  if (p.io) {
-    const StepIO io = load_io(p.io);
-    p.q = io.q;
-    p.out = io.out;
-  }
+  if (p.io) p.out = load_io(p.io).out;  // used at the end
   if (tid == 0) s_stop = load_err(s.err);
-  tc_zero_staging<SH>(smem);
   cp_async_wait<0>();
   __syncthreads();
   if (s_stop) return;
@@ -772,6 +793,7 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
   a.tok = tok;
   a.ent_base = 0;
   a.list = list;
+  a.qs = s_q;
   a.rows = nlist * p.ET;
   a.ta = 0;
   a.tb = (a.rows + kTileRows - 1) / kTileRows;
@@ -854,20 +876,32 @@ cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int
     // ahead of the reservation and the gather on the other streams.
     return launch_ex(false, attn_tc_hits_kernel<SH>, grid, dim3(kThreadsTc), SH::SMEM, st, s, p);
   }
-  if (s.MS % splits_m != 0 || s.MS / splits_m > kScanMax || (s.MS / splits_m) % 2 != 0 ||
+  if (s.MS % splits_m != 0 || s.MS / splits_m > SH::SCAN_MAX || (s.MS / splits_m) % 2 != 0 ||
       splits_h + splits_m > SH::MAX_SEG)
     return cudaErrorInvalidValue;
   p.place_k = placed->kbuf;
   p.place_v = placed->vbuf;
   p.place_B = placed->B;
   p.mslot = placed->mslot;
-  const size_t smem = SH::SMEM + (size_t)kScanMax * (sizeof(int32_t) + sizeof(unsigned long long));
-  cudaError_t e = ensure_smem((const void*)attn_tc_miss_kernel<SH>, smem, &smem_miss);
+  const size_t smem = SH::SMEM + (size_t)(s.MS / splits_m) * sizeof(int32_t);
+  cudaError_t e = ensure_smem((const void*)attn_tc_miss_kernel<SH>,
+                              SH::SMEM + (size_t)SH::SCAN_MAX * sizeof(int32_t), &smem_miss);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_tc_miss_kernel<SH>, grid, dim3(kThreadsTc), smem, st, s, p);
 }
 
 }  // namespace
+
+int attention_tc_scan_max(int D, int G, int kv_shared) {
+#define X(d, g, sh) \
+  if (D == d && G == g && (kv_shared != 0) == sh) return TcShape<d, g, sh>::SCAN_MAX;
+  X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
+  X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
+  X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)
+  X(64, 1, true) X(64, 2, true) X(64, 4, true) X(64, 8, true)
+#undef X
+  return 0;
+}
 
 int attention_tc_max_segments(int D, int G, int kv_shared) {
 #define X(d, g, sh) \

@@ -14,7 +14,7 @@ constexpr unsigned long long kMissEmpty = ~0ull;
 constexpr int kOrders = 64;                    // reservation classes 0..63
 constexpr int kNotCandidate = 255;
 constexpr int kMaxTokens = 8;
-constexpr int kMissScanMax = 4096;             // miss-set cells one miss-pass CTA scans
+constexpr int kMissScanMax = 4096;             // most miss-set cells one miss-pass CTA scans
 constexpr int kMatchCluster = 8;               // match: one cluster of CTAs per unit
 constexpr int kMatchThreads = 256;             // threads per match CTA
 constexpr int kMatchPerThread = 4;             // selected ids per match thread (n_tok * k <= 8192)
@@ -61,6 +61,7 @@ struct DeviceState {
   int32_t HW, HT;                  // hit bitmaps: 32-slot words per token, token rows per unit
   int32_t kv_shared;
   StepIO* io;                      // this step's inputs and outputs (see StepIO)
+  float* qbuf;                     // [U][n_tok][G][D] this step's q, copied by match
   int64_t ek, ev;                  // bytes of one entry's K row / V row (ev 0 if shared)
   const unsigned char* host_k;     // mapped host KV (device-visible pointers)
   const unsigned char* host_v;
@@ -178,7 +179,8 @@ struct AttnLaunch {
   const float* q;
   float* out;
   const int32_t* slot_map;
-  const StepIO* io;                // when set, q, out and slot_map are read from here
+  const StepIO* io;                // when set, out and slot_map are read from here, and q too
+                                   // when q is null
   int num_sms;                     // SMs of the device (persistent grid size)
   size_t part_capacity;            // floats available at DeviceState::part
 };
@@ -192,13 +194,15 @@ cudaError_t launch_attention_tc(const DeviceState& s, const AttnLaunch& a, int n
                                 cudaStream_t st);
 // pass 0: hit rows of every (unit, token), splits_h CTAs per pair.  pass 1:
 // miss rows from the staging area (s is the staged view), splits_m CTAs per
-// pair (MS / splits_m <= kMissScanMax), each staged row also stored into its
-// reserved slot of `placed` (the real state); then the merge.
+// pair (MS / splits_m <= the shape's scan limit), each staged row also stored
+// into its reserved slot of `placed` (the real state); then the merge.
 cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
                                      int splits_h, int splits_m, const DeviceState* placed,
                                      cudaStream_t st);
 // Most partials (hit + miss splits) one pair's merge takes.
 int attention_tc_max_segments(int D, int G, int kv_shared);
+// Most miss-set cells one miss-pass CTA scans (a power of two).
+int attention_tc_scan_max(int D, int G, int kv_shared);
 bool attention_tc_enabled();
 
 }  // namespace avsg

@@ -21,7 +21,8 @@
 //     claimed or extended with one compare-and-swap; token bits merged, so a
 //     multi-token iteration reserves each id once); the slot map gets
 //     -2 - cell until the reservation kernel resolves it.
-// The miss set and the hit bitmaps are then written out whole (coalesced),
+// The unit's q is also copied to a fixed device buffer for the attention
+// kernels.  The miss set and the hit bitmaps are then written out whole (coalesced),
 // so neither needs clearing between steps.  Nothing in the buffer state
 // (tags, last_step, hash table) changes here, so a BAD_SELECTION leaves the
 // state as it was.
@@ -62,6 +63,12 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
   if (u == 0 && rank == 0 && tid == 0) {
     *s.desc_count = 0;
     *s.io = v;  // for the kernels after this one
+  }
+  {  // this unit's q, copied to a buffer the attention kernels read at a fixed place
+    const int nq = n_tok * s.G * s.D;
+    const float* src = v.q + (size_t)u * nq;
+    float* dst = s.qbuf + (size_t)u * nq;
+    for (int i = rank * kThreads + tid; i < nq; i += kC * kThreads) dst[i] = __ldcg(src + i);
   }
   if (tid == 0) s_stop = load_err(s.err);  // a latched error from an earlier step
   const size_t ubase = (size_t)u * n;
