@@ -193,10 +193,11 @@ def run_ours(args, rank, world, torch):
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
 
-    def make(no_reuse=False):
+    def make(no_reuse=False, request_gather=False):
         cfg = make_config(w.requests, w.kv_heads, w.q_per_kv, w.num_entries, w.head_dim, w.v_dim,
                           w.slots, w.k, entry_tokens=w.entry_tokens, kv_shared=w.kv_shared,
-                          max_tokens_per_step=w.tokens_per_step, no_reuse=no_reuse)
+                          max_tokens_per_step=w.tokens_per_step, no_reuse=no_reuse,
+                          request_gather=request_gather)
         return Session(cfg, hk.ptr, hv.ptr if hv is not None else None)
 
     def timed_pass(sess, steps, profile, sample_clocks=True):
@@ -282,6 +283,24 @@ def run_ours(args, rank, world, torch):
         for p in (sel_h, q_h, out_h):
             p.free()
     sess.close()
+
+    # transfer assignment (AVSG page: even split of the miss transfers across
+    # cores against request-level assignment): the same steps with one gather
+    # CTA per request, the gather timed by the library's events as above
+    res["assign"] = None
+    if not args.skip_no_reuse and w.tokens_per_step >= 1:
+        try:
+            sess = make(request_gather=True)
+        except Exception as exc:  # a shape without the staged gather
+            res["assign"] = {"unavailable": str(exc)}
+        else:
+            a_steps = min(args.steps, 300)
+            info_r = sess.info()
+            _, _, prof_r, _, s0, s1 = timed_pass(sess, a_steps, True, sample_clocks=False)
+            sess.close()
+            res["assign"] = {"request": prof_r.get("gather"), "request_ctas": info_r.gather_ctas,
+                             "request_misses": s1.misses - s0.misses, "steps": a_steps,
+                             "even_ctas": info.gather_ctas}
 
     # no-reuse comparison: every selected row crosses the host link each step
     res["no_reuse_ms_per_step"] = None
@@ -430,6 +449,25 @@ def ncu_traffic() -> dict:
     return out
 
 
+def transfer_assignment(res, w, kernels):
+    """Effective host-link bandwidth of the miss gather (miss bytes / gather
+    time) with the even split over CTAs and with one CTA per request."""
+    a = res.get("assign")
+    if not a or "unavailable" in a or not a.get("request") or not a["request"][1]:
+        return a
+    even = kernels.get("gather")
+    ms_total, n = a["request"]
+    req_us = ms_total / n * 1e3
+    req_bytes = a["request_misses"] / a["steps"] * w.entry_bytes
+    req_gbs = req_bytes / (req_us * 1e-6) / 1e9
+    out = {"request": {"ctas": a["request_ctas"], "gather_us": req_us, "gbs": req_gbs},
+           "even": None, "even_over_request": None}
+    if even:
+        out["even"] = {"ctas": a["even_ctas"], "gather_us": even["avg_us"], "gbs": even["achieved"]}
+        out["even_over_request"] = even["achieved"] / req_gbs if req_gbs else None
+    return out
+
+
 def report_ours(args, res, world, max_ms, max_e2e_ms) -> dict:
     w = res["w"]
     K = args.steps
@@ -490,6 +528,7 @@ def report_ours(args, res, world, max_ms, max_e2e_ms) -> dict:
         "match_victims_attention_hbm": {"gbs": hbm_bytes / (hbm_us * 1e-6) / 1e9 if hbm_us else None,
                                         "frac": (hbm_bytes / (hbm_us * 1e-6) / 1e9) / hbm_peak
                                         if hbm_us else None},
+        "transfer_assignment": transfer_assignment(res, w, kernels),
         "no_reuse": None if res["no_reuse_ms_per_step"] is None else {
             "ms_per_step": res["no_reuse_ms_per_step"],
             "steps_per_s": 1e3 / res["no_reuse_ms_per_step"],

@@ -23,6 +23,7 @@ AVSG_ERR_BAD_STEP = -6
 AVSG_ERR_UNSUPPORTED = -7
 AVSG_ERR_LATCHED = -8
 AVSG_FLAG_NO_REUSE = 1
+AVSG_FLAG_REQUEST_GATHER = 2
 
 ERROR_NAMES = {0: "OK", -1: "INVALID_ARG", -2: "CAPACITY", -3: "CUDA", -4: "BAD_SELECTION",
                -5: "TIMEOUT", -6: "BAD_STEP", -7: "UNSUPPORTED", -8: "LATCHED"}

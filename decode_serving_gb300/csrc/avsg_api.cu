@@ -275,7 +275,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
       c.entry_tokens > 64 || c.head_dim < 8 || c.v_dim < 8 || c.head_dim % 8 || c.v_dim % 8 ||
       c.num_entries < 1 || c.num_entries > 0x7FFFFFFF || c.buffer_slots < 1 || c.max_select < 1 ||
       c.max_tokens_per_step < 1 || c.max_tokens_per_step > kMaxTokens || c.reserved0 || c.reserved1 ||
-      (c.flags & ~AVSG_FLAG_NO_REUSE) || !(c.softmax_scale >= 0.f) || isinf(c.softmax_scale) ||
+      (c.flags & ~(AVSG_FLAG_NO_REUSE | AVSG_FLAG_REQUEST_GATHER)) || !(c.softmax_scale >= 0.f) ||
+      isinf(c.softmax_scale) ||
       (shared && (c.v_dim != c.head_dim || (host_v && host_v != host_k))) || (!shared && !host_v))
     return AVSG_ERR_INVALID_ARG;
   const int64_t U = (int64_t)c.num_requests * c.num_kv_heads;
@@ -289,6 +290,9 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
                                      (c.buffer_slots + 31) / 32) > kMatchSmemMax))
     return AVSG_ERR_CAPACITY;
   if (!attention_supported(c.head_dim, c.v_dim, c.q_per_kv, c.kv_shared)) return AVSG_ERR_UNSUPPORTED;
+  if ((c.flags & AVSG_FLAG_REQUEST_GATHER) && !no_reuse &&
+      !attention_tc_supported(c.head_dim, c.v_dim, c.q_per_kv, c.kv_shared))
+    return AVSG_ERR_UNSUPPORTED;  // request-level assignment exists in the staged gather only
   const int64_t ek = (int64_t)c.entry_tokens * c.head_dim * 2;
   const int64_t ev = shared ? 0 : (int64_t)c.entry_tokens * c.v_dim * 2;
   if ((double)U * max_union * ((ek + ev) / 16) >= 2147483647.0) return AVSG_ERR_INVALID_ARG;
@@ -329,7 +333,10 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   h->tile_rows = attention_rows_per_tile(s.D, s.DV, s.G, s.kv_shared);
   h->target_ctas = h->num_sms * env_int("AVSG_ATTN_CTAS_PER_SM", 4);
   h->gather_ctas = h->num_sms * env_int("AVSG_GATHER_CTAS_PER_SM", 4);
-  h->stage_ctas = env_int("AVSG_STAGE_CTAS", h->num_sms * 2 / 5);
+  // The staged gather splits all units' miss-set cells evenly over its CTAs;
+  // with one CTA per request each CTA's range is exactly one request's units.
+  h->stage_ctas = (c.flags & AVSG_FLAG_REQUEST_GATHER) ? c.num_requests
+                                                       : env_int("AVSG_STAGE_CTAS", h->num_sms * 2 / 5);
   h->miss_splits = env_int("AVSG_MISS_SPLITS", 1);  // at least this many miss-pass CTAs per pair
   {
     int64_t cap = (h->target_ctas + U - 1) / U;
@@ -754,7 +761,8 @@ extern "C" int avsg_get_info(avsg_handle h, avsg_info* out) {
   out->hash_capacity = h->no_reuse ? 0 : h->ds.HS;
   out->miss_set_capacity = h->no_reuse ? 0 : h->ds.MS;
   out->attn_splits = attn_splits(h, 1, h->cfg.max_select);
-  out->gather_ctas = h->gather_ctas;
+  out->gather_ctas = h->staged && overlap_enabled() && attention_tc_enabled() ? h->stage_ctas
+                                                                            : h->gather_ctas;
   out->num_sms = h->num_sms;
   out->host_registered = (h->reg_k || h->reg_v) ? 1 : 0;
   return AVSG_OK;

@@ -37,11 +37,12 @@ class PinnedArray:
 
 def make_config(requests, kv_heads, q_per_kv, num_entries, head_dim, v_dim, buffer_slots,
                 max_select, entry_tokens=1, kv_shared=False, max_tokens_per_step=1,
-                softmax_scale=0.0, no_reuse=False) -> C.avsg_config:
+                softmax_scale=0.0, no_reuse=False, request_gather=False) -> C.avsg_config:
+    flags = (C.AVSG_FLAG_NO_REUSE if no_reuse else 0) | (C.AVSG_FLAG_REQUEST_GATHER if request_gather else 0)
     return C.avsg_config(int(requests), int(kv_heads), int(q_per_kv), int(entry_tokens),
                          int(head_dim), int(v_dim), 1 if kv_shared else 0, 0, int(num_entries),
                          int(buffer_slots), int(max_select), int(max_tokens_per_step),
-                         float(softmax_scale), C.AVSG_FLAG_NO_REUSE if no_reuse else 0, 0)
+                         float(softmax_scale), flags, 0)
 
 
 class Session:

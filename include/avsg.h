@@ -59,6 +59,13 @@ extern "C" {
 
 /* avsg_config.flags */
 #define AVSG_FLAG_NO_REUSE 1u /* no buffer reuse: copy every selected row every step */
+/* The miss gather is assigned by request: one CTA copies all the misses of one
+ * request (its kv-heads' units), the assignment the AVSG page measures its even
+ * split against.  Default: the misses of all units are split evenly over the
+ * gather's CTAs.  Results are identical either way; only the copy's speed
+ * differs.  Needs a shape with a tensor-core attention (else
+ * AVSG_ERR_UNSUPPORTED at create); ignored with AVSG_FLAG_NO_REUSE. */
+#define AVSG_FLAG_REQUEST_GATHER 2u
 
 typedef struct avsg_handle_s* avsg_handle;
 

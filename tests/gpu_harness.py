@@ -23,10 +23,11 @@ def make_host_kv(w):
     return hk, hv
 
 
-def make_session(w, hk, hv, no_reuse=False):
+def make_session(w, hk, hv, no_reuse=False, request_gather=False):
     cfg = make_config(w.requests, w.kv_heads, w.q_per_kv, w.num_entries, w.head_dim, w.v_dim,
                       w.slots, w.k, entry_tokens=w.entry_tokens, kv_shared=w.kv_shared,
-                      max_tokens_per_step=w.tokens_per_step, no_reuse=no_reuse)
+                      max_tokens_per_step=w.tokens_per_step, no_reuse=no_reuse,
+                      request_gather=request_gather)
     return Session(cfg, hk.ptr, hv.ptr if hv is not None else None)
 
 
@@ -38,7 +39,8 @@ def distinct_hits(sel_u, hit_u):
 class Parity:
     """GPU and oracle over the same inputs; ``units`` limits the oracle side."""
 
-    def __init__(self, w, steps=None, units=None, sel=None, q=None, no_reuse=False, seed=W.DEFAULT_SEED):
+    def __init__(self, w, steps=None, units=None, sel=None, q=None, no_reuse=False, seed=W.DEFAULT_SEED,
+                 request_gather=False):
         self.w = w
         self.steps = w.steps if steps is None else steps
         self.sel = W.selections(w, self.steps, seed=seed) if sel is None else sel
@@ -46,7 +48,7 @@ class Parity:
         self.units = list(range(w.units)) if units is None else list(units)
         self.no_reuse = no_reuse
         self.hk, self.hv = make_host_kv(w)
-        self.sess = make_session(w, self.hk, self.hv, no_reuse)
+        self.sess = make_session(w, self.hk, self.hv, no_reuse, request_gather)
         self.ref = oracle.OracleRun(w.slots, self.hk.array, None if self.hv is None else self.hv.array,
                                     w.head_dim, w.v_dim, w.softmax_scale, units=self.units)
         dev = torch.device("cuda")

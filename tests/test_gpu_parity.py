@@ -73,6 +73,15 @@ def test_no_reuse_path(name):
     assert err <= ATTN_TOL
 
 
+@pytest.mark.parametrize("name", ["batch_small", "mtp_small", "pages_small"])
+def test_request_level_gather_gives_the_same_results(name):
+    """Transfer assignment by request (one gather CTA per request) changes only
+    which CTA copies which miss: every slot map, buffer row and output still
+    follows the oracle."""
+    err, _ = run_parity(SMALL[name].replace(steps=8), request_gather=True)
+    assert err <= ATTN_TOL
+
+
 def test_single_entry_returns_its_v_row():
     w = W.get_workload("tiny", k=1, slots=8, steps=3, forced="none")
     p = Parity(w)
