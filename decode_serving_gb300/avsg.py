@@ -45,7 +45,7 @@ class avsg_config(ctypes.Structure):
         ("max_tokens_per_step", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
         ("flags", ctypes.c_uint32),
-        ("reserved1", ctypes.c_int32),
+        ("initial_entries", ctypes.c_int32),
     ]
 
 
@@ -93,6 +93,7 @@ SIGNATURES = {
     "avsg_destroy": [_P],
     "avsg_step": [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P],
     "avsg_step_host": [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P],
+    "avsg_append": [_P, _P, _P, _P],
     "avsg_get_stats": [_P, ctypes.POINTER(avsg_stats)],
     "avsg_get_info": [_P, ctypes.POINTER(avsg_info)],
     "avsg_read_state": [_P, _I32, _P, _P, _P, _P],
@@ -152,6 +153,10 @@ def avsg_create(cfg: avsg_config, host_k: int, host_v: int | None) -> int:
 
 def avsg_destroy(h: int) -> None:
     _check(load_library().avsg_destroy(h), "avsg_destroy")
+
+
+def avsg_append(h, d_k, d_v=0, stream=0) -> None:
+    _check(load_library().avsg_append(h, d_k, d_v or None, stream or None), "avsg_append", h)
 
 
 def avsg_step(h, t, n_tok, k, d_sel, d_q, d_out, d_slot_map=0, d_hit=0, stream=0) -> None:

@@ -28,6 +28,7 @@ struct avsg_handle_s {
   cudaStream_t last_stream = nullptr;
   cudaError_t cuda_err = cudaSuccess;
   uint64_t steps = 0, selected = 0, host_misses = 0;
+  int64_t live = 0;  // entries per unit selectable (avsg_append adds one)
   float scale_log2 = 0.f;
   size_t part_floats = 0;
   int32_t* slot_scratch = nullptr;  // [U][max_union] when the caller passes no slot map
@@ -108,8 +109,10 @@ void rebase(T** p, void* base) {
 }
 
 // Maps caller host memory for device reads: mapped allocations are used in
-// place, anything else is registered here (and unregistered on destroy).
-int map_host(avsg_handle h, const void* p, size_t bytes, const unsigned char** dptr, bool* registered) {
+// place, anything else is registered here (and unregistered on destroy),
+// read-only unless entries can still be appended.
+int map_host(avsg_handle h, const void* p, size_t bytes, bool read_only, const unsigned char** dptr,
+             bool* registered) {
   cudaPointerAttributes attr;
   cudaError_t e = cudaPointerGetAttributes(&attr, p);
   if (e == cudaSuccess && attr.type == cudaMemoryTypeHost && attr.devicePointer) {
@@ -118,7 +121,8 @@ int map_host(avsg_handle h, const void* p, size_t bytes, const unsigned char** d
     return AVSG_OK;
   }
   cudaGetLastError();
-  e = cudaHostRegister(const_cast<void*>(p), bytes, cudaHostRegisterMapped | cudaHostRegisterReadOnly);
+  e = cudaHostRegister(const_cast<void*>(p), bytes,
+                       cudaHostRegisterMapped | (read_only ? cudaHostRegisterReadOnly : 0u));
   if (e != cudaSuccess) {
     cudaGetLastError();
     e = cudaHostRegister(const_cast<void*>(p), bytes, cudaHostRegisterMapped);
@@ -274,7 +278,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   if (c.num_requests < 1 || c.num_kv_heads < 1 || c.q_per_kv < 1 || c.entry_tokens < 1 ||
       c.entry_tokens > 64 || c.head_dim < 8 || c.v_dim < 8 || c.head_dim % 8 || c.v_dim % 8 ||
       c.num_entries < 1 || c.num_entries > 0x7FFFFFFF || c.buffer_slots < 1 || c.max_select < 1 ||
-      c.max_tokens_per_step < 1 || c.max_tokens_per_step > kMaxTokens || c.reserved0 || c.reserved1 ||
+      c.max_tokens_per_step < 1 || c.max_tokens_per_step > kMaxTokens || c.reserved0 ||
+      c.initial_entries < 0 || (int64_t)c.initial_entries > c.num_entries ||
       (c.flags & ~(AVSG_FLAG_NO_REUSE | AVSG_FLAG_REQUEST_GATHER)) || !(c.softmax_scale >= 0.f) ||
       isinf(c.softmax_scale) ||
       (shared && (c.v_dim != c.head_dim || (host_v && host_v != host_k))) || (!shared && !host_v))
@@ -302,6 +307,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   h->no_reuse = no_reuse;
   h->host_k = host_k;
   h->host_v = shared ? nullptr : host_v;
+  h->live = c.initial_entries > 0 ? c.initial_entries : c.num_entries;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e != cudaSuccess) {
@@ -347,9 +353,10 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   const float scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / sqrtf((float)c.head_dim);
   h->scale_log2 = scale * 1.4426950408889634f;
 
-  int rc = map_host(h, host_k, (size_t)(U * c.num_entries * ek), &s.host_k, &h->reg_k);
+  const bool read_only = h->live >= c.num_entries;  // nothing left to append
+  int rc = map_host(h, host_k, (size_t)(U * c.num_entries * ek), read_only, &s.host_k, &h->reg_k);
   if (rc == AVSG_OK && !shared)
-    rc = map_host(h, host_v, (size_t)(U * c.num_entries * ev), &s.host_v, &h->reg_v);
+    rc = map_host(h, host_v, (size_t)(U * c.num_entries * ev), read_only, &s.host_v, &h->reg_v);
   if (shared) s.host_v = s.host_k;
   if (rc != AVSG_OK) {
     release(h);
@@ -662,6 +669,7 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
   v.slot_map = d_slot_map ? d_slot_map : h->slot_scratch;
   v.hit = d_hit;
   v.t = t;
+  v.live = (int32_t)h->live;
   if (h->prof || !graphs_enabled()) return enqueue_dag(h, n_tok, k, v, st, nullptr, nullptr);
   avsg_handle_s::StepGraph* g = nullptr;
   const int rc = step_graph(h, n_tok, k, v, &g);
@@ -724,6 +732,28 @@ extern "C" int avsg_step_host(avsg_handle h, int32_t t, int32_t n_tok, int32_t k
   if (e == cudaSuccess && h_hit && n_sel)
     e = cudaMemcpyAsync(h_hit, h->hit_scratch, n_sel, cudaMemcpyDeviceToHost, st);
   return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
+}
+
+extern "C" int avsg_append(avsg_handle h, const void* d_k, const void* d_v, void* stream) {
+  if (!h || !d_k || (!h->cfg.kv_shared && !d_v)) return AVSG_ERR_INVALID_ARG;
+  if (h->latched) return AVSG_ERR_LATCHED;
+  if (h->live >= h->cfg.num_entries) return AVSG_ERR_CAPACITY;
+  const DeviceState& s = h->ds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // one entry per unit: unit u's new row goes to host row (u * L + live)
+  const size_t ek = (size_t)s.ek, pitch = (size_t)h->cfg.num_entries * ek;
+  cudaError_t e = cudaMemcpy2DAsync(static_cast<unsigned char*>(const_cast<void*>(h->host_k)) +
+                                        (size_t)h->live * ek,
+                                    pitch, d_k, ek, ek, (size_t)s.U, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && !h->cfg.kv_shared) {
+    const size_t ev = (size_t)s.ev, vpitch = (size_t)h->cfg.num_entries * ev;
+    e = cudaMemcpy2DAsync(static_cast<unsigned char*>(const_cast<void*>(h->host_v)) +
+                              (size_t)h->live * ev,
+                          vpitch, d_v, ev, ev, (size_t)s.U, cudaMemcpyDeviceToHost, st);
+  }
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  h->live += 1;
+  return AVSG_OK;
 }
 
 extern "C" int avsg_get_stats(avsg_handle h, avsg_stats* out) {

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) gather_all_kernel(DeviceState s, Ste
     unit = (int)(d / per_unit);
     slot = (int)(d - (uint32_t)unit * per_unit);
     id = __ldg(sel + d);
-    if (id < 0 || (int64_t)id >= s.L) {
+    if (id < 0 || id >= v.live) {
       raise_error(s.err, AVSG_ERR_BAD_SELECTION, unit, slot);
       return false;
     }

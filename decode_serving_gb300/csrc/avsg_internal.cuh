@@ -49,7 +49,7 @@ struct StepIO {
   int32_t* slot_map;
   uint8_t* hit;
   int32_t t;
-  int32_t pad;
+  int32_t live;                    // entries per unit selectable this step (ids below it)
 };
 
 struct DeviceState {

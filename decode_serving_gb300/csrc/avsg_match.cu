@@ -11,7 +11,7 @@
 // position of the unit's n_tok * k selected ids (at most kMatchPerThread),
 // loads all of them and then all of their first hash windows before it
 // resolves any.  Per id:
-//   * range check (id in [0, L)), else BAD_SELECTION;
+//   * range check (id in [0, live), the entries live this step), else BAD_SELECTION;
 //   * lookup in the unit's open-addressed table (linear probing, Fibonacci
 //     hash; a probe reads a 16-byte window of two cells);
 //   * a hit writes its slot (slot map and the hit-slot list the attention
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
   int4 win[kMatchPerThread];
 #pragma unroll
   for (int j = 0; j < kMatchPerThread; ++j) {
-    const bool valid = !stop && first + j * kC * kThreads < n && id[j] >= 0 && (int64_t)id[j] < s.L;
+    const bool valid = !stop && first + j * kC * kThreads < n && id[j] >= 0 && id[j] < v.live;
     win[j] = valid ? __ldcg(reinterpret_cast<const int4*>(tab + (fib_hash(id[j], s.hs_shift) & ~1u)))
                    : make_int4(kEmpty, -1, kEmpty, -1);
   }
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
     const size_t off = ubase + pos;
     const int tok = pos / k;
     const int32_t x = id[j];
-    if (x < 0 || (int64_t)x >= s.L) {
+    if (x < 0 || x >= v.live) {
       raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
       slot_map[off] = -1;
       s.hslot[off] = -1;

@@ -37,12 +37,13 @@ class PinnedArray:
 
 def make_config(requests, kv_heads, q_per_kv, num_entries, head_dim, v_dim, buffer_slots,
                 max_select, entry_tokens=1, kv_shared=False, max_tokens_per_step=1,
-                softmax_scale=0.0, no_reuse=False, request_gather=False) -> C.avsg_config:
+                softmax_scale=0.0, no_reuse=False, request_gather=False,
+                initial_entries=0) -> C.avsg_config:
     flags = (C.AVSG_FLAG_NO_REUSE if no_reuse else 0) | (C.AVSG_FLAG_REQUEST_GATHER if request_gather else 0)
     return C.avsg_config(int(requests), int(kv_heads), int(q_per_kv), int(entry_tokens),
                          int(head_dim), int(v_dim), 1 if kv_shared else 0, 0, int(num_entries),
                          int(buffer_slots), int(max_select), int(max_tokens_per_step),
-                         float(softmax_scale), flags, 0)
+                         float(softmax_scale), flags, int(initial_entries))
 
 
 class Session:
@@ -69,6 +70,12 @@ class Session:
         C.avsg_step_host(self.handle, int(t), n_tok, k, sel.ctypes.data, q.ctypes.data,
                          out.ctypes.data, slot_map.ctypes.data if slot_map is not None else 0,
                          hit.ctypes.data if hit is not None else 0, stream)
+
+    def append(self, k_rows, v_rows=None, stream=0):
+        """One new entry per unit (Offload): k_rows [U][entry_tokens*D] bf16 bits,
+        v_rows like it for V (None when K and V are shared): CUDA tensors."""
+        C.avsg_append(self.handle, k_rows.data_ptr(),
+                      v_rows.data_ptr() if v_rows is not None else 0, stream)
 
     def stats(self) -> C.avsg_stats:
         return C.avsg_get_stats(self.handle)

@@ -74,7 +74,9 @@ typedef struct avsg_handle_s* avsg_handle;
  * Host K is laid out [R][H][num_entries][entry_tokens][head_dim] bf16, host V
  * [R][H][num_entries][entry_tokens][v_dim] bf16: one entry of a unit is a
  * contiguous row of entry_tokens tokens (a head-wise page when > 1, Spin page
- * section 2B "head-wise physical pages").
+ * section 2B "head-wise physical pages").  The first initial_entries entries
+ * of every unit are live at create (all num_entries when 0); selected ids must
+ * be below the live count, which avsg_append raises by one per call.
  */
 typedef struct avsg_config {
   int32_t num_requests;        /* R >= 1 */
@@ -85,13 +87,14 @@ typedef struct avsg_config {
   int32_t v_dim;               /* Dv: V row width (== head_dim when kv_shared) */
   int32_t kv_shared;           /* 1: V is the K row itself (latent cache) */
   int32_t reserved0;           /* must be 0 */
-  int64_t num_entries;         /* entries per unit, 1 .. 2^31 - 1 */
+  int64_t num_entries;         /* entries per unit the host arrays hold, 1 .. 2^31 - 1 */
   int32_t buffer_slots;        /* B: device slots per unit */
   int32_t max_select;          /* largest k accepted by avsg_step */
   int32_t max_tokens_per_step; /* largest n_tok (1 .. 8) */
   float softmax_scale;         /* 0 selects 1/sqrt(head_dim) */
   uint32_t flags;              /* AVSG_FLAG_* */
-  int32_t reserved1;           /* must be 0 */
+  int32_t initial_entries;     /* entries live at create, 0 .. num_entries (0: all of
+                                  them); avsg_append adds one per unit per call */
 } avsg_config;
 
 typedef struct avsg_stats {
@@ -195,6 +198,21 @@ int avsg_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32_t*
 int avsg_step_host(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32_t* h_sel,
                    const float* h_q, float* h_out, int32_t* h_slot_map, uint8_t* h_hit,
                    void* stream);
+
+/*
+ * Offload of a decode step's new KV (Spin page, section 2A, the Offload
+ * operation): writes one new entry per unit into the host arrays at entry
+ * index `live` (the current live count) and makes it selectable from the next
+ * step on.  d_k: device bf16 [R][H][entry_tokens * head_dim]; d_v: device bf16
+ * [R][H][entry_tokens * v_dim], NULL when kv_shared.  One strided copy per
+ * array, device to host, enqueued on `stream` (ordered before later steps on
+ * that stream); the buffer is not touched (a new entry is a miss until it is
+ * selected).  For paged entries, a page is appended once it is full.
+ * Works the same with AVSG_FLAG_NO_REUSE (both paths read host rows by id).
+ * Returns CAPACITY when all num_entries entries are live, INVALID_ARG for
+ * NULL rows, CUDA if the copy cannot be enqueued.
+ */
+int avsg_append(avsg_handle h, const void* d_k, const void* d_v, void* stream);
 
 /* avsg_get_stats -- synchronise the last stream used and read the counters. */
 int avsg_get_stats(avsg_handle h, avsg_stats* out);

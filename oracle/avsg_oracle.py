@@ -26,6 +26,11 @@ What it computes, and where that comes from:
   then the probability-weighted sum of the V rows; computed in fp64, straight
   from the host KV rows of the selected ids, so it does not depend on the
   buffer at all.
+* Offload (Spin page, section 2A, the Offload operation): a decode step's new
+  KV entry is written to the host store; it is selectable from the next step
+  on and, like any id, enters the buffer only as a miss.  Here the host store
+  holds ``capacity`` entries per unit, of which the first ``live`` are
+  selectable; ``append`` writes entry ``live`` and raises the count.
 
 Everything is written as the plain definition: a dense id -> slot table, a
 library sort for the victim order, a matmul and ``exp`` for attention.
@@ -77,11 +82,13 @@ class UnitBuffer:
     host_v is None when V aliases K (latent cache).
     """
 
-    def __init__(self, num_slots: int, host_k: np.ndarray, host_v: np.ndarray | None = None):
+    def __init__(self, num_slots: int, host_k: np.ndarray, host_v: np.ndarray | None = None,
+                 live: int | None = None):
         self.B = int(num_slots)
         self.host_k = host_k
         self.host_v = host_v
-        self.L = host_k.shape[0]
+        self.L = host_k.shape[0]            # capacity of the host store
+        self.live = self.L if live is None else int(live)
         self.tag = np.full(self.B, EMPTY, dtype=np.int64)
         self.last = np.full(self.B, -1, dtype=np.int64)
         self.slot_of = np.full(self.L, EMPTY, dtype=np.int64)
@@ -94,7 +101,7 @@ class UnitBuffer:
         if t < 0 or (self.prev_t is not None and t <= self.prev_t):
             raise OracleError(ERR_BAD_STEP, f"t={t} after t={self.prev_t}")
         for s in sels:
-            if s.size and (s.min() < 0 or s.max() >= self.L):
+            if s.size and (s.min() < 0 or s.max() >= self.live):
                 raise OracleError(ERR_BAD_SELECTION, "id out of range")
             if np.unique(s).size != s.size:
                 raise OracleError(ERR_BAD_SELECTION, "duplicate id in one selection")
@@ -102,6 +109,17 @@ class UnitBuffer:
         if union.size > self.B:
             raise OracleError(ERR_CAPACITY, f"{union.size} distinct ids > {self.B} slots")
         return union
+
+    # -- offload ------------------------------------------------------------
+    def append(self, k_row: np.ndarray, v_row: np.ndarray | None = None) -> int:
+        """Writes a new entry to the host store; returns its id."""
+        if self.live >= self.L:
+            raise OracleError(ERR_CAPACITY, "host store full")
+        self.host_k[self.live] = k_row
+        if self.host_v is not None:
+            self.host_v[self.live] = v_row
+        self.live += 1
+        return self.live - 1
 
     # -- the step -----------------------------------------------------------
     def victim_order(self, t: int) -> np.ndarray:
@@ -193,14 +211,20 @@ class OracleRun:
     """
 
     def __init__(self, num_slots: int, host_k: np.ndarray, host_v: np.ndarray | None,
-                 head_dim: int, v_dim: int, scale: float, units=None):
+                 head_dim: int, v_dim: int, scale: float, units=None, live: int | None = None):
         self.units = list(range(host_k.shape[0])) if units is None else list(units)
-        self.state = {u: UnitBuffer(num_slots, host_k[u], None if host_v is None else host_v[u])
+        self.state = {u: UnitBuffer(num_slots, host_k[u], None if host_v is None else host_v[u],
+                                    live)
                       for u in self.units}
         self.host_k, self.host_v = host_k, host_v
         self.head_dim, self.v_dim, self.scale = head_dim, v_dim, scale
         self.hits = 0
         self.misses = 0
+
+    def append(self, k_rows: np.ndarray, v_rows: np.ndarray | None = None):
+        """One new entry per unit: k_rows / v_rows [units of the host store][row]."""
+        for u in self.units:
+            self.state[u].append(k_rows[u], None if v_rows is None else v_rows[u])
 
     def step(self, t: int, sel_t: np.ndarray, q_t: np.ndarray | None = None,
              attention: bool = True):

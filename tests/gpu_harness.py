@@ -23,11 +23,11 @@ def make_host_kv(w):
     return hk, hv
 
 
-def make_session(w, hk, hv, no_reuse=False, request_gather=False):
+def make_session(w, hk, hv, no_reuse=False, request_gather=False, initial_entries=0):
     cfg = make_config(w.requests, w.kv_heads, w.q_per_kv, w.num_entries, w.head_dim, w.v_dim,
                       w.slots, w.k, entry_tokens=w.entry_tokens, kv_shared=w.kv_shared,
                       max_tokens_per_step=w.tokens_per_step, no_reuse=no_reuse,
-                      request_gather=request_gather)
+                      request_gather=request_gather, initial_entries=initial_entries)
     return Session(cfg, hk.ptr, hv.ptr if hv is not None else None)
 
 
@@ -40,7 +40,7 @@ class Parity:
     """GPU and oracle over the same inputs; ``units`` limits the oracle side."""
 
     def __init__(self, w, steps=None, units=None, sel=None, q=None, no_reuse=False, seed=W.DEFAULT_SEED,
-                 request_gather=False):
+                 request_gather=False, initial_entries=0):
         self.w = w
         self.steps = w.steps if steps is None else steps
         self.sel = W.selections(w, self.steps, seed=seed) if sel is None else sel
@@ -48,9 +48,17 @@ class Parity:
         self.units = list(range(w.units)) if units is None else list(units)
         self.no_reuse = no_reuse
         self.hk, self.hv = make_host_kv(w)
-        self.sess = make_session(w, self.hk, self.hv, no_reuse, request_gather)
-        self.ref = oracle.OracleRun(w.slots, self.hk.array, None if self.hv is None else self.hv.array,
-                                    w.head_dim, w.v_dim, w.softmax_scale, units=self.units)
+        self.sess = make_session(w, self.hk, self.hv, no_reuse, request_gather, initial_entries)
+        if initial_entries:
+            # appends write the GPU side's host arrays: the oracle keeps its own copy
+            self.ref = oracle.OracleRun(w.slots, self.hk.array.copy(),
+                                        None if self.hv is None else self.hv.array.copy(),
+                                        w.head_dim, w.v_dim, w.softmax_scale, units=self.units,
+                                        live=initial_entries)
+        else:
+            self.ref = oracle.OracleRun(w.slots, self.hk.array,
+                                        None if self.hv is None else self.hv.array,
+                                        w.head_dim, w.v_dim, w.softmax_scale, units=self.units)
         dev = torch.device("cuda")
         shape = (w.units, w.tokens_per_step, w.k)
         self.out = torch.empty((w.units, w.tokens_per_step, w.q_per_kv, w.v_dim), dtype=torch.float32,
@@ -96,6 +104,13 @@ class Parity:
             self.max_err = max(self.max_err, err)
             assert err <= ATTN_TOL, f"attention error {err} t={t} unit={u}"
         return res
+
+    def append(self, k_rows, v_rows=None):
+        """One new entry per unit on both sides: k_rows / v_rows uint16 [U][row]."""
+        kd = torch.from_numpy(np.ascontiguousarray(k_rows).view(np.int16)).cuda()
+        vd = None if v_rows is None else torch.from_numpy(np.ascontiguousarray(v_rows).view(np.int16)).cuda()
+        self.sess.append(kd, vd)
+        self.ref.append(k_rows, v_rows)
 
     def check_state(self, rows=True):
         for u in self.units:
