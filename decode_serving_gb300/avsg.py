@@ -10,6 +10,8 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
+
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libavsg.so")
 
@@ -94,6 +96,8 @@ SIGNATURES = {
     "avsg_step": [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P],
     "avsg_step_host": [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P],
     "avsg_append": [_P, _P, _P, _P],
+    "avsg_set_budget": [_P, _P, _P],
+    "avsg_plan_budget": [ctypes.c_int64, _I32, _I32, _I32, _P, _P],
     "avsg_get_stats": [_P, ctypes.POINTER(avsg_stats)],
     "avsg_get_info": [_P, ctypes.POINTER(avsg_info)],
     "avsg_read_state": [_P, _I32, _P, _P, _P, _P],
@@ -153,6 +157,21 @@ def avsg_create(cfg: avsg_config, host_k: int, host_v: int | None) -> int:
 
 def avsg_destroy(h: int) -> None:
     _check(load_library().avsg_destroy(h), "avsg_destroy")
+
+
+def avsg_set_budget(h, slots_per_unit: np.ndarray, stream=0) -> None:
+    a = np.ascontiguousarray(slots_per_unit, dtype=np.int32)
+    _check(load_library().avsg_set_budget(h, a.ctypes.data, stream or None), "avsg_set_budget", h)
+
+
+def avsg_plan_budget(total_slots: int, num_units: int, mandatory: int, max_slots: int,
+                     weights=None) -> np.ndarray:
+    out = np.zeros(num_units, np.int32)
+    w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32)
+    _check(load_library().avsg_plan_budget(int(total_slots), int(num_units), int(mandatory),
+                                           int(max_slots), None if w is None else w.ctypes.data,
+                                           out.ctypes.data), "avsg_plan_budget")
+    return out
 
 
 def avsg_append(h, d_k, d_v=0, stream=0) -> None:

@@ -29,6 +29,9 @@ struct avsg_handle_s {
   cudaError_t cuda_err = cudaSuccess;
   uint64_t steps = 0, selected = 0, host_misses = 0;
   int64_t live = 0;  // entries per unit selectable (avsg_append adds one)
+  std::vector<int32_t> budget;  // usable slots per unit (avsg_set_budget)
+  int32_t min_budget = 0;
+  int32_t* budget_new = nullptr;  // device [U]: the budgets a set_budget call brings
   float scale_log2 = 0.f;
   size_t part_floats = 0;
   int32_t* slot_scratch = nullptr;  // [U][max_union] when the caller passes no slot map
@@ -250,6 +253,8 @@ int init_state(avsg_handle h, cudaStream_t st) {
     AVSG_SET(s.hitbits, 0, (size_t)s.U * s.HT * s.HW * 4);
     AVSG_SET(s.htab, 0xFF, (size_t)s.U * s.HS * sizeof(int2));
     AVSG_SET(s.hused, 0, (size_t)s.U * 4);
+    if (e == cudaSuccess && !h->budget.empty())
+      e = cudaMemcpyAsync(s.budget, h->budget.data(), (size_t)s.U * 4, cudaMemcpyHostToDevice, st);
     AVSG_SET(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
   }
   AVSG_SET(s.desc_count, 0, 4);
@@ -406,6 +411,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.part_count, (size_t)U * kMaxTokens);
   cv.take(&s.counters, (size_t)U);
   cv.take(&s.err, 1);
+  cv.take(&s.budget, (size_t)U);
+  cv.take(&h->budget_new, (size_t)U);
   cv.take(&h->slot_scratch, (size_t)U * max_union);
   cv.take(&h->hit_scratch, (size_t)U * max_union);
   cv.take(&h->stage_sel, (size_t)U * max_union);
@@ -425,7 +432,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   rebase(&s.desc_count, b); rebase(&s.part, b);
   rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&s.mset, b); rebase(&s.hslot, b);
   rebase(&s.part_count, b);
-  rebase(&s.counters, b); rebase(&s.err, b);
+  rebase(&s.counters, b); rebase(&s.err, b); rebase(&s.budget, b); rebase(&h->budget_new, b);
   rebase(&h->slot_scratch, b); rebase(&h->hit_scratch, b); rebase(&h->stage_sel, b);
   rebase(&h->stage_q, b); rebase(&h->stage_out, b);
   if (shared) {
@@ -448,6 +455,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     release(h);
     return AVSG_ERR_CUDA;
   }
+  h->budget.assign((size_t)U, s.B);
+  h->min_budget = s.B;
   rc = init_state(h, nullptr);
   if (rc == AVSG_OK) {
     e = cudaDeviceSynchronize();
@@ -690,6 +699,7 @@ int check_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k) {
   if (n_tok < 1 || n_tok > h->cfg.max_tokens_per_step || k < 0) return AVSG_ERR_INVALID_ARG;
   if (k > h->cfg.max_select) return AVSG_ERR_CAPACITY;
   if ((int64_t)n_tok * k > h->ds.max_union) return AVSG_ERR_CAPACITY;
+  if (!h->no_reuse && (int64_t)n_tok * k > h->min_budget) return AVSG_ERR_CAPACITY;
   if (t < 0 || (h->has_t && t <= h->last_t)) return AVSG_ERR_BAD_STEP;
   return AVSG_OK;
 }
@@ -753,6 +763,50 @@ extern "C" int avsg_append(avsg_handle h, const void* d_k, const void* d_v, void
   }
   if (e != cudaSuccess) return fail_cuda(h, e);
   h->live += 1;
+  return AVSG_OK;
+}
+
+extern "C" int avsg_set_budget(avsg_handle h, const int32_t* slots_per_unit, void* stream) {
+  if (!h || !slots_per_unit) return AVSG_ERR_INVALID_ARG;
+  if (h->no_reuse) return AVSG_ERR_UNSUPPORTED;
+  if (h->latched) return AVSG_ERR_LATCHED;
+  const DeviceState& s = h->ds;
+  int32_t lo = s.B;
+  for (int u = 0; u < s.U; ++u) {
+    if (slots_per_unit[u] < 1 || slots_per_unit[u] > s.B) return AVSG_ERR_INVALID_ARG;
+    lo = slots_per_unit[u] < lo ? slots_per_unit[u] : lo;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h->budget_new, slots_per_unit, (size_t)s.U * sizeof(int32_t),
+                                  cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = launch_budget(s, h->budget_new, st);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  h->budget.assign(slots_per_unit, slots_per_unit + s.U);
+  h->min_budget = lo;
+  return AVSG_OK;
+}
+
+extern "C" int avsg_plan_budget(int64_t total_slots, int32_t num_units, int32_t mandatory,
+                                int32_t max_slots, const float* weights, int32_t* out) {
+  if (num_units < 1 || mandatory < 1 || max_slots < mandatory || !out || total_slots < 0)
+    return AVSG_ERR_INVALID_ARG;
+  const int64_t extra = total_slots - (int64_t)num_units * mandatory;
+  if (extra < 0) return AVSG_ERR_CAPACITY;
+  double wsum = 0.0;
+  if (weights)
+    for (int u = 0; u < num_units; ++u) {
+      if (!(weights[u] >= 0.f) || isinf(weights[u])) return AVSG_ERR_INVALID_ARG;
+      wsum += weights[u];
+    }
+  for (int u = 0; u < num_units; ++u) {
+    int64_t share;
+    if (wsum > 0.0)
+      share = (int64_t)floor((double)extra * (double)weights[u] / wsum);
+    else
+      share = extra / num_units + (u < extra % num_units ? 1 : 0);
+    const int64_t b = (int64_t)mandatory + share;
+    out[u] = (int32_t)(b < max_slots ? b : max_slots);
+  }
   return AVSG_OK;
 }
 

@@ -86,6 +86,7 @@ struct DeviceState {
   int32_t* part_count;             // [U][max_tokens] arrival counters, 0 between steps
   DevCounters* counters;           // [U] distinct hits / misses, summed over steps
   DevErr* err;
+  int32_t* budget;                 // [U] usable slots per unit (buffer elasticity), <= B
 };
 
 __device__ __forceinline__ uint32_t fib_hash(int32_t id, int shift) {
@@ -161,6 +162,8 @@ size_t match_smem_bytes(int MS, int n_tok, int HW);
 cudaError_t launch_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st);
 size_t victims_smem_bytes(const DeviceState& s);
 cudaError_t launch_victims(const DeviceState& s, int n_tok, int k, cudaStream_t st);
+// New per-unit slot budgets (device [U]): evicts entries above lowered budgets.
+cudaError_t launch_budget(const DeviceState& s, const int32_t* budget_new, cudaStream_t st);
 // Hash-table update of a step (erase evicted ids, insert new ones, rebuild):
 // needed only by the next step's match, so it may run beside the gather and
 // the attention.

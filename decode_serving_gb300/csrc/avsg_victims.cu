@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   griddep_launch();
   const StepIO io = load_io(s.io);
   const int t = io.t;
+  const int budget = __ldcg(s.budget + u);  // this unit's usable slots (buffer elasticity)
   int32_t* __restrict__ slot_map = io.slot_map;
   if (tid == 0) {
     s_stop = load_err(s.err);
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
       if (sn[b] > 0) {
         s.last[ub + sl] = t;  // selected this step: refreshed, never a victim
         ++hits;
-      } else if (sn[b] == 0) {
+      } else if (sn[b] == 0 && sl < budget) {  // slots at or above the budget are not used
         if (tg[b] == kEmpty) {
           o = 0;
         } else {
@@ -438,6 +439,40 @@ int g_victims_smem = 0;
 }  // namespace
 
 size_t victims_smem_bytes(const DeviceState& s) { return victims_layout(s.max_union, s.B).total; }
+
+namespace {
+
+// Buffer elasticity (Spin page, section 2B): a unit's budget of usable slots
+// changes between steps.  Entries held in slots at or above a lowered budget
+// are dropped: erased from the hash table, the slot emptied.  Slots above a
+// raised budget are already empty.  budget_new [U] takes effect here.
+__global__ void __launch_bounds__(kCommitThreads) budget_kernel(DeviceState s,
+                                                                 const int32_t* __restrict__ budget_new) {
+  const int u = blockIdx.x;
+  griddep_wait();
+  griddep_launch();
+  if (load_err(s.err) != 0) return;
+  const int old_b = __ldcg(s.budget + u), new_b = budget_new[u];
+  int2* tab = s.htab + (size_t)u * s.HS;
+  const uint32_t hmask = (uint32_t)s.HS - 1u;
+  const size_t ub = (size_t)u * s.B;
+  for (int sl = new_b + (int)threadIdx.x; sl < old_b; sl += kCommitThreads) {
+    const int32_t tg = s.tag[ub + sl];
+    if (tg != kEmpty) {
+      hash_erase(tab, hmask, s.hs_shift, tg);
+      s.tag[ub + sl] = kEmpty;
+      s.last[ub + sl] = -1;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) s.budget[u] = new_b;
+}
+
+}  // namespace
+
+cudaError_t launch_budget(const DeviceState& s, const int32_t* budget_new, cudaStream_t st) {
+  return launch_pdl(budget_kernel, dim3(s.U), dim3(kCommitThreads), 0, st, s, budget_new);
+}
 
 cudaError_t launch_victims(const DeviceState& s, int n_tok, int k, cudaStream_t st) {
   const size_t smem = victims_smem_bytes(s);

@@ -77,6 +77,10 @@ class Session:
         C.avsg_append(self.handle, k_rows.data_ptr(),
                       v_rows.data_ptr() if v_rows is not None else 0, stream)
 
+    def set_budget(self, slots_per_unit, stream=0):
+        """Usable slots per unit from the next step on (buffer elasticity)."""
+        C.avsg_set_budget(self.handle, slots_per_unit, stream)
+
     def stats(self) -> C.avsg_stats:
         return C.avsg_get_stats(self.handle)
 

@@ -214,6 +214,32 @@ int avsg_step_host(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int
  */
 int avsg_append(avsg_handle h, const void* d_k, const void* d_v, void* stream);
 
+/*
+ * Buffer elasticity (Spin page, section 2B): the buffer of each unit is sized
+ * per step, split into mandatory slots (the current step's selection) and
+ * buffer slots kept for temporal locality, under a system-wide budget.
+ * avsg_set_budget gives every unit u a budget of usable slots, slots_per_unit
+ * (host int32 [R][H]), each in 1 .. buffer_slots; it applies from the next
+ * step on (enqueued on `stream`).  Entries held in slots at or above a lowered
+ * budget are dropped (a later selection of them is a miss); the reservation
+ * takes only slots below the budget.  A step needs n_tok * k <= every unit's
+ * budget (else CAPACITY).  At create every budget is buffer_slots; avsg_reset
+ * keeps the budgets.  Not available with AVSG_FLAG_NO_REUSE (UNSUPPORTED).
+ */
+int avsg_set_budget(avsg_handle h, const int32_t* slots_per_unit, void* stream);
+
+/*
+ * A planner for avsg_set_budget (host only, no handle): splits total_slots over
+ * num_units units, each first given `mandatory` slots (the largest n_tok * k
+ * it will run), the rest in proportion to weights[u] >= 0 (equal shares when
+ * weights is NULL or all zero; the remainder of an equal split goes to the
+ * lowest units), each capped at max_slots (buffer_slots).  Slots above a cap
+ * stay unassigned.  out: host int32 [num_units].  Returns CAPACITY when
+ * total_slots < num_units * mandatory, INVALID_ARG for bad arguments.
+ */
+int avsg_plan_budget(int64_t total_slots, int32_t num_units, int32_t mandatory, int32_t max_slots,
+                     const float* weights, int32_t* out);
+
 /* avsg_get_stats -- synchronise the last stream used and read the counters. */
 int avsg_get_stats(avsg_handle h, avsg_stats* out);
 

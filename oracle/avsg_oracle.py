@@ -31,6 +31,11 @@ What it computes, and where that comes from:
   on and, like any id, enters the buffer only as a miss.  Here the host store
   holds ``capacity`` entries per unit, of which the first ``live`` are
   selectable; ``append`` writes entry ``live`` and raises the count.
+* Buffer elasticity (Spin page, section 2B): each unit's buffer is sized per
+  step, mandatory slots (the current step's selection) plus buffer slots kept
+  for locality, under a system-wide budget.  Here a unit has a budget of
+  usable slots, slots [0, budget): lowering it drops the entries held at or
+  above it, and the reservation takes only slots below it.
 
 Everything is written as the plain definition: a dense id -> slot table, a
 library sort for the victim order, a matmul and ``exp`` for attention.
@@ -89,6 +94,7 @@ class UnitBuffer:
         self.host_v = host_v
         self.L = host_k.shape[0]            # capacity of the host store
         self.live = self.L if live is None else int(live)
+        self.budget = self.B                # usable slots [0, budget)
         self.tag = np.full(self.B, EMPTY, dtype=np.int64)
         self.last = np.full(self.B, -1, dtype=np.int64)
         self.slot_of = np.full(self.L, EMPTY, dtype=np.int64)
@@ -106,8 +112,8 @@ class UnitBuffer:
             if np.unique(s).size != s.size:
                 raise OracleError(ERR_BAD_SELECTION, "duplicate id in one selection")
         union = np.unique(np.concatenate(sels)) if sels else np.zeros(0, np.int64)
-        if union.size > self.B:
-            raise OracleError(ERR_CAPACITY, f"{union.size} distinct ids > {self.B} slots")
+        if union.size > self.budget:
+            raise OracleError(ERR_CAPACITY, f"{union.size} distinct ids > {self.budget} usable slots")
         return union
 
     # -- offload ------------------------------------------------------------
@@ -121,10 +127,25 @@ class UnitBuffer:
         self.live += 1
         return self.live - 1
 
+    # -- elasticity -----------------------------------------------------------
+    def set_budget(self, budget: int) -> None:
+        """Usable slots [0, budget) from the next step on; entries held at or
+        above a lowered budget are dropped."""
+        budget = int(budget)
+        if not 1 <= budget <= self.B:
+            raise OracleError(ERR_CAPACITY, f"budget {budget} outside 1..{self.B}")
+        for slot in range(budget, self.B):
+            if self.tag[slot] != EMPTY:
+                self.slot_of[self.tag[slot]] = EMPTY
+                self.tag[slot] = EMPTY
+                self.last[slot] = -1
+        self.budget = budget
+
     # -- the step -----------------------------------------------------------
     def victim_order(self, t: int) -> np.ndarray:
         """Slots that may take a missing id at step t, in reservation order."""
-        cand = np.nonzero((self.tag == EMPTY) | (self.last < t))[0]
+        usable = np.arange(self.B) < self.budget
+        cand = np.nonzero(((self.tag == EMPTY) | (self.last < t)) & usable)[0]
         bucket = np.where(self.tag[cand] == EMPTY, EMPTY_BUCKET,
                           np.minimum(MAX_AGE_BUCKET, t - self.last[cand]))
         # primary key: bucket, highest first; secondary: slot index, lowest first
@@ -220,6 +241,11 @@ class OracleRun:
         self.head_dim, self.v_dim, self.scale = head_dim, v_dim, scale
         self.hits = 0
         self.misses = 0
+
+    def set_budget(self, budgets) -> None:
+        """budgets: usable slots per unit (indexed like the host store)."""
+        for u in self.units:
+            self.state[u].set_budget(budgets[u])
 
     def append(self, k_rows: np.ndarray, v_rows: np.ndarray | None = None):
         """One new entry per unit: k_rows / v_rows [units of the host store][row]."""

@@ -18,3 +18,12 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The C library, built in place (loads without a GPU)."""
+    from decode_serving_gb300 import build as b
+    b.build()
+    from decode_serving_gb300 import avsg
+    return avsg.load_library()

@@ -13,14 +13,6 @@ from conftest import ROOT
 HEADER = os.path.join(ROOT, "include", "avsg.h")
 
 
-@pytest.fixture(scope="module")
-def lib():
-    from decode_serving_gb300 import build as b
-    b.build()
-    from decode_serving_gb300 import avsg
-    return avsg.load_library()
-
-
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
