@@ -145,7 +145,7 @@ def pinned_h2d_peak_gbs(torch) -> float:
     return best
 
 
-def algorithmic_bytes(w, hits, misses, steps) -> dict:
+def algorithmic_bytes(w, hits, misses, steps, num_sms=152) -> dict:
     """Bytes each kernel must move per launch (averaged over the timed steps).
 
     attention: slot id + K row + V row per selected entry, plus q and out
@@ -156,7 +156,11 @@ def algorithmic_bytes(w, hits, misses, steps) -> dict:
     victims: tag and last_step (8 bytes) per slot + the hit bitmaps, + 40 per
            miss (sorted key, tag/last/slot writes, descriptor, slot map fix-up);
     gather: one entry (K + V) per miss, read over the host link and written
-           to HBM (host-link bytes are the read half)."""
+           to HBM (host-link bytes are the read half);
+    finish: the partials it merges (about 2 * SMs / pairs hit-pass partials
+           and one miss-pass partial per pair) and the output;
+    place: one entry per miss read from the staging area and written to its
+           slot."""
     U, n_tok, k = w.units, w.tokens_per_step, w.k
     sel = U * n_tok * k
     hits_ps, miss_ps = hits / steps, misses / steps
@@ -167,7 +171,10 @@ def algorithmic_bytes(w, hits, misses, steps) -> dict:
     gather_host = miss_ps * w.entry_bytes
     commit = miss_ps * 40   # descriptor, evicted-id probe window, new-id probe window
     return {"attention": attn, "match": match, "victims": victims, "gather": 2 * gather_host,
-            "gather_host_link": gather_host, "commit": commit}
+            "gather_host_link": gather_host, "commit": commit,
+            "finish": U * n_tok * (max(1, 2 * num_sms // (U * n_tok)) + 1) * w.q_per_kv
+            * (w.v_dim + 2) * 4 + U * n_tok * w.q_per_kv * w.v_dim * 4,
+            "place": 2 * gather_host}
 
 
 def run_ours(args, rank, world, torch):
@@ -474,7 +481,7 @@ def report_ours(args, res, world, max_ms, max_e2e_ms) -> dict:
     sel_step = w.units * w.tokens_per_step * w.k
     value = whole_job_value(w, world, max_ms)
     hbm_peak, peak_kind = measured_peaks()
-    ab = algorithmic_bytes(w, res["hits"], res["misses"], K)
+    ab = algorithmic_bytes(w, res["hits"], res["misses"], K, res["info"].num_sms)
     traffic = ncu_traffic()
     kernels = {}
     prof = dict(res["prof"])

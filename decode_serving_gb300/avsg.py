@@ -78,7 +78,7 @@ class avsg_info(ctypes.Structure):
     ]
 
 
-AVSG_NUM_KERNELS = 6
+AVSG_NUM_KERNELS = 8
 
 
 class avsg_kernel_times(ctypes.Structure):
@@ -86,7 +86,8 @@ class avsg_kernel_times(ctypes.Structure):
                 ("launches", ctypes.c_uint64 * AVSG_NUM_KERNELS)]
 
 
-KERNEL_NAMES = ("match", "victims", "gather", "attention", "attention_miss", "commit")
+KERNEL_NAMES = ("match", "victims", "gather", "attention", "attention_miss", "commit", "finish",
+                "place")
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32

@@ -53,7 +53,8 @@ struct avsg_handle_s {
   // side stream: the miss gather and the table commit run there while the
   // caller's stream runs attention over the hit rows
   cudaStream_t side = nullptr, side2 = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_reserve = nullptr, ev_commit = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_reserve = nullptr, ev_commit = nullptr,
+              ev_staged = nullptr, ev_place = nullptr;
   bool staged = false;  // staging area allocated: the two-pass pipeline is available
   bool overlap = false;  // steps run the two-pass pipeline
   // Captured steps: one CUDA graph per (tokens, k), re-pointed at each step
@@ -151,7 +152,7 @@ void release(avsg_handle h) {
   }
   if (h->cap) cudaStreamDestroy(h->cap);
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
-  for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_reserve, h->ev_commit})
+  for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_reserve, h->ev_commit, h->ev_staged, h->ev_place})
     if (e) cudaEventDestroy(e);
   if (h->side) cudaStreamDestroy(h->side);
   if (h->side2) cudaStreamDestroy(h->side2);
@@ -348,7 +349,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   // with one CTA per request each CTA's range is exactly one request's units.
   h->stage_ctas = (c.flags & AVSG_FLAG_REQUEST_GATHER) ? c.num_requests
                                                        : env_int("AVSG_STAGE_CTAS", h->num_sms * 2 / 5);
-  h->miss_splits = env_int("AVSG_MISS_SPLITS", 1);  // at least this many miss-pass CTAs per pair
+  h->miss_splits = env_int("AVSG_MISS_SPLITS", 2);  // at least this many miss-pass CTAs per pair
   {
     int64_t cap = (h->target_ctas + U - 1) / U;
     const int64_t by_rows = ((int64_t)c.max_select * c.entry_tokens + h->tile_rows - 1) / h->tile_rows;
@@ -449,7 +450,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   if (e == cudaSuccess)
     e = cudaStreamCreateWithPriority(&h->side2, cudaStreamNonBlocking, prio_high);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking);
-  for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_gather, &h->ev_reserve, &h->ev_commit})
+  for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_gather, &h->ev_reserve, &h->ev_commit, &h->ev_staged, &h->ev_place})
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     release(h);
@@ -571,36 +572,43 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   // Two-pass pipeline (the tensor-core shapes).  After match, three
   // streams run side by side:
   //   st:     attention over the hit rows (their slots are known);
-  //   side:   the missed rows, host -> staging area (host link);
+  //   side:   the missed rows, host -> staging area (host link), then the
+  //           attention over them (launched early: it lists its rows while
+  //           the gather drains);
   //   side2:  the reservation, then the hash-table update.
-  // The attention over the missed rows (read from staging) follows the
-  // gather and the reservation, and stores each staged row into its slot.
+  // Once the gather has staged the rows, a place kernel moves them into the
+  // slots the reservation gave them (on side2, beside the miss pass); the
+  // finish kernel merges the two passes' partials into the output.
   int splits_h = 0, splits_m = 0;
   two_pass_splits(h, n_tok, &splits_h, &splits_m);
   e = cudaEventRecord(h->ev_fork, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side2, h->ev_fork, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
+  DeviceState staged = sc;  // miss rows are read from the staging area, by cell
+  staged.kbuf = s.kstage;
+  staged.vbuf = s.vstage;
+  staged.B = s.MS;
   AVSG_RUN(AVSG_KERNEL_GATHER, h->side, launch_gather_stage(sc, h->stage_ctas, h->side));
+  e = cudaEventRecord(h->ev_staged, h->side);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, h->side,
+           launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, h->side));
   e = cudaEventRecord(h->ev_gather, h->side);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_RESERVE, h->side2, launch_victims(sc, n_tok, k, h->side2));
   e = cudaEventRecord(h->ev_reserve, h->side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_COMMIT, h->side2, launch_commit(sc, h->side2));
+  e = cudaStreamWaitEvent(h->side2, h->ev_staged, 0);  // staged rows -> slots, beside the miss pass
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_PLACE, h->side2, launch_place(sc, h->side2));
   e = cudaEventRecord(h->ev_commit, h->side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_ATTENTION, st,
-           launch_attention_tc_pass(sc, a, 0, splits_h, splits_m, nullptr, st));
+  AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, splits_h, splits_m, st));
   e = cudaStreamWaitEvent(st, h->ev_gather, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_reserve, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  DeviceState staged = sc;  // miss rows are read from the staging area, by cell
-  staged.kbuf = s.kstage;
-  staged.vbuf = s.vstage;
-  staged.B = s.MS;
-  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, st,
-           launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, &sc, st));
+  AVSG_RUN(AVSG_KERNEL_FINISH, st, launch_attention_tc_finish(sc, a, splits_h, splits_m, st));
   e = cudaStreamWaitEvent(st, h->ev_commit, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
 #undef AVSG_RUN

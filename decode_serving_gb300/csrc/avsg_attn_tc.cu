@@ -42,8 +42,6 @@ constexpr int kTileRows = 16;
 constexpr int kStages = 3;
 constexpr int kCtasPerSm = 2;
 constexpr int kScanMax = kMissScanMax;          // miss-set cells one miss-pass CTA scans
-constexpr int32_t kPlaceBit = (int32_t)0x80000000;
-constexpr int32_t kCellMask = 0x7FFFFFFF;
 
 constexpr int pow2_floor_capped(int x, int cap) {
   int q = 1;
@@ -145,12 +143,6 @@ struct TcParams {
   float* out;
   const int32_t* slots;         // [pairs][k] slot of each listed entry
   const StepIO* io;             // when set, q and out (and slots, single pass) come from here
-  // miss pass: rows are read from the staging area and also stored into
-  // their reserved slots: place_k/place_v rows (unit * place_B + slot) * ET + sub
-  unsigned char* place_k;
-  unsigned char* place_v;
-  int place_B;
-  const int32_t* mslot;         // [U][MS] reserved slot of each miss-set cell
   // persistent single pass
   int rows_per_pair, tiles_per_pair;
   long long tiles;              // all pairs
@@ -164,8 +156,7 @@ struct SegArgs {
   int ent_base;                 // first listed entry of the range
   int rows;                     // rows of the range (entries * ET)
   int ta, tb;                   // this CTA's tiles [ta, tb) of the range
-  const int32_t* list;          // when set: entry e is list[e] & kCellMask (shared memory);
-                                // bit 31 set: this pass stores the row into its slot
+  const int32_t* list;          // when set: the slot of entry e is list[e] (shared memory)
   const float* qs;              // when set: the pair's q [G][D] in shared memory
 };
 
@@ -236,7 +227,7 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
     if (i >= n_my || row >= a.rows) return -1;
     const int ent = a.ent_base + (p.ET == 1 ? row : row / p.ET);
     const int sub = row - (ent - a.ent_base) * p.ET;
-    const int slot = a.list ? (a.list[ent] & kCellMask)
+    const int slot = a.list ? a.list[ent]
                    : p.identity ? tok * p.k + ent
                                 : __ldg(p.slots + (size_t)pair * p.k + ent);
     if (slot < 0) return -1;  // not a row of this pass (a miss in the pass over hit rows)
@@ -245,23 +236,6 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
   constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
   constexpr int RPI = 32 / CPR;    // rows per warp instruction
   unsigned long long vmasks = 0;  // 16 bits per stage: which rows of the staged tile are real
-  // Miss pass: for row (lane & 15) of the next three tiles (in order), the
-  // reserved slot (loaded when the tile is issued, used after it is
-  // consumed) and the row's sub-index, or -1 when this pass does not store it.
-  const bool place = p.place_k != nullptr;
-  int pslot[kStages], psub[kStages];
-#pragma unroll
-  for (int i = 0; i < kStages; ++i) pslot[i] = psub[i] = -1;
-  auto place_info = [&](int i, int& slot, int& sub) {
-    slot = sub = -1;
-    const int row = (a.ta + warp + i * kWarpsTc) * kTileRows + (lane & 15);
-    if (!place || i >= n_my || row >= a.rows) return;
-    const int ent = a.ent_base + (p.ET == 1 ? row : row / p.ET);
-    const int e = a.list[ent];
-    if (!(e & kPlaceBit)) return;
-    slot = __ldcg(p.mslot + (size_t)u * s.MS + (e & kCellMask));
-    sub = row - (ent - a.ent_base) * p.ET;
-  };
   auto issue = [&](long long myrow, int st) {
     const unsigned long long vm = __ballot_sync(0xffffffffu, myrow >= 0) & 0xFFFFu;
     vmasks = (vmasks & ~(0xFFFFull << (16 * st))) | (vm << (16 * st));
@@ -291,9 +265,6 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
 #pragma unroll
     for (int i = 0; i < kStages; ++i) issue(first_rows[i], i);
     next_row = first_rows[kStages];
-    if (place)
-#pragma unroll
-      for (int i = 0; i < kStages; ++i) place_info(i, pslot[i], psub[i]);
   }
   uint32_t qb[KS][NTN][2];
 #pragma unroll
@@ -437,30 +408,6 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
 #pragma unroll
         for (int nt = 0; nt < NTN; ++nt) mma_bf16(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
       }
-    }
-    if (place) {  // the tile's rows that this pass owns -> their reserved slots
-      const long long drow =
-          (pslot[0] >= 0 && psub[0] >= 0) ? ((long long)u * p.place_B + pslot[0]) * p.ET + psub[0] : -1;
-      const int ch = lane % CPR, rsub = lane / CPR;
-#pragma unroll
-      for (int it = 0; it < kTileRows / RPI; ++it) {
-        const int r = it * RPI + rsub;
-        const long long dr = __shfl_sync(0xffffffffu, drow, r);
-        if (dr >= 0) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(kst + r * PITCH + ch * 16);
-          *reinterpret_cast<uint4*>(p.place_k + dr * (2 * D) + ch * 16) = kv;
-          if (!SH::SHARED) {
-            const uint4 vv = *reinterpret_cast<const uint4*>(vst + r * PITCH + ch * 16);
-            *reinterpret_cast<uint4*>(p.place_v + dr * (2 * D) + ch * 16) = vv;
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j + 1 < kStages; ++j) {
-        pslot[j] = pslot[j + 1];
-        psub[j] = psub[j + 1];
-      }
-      place_info(i + kStages, pslot[kStages - 1], psub[kStages - 1]);
     }
     __syncwarp();  // every lane has read stage st
     issue(next_row, st);
@@ -707,11 +654,11 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_hits_kernel(DeviceState s,
 // Miss pass: CTA (sp, pair) copies its range of the unit's miss set into
 // shared memory (one round of 16-byte async copies), lists the claimed cells
 // that carry this token (a fixed order: by thread, then by stride), attends
-// over their rows in the staging area, and stores every row whose lowest
-// token is this one into its reserved slot.  With one CTA per pair it then
-// merges its result with the hit pass's partials and writes the output;
-// otherwise the last CTA of the pair does.  `s` is the staged view of the
-// state: kbuf/vbuf are the staging rows and B the miss-set capacity.
+// over their rows in the staging area and writes partial splits_h + sp of the
+// pair (the finish kernel merges).  It follows the staged gather on the same
+// stream: the list is built while the gather's last copies drain, and the
+// rows are read after the grid-dependency wait.  `s` is the staged view of
+// the state: kbuf/vbuf are the staging rows and B the miss-set capacity.
 template <class SH>
 __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s, TcParams p) {
   constexpr int D = SH::D, G = SH::G;
@@ -723,30 +670,26 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
   int32_t* list = reinterpret_cast<int32_t*>(smem + kWarpsTc * SH::WARP_BYTES);       // [span]
   __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G], cm[G], cl[G];
   __shared__ __align__(16) float s_q[G * D];
-  __shared__ int s_stop, s_last, s_wsum[kWarpsTc];
+  __shared__ int s_stop, s_wsum[kWarpsTc];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sp = blockIdx.x, pair = blockIdx.y;
   const int u = pair / p.n_tok, tok = pair - u * p.n_tok;
   const int span = s.MS / p.splits_m;  // both powers of two, span <= SH::SCAN_MAX
   const int c_lo = sp * span;
-  griddep_wait();
-  griddep_launch();
-  {  // the range of the miss set, and q (the copy match made), in one group
+  // The miss set and the q copy were written by match, which completed before
+  // the gather began: they are read before the wait on the gather.
+  {  // the range of the miss set, and q, in one group
     const unsigned long long* src = s.mset + (size_t)u * s.MS + c_lo;
     for (int i = tid; i < span / 2; i += kThreadsTc) cp_async16(cells + 2 * i, src + 2 * i);
     for (int i = tid; i < G * D / 4; i += kThreadsTc) cp_async16(s_q + 4 * i, p.q + (size_t)pair * G * D + 4 * i);
     cp_async_commit();
   }
-  if (p.io) p.out = load_io(p.io).out;  // used at the end
-  if (tid == 0) s_stop = load_err(s.err);
   cp_async_wait<0>();
   __syncthreads();
-  if (s_stop) return;
 
   // cells tid, tid + 128, ... of the range: those carrying this token, in a
-  // fixed order (thread, then stride); bit 31 marks the lowest token of a cell
+  // fixed order (thread, then stride)
   const unsigned long long tokbit = 1ull << (32 + tok);
-  const unsigned long long below = (tokbit - 1ull) & ~0xFFFFFFFFull;  // lower tokens' bits
   int cnt = 0;
   for (int c0 = tid; c0 < span; c0 += 8 * kThreadsTc) {
     unsigned long long w[8];
@@ -781,10 +724,14 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (w[j] != kMissEmpty && (w[j] & tokbit))
-        list[base++] = (c_lo + c0 + j * kThreadsTc) | ((w[j] & below) ? 0 : kPlaceBit);
+      if (w[j] != kMissEmpty && (w[j] & tokbit)) list[base++] = c_lo + c0 + j * kThreadsTc;
   }
   __syncthreads();
+  griddep_wait();  // the gather's rows are in the staging area
+  griddep_launch();
+  if (tid == 0) s_stop = load_err(s.err);
+  __syncthreads();
+  if (s_stop) return;
 
   float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
   SegArgs a;
@@ -801,22 +748,25 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
 
   const int nseg = p.splits_h + p.splits_m;
   const size_t stride = (size_t)G * (D + 2);
-  float* pbase = s.part + (size_t)pair * nseg * stride;
-  tc_write_partial<G, D>(pbase + (size_t)(p.splits_h + sp) * stride, cm, cl, co);
-  if (p.splits_m == 1) {  // the hit pass has finished: merge now
-    __syncthreads();
-    tc_merge_partials<G, D>(pbase, nseg, p.out + (size_t)pair * G * D, co + G * D);
-    return;
-  }
-  __threadfence();
+  tc_write_partial<G, D>(s.part + ((size_t)pair * nseg + p.splits_h + sp) * stride, cm, cl, co);
+}
+
+// Finish of a step, one CTA per (unit, token): merges the pair's partials
+// (hit pass, then miss pass) into the output.
+template <class SH>
+__global__ void __launch_bounds__(kThreadsTc) attn_tc_finish_kernel(DeviceState s, TcParams p) {
+  constexpr int D = SH::D, G = SH::G;
+  extern __shared__ float wseg[];  // [2][nseg][G]
+  __shared__ int s_stop;
+  const int pair = blockIdx.x, tid = threadIdx.x;
+  griddep_wait();
+  griddep_launch();
+  if (tid == 0) s_stop = load_err(s.err);
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&s.part_count[u * kMaxTokens + tok], 1) == p.splits_m - 1;
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    tc_merge_partials<G, D>(pbase, nseg, p.out + (size_t)pair * G * D, co + G * D);
-    if (tid == 0) s.part_count[u * kMaxTokens + tok] = 0;
-  }
+  if (s_stop) return;
+  const int nseg = p.splits_h + p.splits_m;
+  float* out = load_io(s.io).out + (size_t)pair * G * D;
+  tc_merge_partials<G, D>(s.part + (size_t)pair * nseg * G * (D + 2), nseg, out, wseg);
 }
 
 template <class SH>
@@ -861,7 +811,7 @@ cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaS
 
 template <class SH>
 cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int splits_h,
-                        int splits_m, const DeviceState* placed, cudaStream_t st) {
+                        int splits_m, cudaStream_t st) {
   static int smem_hits = 0, smem_miss = 0;
   TcParams p = tc_params<SH>(s, a);
   p.slots = s.hslot;
@@ -879,15 +829,25 @@ cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int
   if (s.MS % splits_m != 0 || s.MS / splits_m > SH::SCAN_MAX || (s.MS / splits_m) % 2 != 0 ||
       splits_h + splits_m > SH::MAX_SEG)
     return cudaErrorInvalidValue;
-  p.place_k = placed->kbuf;
-  p.place_v = placed->vbuf;
-  p.place_B = placed->B;
-  p.mslot = placed->mslot;
   const size_t smem = SH::SMEM + (size_t)(s.MS / splits_m) * sizeof(int32_t);
   cudaError_t e = ensure_smem((const void*)attn_tc_miss_kernel<SH>,
                               SH::SMEM + (size_t)SH::SCAN_MAX * sizeof(int32_t), &smem_miss);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_tc_miss_kernel<SH>, grid, dim3(kThreadsTc), smem, st, s, p);
+}
+
+template <class SH>
+cudaError_t run_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_h, int splits_m,
+                          cudaStream_t st) {
+  static int smem_done = 0;
+  TcParams p = tc_params<SH>(s, a);
+  p.splits_h = splits_h;
+  p.splits_m = splits_m;
+  const size_t smem = 2 * (size_t)(splits_h + splits_m) * SH::G * sizeof(float);
+  cudaError_t e = ensure_smem((const void*)attn_tc_finish_kernel<SH>, smem, &smem_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_tc_finish_kernel<SH>, dim3((unsigned)(s.U * a.n_tok)), dim3(kThreadsTc),
+                    smem, st, s, p);
 }
 
 }  // namespace
@@ -926,11 +886,23 @@ size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sm
 }
 
 cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
-                                     int splits_h, int splits_m, const DeviceState* placed,
-                                     cudaStream_t st) {
+                                     int splits_h, int splits_m, cudaStream_t st) {
 #define X(d, g, sh)                                                         \
   if (s.D == d && s.G == g && (s.kv_shared != 0) == sh)                     \
-    return run_tc_pass<TcShape<d, g, sh>>(s, a, pass, splits_h, splits_m, placed, st);
+    return run_tc_pass<TcShape<d, g, sh>>(s, a, pass, splits_h, splits_m, st);
+  X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
+  X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
+  X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)
+  X(64, 1, true) X(64, 2, true) X(64, 4, true) X(64, 8, true)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_h,
+                                       int splits_m, cudaStream_t st) {
+#define X(d, g, sh)                                                         \
+  if (s.D == d && s.G == g && (s.kv_shared != 0) == sh)                     \
+    return run_tc_finish<TcShape<d, g, sh>>(s, a, splits_h, splits_m, st);
   X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
   X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
   X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)

@@ -102,7 +102,8 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
   __shared__ int32_t s_id[kStageCells];
   __shared__ int s_n;
   griddep_wait();
-  griddep_launch();
+  // (dependents are released at the end: the miss pass that follows this
+  // kernel prepares its lists meanwhile, but must not take SMs any earlier)
   if (load_err(s.err) != 0) return;  // uniform over the CTA
   const int lane = threadIdx.x & 31;
   const long long ncell = (long long)s.U * s.MS;
@@ -165,6 +166,51 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
     }
     __syncthreads();  // the list is rewritten by the next round
   }
+  griddep_launch();
+}
+
+// Place: every miss's staged row (by miss-set cell) into its reserved slot
+// (device to device), grid (U, kPlaceSplit): CTA (u, z) takes every
+// kPlaceSplit-th of unit u's reservation descriptors.  A warp reads
+// kPlaceRows descriptors, then their rows' 16-byte chunks, then stores.
+constexpr int kPlaceSplit = 4;
+constexpr int kPlaceRows = 8;
+
+__global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s) {
+  griddep_wait();
+  griddep_launch();
+  if (load_err(s.err) != 0) return;
+  const int u = blockIdx.x, z = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int base = s.dbase[u], cnt = s.dcount[u];
+  const uint32_t cpk = (uint32_t)(s.ek >> 4), cpe = cpk + (uint32_t)(s.ev >> 4);
+  const int step = (kThreads / 32) * kPlaceSplit;
+  for (int d0 = z + warp * kPlaceSplit; d0 < cnt; d0 += step * kPlaceRows) {
+    size_t srow[kPlaceRows], drow[kPlaceRows];
+    bool ok[kPlaceRows];
+#pragma unroll
+    for (int r = 0; r < kPlaceRows; ++r) {
+      const int d = d0 + r * step;
+      ok[r] = d < cnt;
+      const GatherDesc g = ok[r] ? s.desc[base + d] : GatherDesc{};
+      srow[r] = (size_t)u * s.MS + g.cell;
+      drow[r] = (size_t)u * s.B + g.slot;
+    }
+    for (uint32_t c = lane; c < cpe; c += 32) {
+      uint4 v[kPlaceRows];
+#pragma unroll
+      for (int r = 0; r < kPlaceRows; ++r)
+        if (ok[r])
+          v[r] = c < cpk ? __ldcg(reinterpret_cast<const uint4*>(s.kstage + srow[r] * s.ek) + c)
+                         : __ldcg(reinterpret_cast<const uint4*>(s.vstage + srow[r] * s.ev) + (c - cpk));
+#pragma unroll
+      for (int r = 0; r < kPlaceRows; ++r)
+        if (ok[r])
+          store16(c < cpk ? static_cast<void*>(reinterpret_cast<uint4*>(s.kbuf + drow[r] * s.ek) + c)
+                          : static_cast<void*>(reinterpret_cast<uint4*>(s.vbuf + drow[r] * s.ev) + (c - cpk)),
+                  v[r]);
+    }
+  }
 }
 
 // No-reuse comparison path: every selected row of every token is copied to
@@ -220,6 +266,13 @@ cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st)
 
 
 static_assert(kStageCells % kThreads == 0, "a round is whole passes of the CTA");
+
+cudaError_t launch_place(const DeviceState& s, cudaStream_t st) {
+  static int attr_done = 0;
+  const cudaError_t e = ensure_smem((const void*)place_kernel, 0, &attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(place_kernel, dim3(s.U, kPlaceSplit), dim3(kThreads), 0, st, s);
+}
 
 cudaError_t launch_gather_all(const DeviceState& s, const StepIO& v, int n_tok, int k, int ctas,
                               cudaStream_t st) {

@@ -172,6 +172,8 @@ cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
 // Staged gather: right after match, the host row of every claimed miss-set
 // cell is copied to kstage/vstage at that cell (no slot needed yet).
 cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st);
+// Staged rows -> their reserved slots (after the gather and the reservation).
+cudaError_t launch_place(const DeviceState& s, cudaStream_t st);
 cudaError_t launch_gather_all(const DeviceState& s, const StepIO& v, int n_tok, int k, int ctas,
                               cudaStream_t st);
 
@@ -197,11 +199,13 @@ cudaError_t launch_attention_tc(const DeviceState& s, const AttnLaunch& a, int n
                                 cudaStream_t st);
 // pass 0: hit rows of every (unit, token), splits_h CTAs per pair.  pass 1:
 // miss rows from the staging area (s is the staged view), splits_m CTAs per
-// pair (MS / splits_m <= the shape's scan limit), each staged row also stored
-// into its reserved slot of `placed` (the real state); then the merge.
+// pair (MS / splits_m <= the shape's scan limit), launched right after the
+// staged gather on its stream.  Each writes partials; the finish kernel
+// merges them (s: real state).
 cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
-                                     int splits_h, int splits_m, const DeviceState* placed,
-                                     cudaStream_t st);
+                                     int splits_h, int splits_m, cudaStream_t st);
+cudaError_t launch_attention_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_h,
+                                       int splits_m, cudaStream_t st);
 // Most partials (hit + miss splits) one pair's merge takes.
 int attention_tc_max_segments(int D, int G, int kv_shared);
 // Most miss-set cells one miss-pass CTA scans (a power of two).

@@ -130,10 +130,11 @@ typedef struct avsg_info {
 #define AVSG_KERNEL_RESERVE 1
 #define AVSG_KERNEL_GATHER 2
 #define AVSG_KERNEL_ATTENTION 3      /* single pass, or the pass over hit rows */
-#define AVSG_KERNEL_ATTENTION_MISS 4 /* pass over miss rows (which also stores them
-                                        into their slots) and the merge */
+#define AVSG_KERNEL_ATTENTION_MISS 4 /* pass over miss rows */
 #define AVSG_KERNEL_COMMIT 5         /* hash-table update */
-#define AVSG_NUM_KERNELS 6
+#define AVSG_KERNEL_FINISH 6         /* merge of the two attention passes */
+#define AVSG_KERNEL_PLACE 7          /* staged missed rows into their slots */
+#define AVSG_NUM_KERNELS 8
 typedef struct avsg_kernel_times {
   double ms[AVSG_NUM_KERNELS];
   uint64_t launches[AVSG_NUM_KERNELS];
