@@ -348,7 +348,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   // The staged gather splits all units' miss-set cells evenly over its CTAs;
   // with one CTA per request each CTA's range is exactly one request's units.
   h->stage_ctas = (c.flags & AVSG_FLAG_REQUEST_GATHER) ? c.num_requests
-                                                       : env_int("AVSG_STAGE_CTAS", h->num_sms * 2 / 5);
+                                                       : env_int("AVSG_STAGE_CTAS", h->num_sms / 2);
   h->miss_splits = env_int("AVSG_MISS_SPLITS", 2);  // at least this many miss-pass CTAs per pair
   {
     int64_t cap = (h->target_ctas + U - 1) / U;

@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(DeviceState s) {
 // cells, consecutive threads on consecutive 16-byte chunks of a row and
 // kUnroll chunks in flight per thread.  Few CTAs keep the host link busy, so
 // the reservation kernel finds free SMs beside this one.
-constexpr int kStageCells = 4096;
+constexpr int kStageCells = 1024;
 constexpr int kStageWarps = kThreads / 32;
 
 __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
@@ -102,8 +102,8 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
   __shared__ int32_t s_id[kStageCells];
   __shared__ int s_n;
   griddep_wait();
-  // (dependents are released at the end: the miss pass that follows this
-  // kernel prepares its lists meanwhile, but must not take SMs any earlier)
+  // (dependents are released when the last round begins: the miss pass that
+  // follows prepares its lists meanwhile, but must not take SMs any earlier)
   if (load_err(s.err) != 0) return;  // uniform over the CTA
   const int lane = threadIdx.x & 31;
   const long long ncell = (long long)s.U * s.MS;
@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
   const long long c_end = (blockIdx.x + 1) * ncell / gridDim.x;
   const uint32_t cpk = (uint32_t)(s.ek >> 4), cpv = (uint32_t)(s.ev >> 4), cpe = cpk + cpv;
   for (long long r0 = c_begin; r0 < c_end; r0 += kStageCells) {
+    if (r0 + kStageCells >= c_end) griddep_launch();  // last round: the miss pass may start listing
     if (threadIdx.x == 0) s_n = 0;
     __syncthreads();
     const int span = (int)min((long long)kStageCells, c_end - r0);
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
     }
     __syncthreads();  // the list is rewritten by the next round
   }
-  griddep_launch();
+  griddep_launch();  // (no round at all)
 }
 
 // Place: every miss's staged row (by miss-set cell) into its reserved slot
