@@ -37,18 +37,28 @@ __device__ __forceinline__ int next_pow2(int x) {
   return p;
 }
 
-// Linear-probing erase of a key known to be present.
-__device__ void hash_erase(int2* tab, uint32_t mask, int shift, int32_t key) {
+// Linear-probing erase of a key known to be present.  The cell becomes empty
+// when the next cell is empty (then no probe path runs through it: a key
+// stored further on would have stopped at that empty cell), otherwise a
+// tombstone.  Concurrent erases stay valid: a cell only turns empty behind an
+// empty cell.  Returns 1 when a cell was freed.
+__device__ int hash_erase(int2* tab, uint32_t mask, int shift, int32_t key) {
   uint32_t c = fib_hash(key, shift);
   for (uint32_t i = 0; i <= mask; ++i, ++c) {
     int2* p = tab + (c & mask);
     const int32_t kk = *(volatile int32_t*)&p->x;
     if (kk == key) {
+      const int32_t next = *(volatile int32_t*)&tab[(c + 1) & mask].x;
+      if (next == kEmpty) {
+        p->x = kEmpty;
+        return 1;
+      }
       p->x = kTomb;
-      return;
+      return 0;
     }
-    if (kk == kEmpty) return;
+    if (kk == kEmpty) return 0;
   }
+  return 0;
 }
 
 // Linear-probing insert of a key known to be absent; takes the first empty or
@@ -380,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
 constexpr int kCommitThreads = 256;  // small CTAs: they share SMs with the attention
 
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
-  __shared__ int s_stop, s_used, s_rebuild, s_live;
+  __shared__ int s_stop, s_used, s_freed, s_rebuild, s_live;
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
   griddep_wait();
@@ -388,6 +398,7 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
   if (tid == 0) {
     s_stop = load_err(s.err);
     s_used = 0;
+    s_freed = 0;
     s_live = 0;
   }
   __syncthreads();
@@ -395,10 +406,13 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
   const int m = s.dcount[u], base = s.dbase[u];
   int2* tab = s.htab + (size_t)u * s.HS;
   const uint32_t hmask = (uint32_t)s.HS - 1u;
+  int freed = 0;
   for (int i = tid; i < m; i += kCommitThreads) {
     const int32_t old = s.desc[base + i].old_id;
-    if (old != kEmpty) hash_erase(tab, hmask, s.hs_shift, old);
+    if (old != kEmpty) freed += hash_erase(tab, hmask, s.hs_shift, old);
   }
+  freed = __reduce_add_sync(0xffffffffu, freed);
+  if (lane == 0 && freed) atomicAdd(&s_freed, freed);
   __syncthreads();
   int used = 0;
   for (int i = tid; i < m; i += kCommitThreads) {
@@ -409,7 +423,7 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
   if (lane == 0 && used) atomicAdd(&s_used, used);
   __syncthreads();
   if (tid == 0) {
-    const int total = s.hused[u] + s_used;
+    const int total = s.hused[u] + s_used - s_freed;  // cells not empty: live keys and tombstones
     s_rebuild = total > s.HS / 4;
     s.hused[u] = total;
   }
@@ -456,14 +470,16 @@ __global__ void __launch_bounds__(kCommitThreads) budget_kernel(DeviceState s,
   int2* tab = s.htab + (size_t)u * s.HS;
   const uint32_t hmask = (uint32_t)s.HS - 1u;
   const size_t ub = (size_t)u * s.B;
+  int freed = 0;
   for (int sl = new_b + (int)threadIdx.x; sl < old_b; sl += kCommitThreads) {
     const int32_t tg = s.tag[ub + sl];
     if (tg != kEmpty) {
-      hash_erase(tab, hmask, s.hs_shift, tg);
+      freed += hash_erase(tab, hmask, s.hs_shift, tg);
       s.tag[ub + sl] = kEmpty;
       s.last[ub + sl] = -1;
     }
   }
+  if (freed) atomicSub(&s.hused[u], freed);
   __syncthreads();
   if (threadIdx.x == 0) s.budget[u] = new_b;
 }
