@@ -166,13 +166,15 @@ void release(avsg_handle h) {
 // about two CTAs per SM; the miss pass scans at most kMissScanMax miss-set
 // cells per CTA (and at least AVSG_MISS_SPLITS CTAs); together they stay
 // within what one merge takes.
-void two_pass_splits(const avsg_handle h, int n_tok, int* splits_h, int* splits_m) {
+void two_pass_splits(const avsg_handle h, int n_tok, int k, int* splits_h, int* splits_m) {
   const DeviceState& s = h->ds;
   const int pairs = s.U * n_tok;
   const int scan = attention_tc_scan_max(s.D, s.G, s.kv_shared);
   int sm = scan > 0 && s.MS > scan ? s.MS / scan : 1;
   while (sm < h->miss_splits && s.MS / sm > 2) sm *= 2;
   int sh = 2 * h->num_sms / pairs > 0 ? 2 * h->num_sms / pairs : 1;
+  const int tiles = (int)(((int64_t)k * s.ET + 15) / 16);  // 16-row tiles of a pair
+  if (sh > tiles / 2) sh = tiles / 2 > 1 ? tiles / 2 : 1;  // two tiles or more per CTA
   const int cap = attention_tc_max_segments(s.D, s.G, s.kv_shared);
   if (sh + sm > cap) sh = cap - sm > 1 ? cap - sm : 1;
   *splits_h = sh;
@@ -187,6 +189,10 @@ int attn_splits(const avsg_handle h, int n_tok, int k) {
   const int64_t by_rows = ((int64_t)k * h->ds.ET + h->tile_rows - 1) / h->tile_rows;
   if (s > by_rows) s = by_rows;
   if (s > h->splits_cap) s = h->splits_cap;
+  // the merge reads every split's partial: at most about 2 MiB of them per pair
+  const int64_t part_bytes = (int64_t)h->ds.G * (h->ds.DV + 2) * 4;
+  const int64_t by_merge = ((int64_t)2 << 20) / part_bytes;
+  if (s > by_merge) s = by_merge > 4 ? by_merge : 4;
   return (int)(s < 1 ? 1 : s);
 }
 
@@ -400,7 +406,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     for (int nt = 1; nt <= c.max_tokens_per_step; ++nt) {
       const int pairs = (int)U * nt;
       int sh = 0, sm = 0;
-      two_pass_splits(h, nt, &sh, &sm);
+      two_pass_splits(h, nt, c.max_select, &sh, &sm);
       const size_t need = (size_t)pairs * (sh + sm) * s.G * (s.DV + 2);
       two = need > two ? need : two;
     }
@@ -580,7 +586,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   // slots the reservation gave them (on side2, beside the miss pass); the
   // finish kernel merges the two passes' partials into the output.
   int splits_h = 0, splits_m = 0;
-  two_pass_splits(h, n_tok, &splits_h, &splits_m);
+  two_pass_splits(h, n_tok, k, &splits_h, &splits_m);
   e = cudaEventRecord(h->ev_fork, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side2, h->ev_fork, 0);

@@ -15,8 +15,9 @@
 // fits), an online-softmax update per head in the log2 domain, then the
 // probability-weighted V sum (each thread owns a slice of output dims for a
 // group of heads and a subset of rows).  The CTA's partial (max, sum, acc) is
-// written out; the last CTA of a (unit, token) to arrive merges the splits and
-// writes the output -- no second kernel, no waiting.
+// written out, and a merge kernel spread over the output columns combines the
+// splits of every (unit, token) (a CTA with the whole range writes the output
+// itself).
 #include <math.h>
 
 #include "avsg_internal.cuh"
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(SH::NT) attn_kernel(DeviceState s, AttnLaunch 
   __shared__ __align__(16) float Ss[TR * G];
   __shared__ __align__(16) float Ps[TR * G];
   __shared__ float alpha_s[G], mrun[G], lrun[G];
-  __shared__ int s_stop, s_last;
+  __shared__ int s_stop;
 
   unsigned char* kt = smem;                                           // [2][TR][D] bf16
   unsigned char* vt = SH::SHARED ? smem : smem + 2ull * TR * D * 2;   // [2][TR][DV] bf16
@@ -304,30 +305,70 @@ __global__ void __launch_bounds__(SH::NT) attn_kernel(DeviceState s, AttnLaunch 
     pp[tid] = mrun[tid];
     pp[G + tid] = lrun[tid];
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&s.part_count[u * kMaxTokens + tok], 1);
-    s_last = prev == a.splits - 1;
+}
+
+// Merge of the splits (launched after the attention when it has more than one
+// split): CTA (pair, x) takes output columns [x * kMergeCols, ...) of the
+// pair.  The (m, l) of every split for the CTA's heads are loaded at once into
+// shared memory and turned into weights; each thread then sums its column
+// over the splits, kMergeQB partials per round of loads.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeCols = kMergeThreads;
+constexpr int kMergeQB = 8;
+constexpr int kMergeMaxW = 4096;  // (split, head) weights held in shared memory
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(DeviceState s, AttnLaunch a) {
+  __shared__ float s_w[kMergeMaxW];
+  __shared__ float s_l[kMergeMaxW];
+  __shared__ int s_stop;
+  const int G = s.G, DV = s.DV;
+  const int pair = blockIdx.x, tid = threadIdx.x;
+  const int c0 = blockIdx.y * kMergeCols;
+  const int h0 = c0 / DV, h1 = min(G - 1, (c0 + kMergeCols - 1) / DV), nh = h1 - h0 + 1;
+  const int S = a.splits;
+  griddep_wait();
+  griddep_launch();
+  if (a.io) {
+    const StepIO io = load_io(a.io);
+    a.out = io.out;
+  }
+  if (tid == 0) s_stop = load_err(s.err);
+  const size_t stride = (size_t)G * (DV + 2);
+  const float* pbase = s.part + (size_t)pair * S * stride;
+  for (int i = tid; i < S * nh; i += kMergeThreads) {
+    const int q = i / nh, h = h0 + (i - q * nh);
+    s_w[i] = __ldcg(pbase + q * stride + h);
+    s_l[i] = __ldcg(pbase + q * stride + G + h);
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int o = tid; o < G * DV; o += NT) {  // the last CTA merges every split
-    const int g = o / DV;
+  if (s_stop) return;
+  if (tid < nh) {  // per head: exp2(m_q - M) / L
     float M = -INFINITY;
-    for (int q = 0; q < a.splits; ++q) M = fmaxf(M, __ldcg(pbase + q * stride + g));
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-      for (int q = 0; q < a.splits; ++q) {
-        const float w = exp2f(__ldcg(pbase + q * stride + g) - M);
-        L = fmaf(__ldcg(pbase + q * stride + G + g), w, L);
-        O = fmaf(__ldcg(pbase + q * stride + 2 * G + o), w, O);
-      }
+    for (int q = 0; q < S; ++q) M = fmaxf(M, s_w[q * nh + tid]);
+    float L = 0.f;
+    for (int q = 0; q < S; ++q) {
+      const float e = M == -INFINITY ? 0.f : exp2f(s_w[q * nh + tid] - M);
+      s_w[q * nh + tid] = e;
+      L = fmaf(s_l[q * nh + tid], e, L);
     }
-    out[o] = L > 0.f ? O / L : 0.f;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int q = 0; q < S; ++q) s_w[q * nh + tid] *= inv;
   }
-  if (tid == 0) s.part_count[u * kMaxTokens + tok] = 0;
+  __syncthreads();
+  const int o = c0 + tid;
+  if (o >= G * DV) return;
+  const int hh = o / DV - h0;
+  float O = 0.f;
+  for (int q0 = 0; q0 < S; q0 += kMergeQB) {
+    float v[kMergeQB];
+#pragma unroll
+    for (int j = 0; j < kMergeQB; ++j)
+      v[j] = q0 + j < S ? __ldcg(pbase + (q0 + j) * stride + 2 * G + o) : 0.f;
+#pragma unroll
+    for (int j = 0; j < kMergeQB; ++j)
+      if (q0 + j < S) O = fmaf(v[j], s_w[(q0 + j) * nh + hh], O);
+  }
+  a.out[(size_t)pair * G * DV + o] = O;
 }
 
 template <class SH>
@@ -338,7 +379,11 @@ cudaError_t run(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
   cudaError_t e = ensure_smem((const void*)attn_kernel<SH>, smem, &smem_done);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)a.splits, (unsigned)s.U, (unsigned)a.n_tok);
-  return launch_pdl(attn_kernel<SH>, grid, dim3(SH::NT), smem, st, s, a);
+  e = launch_pdl(attn_kernel<SH>, grid, dim3(SH::NT), smem, st, s, a);
+  if (e != cudaSuccess || a.splits == 1) return e;
+  if ((size_t)a.splits * ((kMergeCols + SH::DV - 1) / SH::DV + 1) > kMergeMaxW) return cudaErrorInvalidValue;
+  dim3 mgrid((unsigned)(s.U * a.n_tok), (unsigned)((SH::G * SH::DV + kMergeCols - 1) / kMergeCols));
+  return launch_pdl(merge_kernel, mgrid, dim3(kMergeThreads), 0, st, s, a);
 }
 
 // Compiled shapes: (D, Dv, G, shared).
