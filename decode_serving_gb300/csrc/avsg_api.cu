@@ -349,7 +349,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   if (s.hs_shift >= 32) s.hs_shift = 31;
   if (s.ms_shift >= 32) s.ms_shift = 31;
   h->tile_rows = attention_rows_per_tile(s.D, s.DV, s.G, s.kv_shared);
-  h->target_ctas = h->num_sms * env_int("AVSG_ATTN_CTAS_PER_SM", 4);
+  h->target_ctas = h->num_sms * env_int("AVSG_ATTN_CTAS_PER_SM",
+                                         attention_ctas_per_sm(s.D, s.DV, s.G, s.kv_shared));
   h->gather_ctas = h->num_sms * env_int("AVSG_GATHER_CTAS_PER_SM", 4);
   // The staged gather splits all units' miss-set cells evenly over its CTAs;
   // with one CTA per request each CTA's range is exactly one request's units.
@@ -465,6 +466,14 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   h->budget.assign((size_t)U, s.B);
   h->min_budget = s.B;
   rc = init_state(h, nullptr);
+  if (rc == AVSG_OK) {  // the host store's translations, once, before the first step
+    const size_t kb = (size_t)U * c.num_entries * ek, vb = shared ? 0 : (size_t)U * c.num_entries * ev;
+    unsigned* sink = reinterpret_cast<unsigned*>(s.desc_count);  // zeroed again below
+    e = launch_host_touch(s.host_k, kb, sink, h->num_sms, nullptr);
+    if (e == cudaSuccess) e = launch_host_touch(s.host_v, vb, sink, h->num_sms, nullptr);
+    if (e == cudaSuccess) e = cudaMemsetAsync(s.desc_count, 0, 4, nullptr);
+    if (e != cudaSuccess) rc = AVSG_ERR_CUDA;
+  }
   if (rc == AVSG_OK) {
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) rc = AVSG_ERR_CUDA;

@@ -19,6 +19,7 @@
 // splits of every (unit, token) (a CTA with the whole range writes the output
 // itself).
 #include <math.h>
+#include <stdlib.h>
 
 #include "avsg_internal.cuh"
 
@@ -381,9 +382,7 @@ cudaError_t run(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
   dim3 grid((unsigned)a.splits, (unsigned)s.U, (unsigned)a.n_tok);
   e = launch_pdl(attn_kernel<SH>, grid, dim3(SH::NT), smem, st, s, a);
   if (e != cudaSuccess || a.splits == 1) return e;
-  if ((size_t)a.splits * ((kMergeCols + SH::DV - 1) / SH::DV + 1) > kMergeMaxW) return cudaErrorInvalidValue;
-  dim3 mgrid((unsigned)(s.U * a.n_tok), (unsigned)((SH::G * SH::DV + kMergeCols - 1) / kMergeCols));
-  return launch_pdl(merge_kernel, mgrid, dim3(kMergeThreads), 0, st, s, a);
+  return launch_attention_merge(s, a, st);
 }
 
 // Compiled shapes: (D, Dv, G, shared).
@@ -400,6 +399,20 @@ cudaError_t run(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
 
 }  // namespace
 
+cudaError_t launch_attention_merge(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
+  if ((size_t)a.splits * ((kMergeCols + s.DV - 1) / s.DV + 1) > kMergeMaxW) return cudaErrorInvalidValue;
+  dim3 mgrid((unsigned)(s.U * a.n_tok), (unsigned)((s.G * s.DV + kMergeCols - 1) / kMergeCols));
+  return launch_pdl(merge_kernel, mgrid, dim3(kMergeThreads), 0, st, s, a);
+}
+
+bool attention_h16_enabled() {
+  static const int on = [] {
+    const char* v = getenv("AVSG_ATTN_H16");
+    return (v && *v) ? atoi(v) : 1;
+  }();
+  return on != 0;
+}
+
 bool attention_supported(int D, int DV, int G, int kv_shared) {
 #define X(d, dv, g, sh, cw, hgp) \
   if (D == d && DV == dv && G == g && (kv_shared != 0) == sh) return true;
@@ -409,6 +422,8 @@ bool attention_supported(int D, int DV, int G, int kv_shared) {
 }
 
 int attention_rows_per_tile(int D, int DV, int G, int kv_shared) {
+  if (attention_h16_enabled() && attention_h16_supported(D, DV, G, kv_shared))
+    return attention_h16_rows_per_tile();
 #define X(d, dv, g, sh, cw, hgp) \
   if (D == d && DV == dv && G == g && (kv_shared != 0) == sh) return Shape<d, dv, g, sh, cw, hgp>::TR;
   AVSG_ATTN_SHAPES(X)
@@ -416,10 +431,19 @@ int attention_rows_per_tile(int D, int DV, int G, int kv_shared) {
   return 0;
 }
 
+int attention_ctas_per_sm(int D, int DV, int G, int kv_shared) {
+  // the 16-head kernel keeps 2 CTAs per SM resident, and each split adds a
+  // 16 x (Dv + 2) partial for the merge: one CTA per SM in all
+  if (attention_h16_enabled() && attention_h16_supported(D, DV, G, kv_shared)) return 1;
+  return 4;
+}
+
 cudaError_t launch_attention(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
   if (attention_tc_enabled() && attention_tc_supported(s.D, s.DV, s.G, s.kv_shared) &&
       a.num_sms > 0)
     return launch_attention_tc(s, a, a.num_sms, st);
+  if (attention_h16_enabled() && attention_h16_supported(s.D, s.DV, s.G, s.kv_shared))
+    return launch_attention_h16(s, a, st);
 #define X(d, dv, g, sh, cw, hgp)                                      \
   if (s.D == d && s.DV == dv && s.G == g && (s.kv_shared != 0) == sh) \
     return run<Shape<d, dv, g, sh, cw, hgp>>(s, a, st);

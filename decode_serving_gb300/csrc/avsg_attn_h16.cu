@@ -1,0 +1,399 @@
+// avsg_attn_h16: split-K decode attention on the tensor cores for 16 query
+// heads per kv-head over wide rows whose K and V are one array (the latent
+// cache: K = V = the 576-wide latent row).
+//
+// Same operation as avsg_attn.cu (the Attention operation of the Spin page,
+// "Unifying Sparse Attention with Hierarchical Memory for Scalable
+// Long-Context LLM Serving", section 2A, over exactly the rows DSA selected,
+// AVSG page arxivdaily 2609.37538, English abstract).  At 16 heads a staged
+// row is worth 32 flop per byte, more than the fp32 pipes keep up with, and
+// the 16 heads fill the M = 16 side of mma.m16n8k16 (bf16 in, fp32
+// accumulate) exactly:
+// * scores S = Q K^T: A = the 16 query rows, as scale*log2(e)*q rounded to
+//   bf16 (hi) plus the bf16 rounding of the remainder (lo), two MMAs per
+//   k-step, so the scores keep about 16 more bits than a bf16 q would.  The
+//   8 warps split the row width: each holds the A fragments of its k-steps
+//   in registers for the whole CTA and covers all 32 rows of a tile (four
+//   n-tiles, B read by ldmatrix); the 8 partial score tiles are summed by
+//   the softmax.
+// * online softmax in the log2 domain: one warp per 2 heads, lane = row.
+// * O += P V: A = P (16 heads x 32 rows, split hi/lo the same way), B = the
+//   staged rows through ldmatrix.trans; each warp owns 72 of the 576 output
+//   columns, so the accumulators need no cross-warp sum.
+// Rows are staged by 16-byte cp.async into padded rows (the ldmatrix reads
+// are free of bank conflicts), two tiles in flight; the rows past the range
+// are zero-filled so that masked rows add exact zeros.  A CTA writes one
+// (max, sum, acc) partial in the layout of avsg_attn.cu, whose merge kernel
+// combines the splits (a CTA that covers the whole range writes the output).
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "avsg_internal.cuh"
+
+namespace avsg {
+namespace {
+
+constexpr int kH = 16;                 // query heads per kv-head (the MMA's M)
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRows = 32;              // rows per tile
+constexpr int kStagesH = 2;
+constexpr int kSPitch = 40;            // floats per head row of a partial score tile
+constexpr int kPPitch = kRows * 2 + 16;  // bytes per head row of the bf16 P tile
+
+template <int D_>
+struct H16Shape {
+  static constexpr int D = D_;
+  static constexpr int PITCH = 2 * D + 16;              // bytes per staged row
+  static constexpr int CH = D / 8;                      // 16-byte chunks per row
+  static constexpr int KS = D / 16;                     // k-steps of the score MMA
+  static constexpr int KSW = (KS + kWarps - 1) / kWarps;  // most k-steps one warp takes
+  static constexpr int NCOL = D / kWarps;               // output columns per warp
+  static constexpr int NTW = NCOL / 8;                  // n-tiles per warp in O += P V
+  static constexpr int STAGE_BYTES = kRows * PITCH;
+  static constexpr int SRED_BYTES = kWarps * kH * kSPitch * 4;
+  static constexpr int P_BYTES = 2 * kH * kPPitch;
+  static constexpr int FIXED = kStagesH * STAGE_BYTES + SRED_BYTES + P_BYTES;
+  static_assert(D % (8 * kWarps) == 0, "row width must split into 8-column tiles per warp");
+  static_assert(NTW >= 1 && NTW <= 16, "bad per-warp column count");
+  static_assert(FIXED % 16 == 0, "alignment");
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte async copy; src_bytes 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// bf16 pair (x in the low half: the lower column) of the rounding of x, y and
+// of what that rounding leaves.
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat16 hx = __float2bfloat16_rn(x), hy = __float2bfloat16_rn(y);
+  const __nv_bfloat16 lx = __float2bfloat16_rn(x - __bfloat162float(hx));
+  const __nv_bfloat16 ly = __float2bfloat16_rn(y - __bfloat162float(hy));
+  hi = (uint32_t)__bfloat16_as_ushort(hx) | ((uint32_t)__bfloat16_as_ushort(hy) << 16);
+  lo = (uint32_t)__bfloat16_as_ushort(lx) | ((uint32_t)__bfloat16_as_ushort(ly) << 16);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <class SH>
+__global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, AttnLaunch a) {
+  constexpr int D = SH::D, PITCH = SH::PITCH, CH = SH::CH, KS = SH::KS, KSW = SH::KSW;
+  constexpr int NTW = SH::NTW;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* stage = smem;                                              // [2][kRows][PITCH]
+  float* sred = reinterpret_cast<float*>(smem + kStagesH * SH::STAGE_BYTES);  // [8][16][kSPitch]
+  unsigned char* pt = smem + kStagesH * SH::STAGE_BYTES + SH::SRED_BYTES;     // [hi,lo][16][kPPitch]
+  int32_t* slots = reinterpret_cast<int32_t*>(smem + SH::FIXED);
+  __shared__ float alpha_s[kH], m_s[kH], l_s[kH];
+  __shared__ int s_stop;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;  // fragment row (head) and column pair
+  const int sp = blockIdx.x, u = blockIdx.y, tok = blockIdx.z;
+  griddep_wait();
+  griddep_launch();
+  if (a.io) {
+    const StepIO io = load_io(a.io);
+    if (!a.q) a.q = io.q;
+    a.out = io.out;
+    a.slot_map = io.slot_map;
+  }
+  if (tid == 0) s_stop = load_err(s.err);
+  __syncthreads();
+  if (s_stop) return;
+
+  const int k = a.k, ET = s.ET;
+  const int eps = (k + a.splits - 1) / a.splits;
+  const int e0 = sp * eps;
+  const int ne = max(0, min(k, e0 + eps) - e0);
+  const int rows = ne * ET;
+  const int ntiles = (rows + kRows - 1) / kRows;
+  const size_t sel_base = ((size_t)u * a.n_tok + tok) * (size_t)k;
+  for (int i = tid; i < ne; i += kThreads)
+    slots[i] = a.identity_slots ? tok * k + e0 + i : a.slot_map[sel_base + e0 + i];
+  __syncthreads();
+
+  const uint32_t stage_u = smem_u32(stage);
+  const unsigned char* kb = s.kbuf;
+  auto issue = [&](int tile, int buf) {
+    const int r0 = tile * kRows;
+    for (int i = tid; i < kRows * CH; i += kThreads) {
+      const int r = i / CH, w = i - r * CH;
+      const int row = r0 + r;
+      const uint32_t dst = stage_u + (uint32_t)((buf * kRows + r) * PITCH + w * 16);
+      if (row < rows) {
+        const int ent = row / ET, sub = row - ent * ET;
+        const size_t srow = ((size_t)u * s.B + slots[ent]) * ET + sub;
+        cp_async16_zfill(dst, kb + srow * (size_t)(2 * D) + w * 16, 16);
+      } else {
+        cp_async16_zfill(dst, kb, 0);
+      }
+    }
+  };
+  issue(0, 0);
+  cp_async_commit();
+  if (ntiles > 1) issue(1, 1);
+  cp_async_commit();
+
+  // A fragments of this warp's k-steps (q pre-scaled, hi and lo), for the
+  // whole CTA: rows g and g + 8, columns 2c, 2c + 1 and 2c + 8, 2c + 9.
+  const int ks0 = warp * KS / kWarps, ks1 = (warp + 1) * KS / kWarps;
+  uint32_t qa[KSW][2][4];
+  {
+    const float* q0 = a.q + (((size_t)u * a.n_tok + tok) * kH + g) * D;
+    const float* q1 = q0 + 8 * D;
+    const float sc = a.scale_log2;
+#pragma unroll
+    for (int kk = 0; kk < KSW; ++kk) {
+      const int ks = ks0 + kk;
+      if (ks < ks1) {
+        const int col = ks * 16 + 2 * c;
+        const float2 x0 = *reinterpret_cast<const float2*>(q0 + col);
+        const float2 x1 = *reinterpret_cast<const float2*>(q1 + col);
+        const float2 x2 = *reinterpret_cast<const float2*>(q0 + col + 8);
+        const float2 x3 = *reinterpret_cast<const float2*>(q1 + col + 8);
+        split_pair(x0.x * sc, x0.y * sc, qa[kk][0][0], qa[kk][1][0]);
+        split_pair(x1.x * sc, x1.y * sc, qa[kk][0][1], qa[kk][1][1]);
+        split_pair(x2.x * sc, x2.y * sc, qa[kk][0][2], qa[kk][1][2]);
+        split_pair(x3.x * sc, x3.y * sc, qa[kk][0][3], qa[kk][1][3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) qa[kk][0][j] = qa[kk][1][j] = 0u;
+      }
+    }
+  }
+
+  float acc[NTW][4];
+#pragma unroll
+  for (int n = 0; n < NTW; ++n)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[n][j] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // heads 2*warp, 2*warp + 1
+
+  const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix index and row of the address
+  const uint32_t pt_u = smem_u32(pt);
+  for (int tl = 0; tl < ntiles; ++tl) {
+    const int buf = tl & 1;
+    const int nvalid = min(kRows, rows - tl * kRows);
+    const uint32_t tile_u = stage_u + (uint32_t)(buf * SH::STAGE_BYTES);
+    cp_async_wait<1>();
+    __syncthreads();
+    {  // this warp's k-steps of S = Q K^T for the tile's 32 rows
+      float sacc[4][4];
+#pragma unroll
+      for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sacc[n][j] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KSW; ++kk) {
+        const int ks = ks0 + kk;
+        if (ks < ks1) {
+          // matrix lm of each x4: n-tile (lm >> 1) (+2), columns ks*16 + (lm & 1)*8
+          uint32_t b01[4], b23[4];
+          const uint32_t off = (uint32_t)(((lm >> 1) * 8 + lr) * PITCH + (ks * 16 + (lm & 1) * 8) * 2);
+          ldsm_x4(tile_u + off, b01);
+          ldsm_x4(tile_u + off + 16 * PITCH, b23);
+          mma_bf16(sacc[0], qa[kk][0], b01[0], b01[1]);
+          mma_bf16(sacc[0], qa[kk][1], b01[0], b01[1]);
+          mma_bf16(sacc[1], qa[kk][0], b01[2], b01[3]);
+          mma_bf16(sacc[1], qa[kk][1], b01[2], b01[3]);
+          mma_bf16(sacc[2], qa[kk][0], b23[0], b23[1]);
+          mma_bf16(sacc[2], qa[kk][1], b23[0], b23[1]);
+          mma_bf16(sacc[3], qa[kk][0], b23[2], b23[3]);
+          mma_bf16(sacc[3], qa[kk][1], b23[2], b23[3]);
+        }
+      }
+      float* sw = sred + warp * kH * kSPitch;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        *reinterpret_cast<float2*>(sw + g * kSPitch + n * 8 + 2 * c) = make_float2(sacc[n][0], sacc[n][1]);
+        *reinterpret_cast<float2*>(sw + (g + 8) * kSPitch + n * 8 + 2 * c) =
+            make_float2(sacc[n][2], sacc[n][3]);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {  // online softmax, heads 2*warp and 2*warp + 1, lane = row
+      const int h = 2 * warp + hh;
+      float sv = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) sv += sred[(w2 * kH + h) * kSPitch + lane];
+      sv = lane < nvalid ? sv : -INFINITY;
+      const float m_new = fmaxf(m_run[hh], warp_max(sv));
+      float alpha = 1.f, p = 0.f;
+      if (m_new != -INFINITY) {
+        alpha = exp2f(m_run[hh] - m_new);
+        p = exp2f(sv - m_new);
+      }
+      l_run[hh] = l_run[hh] * alpha + warp_sum(p);
+      m_run[hh] = m_new;
+      const __nv_bfloat16 ph = __float2bfloat16_rn(p);
+      const __nv_bfloat16 pl = __float2bfloat16_rn(p - __bfloat162float(ph));
+      reinterpret_cast<__nv_bfloat16*>(pt + h * kPPitch)[lane] = ph;
+      reinterpret_cast<__nv_bfloat16*>(pt + (kH + h) * kPPitch)[lane] = pl;
+      if (lane == 0) alpha_s[h] = alpha;
+    }
+    __syncthreads();
+    {  // O += P V over this warp's columns
+      const float al0 = alpha_s[g], al1 = alpha_s[g + 8];
+#pragma unroll
+      for (int n = 0; n < NTW; ++n) {
+        acc[n][0] *= al0;
+        acc[n][1] *= al0;
+        acc[n][2] *= al1;
+        acc[n][3] *= al1;
+      }
+      const int cbase = warp * SH::NCOL;
+#pragma unroll
+      for (int kq = 0; kq < kRows / 16; ++kq) {
+        // A: matrix lm = heads (lm & 1)*8.., rows kq*16 + (lm >> 1)*8..
+        uint32_t pa_hi[4], pa_lo[4];
+        const uint32_t aoff = (uint32_t)(((lm & 1) * 8 + lr) * kPPitch + (kq * 16 + (lm >> 1) * 8) * 2);
+        ldsm_x4(pt_u + aoff, pa_hi);
+        ldsm_x4(pt_u + kH * kPPitch + aoff, pa_lo);
+        // B: matrix lm = rows kq*16 + (lm & 1)*8.., columns of n-tile 2j + (lm >> 1)
+        const uint32_t brow = tile_u + (uint32_t)((kq * 16 + (lm & 1) * 8 + lr) * PITCH);
+#pragma unroll
+        for (int j = 0; j < NTW / 2; ++j) {
+          uint32_t b[4];
+          ldsm_x4_t(brow + (uint32_t)((cbase + (2 * j + (lm >> 1)) * 8) * 2), b);
+          mma_bf16(acc[2 * j], pa_hi, b[0], b[1]);
+          mma_bf16(acc[2 * j], pa_lo, b[0], b[1]);
+          mma_bf16(acc[2 * j + 1], pa_hi, b[2], b[3]);
+          mma_bf16(acc[2 * j + 1], pa_lo, b[2], b[3]);
+        }
+        if (NTW & 1) {
+          uint32_t b0, b1;
+          ldsm_x2_t(brow + (uint32_t)((cbase + (NTW - 1) * 8) * 2), b0, b1);
+          mma_bf16(acc[NTW - 1], pa_hi, b0, b1);
+          mma_bf16(acc[NTW - 1], pa_lo, b0, b1);
+        }
+      }
+    }
+    __syncthreads();
+    if (tl + 2 < ntiles) issue(tl + 2, buf);
+    cp_async_commit();
+  }
+  cp_async_wait<0>();
+  if (lane == 0) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      m_s[2 * warp + hh] = m_run[hh];
+      l_s[2 * warp + hh] = l_run[hh];
+    }
+  }
+  __syncthreads();
+
+  const int DV = D;
+  const int cbase = warp * SH::NCOL;
+  if (a.splits == 1) {
+    float* out = a.out + ((size_t)u * a.n_tok + tok) * (size_t)kH * DV;
+    const float l0 = l_s[g], l1 = l_s[g + 8];
+    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+    for (int n = 0; n < NTW; ++n) {
+      const int col = cbase + n * 8 + 2 * c;
+      *reinterpret_cast<float2*>(out + (size_t)g * DV + col) = make_float2(acc[n][0] * i0, acc[n][1] * i0);
+      *reinterpret_cast<float2*>(out + (size_t)(g + 8) * DV + col) =
+          make_float2(acc[n][2] * i1, acc[n][3] * i1);
+    }
+    return;
+  }
+  const size_t stride = (size_t)kH * (DV + 2);
+  float* pp = s.part + (((size_t)u * a.n_tok + tok) * (size_t)a.splits + sp) * stride;
+#pragma unroll
+  for (int n = 0; n < NTW; ++n) {
+    const int col = cbase + n * 8 + 2 * c;
+    *reinterpret_cast<float2*>(pp + 2 * kH + (size_t)g * DV + col) = make_float2(acc[n][0], acc[n][1]);
+    *reinterpret_cast<float2*>(pp + 2 * kH + (size_t)(g + 8) * DV + col) =
+        make_float2(acc[n][2], acc[n][3]);
+  }
+  if (tid < kH) {
+    pp[tid] = m_s[tid];
+    pp[kH + tid] = l_s[tid];
+  }
+}
+
+template <class SH>
+cudaError_t run(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
+  static int smem_done = 0;
+  const int eps = (a.k + a.splits - 1) / a.splits;
+  const size_t smem = SH::FIXED + ((size_t)eps * 4 + 15) / 16 * 16;
+  cudaError_t e = ensure_smem((const void*)attn_h16_kernel<SH>, smem, &smem_done);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)a.splits, (unsigned)s.U, (unsigned)a.n_tok);
+  e = launch_pdl(attn_h16_kernel<SH>, grid, dim3(kThreads), smem, st, s, a);
+  if (e != cudaSuccess || a.splits == 1) return e;
+  return launch_attention_merge(s, a, st);
+}
+
+// Compiled row widths (K = V, 16 heads).
+#define AVSG_H16_WIDTHS(X) X(576)
+
+}  // namespace
+
+bool attention_h16_supported(int D, int DV, int G, int kv_shared) {
+  if (G != kH || D != DV || !kv_shared) return false;
+#define X(d) \
+  if (D == d) return true;
+  AVSG_H16_WIDTHS(X)
+#undef X
+  return false;
+}
+
+int attention_h16_rows_per_tile() { return kRows; }
+
+cudaError_t launch_attention_h16(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
+#define X(d) \
+  if (s.D == d) return run<H16Shape<d>>(s, a, st);
+  AVSG_H16_WIDTHS(X)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace avsg

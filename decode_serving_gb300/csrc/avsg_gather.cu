@@ -258,6 +258,27 @@ cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st) {
   return launch_pdl(gather_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
 }
 
+// One 4-byte read in every 4 KiB page of a mapped host range.  The first
+// device access to a region of the host store costs a translation the
+// device then keeps; taking them all at once when a handle is created keeps
+// them out of the first decode steps (4.5 GiB: about 0.3 ms).
+__global__ void host_touch_kernel(const unsigned char* __restrict__ p, size_t bytes,
+                                  unsigned* __restrict__ sink) {
+  constexpr size_t kPage = 4096;
+  unsigned acc = 0;
+  for (size_t off = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * kPage; off + 4 <= bytes;
+       off += (size_t)gridDim.x * blockDim.x * kPage)
+    acc += __ldcg(reinterpret_cast<const unsigned*>(p + off));
+  if (acc == 0x9E3779B9u) *sink = acc;  // keeps the loads; practically never taken
+}
+
+cudaError_t launch_host_touch(const unsigned char* p, size_t bytes, unsigned* sink, int num_sms,
+                              cudaStream_t st) {
+  if (!p || bytes < 4) return cudaSuccess;
+  host_touch_kernel<<<dim3((unsigned)(num_sms * 8)), dim3(256), 0, st>>>(p, bytes, sink);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st) {
   static int attr_done = 0;
   const cudaError_t e = ensure_smem((const void*)gather_stage_kernel, 0, &attr_done);

@@ -174,6 +174,10 @@ cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
 cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st);
 // Staged rows -> their reserved slots (after the gather and the reservation).
 cudaError_t launch_place(const DeviceState& s, cudaStream_t st);
+// Reads one word of every 4 KiB page of a mapped host range (sink: a device
+// word it may write), so the device's translations of the range are in place.
+cudaError_t launch_host_touch(const unsigned char* p, size_t bytes, unsigned* sink, int num_sms,
+                              cudaStream_t st);
 cudaError_t launch_gather_all(const DeviceState& s, const StepIO& v, int n_tok, int k, int ctas,
                               cudaStream_t st);
 
@@ -192,6 +196,16 @@ struct AttnLaunch {
 bool attention_supported(int D, int DV, int G, int kv_shared);
 int attention_rows_per_tile(int D, int DV, int G, int kv_shared);
 cudaError_t launch_attention(const DeviceState& s, const AttnLaunch& a, cudaStream_t st);
+// Merge of the split partials of launch_attention's generic and 16-head paths.
+cudaError_t launch_attention_merge(const DeviceState& s, const AttnLaunch& a, cudaStream_t st);
+// Tensor-core attention for 16 heads per kv-head over shared K = V rows
+// (avsg_attn_h16.cu), used by launch_attention where it applies.
+bool attention_h16_enabled();
+bool attention_h16_supported(int D, int DV, int G, int kv_shared);
+int attention_h16_rows_per_tile();
+cudaError_t launch_attention_h16(const DeviceState& s, const AttnLaunch& a, cudaStream_t st);
+// Default attention CTAs per SM for a shape (the target of the split count).
+int attention_ctas_per_sm(int D, int DV, int G, int kv_shared);
 // Tensor-core attention (avsg_attn_tc.cu): K rows of 64 or 128, G <= 8, Dv == D.
 bool attention_tc_supported(int D, int DV, int G, int kv_shared);
 size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sms);

@@ -50,6 +50,12 @@ SMALL = {
                                   steps=16),
     "latent_small": W.get_workload("latent", requests=2, context=65536, k=256, slots=512, steps=16),
     "latent_k_eq_b": W.get_workload("latent", requests=2, context=65536, k=256, slots=256, steps=12),
+    # one CTA per (unit, token) over a ragged 20-row tile: output written without a merge
+    "latent_one_tile": W.get_workload("latent", requests=2, context=4096, k=20, slots=64, steps=6,
+                                      forced="none"),
+    # 19 splits of 106 rows each: four tiles per CTA, the last one ragged
+    "latent_multi_tile": W.get_workload("latent", requests=8, context=16384, k=2000, slots=2048,
+                                        steps=4),
     "k1": W.get_workload("tiny", k=1, slots=32, steps=8, forced="none"),
     "g2": W.get_workload("tiny", q_per_kv=2, steps=8),
     "g8": W.get_workload("tiny", q_per_kv=8, steps=8),
