@@ -567,6 +567,10 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   };
   const DeviceState& sc = s;
   if (sc_out) *sc_out = sc;
+  // With the per-kernel events on, every kernel runs on st in an order that
+  // keeps the dependencies, so each is timed alone (as a serialised profiler
+  // sees it) rather than beside the kernels of the other streams.
+  cudaStream_t side = h->prof ? st : h->side, side2 = h->prof ? st : h->side2;
   if (h->no_reuse) {
     AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather_all(sc, v, n_tok, k, h->gather_ctas, st));
     e = take_first();
@@ -578,10 +582,19 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   e = take_first();
   if (e != cudaSuccess) return fail_cuda(h, e);
   if (!h->overlap) {
+    // The hash-table update is needed only by the next step's match: it runs
+    // on side2 beside the gather and the attention.
     AVSG_RUN(AVSG_KERNEL_RESERVE, st, launch_victims(sc, n_tok, k, st));
+    e = cudaEventRecord(h->ev_reserve, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_reserve, 0);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
+    e = cudaEventRecord(h->ev_commit, side2);
+    if (e != cudaSuccess) return fail_cuda(h, e);
     AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(sc, h->gather_ctas, st));
-    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(sc, st));
     AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(sc, a, st));
+    e = cudaStreamWaitEvent(st, h->ev_commit, 0);
+    if (e != cudaSuccess) return fail_cuda(h, e);
     return AVSG_OK;
   }
   // Two-pass pipeline (the tensor-core shapes).  After match, three
@@ -597,28 +610,28 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   int splits_h = 0, splits_m = 0;
   two_pass_splits(h, n_tok, k, &splits_h, &splits_m);
   e = cudaEventRecord(h->ev_fork, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side2, h->ev_fork, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_fork, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_fork, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
   DeviceState staged = sc;  // miss rows are read from the staging area, by cell
   staged.kbuf = s.kstage;
   staged.vbuf = s.vstage;
   staged.B = s.MS;
-  AVSG_RUN(AVSG_KERNEL_GATHER, h->side, launch_gather_stage(sc, h->stage_ctas, h->side));
-  e = cudaEventRecord(h->ev_staged, h->side);
+  AVSG_RUN(AVSG_KERNEL_GATHER, side, launch_gather_stage(sc, h->stage_ctas, side));
+  e = cudaEventRecord(h->ev_staged, side);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, h->side,
-           launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, h->side));
-  e = cudaEventRecord(h->ev_gather, h->side);
+  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, side,
+           launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, side));
+  e = cudaEventRecord(h->ev_gather, side);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_RESERVE, h->side2, launch_victims(sc, n_tok, k, h->side2));
-  e = cudaEventRecord(h->ev_reserve, h->side2);
+  AVSG_RUN(AVSG_KERNEL_RESERVE, side2, launch_victims(sc, n_tok, k, side2));
+  e = cudaEventRecord(h->ev_reserve, side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_COMMIT, h->side2, launch_commit(sc, h->side2));
-  e = cudaStreamWaitEvent(h->side2, h->ev_staged, 0);  // staged rows -> slots, beside the miss pass
+  AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
+  e = cudaStreamWaitEvent(side2, h->ev_staged, 0);  // staged rows -> slots, beside the miss pass
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_PLACE, h->side2, launch_place(sc, h->side2));
-  e = cudaEventRecord(h->ev_commit, h->side2);
+  AVSG_RUN(AVSG_KERNEL_PLACE, side2, launch_place(sc, side2));
+  e = cudaEventRecord(h->ev_commit, side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, splits_h, splits_m, st));
   e = cudaStreamWaitEvent(st, h->ev_gather, 0);

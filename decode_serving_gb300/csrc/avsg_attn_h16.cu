@@ -22,16 +22,25 @@
 //   columns, so the accumulators need no cross-warp sum.
 // Rows are staged by 16-byte cp.async into padded rows (the ldmatrix reads
 // are free of bank conflicts), two tiles in flight; the rows past the range
-// are zero-filled so that masked rows add exact zeros.  A CTA writes one
-// (max, sum, acc) partial in the layout of avsg_attn.cu, whose merge kernel
-// combines the splits (a CTA that covers the whole range writes the output).
+// are zero-filled so that masked rows add exact zeros.
+// The CTAs of a (unit, token) form clusters of 8 over consecutive row ranges.
+// A cluster merges its 8 partial softmaxes in distributed shared memory:
+// each CTA publishes (max, sum) per head and its accumulators rescaled to
+// the cluster's max, then sums one eighth of the output columns over the 8
+// CTAs.  One cluster per pair writes the output; several write one (max,
+// sum, acc) partial each in the layout of avsg_attn.cu, whose merge kernel
+// combines them.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include "avsg_internal.cuh"
 
 namespace avsg {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kH = 16;                 // query heads per kv-head (the MMA's M)
 constexpr int kWarps = 8;
@@ -40,12 +49,14 @@ constexpr int kRows = 32;              // rows per tile
 constexpr int kStagesH = 2;
 constexpr int kSPitch = 40;            // floats per head row of a partial score tile
 constexpr int kPPitch = kRows * 2 + 16;  // bytes per head row of the bf16 P tile
+constexpr int kCl = 8;                 // CTAs per cluster (the in-cluster merge)
 
 template <int D_>
 struct H16Shape {
   static constexpr int D = D_;
   static constexpr int PITCH = 2 * D + 16;              // bytes per staged row
   static constexpr int CH = D / 8;                      // 16-byte chunks per row
+  static constexpr int CPL = (CH + 31) / 32;            // chunks per lane of a row copy
   static constexpr int KS = D / 16;                     // k-steps of the score MMA
   static constexpr int KSW = (KS + kWarps - 1) / kWarps;  // most k-steps one warp takes
   static constexpr int NCOL = D / kWarps;               // output columns per warp
@@ -54,7 +65,11 @@ struct H16Shape {
   static constexpr int SRED_BYTES = kWarps * kH * kSPitch * 4;
   static constexpr int P_BYTES = 2 * kH * kPPitch;
   static constexpr int FIXED = kStagesH * STAGE_BYTES + SRED_BYTES + P_BYTES;
+  static constexpr int RPITCH = D + 8;                  // floats per head row of the merge buffer
+  static constexpr int CCOL = D / kCl;                  // output columns each cluster rank sums
   static_assert(D % (8 * kWarps) == 0, "row width must split into 8-column tiles per warp");
+  static_assert(CCOL % 4 == 0, "cluster ranks sum float4 columns");
+  static_assert(kH * RPITCH * 4 <= kStagesH * STAGE_BYTES, "merge buffer reuses the staging");
   static_assert(NTW >= 1 && NTW <= 16, "bad per-warp column count");
   static_assert(FIXED % 16 == 0, "alignment");
 };
@@ -129,62 +144,74 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   float* sred = reinterpret_cast<float*>(smem + kStagesH * SH::STAGE_BYTES);  // [8][16][kSPitch]
   unsigned char* pt = smem + kStagesH * SH::STAGE_BYTES + SH::SRED_BYTES;     // [hi,lo][16][kPPitch]
   int32_t* slots = reinterpret_cast<int32_t*>(smem + SH::FIXED);
-  __shared__ float alpha_s[kH], m_s[kH], l_s[kH];
+  __shared__ float alpha_s[kH], m_s[kH], l_s[kH], w_s[kH], mc_s[kH], lc_s[kH];
   __shared__ int s_stop;
+  cg::cluster_group cl = cg::this_cluster();
+  const int crank = (int)cl.block_rank();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;  // fragment row (head) and column pair
   const int sp = blockIdx.x, u = blockIdx.y, tok = blockIdx.z;
-  griddep_wait();
   griddep_launch();
-  if (a.io) {
-    const StepIO io = load_io(a.io);
-    if (!a.q) a.q = io.q;
-    a.out = io.out;
-    a.slot_map = io.slot_map;
-  }
-  if (tid == 0) s_stop = load_err(s.err);
-  __syncthreads();
-  if (s_stop) return;
-
-  const int k = a.k, ET = s.ET;
-  const int eps = (k + a.splits - 1) / a.splits;
+  const int k = a.k, ET = s.ET, S = gridDim.x;
+  const int eps = (k + S - 1) / S;
   const int e0 = sp * eps;
   const int ne = max(0, min(k, e0 + eps) - e0);
   const int rows = ne * ET;
-  const int ntiles = (rows + kRows - 1) / kRows;
   const size_t sel_base = ((size_t)u * a.n_tok + tok) * (size_t)k;
-  for (int i = tid; i < ne; i += kThreads)
-    slots[i] = a.identity_slots ? tok * k + e0 + i : a.slot_map[sel_base + e0 + i];
-  __syncthreads();
-
   const uint32_t stage_u = smem_u32(stage);
   const unsigned char* kb = s.kbuf;
-  auto issue = [&](int tile, int buf) {
+  // slots[e]: >= 0 the slot of a row resident before this step (a hit);
+  // -1 not known yet; <= -2 the slot (-2 - value) of a row this step's
+  // gather writes.  which: 0 every row, 1 the resident rows and the zero
+  // rows past the range, 2 the gathered rows.  A slot outside the buffer
+  // (only after a latched error) reads as a zero row.
+  // Warp w copies rows w, w + 8, ... of a tile (the row's slot and address
+  // are worked out once per warp); lane l takes its 16-byte chunks l, l + 32
+  // and l + 64.
+  auto issue = [&](int tile, int buf, int which) {
     const int r0 = tile * kRows;
-    for (int i = tid; i < kRows * CH; i += kThreads) {
-      const int r = i / CH, w = i - r * CH;
+    for (int r = warp; r < kRows; r += kWarps) {
       const int row = r0 + r;
-      const uint32_t dst = stage_u + (uint32_t)((buf * kRows + r) * PITCH + w * 16);
+      const uint32_t dst = stage_u + (uint32_t)((buf * kRows + r) * PITCH) + lane * 16;
+      const unsigned char* src = nullptr;  // a zero row
       if (row < rows) {
-        const int ent = row / ET, sub = row - ent * ET;
-        const size_t srow = ((size_t)u * s.B + slots[ent]) * ET + sub;
-        cp_async16_zfill(dst, kb + srow * (size_t)(2 * D) + w * 16, 16);
-      } else {
-        cp_async16_zfill(dst, kb, 0);
+        const int ent = ET == 1 ? row : row / ET, sub = row - ent * ET;
+        int sl = slots[ent];
+        const bool late = sl <= -2;
+        if ((which == 1 && sl < 0) || (which == 2 && !late)) continue;
+        if (late) sl = -2 - sl;
+        if (sl >= 0 && sl < s.B)
+          src = kb + (((size_t)u * s.B + sl) * ET + sub) * (size_t)(2 * D) + lane * 16;
+      } else if (which == 2) {
+        continue;
       }
+#pragma unroll
+      for (int j = 0; j < SH::CPL; ++j)
+        if (lane + 32 * j < CH) cp_async16_zfill(dst + 512 * j, src ? src + 512 * j : kb, src ? 16 : 0);
     }
   };
-  issue(0, 0);
-  cp_async_commit();
-  if (ntiles > 1) issue(1, 1);
-  cp_async_commit();
+  const int ntiles_all = (rows + kRows - 1) / kRows;
+
+  // Reuse path: match (this step's first kernel) wrote the hit slots and the
+  // copy of q, and no kernel of the step writes a hit row's slot, so those
+  // rows stream in while the gather (the kernel this one waits for) runs.
+  const bool early = !a.identity_slots && a.io != nullptr;
+  if (early) {
+    for (int i = tid; i < ne; i += kThreads) {
+      const int sl = __ldcg(s.hslot + sel_base + e0 + i);
+      slots[i] = sl >= 0 ? sl : -1;
+    }
+    __syncthreads();
+    issue(0, 0, 1);
+    if (ntiles_all > 1) issue(1, 1, 1);
+  }
 
   // A fragments of this warp's k-steps (q pre-scaled, hi and lo), for the
   // whole CTA: rows g and g + 8, columns 2c, 2c + 1 and 2c + 8, 2c + 9.
   const int ks0 = warp * KS / kWarps, ks1 = (warp + 1) * KS / kWarps;
   uint32_t qa[KSW][2][4];
-  {
+  auto load_q = [&]() {
     const float* q0 = a.q + (((size_t)u * a.n_tok + tok) * kH + g) * D;
     const float* q1 = q0 + 8 * D;
     const float sc = a.scale_log2;
@@ -193,10 +220,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
       const int ks = ks0 + kk;
       if (ks < ks1) {
         const int col = ks * 16 + 2 * c;
-        const float2 x0 = *reinterpret_cast<const float2*>(q0 + col);
-        const float2 x1 = *reinterpret_cast<const float2*>(q1 + col);
-        const float2 x2 = *reinterpret_cast<const float2*>(q0 + col + 8);
-        const float2 x3 = *reinterpret_cast<const float2*>(q1 + col + 8);
+        const float2 x0 = __ldcg(reinterpret_cast<const float2*>(q0 + col));
+        const float2 x1 = __ldcg(reinterpret_cast<const float2*>(q1 + col));
+        const float2 x2 = __ldcg(reinterpret_cast<const float2*>(q0 + col + 8));
+        const float2 x3 = __ldcg(reinterpret_cast<const float2*>(q1 + col + 8));
         split_pair(x0.x * sc, x0.y * sc, qa[kk][0][0], qa[kk][1][0]);
         split_pair(x1.x * sc, x1.y * sc, qa[kk][0][1], qa[kk][1][1]);
         split_pair(x2.x * sc, x2.y * sc, qa[kk][0][2], qa[kk][1][2]);
@@ -206,7 +233,44 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
         for (int j = 0; j < 4; ++j) qa[kk][0][j] = qa[kk][1][j] = 0u;
       }
     }
+  };
+  const bool q_early = a.q != nullptr;  // match's copy; else the caller's q, known after the wait
+  if (q_early) load_q();
+
+  griddep_wait();
+  if (a.io) {
+    const StepIO io = load_io(a.io);
+    if (!a.q) a.q = io.q;
+    a.out = io.out;
+    a.slot_map = io.slot_map;
   }
+  if (tid == 0) s_stop = load_err(s.err);
+  __syncthreads();
+  // A stopped CTA skips its rows but still takes part in every cluster
+  // barrier below, so no CTA of the cluster waits for one that left.
+  const bool run = s_stop == 0;
+  if (!q_early) load_q();
+  if (run) {
+    if (early) {  // the gathered rows' slots, from the slot map
+      for (int i = tid; i < ne; i += kThreads)
+        if (slots[i] < 0) {
+          const int sl = __ldcg(a.slot_map + sel_base + e0 + i);
+          slots[i] = -2 - (sl >= 0 && sl < s.B ? sl : s.B);
+        }
+      __syncthreads();
+      issue(0, 0, 2);
+      if (ntiles_all > 1) issue(1, 1, 2);
+    } else {
+      for (int i = tid; i < ne; i += kThreads)
+        slots[i] = a.identity_slots ? tok * k + e0 + i : __ldcg(a.slot_map + sel_base + e0 + i);
+      __syncthreads();
+      issue(0, 0, 0);
+      if (ntiles_all > 1) issue(1, 1, 0);
+    }
+  }
+  cp_async_commit();  // tiles 0 and 1 (both in this group)
+  cp_async_commit();  // (empty: the loop expects one group per tile)
+  const int ntiles = run ? ntiles_all : 0;
 
   float acc[NTW][4];
 #pragma unroll
@@ -316,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
       }
     }
     __syncthreads();
-    if (tl + 2 < ntiles) issue(tl + 2, buf);
+    if (tl + 2 < ntiles) issue(tl + 2, buf, 0);
     cp_async_commit();
   }
   cp_async_wait<0>();
@@ -327,49 +391,117 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
       l_s[2 * warp + hh] = l_run[hh];
     }
   }
-  __syncthreads();
+  cl.sync();  // every rank's (max, sum) is published; the staging is free
 
-  const int DV = D;
-  const int cbase = warp * SH::NCOL;
-  if (a.splits == 1) {
-    float* out = a.out + ((size_t)u * a.n_tok + tok) * (size_t)kH * DV;
-    const float l0 = l_s[g], l1 = l_s[g + 8];
-    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  // per head: the cluster's max and sum, and this rank's weight
+  if (tid < kH) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kCl; ++r) M = fmaxf(M, *cl.map_shared_rank(&m_s[tid], r));
+    float L = 0.f;
+#pragma unroll
+    for (int r = 0; r < kCl; ++r) {
+      const float mr = *cl.map_shared_rank(&m_s[tid], r);
+      if (mr != -INFINITY) L = fmaf(*cl.map_shared_rank(&l_s[tid], r), exp2f(mr - M), L);
+    }
+    mc_s[tid] = M;
+    lc_s[tid] = L;
+    w_s[tid] = m_s[tid] == -INFINITY ? 0.f : exp2f(m_s[tid] - M);
+  }
+  __syncthreads();
+  float* red = reinterpret_cast<float*>(stage);  // [16][RPITCH], this rank's rescaled acc
+  {
+    const float w0 = w_s[g], w1 = w_s[g + 8];
+    const int cbase = warp * SH::NCOL;
 #pragma unroll
     for (int n = 0; n < NTW; ++n) {
       const int col = cbase + n * 8 + 2 * c;
-      *reinterpret_cast<float2*>(out + (size_t)g * DV + col) = make_float2(acc[n][0] * i0, acc[n][1] * i0);
-      *reinterpret_cast<float2*>(out + (size_t)(g + 8) * DV + col) =
-          make_float2(acc[n][2] * i1, acc[n][3] * i1);
+      *reinterpret_cast<float2*>(red + g * SH::RPITCH + col) = make_float2(acc[n][0] * w0, acc[n][1] * w0);
+      *reinterpret_cast<float2*>(red + (g + 8) * SH::RPITCH + col) =
+          make_float2(acc[n][2] * w1, acc[n][3] * w1);
     }
-    return;
   }
-  const size_t stride = (size_t)kH * (DV + 2);
-  float* pp = s.part + (((size_t)u * a.n_tok + tok) * (size_t)a.splits + sp) * stride;
+  cl.sync();  // every rank's rescaled acc is in place
+
+  // this rank's columns, summed over the cluster
+  const int DV = D;
+  const int nclu = S / kCl, clu = sp / kCl;
+  const size_t pair = (size_t)u * a.n_tok + tok;
+  float* dst;
+  size_t hstride;
+  if (nclu == 1) {
+    dst = a.out + pair * (size_t)kH * DV;
+    hstride = DV;
+  } else {
+    float* pp = s.part + (pair * nclu + clu) * (size_t)kH * (DV + 2);
+    if (crank == 0 && tid < kH && run) {
+      pp[tid] = mc_s[tid];
+      pp[kH + tid] = lc_s[tid];
+    }
+    dst = pp + 2 * kH;
+    hstride = DV;
+  }
+  constexpr int C4 = SH::CCOL / 4;
+  for (int i = tid; i < kH * C4; i += kThreads) {
+    const int h = i / C4, col = crank * SH::CCOL + (i - h * C4) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int n = 0; n < NTW; ++n) {
-    const int col = cbase + n * 8 + 2 * c;
-    *reinterpret_cast<float2*>(pp + 2 * kH + (size_t)g * DV + col) = make_float2(acc[n][0], acc[n][1]);
-    *reinterpret_cast<float2*>(pp + 2 * kH + (size_t)(g + 8) * DV + col) =
-        make_float2(acc[n][2], acc[n][3]);
+    for (int r = 0; r < kCl; ++r) {
+      const float4 x = *reinterpret_cast<const float4*>(cl.map_shared_rank(red + h * SH::RPITCH + col, r));
+      v.x += x.x;
+      v.y += x.y;
+      v.z += x.z;
+      v.w += x.w;
+    }
+    if (nclu == 1) {
+      const float L = lc_s[h];
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      v.x *= inv;
+      v.y *= inv;
+      v.z *= inv;
+      v.w *= inv;
+    }
+    if (run) *reinterpret_cast<float4*>(dst + (size_t)h * hstride + col) = v;
   }
-  if (tid < kH) {
-    pp[tid] = m_s[tid];
-    pp[kH + tid] = l_s[tid];
-  }
+  cl.sync();  // no rank leaves while another still reads its shared memory
 }
 
+// a.splits (the caller's split count) rounded up to whole clusters: 8 CTAs
+// per cluster, and one merged partial per cluster.
 template <class SH>
 cudaError_t run(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
   static int smem_done = 0;
-  const int eps = (a.k + a.splits - 1) / a.splits;
+  static const int nclu_env = [] {
+    const char* v = getenv("AVSG_H16_CLUSTERS");
+    return (v && *v) ? atoi(v) : 0;
+  }();
+  const int nclu = nclu_env > 0 ? nclu_env : (a.splits + kCl - 1) / kCl;
+  const int ctas = nclu * kCl;
+  if ((size_t)s.U * a.n_tok * nclu * kH * (s.DV + 2) > a.part_capacity && nclu > 1)
+    return cudaErrorInvalidValue;
+  const int eps = (a.k + ctas - 1) / ctas;
   const size_t smem = SH::FIXED + ((size_t)eps * 4 + 15) / 16 * 16;
   cudaError_t e = ensure_smem((const void*)attn_h16_kernel<SH>, smem, &smem_done);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)a.splits, (unsigned)s.U, (unsigned)a.n_tok);
-  e = launch_pdl(attn_h16_kernel<SH>, grid, dim3(kThreads), smem, st, s, a);
-  if (e != cudaSuccess || a.splits == 1) return e;
-  return launch_attention_merge(s, a, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, (unsigned)s.U, (unsigned)a.n_tok);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, attn_h16_kernel<SH>, s, a);
+  if (e != cudaSuccess || nclu == 1) return e;
+  AttnLaunch m = a;
+  m.splits = nclu;
+  return launch_attention_merge(s, m, st);
 }
 
 // Compiled row widths (K = V, 16 heads).
