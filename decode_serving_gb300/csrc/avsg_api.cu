@@ -57,6 +57,7 @@ struct avsg_handle_s {
               ev_staged = nullptr, ev_place = nullptr;
   bool staged = false;  // staging area allocated: the two-pass pipeline is available
   bool overlap = false;  // steps run the two-pass pipeline
+  bool overlap_h16 = false;  // ... in its 16-head form (one attention launch after the staged gather)
   // Captured steps: one CUDA graph per (tokens, k), re-pointed at each step
   // by updating its first kernel node (see StepIO).
   struct StepGraph {
@@ -307,8 +308,12 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
                                      (c.buffer_slots + 31) / 32) > kMatchSmemMax))
     return AVSG_ERR_CAPACITY;
   if (!attention_supported(c.head_dim, c.v_dim, c.q_per_kv, c.kv_shared)) return AVSG_ERR_UNSUPPORTED;
-  if ((c.flags & AVSG_FLAG_REQUEST_GATHER) && !no_reuse &&
-      !attention_tc_supported(c.head_dim, c.v_dim, c.q_per_kv, c.kv_shared))
+  // shapes with a staging area: the tensor-core two-pass pipeline and the
+  // 16-head kernel, which both read missed rows from it by miss-set cell
+  const bool tc_shape = attention_tc_supported(c.head_dim, c.v_dim, c.q_per_kv, c.kv_shared);
+  const bool h16_shape = attention_h16_enabled() &&
+                         attention_h16_supported(c.head_dim, c.v_dim, c.q_per_kv, c.kv_shared);
+  if ((c.flags & AVSG_FLAG_REQUEST_GATHER) && !no_reuse && !tc_shape && !h16_shape)
     return AVSG_ERR_UNSUPPORTED;  // request-level assignment exists in the staged gather only
   const int64_t ek = (int64_t)c.entry_tokens * c.head_dim * 2;
   const int64_t ev = shared ? 0 : (int64_t)c.entry_tokens * c.v_dim * 2;
@@ -382,7 +387,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.kbuf, (size_t)U * s.B * ek);
   cv.take(&s.vbuf, (size_t)U * s.B * ev);
   // staging rows for the two-pass pipeline (one per miss-set cell)
-  h->staged = !no_reuse && attention_tc_supported(s.D, s.DV, s.G, s.kv_shared);
+  h->staged = !no_reuse && (tc_shape || h16_shape);
   cv.take(&s.kstage, h->staged ? (size_t)U * s.MS * ek : 0);
   cv.take(&s.vstage, h->staged ? (size_t)U * s.MS * ev : 0);
   cv.take(&s.tag, ub);
@@ -413,7 +418,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     }
     h->part_floats = part > tc ? part : tc;
     h->part_floats = h->part_floats > two ? h->part_floats : two;
-    h->overlap = h->staged && overlap_enabled() && attention_tc_enabled();
+    h->overlap = h->staged && overlap_enabled() && (h16_shape || attention_tc_enabled());
+    h->overlap_h16 = h->overlap && !tc_shape;
     cv.take(&s.part, h->part_floats);
   }
   cv.take(&s.part_count, (size_t)U * kMaxTokens);
@@ -594,6 +600,34 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
     AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(sc, h->gather_ctas, st));
     AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention(sc, a, st));
     e = cudaStreamWaitEvent(st, h->ev_commit, 0);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    return AVSG_OK;
+  }
+  if (h->overlap_h16) {
+    // 16-head shapes: after match, the staged gather and then the attention
+    // on side (the attention reads hit rows from their slots while the
+    // gather runs, missed rows from the staging area once it is done); the
+    // reservation, the hash-table update and the move of the staged rows
+    // into their slots on side2.
+    a.staged_misses = 1;
+    e = cudaEventRecord(h->ev_fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_fork, 0);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    AVSG_RUN(AVSG_KERNEL_GATHER, side, launch_gather_stage(sc, h->stage_ctas, side));
+    e = cudaEventRecord(h->ev_staged, side);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    AVSG_RUN(AVSG_KERNEL_ATTENTION, side, launch_attention(sc, a, side));
+    e = cudaEventRecord(h->ev_gather, side);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    AVSG_RUN(AVSG_KERNEL_RESERVE, side2, launch_victims(sc, n_tok, k, side2));
+    AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
+    e = cudaStreamWaitEvent(side2, h->ev_staged, 0);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    AVSG_RUN(AVSG_KERNEL_PLACE, side2, launch_place(sc, side2));
+    e = cudaEventRecord(h->ev_commit, side2);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_gather, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_commit, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
     return AVSG_OK;
   }

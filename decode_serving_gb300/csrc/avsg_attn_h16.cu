@@ -162,10 +162,15 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   const uint32_t stage_u = smem_u32(stage);
   const unsigned char* kb = s.kbuf;
   // slots[e]: >= 0 the slot of a row resident before this step (a hit);
-  // -1 not known yet; <= -2 the slot (-2 - value) of a row this step's
-  // gather writes.  which: 0 every row, 1 the resident rows and the zero
-  // rows past the range, 2 the gathered rows.  A slot outside the buffer
-  // (only after a latched error) reads as a zero row.
+  // -1 not known yet; <= -2 for a row this step's gather writes: its slot
+  // (-2 - value), or with staged misses its miss-set cell.  which: 0 every
+  // row, 1 the resident rows and the zero rows past the range, 2 the
+  // gathered rows.  A slot or cell out of range (only after a latched
+  // error) reads as a zero row.
+  // Staged misses: the kernel this one waits for is the staged gather, and
+  // both know a miss by its cell from match alone.
+  const bool early = !a.identity_slots && a.io != nullptr;
+  const bool staged = early && a.staged_misses != 0;
   // Warp w copies rows w, w + 8, ... of a tile (the row's slot and address
   // are worked out once per warp); lane l takes its 16-byte chunks l, l + 32
   // and l + 64.
@@ -181,8 +186,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
         const bool late = sl <= -2;
         if ((which == 1 && sl < 0) || (which == 2 && !late)) continue;
         if (late) sl = -2 - sl;
-        if (sl >= 0 && sl < s.B)
-          src = kb + (((size_t)u * s.B + sl) * ET + sub) * (size_t)(2 * D) + lane * 16;
+        const bool stg = late && staged;  // a missed row, at its cell of the staging area
+        const int nb = stg ? s.MS : s.B;
+        if (sl >= 0 && sl < nb)
+          src = (stg ? s.kstage : kb) + (((size_t)u * nb + sl) * ET + sub) * (size_t)(2 * D) + lane * 16;
       } else if (which == 2) {
         continue;
       }
@@ -193,14 +200,17 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   };
   const int ntiles_all = (rows + kRows - 1) / kRows;
 
-  // Reuse path: match (this step's first kernel) wrote the hit slots and the
-  // copy of q, and no kernel of the step writes a hit row's slot, so those
-  // rows stream in while the gather (the kernel this one waits for) runs.
-  const bool early = !a.identity_slots && a.io != nullptr;
+  // Reuse path: match (this step's first kernel) wrote the step's I/O, the
+  // hit slots and the copy of q, and no kernel of the step writes a hit
+  // row's slot, so those rows stream in while the gather (the kernel this
+  // one waits for) runs.
   if (early) {
+    const StepIO io = load_io(a.io);
+    a.out = io.out;
+    a.slot_map = io.slot_map;
     for (int i = tid; i < ne; i += kThreads) {
       const int sl = __ldcg(s.hslot + sel_base + e0 + i);
-      slots[i] = sl >= 0 ? sl : -1;
+      slots[i] = sl >= 0 ? sl : !staged ? -1 : sl <= -2 ? sl : -2 - s.MS;
     }
     __syncthreads();
     issue(0, 0, 1);
@@ -238,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   if (q_early) load_q();
 
   griddep_wait();
-  if (a.io) {
+  if (a.io && !early) {
     const StepIO io = load_io(a.io);
     if (!a.q) a.q = io.q;
     a.out = io.out;
@@ -251,7 +261,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   const bool run = s_stop == 0;
   if (!q_early) load_q();
   if (run) {
-    if (early) {  // the gathered rows' slots, from the slot map
+    if (staged) {
+      issue(0, 0, 2);
+      if (ntiles_all > 1) issue(1, 1, 2);
+    } else if (early) {  // the gathered rows' slots, from the slot map
       for (int i = tid; i < ne; i += kThreads)
         if (slots[i] < 0) {
           const int sl = __ldcg(a.slot_map + sel_base + e0 + i);

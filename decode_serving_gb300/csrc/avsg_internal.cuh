@@ -76,7 +76,8 @@ struct DeviceState {
   int32_t* hused;                  // [U] non-empty hash cells (live + erased)
   unsigned long long* mset;        // [U][MS] {id | token bits << 32}: this step's miss set
                                    // (two sets alternate by step; each is empty when its step starts)
-  int32_t* hslot;                  // [U][n_tok][k] slot of each selected id if it was a hit, else -1
+  int32_t* hslot;                  // [U][n_tok][k] slot of each selected id if it was a hit,
+                                   // else -2 - its miss-set cell (-1 if it has none)
   int32_t* mslot;                  // [U][MS] slot reserved for the miss in that cell
   GatherDesc* desc;                // [U * max_union]
   int32_t* desc_count;             // [1]
@@ -191,6 +192,8 @@ struct AttnLaunch {
   const StepIO* io;                // when set, out and slot_map are read from here, and q too
                                    // when q is null
   int num_sms;                     // SMs of the device (persistent grid size)
+  int staged_misses;               // 16-head kernel: a miss's row is read from the staging
+                                   // area at its miss-set cell (hslot holds -2 - cell)
   size_t part_capacity;            // floats available at DeviceState::part
 };
 bool attention_supported(int D, int DV, int G, int kv_shared);

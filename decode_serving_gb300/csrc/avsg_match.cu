@@ -19,8 +19,10 @@
 //     (a bit already set means the id repeats within one token's list);
 //   * a miss is entered in the step's miss set (one cell per distinct id,
 //     claimed or extended with one compare-and-swap; token bits merged, so a
-//     multi-token iteration reserves each id once); the slot map gets
-//     -2 - cell until the reservation kernel resolves it.
+//     multi-token iteration reserves each id once); the slot map and the
+//     hit-slot list get -2 - cell (the slot map until the reservation
+//     kernel resolves it; the list keeps it for the attention that reads
+//     missed rows from the staging area by cell).
 // The unit's q is also copied to a fixed device buffer for the attention
 // kernels.  The miss set and the hit bitmaps are then written out whole (coalesced),
 // so neither needs clearing between steps.  Nothing in the buffer state
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
       }
       if (miss_cell < 0) raise_error(s.err, AVSG_ERR_CAPACITY, u, pos);  // miss set full
       slot_map[off] = -2 - miss_cell;
-      s.hslot[off] = -1;
+      s.hslot[off] = miss_cell >= 0 ? -2 - miss_cell : -1;
       if (hit) hit[off] = 0;
     }
   }

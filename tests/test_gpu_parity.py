@@ -79,7 +79,7 @@ def test_no_reuse_path(name):
     assert err <= ATTN_TOL
 
 
-@pytest.mark.parametrize("name", ["batch_small", "mtp_small", "pages_small"])
+@pytest.mark.parametrize("name", ["batch_small", "mtp_small", "pages_small", "latent_small"])
 def test_request_level_gather_gives_the_same_results(name):
     """Transfer assignment by request (one gather CTA per request) changes only
     which CTA copies which miss: every slot map, buffer row and output still
@@ -137,3 +137,41 @@ def test_hand_worked_fixtures_on_gpu(name):
         s.close()
         hk.free()
         hv.free()
+
+
+SERIAL_SCRIPT = """
+import sys
+sys.path.insert(0, {tests!r})
+import workload as W
+from gpu_harness import ATTN_TOL, Parity
+for w in ({cases}):
+    p = Parity(w)
+    try:
+        p.run()
+        st = p.sess.stats()
+        assert st.device_error == 0
+        assert st.hits == p.ref.hits and st.misses == p.ref.misses
+        assert p.max_err <= ATTN_TOL, p.max_err
+    finally:
+        p.close()
+print("serial ok")
+"""
+
+
+def test_serial_pipeline_gives_the_same_results():
+    """With the overlapped pipeline switched off (AVSG_OVERLAP=0, read once per
+    process, so in a child process) every kernel runs on one stream: match,
+    reservation, gather into the slots, hash update, attention over the slot
+    map.  Same oracle, same results."""
+    import subprocess
+    import sys
+    cases = ", ".join([
+        'W.get_workload("latent", requests=2, context=65536, k=256, slots=512, steps=8)',
+        'W.get_workload("batch", requests=2, kv_heads=2, context=4096, k=300, slots=1024, steps=8)',
+    ])
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = SERIAL_SCRIPT.format(tests=here, cases=cases + ",")
+    env = dict(os.environ, AVSG_OVERLAP="0")
+    r = subprocess.run([sys.executable, "-c", code], cwd=os.path.dirname(here), env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "serial ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]

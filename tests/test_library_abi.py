@@ -75,8 +75,6 @@ def _cfg(**kw):
     # a step's miss set (2 * 8 * 2048 cells, rounded up) exceeds match's shared memory
     (dict(max_tokens_per_step=8, max_select=2048, buffer_slots=16384, num_entries=1 << 20), -2),
     (dict(q_per_kv=3), -7),                           # no attention kernel for G=3
-    # request-level gather assignment exists for the tensor-core shapes only
-    (dict(head_dim=576, v_dim=576, kv_shared=True, q_per_kv=16, request_gather=True), -7),
     (dict(head_dim=96, v_dim=96), -7),
 ])
 def test_create_rejects_bad_configs_on_the_host(lib, kw, code):
