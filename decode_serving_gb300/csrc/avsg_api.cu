@@ -607,8 +607,8 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
     // 16-head shapes: after match, the staged gather and then the attention
     // on side (the attention reads hit rows from their slots while the
     // gather runs, missed rows from the staging area once it is done); the
-    // reservation, the hash-table update and the move of the staged rows
-    // into their slots on side2.
+    // reservation and then the move of the staged rows into their slots on
+    // side2; the hash-table update on st once the reservation is done.
     a.staged_misses = 1;
     e = cudaEventRecord(h->ev_fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_fork, 0);
@@ -621,12 +621,15 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
     e = cudaEventRecord(h->ev_gather, side);
     if (e != cudaSuccess) return fail_cuda(h, e);
     AVSG_RUN(AVSG_KERNEL_RESERVE, side2, launch_victims(sc, n_tok, k, side2));
-    AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
-    e = cudaStreamWaitEvent(side2, h->ev_staged, 0);
+    e = cudaEventRecord(h->ev_reserve, side2);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_staged, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
     AVSG_RUN(AVSG_KERNEL_PLACE, side2, launch_place(sc, side2));
     e = cudaEventRecord(h->ev_commit, side2);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_gather, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_reserve, 0);
+    if (e != cudaSuccess) return fail_cuda(h, e);
+    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(sc, st));
+    e = cudaStreamWaitEvent(st, h->ev_gather, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_commit, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
     return AVSG_OK;

@@ -25,9 +25,9 @@
 // are zero-filled so that masked rows add exact zeros.
 // The CTAs of a (unit, token) form clusters of 8 over consecutive row ranges.
 // A cluster merges its 8 partial softmaxes in distributed shared memory:
-// each CTA publishes (max, sum) per head and its accumulators rescaled to
-// the cluster's max, then sums one eighth of the output columns over the 8
-// CTAs.  One cluster per pair writes the output; several write one (max,
+// each CTA publishes (max, sum) per head and its accumulators, works out the
+// 8 ranks' weights from the maxima, then sums one eighth of the output
+// columns over the 8 CTAs with those weights.  One cluster per pair writes the output; several write one (max,
 // sum, acc) partial each in the layout of avsg_attn.cu, whose merge kernel
 // combines them.
 #include <cooperative_groups.h>
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   float* sred = reinterpret_cast<float*>(smem + kStagesH * SH::STAGE_BYTES);  // [8][16][kSPitch]
   unsigned char* pt = smem + kStagesH * SH::STAGE_BYTES + SH::SRED_BYTES;     // [hi,lo][16][kPPitch]
   int32_t* slots = reinterpret_cast<int32_t*>(smem + SH::FIXED);
-  __shared__ float alpha_s[kH], m_s[kH], l_s[kH], w_s[kH], mc_s[kH], lc_s[kH];
+  __shared__ float alpha_s[kH], m_s[kH], l_s[kH], w_s[kCl * kH], mc_s[kH], lc_s[kH];
   __shared__ int s_stop;
   cg::cluster_group cl = cg::this_cluster();
   const int crank = (int)cl.block_rank();
@@ -301,11 +301,11 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
     cp_async_wait<1>();
     __syncthreads();
     {  // this warp's k-steps of S = Q K^T for the tile's 32 rows
-      float sacc[4][4];
+      float sacc[4][4], slo[4][4];  // hi and lo products in separate chains, summed after
 #pragma unroll
       for (int n = 0; n < 4; ++n)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sacc[n][j] = 0.f;
+        for (int j = 0; j < 4; ++j) sacc[n][j] = slo[n][j] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < KSW; ++kk) {
         const int ks = ks0 + kk;
@@ -316,15 +316,19 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
           ldsm_x4(tile_u + off, b01);
           ldsm_x4(tile_u + off + 16 * PITCH, b23);
           mma_bf16(sacc[0], qa[kk][0], b01[0], b01[1]);
-          mma_bf16(sacc[0], qa[kk][1], b01[0], b01[1]);
+          mma_bf16(slo[0], qa[kk][1], b01[0], b01[1]);
           mma_bf16(sacc[1], qa[kk][0], b01[2], b01[3]);
-          mma_bf16(sacc[1], qa[kk][1], b01[2], b01[3]);
+          mma_bf16(slo[1], qa[kk][1], b01[2], b01[3]);
           mma_bf16(sacc[2], qa[kk][0], b23[0], b23[1]);
-          mma_bf16(sacc[2], qa[kk][1], b23[0], b23[1]);
+          mma_bf16(slo[2], qa[kk][1], b23[0], b23[1]);
           mma_bf16(sacc[3], qa[kk][0], b23[2], b23[3]);
-          mma_bf16(sacc[3], qa[kk][1], b23[2], b23[3]);
+          mma_bf16(slo[3], qa[kk][1], b23[2], b23[3]);
         }
       }
+#pragma unroll
+      for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sacc[n][j] += slo[n][j];
       float* sw = sred + warp * kH * kSPitch;
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
@@ -397,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
     cp_async_commit();
   }
   cp_async_wait<0>();
+  __syncthreads();  // the staging is free: it takes this rank's accumulators
   if (lane == 0) {
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -404,37 +409,43 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
       l_s[2 * warp + hh] = l_run[hh];
     }
   }
-  cl.sync();  // every rank's (max, sum) is published; the staging is free
-
-  // per head: the cluster's max and sum, and this rank's weight
-  if (tid < kH) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < kCl; ++r) M = fmaxf(M, *cl.map_shared_rank(&m_s[tid], r));
-    float L = 0.f;
-#pragma unroll
-    for (int r = 0; r < kCl; ++r) {
-      const float mr = *cl.map_shared_rank(&m_s[tid], r);
-      if (mr != -INFINITY) L = fmaf(*cl.map_shared_rank(&l_s[tid], r), exp2f(mr - M), L);
-    }
-    mc_s[tid] = M;
-    lc_s[tid] = L;
-    w_s[tid] = m_s[tid] == -INFINITY ? 0.f : exp2f(m_s[tid] - M);
-  }
-  __syncthreads();
-  float* red = reinterpret_cast<float*>(stage);  // [16][RPITCH], this rank's rescaled acc
+  float* red = reinterpret_cast<float*>(stage);  // [16][RPITCH], this rank's acc
   {
-    const float w0 = w_s[g], w1 = w_s[g + 8];
     const int cbase = warp * SH::NCOL;
 #pragma unroll
     for (int n = 0; n < NTW; ++n) {
       const int col = cbase + n * 8 + 2 * c;
-      *reinterpret_cast<float2*>(red + g * SH::RPITCH + col) = make_float2(acc[n][0] * w0, acc[n][1] * w0);
-      *reinterpret_cast<float2*>(red + (g + 8) * SH::RPITCH + col) =
-          make_float2(acc[n][2] * w1, acc[n][3] * w1);
+      *reinterpret_cast<float2*>(red + g * SH::RPITCH + col) = make_float2(acc[n][0], acc[n][1]);
+      *reinterpret_cast<float2*>(red + (g + 8) * SH::RPITCH + col) = make_float2(acc[n][2], acc[n][3]);
     }
   }
-  cl.sync();  // every rank's rescaled acc is in place
+  cl.sync();  // every rank's (max, sum) and accumulators are published
+
+  // weight of rank r for head h: exp2(m_r - M) with M the cluster's max;
+  // the cluster's sum L = sum over r of l_r times that weight
+  if (tid < kCl * kH) {
+    const int r = tid / kH, h = tid - r * kH;
+    float mr[kCl];
+#pragma unroll
+    for (int q = 0; q < kCl; ++q) mr[q] = *cl.map_shared_rank(&m_s[h], q);
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kCl; ++q) M = fmaxf(M, mr[q]);
+    float mine = 0.f;
+#pragma unroll
+    for (int q = 0; q < kCl; ++q)
+      if (q == r) mine = mr[q] == -INFINITY ? 0.f : exp2f(mr[q] - M);
+    w_s[r * kH + h] = mine;
+    if (r == 0) {
+      float L = 0.f;
+#pragma unroll
+      for (int q = 0; q < kCl; ++q)
+        if (mr[q] != -INFINITY) L = fmaf(*cl.map_shared_rank(&l_s[h], q), exp2f(mr[q] - M), L);
+      mc_s[h] = M;
+      lc_s[h] = L;
+    }
+  }
+  __syncthreads();
 
   // this rank's columns, summed over the cluster
   const int DV = D;
@@ -457,14 +468,18 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   constexpr int C4 = SH::CCOL / 4;
   for (int i = tid; i < kH * C4; i += kThreads) {
     const int h = i / C4, col = crank * SH::CCOL + (i - h * C4) * 4;
+    float4 x[kCl];
+#pragma unroll
+    for (int r = 0; r < kCl; ++r)
+      x[r] = *reinterpret_cast<const float4*>(cl.map_shared_rank(red + h * SH::RPITCH + col, r));
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < kCl; ++r) {
-      const float4 x = *reinterpret_cast<const float4*>(cl.map_shared_rank(red + h * SH::RPITCH + col, r));
-      v.x += x.x;
-      v.y += x.y;
-      v.z += x.z;
-      v.w += x.w;
+      const float wr = w_s[r * kH + h];
+      v.x = fmaf(wr, x[r].x, v.x);
+      v.y = fmaf(wr, x[r].y, v.y);
+      v.z = fmaf(wr, x[r].z, v.z);
+      v.w = fmaf(wr, x[r].w, v.w);
     }
     if (nclu == 1) {
       const float L = lc_s[h];
