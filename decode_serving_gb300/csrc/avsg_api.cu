@@ -266,7 +266,7 @@ int init_state(avsg_handle h, cudaStream_t st) {
     AVSG_SET(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
   }
   AVSG_SET(s.desc_count, 0, 4);
-  AVSG_SET(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);
+  AVSG_SET(s.part_count, 0, (size_t)s.U * kMaxTokens * kCountsPerPair * 4);
   AVSG_SET(s.counters, 0, (size_t)s.U * sizeof(DevCounters));
   AVSG_SET(s.err, 0, sizeof(DevErr));
 #undef AVSG_SET
@@ -422,7 +422,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     h->overlap_h16 = h->overlap && !tc_shape;
     cv.take(&s.part, h->part_floats);
   }
-  cv.take(&s.part_count, (size_t)U * kMaxTokens);
+  cv.take(&s.part_count, (size_t)U * kMaxTokens * kCountsPerPair);
   cv.take(&s.counters, (size_t)U);
   cv.take(&s.err, 1);
   cv.take(&s.budget, (size_t)U);
@@ -551,6 +551,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   a.io = s.io;
   a.num_sms = h->num_sms;
   a.part_capacity = h->part_floats;
+  a.count_capacity = (size_t)s.U * kMaxTokens * kCountsPerPair;
   Prof pf{h};
 #define AVSG_RUN(kernel_index, stream, call) \
   do {                                       \
@@ -956,7 +957,7 @@ extern "C" int avsg_clear_error(avsg_handle h) {
     if (e == cudaSuccess) e = cudaMemset(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
   }
   if (e == cudaSuccess) e = cudaMemset(s.desc_count, 0, 4);
-  if (e == cudaSuccess) e = cudaMemset(s.part_count, 0, (size_t)s.U * kMaxTokens * 4);
+  if (e == cudaSuccess) e = cudaMemset(s.part_count, 0, (size_t)s.U * kMaxTokens * kCountsPerPair * 4);
   if (e == cudaSuccess) e = cudaMemset(s.err, 0, sizeof(DevErr));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail_cuda(h, e);

@@ -27,9 +27,12 @@
 // A cluster merges its 8 partial softmaxes in distributed shared memory:
 // each CTA publishes (max, sum) per head and its accumulators, works out the
 // 8 ranks' weights from the maxima, then sums one eighth of the output
-// columns over the 8 CTAs with those weights.  One cluster per pair writes the output; several write one (max,
-// sum, acc) partial each in the layout of avsg_attn.cu, whose merge kernel
-// combines them.
+// columns over the 8 CTAs with those weights.  One cluster per pair writes
+// the output.  With several, rank r of each cluster writes its column slice
+// with the cluster's (max, sum) and counts its arrival; the last to arrive
+// for a slice merges the clusters' slices into the output.  (Without room
+// for the counters, the clusters write (max, sum, acc) partials in the
+// layout of avsg_attn.cu and its merge kernel combines them.)
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -50,6 +53,7 @@ constexpr int kStagesH = 2;
 constexpr int kSPitch = 40;            // floats per head row of a partial score tile
 constexpr int kPPitch = kRows * 2 + 16;  // bytes per head row of the bf16 P tile
 constexpr int kCl = 8;                 // CTAs per cluster (the in-cluster merge)
+constexpr int kMaxFused = 32;          // most clusters per pair the last-arriver merge takes
 
 template <int D_>
 struct H16Shape {
@@ -145,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   unsigned char* pt = smem + kStagesH * SH::STAGE_BYTES + SH::SRED_BYTES;     // [hi,lo][16][kPPitch]
   int32_t* slots = reinterpret_cast<int32_t*>(smem + SH::FIXED);
   __shared__ float alpha_s[kH], m_s[kH], l_s[kH], w_s[kCl * kH], mc_s[kH], lc_s[kH];
-  __shared__ int s_stop;
+  __shared__ float wm_s[kMaxFused * kH];  // fused merge: weight of each cluster per head
+  __shared__ int s_stop, s_last;
   cg::cluster_group cl = cg::this_cluster();
   const int crank = (int)cl.block_rank();
 
@@ -451,11 +456,23 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   const int DV = D;
   const int nclu = S / kCl, clu = sp / kCl;
   const size_t pair = (size_t)u * a.n_tok + tok;
-  float* dst;
+  constexpr int BS = 2 * kH + kH * SH::CCOL;  // a cluster's slice: (max, sum) per head, columns
+  const bool fused = nclu > 1 && a.fused_merge;
+  float* dst;       // where column col of head h goes: dst + h * hstride + col - cbias
   size_t hstride;
+  int cbias = 0;
   if (nclu == 1) {
     dst = a.out + pair * (size_t)kH * DV;
     hstride = DV;
+  } else if (fused) {
+    float* blk = s.part + ((pair * kCl + crank) * nclu + clu) * (size_t)BS;
+    if (tid < kH && run) {
+      blk[tid] = mc_s[tid];
+      blk[kH + tid] = lc_s[tid];
+    }
+    dst = blk + 2 * kH;
+    hstride = SH::CCOL;
+    cbias = crank * SH::CCOL;
   } else {
     float* pp = s.part + (pair * nclu + clu) * (size_t)kH * (DV + 2);
     if (crank == 0 && tid < kH && run) {
@@ -489,9 +506,53 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
       v.z *= inv;
       v.w *= inv;
     }
-    if (run) *reinterpret_cast<float4*>(dst + (size_t)h * hstride + col) = v;
+    if (run) *reinterpret_cast<float4*>(dst + (size_t)h * hstride + col - cbias) = v;
   }
   cl.sync();  // no rank leaves while another still reads its shared memory
+  if (!fused || !run) return;
+
+  // Arrival count per (pair, column slice): the last cluster to write its
+  // slice merges the slices of all nclu clusters and writes the output
+  // columns (the counter goes back to 0 for the next step).
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    int32_t* cnt = s.part_count + pair * kCl + crank;
+    s_last = atomicAdd(cnt, 1) == nclu - 1;
+    if (s_last) *cnt = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* b0 = s.part + (pair * kCl + crank) * nclu * (size_t)BS;
+  if (tid < kH) {
+    float M = -INFINITY;
+    for (int q = 0; q < nclu; ++q) M = fmaxf(M, __ldcg(b0 + (size_t)q * BS + tid));
+    float L = 0.f;
+    for (int q = 0; q < nclu; ++q) {
+      const float mq = __ldcg(b0 + (size_t)q * BS + tid);
+      const float wq = mq == -INFINITY ? 0.f : exp2f(mq - M);
+      wm_s[q * kH + tid] = wq;
+      L = fmaf(__ldcg(b0 + (size_t)q * BS + kH + tid), wq, L);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int q = 0; q < nclu; ++q) wm_s[q * kH + tid] *= inv;
+  }
+  __syncthreads();
+  float* out = a.out + pair * (size_t)kH * DV;
+  for (int i = tid; i < kH * C4; i += kThreads) {
+    const int h = i / C4, c4 = (i - h * C4) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < nclu; ++q) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(b0 + (size_t)q * BS + 2 * kH + h * SH::CCOL + c4));
+      const float wq = wm_s[q * kH + h];
+      v.x = fmaf(wq, x.x, v.x);
+      v.y = fmaf(wq, x.y, v.y);
+      v.z = fmaf(wq, x.z, v.z);
+      v.w = fmaf(wq, x.w, v.w);
+    }
+    *reinterpret_cast<float4*>(out + (size_t)h * DV + crank * SH::CCOL + c4) = v;
+  }
 }
 
 // a.splits (the caller's split count) rounded up to whole clusters: 8 CTAs
@@ -503,10 +564,23 @@ cudaError_t run(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
     const char* v = getenv("AVSG_H16_CLUSTERS");
     return (v && *v) ? atoi(v) : 0;
   }();
-  const int nclu = nclu_env > 0 ? nclu_env : (a.splits + kCl - 1) / kCl;
+  // At most one CTA per SM in all, so that the grid, resident early and
+  // waiting on the gather, leaves room for the reservation's kernels; a
+  // larger grid (many pairs) is launched once the gather is done.
+  const long long pairs = (long long)s.U * a.n_tok;
+  int nclu = nclu_env > 0 ? nclu_env : (a.splits + kCl - 1) / kCl;
+  if (nclu_env <= 0 && a.num_sms > 0) {
+    const long long fit = a.num_sms / (kCl * pairs);
+    if (fit >= 1 && nclu > fit) nclu = (int)fit;
+  }
+  const bool early = a.num_sms > 0 && (long long)nclu * kCl * pairs <= a.num_sms;
   const int ctas = nclu * kCl;
-  if ((size_t)s.U * a.n_tok * nclu * kH * (s.DV + 2) > a.part_capacity && nclu > 1)
-    return cudaErrorInvalidValue;
+  static_assert(kCountsPerPair >= kCl, "one arrival counter per cluster rank");
+  AttnLaunch b = a;
+  b.fused_merge = nclu > 1 && nclu <= kMaxFused && (size_t)pairs * kCl <= a.count_capacity;
+  const size_t part = b.fused_merge ? (size_t)pairs * kCl * nclu * (2 * kH + kH * SH::CCOL)
+                                    : (size_t)pairs * nclu * kH * (s.DV + 2);
+  if (nclu > 1 && part > a.part_capacity) return cudaErrorInvalidValue;
   const int eps = (a.k + ctas - 1) / ctas;
   const size_t smem = SH::FIXED + ((size_t)eps * 4 + 15) / 16 * 16;
   cudaError_t e = ensure_smem((const void*)attn_h16_kernel<SH>, smem, &smem_done);
@@ -522,11 +596,11 @@ cudaError_t run(const DeviceState& s, const AttnLaunch& a, cudaStream_t st) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[1].val.programmaticStreamSerializationAllowed = early && pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, attn_h16_kernel<SH>, s, a);
-  if (e != cudaSuccess || nclu == 1) return e;
+  e = cudaLaunchKernelEx(&cfg, attn_h16_kernel<SH>, s, b);
+  if (e != cudaSuccess || nclu == 1 || b.fused_merge) return e;
   AttnLaunch m = a;
   m.splits = nclu;
   return launch_attention_merge(s, m, st);

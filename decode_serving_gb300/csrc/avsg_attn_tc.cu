@@ -833,7 +833,12 @@ cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int
   cudaError_t e = ensure_smem((const void*)attn_tc_miss_kernel<SH>,
                               SH::SMEM + (size_t)SH::SCAN_MAX * sizeof(int32_t), &smem_miss);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_tc_miss_kernel<SH>, grid, dim3(kThreadsTc), smem, st, s, p);
+  // Launched early (behind the gather, waiting on it) only while its grid
+  // fits one CTA per SM: resident early, a larger grid would hold every SM's
+  // shared memory for the whole gather and keep the hit pass and the
+  // reservation's kernels off the GPU until it ends.
+  const bool early = a.num_sms > 0 && (long long)grid.x * grid.y <= a.num_sms;
+  return launch_ex(early, attn_tc_miss_kernel<SH>, grid, dim3(kThreadsTc), smem, st, s, p);
 }
 
 template <class SH>

@@ -171,9 +171,12 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
 }
 
 // Place: every miss's staged row (by miss-set cell) into its reserved slot
-// (device to device), grid (U, kPlaceSplit): CTA (u, z) takes every
-// kPlaceSplit-th of unit u's reservation descriptors.  A warp reads
-// kPlaceRows descriptors, then their rows' 16-byte chunks, then stores.
+// (device to device), grid (U, kPlaceSplit).  The unit's work is its
+// descriptors' (row, 16-byte chunk) items in row order; the unit's
+// kPlaceSplit * 256 threads take consecutive items (coalesced), kPlaceRows
+// items each per round: the rows' descriptors, then all the loads, then the
+// stores.  Rows of any size keep every thread busy (8 KiB page entries as
+// much as 512-byte token rows).
 constexpr int kPlaceSplit = 4;
 constexpr int kPlaceRows = 8;
 
@@ -181,36 +184,41 @@ __global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s) {
   griddep_wait();
   griddep_launch();
   if (load_err(s.err) != 0) return;
-  const int u = blockIdx.x, z = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int u = blockIdx.x;
   const int base = s.dbase[u], cnt = s.dcount[u];
   const uint32_t cpk = (uint32_t)(s.ek >> 4), cpe = cpk + (uint32_t)(s.ev >> 4);
-  const int step = (kThreads / 32) * kPlaceSplit;
-  for (int d0 = z + warp * kPlaceSplit; d0 < cnt; d0 += step * kPlaceRows) {
-    size_t srow[kPlaceRows], drow[kPlaceRows];
-    bool ok[kPlaceRows];
+  const uint32_t total = (uint32_t)cnt * cpe;
+  const uint32_t nthr = (uint32_t)kPlaceSplit * kThreads;
+  const uint32_t me = blockIdx.y * kThreads + threadIdx.x;
+  for (uint32_t i0 = me; i0 < total; i0 += nthr * kPlaceRows) {
+    uint4 v[kPlaceRows];
+    void* dst[kPlaceRows];
+    const uint4* src[kPlaceRows];
 #pragma unroll
     for (int r = 0; r < kPlaceRows; ++r) {
-      const int d = d0 + r * step;
-      ok[r] = d < cnt;
-      const GatherDesc g = ok[r] ? s.desc[base + d] : GatherDesc{};
-      srow[r] = (size_t)u * s.MS + g.cell;
-      drow[r] = (size_t)u * s.B + g.slot;
+      const uint32_t item = i0 + (uint32_t)r * nthr;
+      dst[r] = nullptr;
+      src[r] = nullptr;
+      if (item < total) {
+        const uint32_t d = item / cpe, c = item - d * cpe;
+        const GatherDesc* g = s.desc + base + d;
+        const size_t srow = (size_t)u * s.MS + __ldcg(&g->cell);
+        const size_t drow = (size_t)u * s.B + __ldcg(&g->slot);
+        if (c < cpk) {
+          src[r] = reinterpret_cast<const uint4*>(s.kstage + srow * s.ek) + c;
+          dst[r] = reinterpret_cast<uint4*>(s.kbuf + drow * s.ek) + c;
+        } else {
+          src[r] = reinterpret_cast<const uint4*>(s.vstage + srow * s.ev) + (c - cpk);
+          dst[r] = reinterpret_cast<uint4*>(s.vbuf + drow * s.ev) + (c - cpk);
+        }
+      }
     }
-    for (uint32_t c = lane; c < cpe; c += 32) {
-      uint4 v[kPlaceRows];
 #pragma unroll
-      for (int r = 0; r < kPlaceRows; ++r)
-        if (ok[r])
-          v[r] = c < cpk ? __ldcg(reinterpret_cast<const uint4*>(s.kstage + srow[r] * s.ek) + c)
-                         : __ldcg(reinterpret_cast<const uint4*>(s.vstage + srow[r] * s.ev) + (c - cpk));
+    for (int r = 0; r < kPlaceRows; ++r)
+      if (src[r]) v[r] = __ldcg(src[r]);
 #pragma unroll
-      for (int r = 0; r < kPlaceRows; ++r)
-        if (ok[r])
-          store16(c < cpk ? static_cast<void*>(reinterpret_cast<uint4*>(s.kbuf + drow[r] * s.ek) + c)
-                          : static_cast<void*>(reinterpret_cast<uint4*>(s.vbuf + drow[r] * s.ev) + (c - cpk)),
-                  v[r]);
-    }
+    for (int r = 0; r < kPlaceRows; ++r)
+      if (dst[r]) store16(dst[r], v[r]);
   }
 }
 

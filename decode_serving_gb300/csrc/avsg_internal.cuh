@@ -14,6 +14,7 @@ constexpr unsigned long long kMissEmpty = ~0ull;
 constexpr int kOrders = 64;                    // reservation classes 0..63
 constexpr int kNotCandidate = 255;
 constexpr int kMaxTokens = 8;
+constexpr int kCountsPerPair = 8;              // arrival counters per (unit, token)
 constexpr int kMissScanMax = 4096;             // most miss-set cells one miss-pass CTA scans
 constexpr int kMatchCluster = 8;               // match: one cluster of CTAs per unit
 constexpr int kMatchThreads = 256;             // threads per match CTA
@@ -84,7 +85,7 @@ struct DeviceState {
   int32_t* dbase;                  // [U] first descriptor of the unit this step
   int32_t* dcount;                 // [U] descriptors of the unit this step
   float* part;                     // split-K partials
-  int32_t* part_count;             // [U][max_tokens] arrival counters, 0 between steps
+  int32_t* part_count;             // [U][max_tokens][8] arrival counters, 0 between steps
   DevCounters* counters;           // [U] distinct hits / misses, summed over steps
   DevErr* err;
   int32_t* budget;                 // [U] usable slots per unit (buffer elasticity), <= B
@@ -194,6 +195,9 @@ struct AttnLaunch {
   int num_sms;                     // SMs of the device (persistent grid size)
   int staged_misses;               // 16-head kernel: a miss's row is read from the staging
                                    // area at its miss-set cell (hslot holds -2 - cell)
+  int fused_merge;                 // 16-head kernel (set by its launcher): the last cluster
+                                   // to finish a column slice merges it (no merge kernel)
+  size_t count_capacity;           // arrival counters available at DeviceState::part_count
   size_t part_capacity;            // floats available at DeviceState::part
 };
 bool attention_supported(int D, int DV, int G, int kv_shared);

@@ -134,7 +134,8 @@ extern "C" int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, 
   s.part = reinterpret_cast<float*>(scratch + kPartOffset);
 
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
-  cudaError_t e = cudaMemsetAsync(scratch, 0, kErrBytes + (size_t)num_units * kMaxTokens * 4, st);
+  const size_t counts = (size_t)num_units * kMaxTokens * kCountsPerPair * 4;
+  cudaError_t e = cudaMemsetAsync(scratch, 0, kErrBytes + (counts < kCountBytes ? counts : kCountBytes), st);
   const size_t n_idx = (size_t)num_units * n_tok * k;
   const int check_blocks = (int)((n_idx + 255) / 256 < (size_t)sms * 4 ? (n_idx + 255) / 256 : sms * 4);
   if (e == cudaSuccess) {
@@ -154,6 +155,7 @@ extern "C" int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, 
     a.slot_map = d_index;
     a.num_sms = sms;
     a.part_capacity = (kScratchBytes - kPartOffset) / sizeof(float);
+    a.count_capacity = kCountBytes / sizeof(int32_t);
     e = launch_attention(s, a, st);
   }
   if (e == cudaSuccess) {
