@@ -52,7 +52,7 @@ struct avsg_handle_s {
   uint64_t prof_launches[AVSG_NUM_KERNELS] = {};
   // side stream: the miss gather and the table commit run there while the
   // caller's stream runs attention over the hit rows
-  cudaStream_t side = nullptr, side2 = nullptr;
+  cudaStream_t side = nullptr, side2 = nullptr, side3 = nullptr;  // side3: lowest priority
   cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_reserve = nullptr, ev_commit = nullptr,
               ev_staged = nullptr, ev_place = nullptr;
   bool staged = false;  // staging area allocated: the two-pass pipeline is available
@@ -157,6 +157,7 @@ void release(avsg_handle h) {
     if (e) cudaEventDestroy(e);
   if (h->side) cudaStreamDestroy(h->side);
   if (h->side2) cudaStreamDestroy(h->side2);
+  if (h->side3) cudaStreamDestroy(h->side3);
   if (h->dev_block) cudaFree(h->dev_block);
   if (h->reg_k && h->host_k) cudaHostUnregister(const_cast<void*>(h->host_k));
   if (h->reg_v && h->host_v) cudaHostUnregister(const_cast<void*>(h->host_v));
@@ -462,6 +463,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     e = cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, prio_high);
   if (e == cudaSuccess)
     e = cudaStreamCreateWithPriority(&h->side2, cudaStreamNonBlocking, prio_high);
+  if (e == cudaSuccess)
+    e = cudaStreamCreateWithPriority(&h->side3, cudaStreamNonBlocking, prio_low);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking);
   for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_gather, &h->ev_reserve, &h->ev_commit, &h->ev_staged, &h->ev_place})
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
@@ -578,6 +581,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   // keeps the dependencies, so each is timed alone (as a serialised profiler
   // sees it) rather than beside the kernels of the other streams.
   cudaStream_t side = h->prof ? st : h->side, side2 = h->prof ? st : h->side2;
+  cudaStream_t side3 = h->prof ? st : h->side3;
   if (h->no_reuse) {
     AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather_all(sc, v, n_tok, k, h->gather_ctas, st));
     e = take_first();
@@ -643,7 +647,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   //           the gather drains);
   //   side2:  the reservation, then the hash-table update.
   // Once the gather has staged the rows, a place kernel moves them into the
-  // slots the reservation gave them (on side2, beside the miss pass); the
+  // slots the reservation gave them (on side3, beside the miss pass); the
   // finish kernel merges the two passes' partials into the output.
   int splits_h = 0, splits_m = 0;
   two_pass_splits(h, n_tok, k, &splits_h, &splits_m);
@@ -666,16 +670,22 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   e = cudaEventRecord(h->ev_reserve, side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
-  e = cudaStreamWaitEvent(side2, h->ev_staged, 0);  // staged rows -> slots, beside the miss pass
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_PLACE, side2, launch_place(sc, side2));
   e = cudaEventRecord(h->ev_commit, side2);
+  // Staged rows -> slots, beside the miss pass, on the lowest-priority stream:
+  // both become ready when the gather ends, and the miss pass (on the
+  // critical path) gets the SMs first; the place is needed by the next step.
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side3, h->ev_reserve, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side3, h->ev_staged, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_PLACE, side3, launch_place(sc, side3));
+  e = cudaEventRecord(h->ev_place, side3);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, splits_h, splits_m, st));
   e = cudaStreamWaitEvent(st, h->ev_gather, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_FINISH, st, launch_attention_tc_finish(sc, a, splits_h, splits_m, st));
   e = cudaStreamWaitEvent(st, h->ev_commit, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_place, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
 #undef AVSG_RUN
   return AVSG_OK;
