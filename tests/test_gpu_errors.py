@@ -21,6 +21,9 @@ def built():
 
 
 W_ERR = W.get_workload("tiny", requests=2, kv_heads=2, q_per_kv=4, k=64, slots=256, steps=6)
+# the 16-head pipeline (staged gather, clustered attention; k = 300 takes several clusters
+# per pair, so the last-arriver merge and its counters are in play)
+W_ERR_LATENT = W.get_workload("latent", requests=2, context=8192, k=300, slots=512, steps=6)
 
 
 def _snapshot(p):
@@ -29,12 +32,15 @@ def _snapshot(p):
 
 def _same(a, b):
     for (t1, l1, k1, v1), (t2, l2, k2, v2) in zip(a, b):
-        assert (t1 == t2).all() and (l1 == l2).all() and (k1 == k2).all() and (v1 == v2).all()
+        assert (t1 == t2).all() and (l1 == l2).all() and (k1 == k2).all()
+        assert (v1 is None and v2 is None) or (v1 == v2).all()  # None: V is the K row
 
 
+@pytest.mark.parametrize("shape", ["gqa4", "latent"])
 @pytest.mark.parametrize("bad", ["duplicate", "out_of_range", "negative", "duplicate_hit"])
-def test_bad_selection_is_latched_before_any_change(bad):
-    p = Parity(W_ERR)
+def test_bad_selection_is_latched_before_any_change(bad, shape):
+    w = W_ERR if shape == "gqa4" else W_ERR_LATENT
+    p = Parity(w)
     try:
         p.step(0)
         before = _snapshot(p)
@@ -42,7 +48,7 @@ def test_bad_selection_is_latched_before_any_change(bad):
         if bad == "duplicate":
             sel[1, 0, 5] = sel[1, 0, 9]
         elif bad == "out_of_range":
-            sel[1, 0, 3] = W_ERR.num_entries
+            sel[1, 0, 3] = w.num_entries
         elif bad == "negative":
             sel[1, 0, 3] = -7
         else:  # repeat an id that is resident (a hit) within one token
@@ -91,19 +97,21 @@ def test_host_side_rejections():
         p.close()
 
 
-def test_empty_selection_gives_zeros_and_keeps_state():
-    p = Parity(W_ERR)
+@pytest.mark.parametrize("shape", ["gqa4", "latent"])
+def test_empty_selection_gives_zeros_and_keeps_state(shape):
+    w = W_ERR if shape == "gqa4" else W_ERR_LATENT
+    p = Parity(w)
     try:
         p.step(0)
         before = _snapshot(p)
-        empty = torch.zeros((W_ERR.units, 1, 0), dtype=torch.int32, device="cuda")
+        empty = torch.zeros((w.units, 1, 0), dtype=torch.int32, device="cuda")
         q_d = torch.from_numpy(p.q[1]).cuda()
         p.out.fill_(float("nan"))
         p.sess.step(1, empty, q_d, p.out)
         torch.cuda.synchronize()
         assert (p.out == 0).all()
         _same(before, _snapshot(p))
-        p.ref.step(1, np.zeros((W_ERR.units, 1, 0), np.int32))
+        p.ref.step(1, np.zeros((w.units, 1, 0), np.int32))
         p.step(2)
         p.check_state()
     finally:
