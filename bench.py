@@ -10,6 +10,11 @@ through the C interface.  Prints one JSON line.
 
 Units are independent, so N GPUs run N copies of the batch (weak scaling, no
 collective on the data path); value = selected entries of all ranks / time.
+
+The timed pass runs the steps as they are served (captured step graphs, the
+kernels of a step overlapping on three streams).  A second pass over the same
+steps, with the library's events between kernels, enqueues each step on one
+stream and gives every kernel's own time, for the per-kernel roofline figures.
 """
 from __future__ import annotations
 
@@ -542,8 +547,8 @@ def report_ours(args, res, world, max_ms, max_e2e_ms) -> dict:
             "reuse_speedup": res["no_reuse_ms_per_step"] / max_ms},
         "roofline": roof, "kernels": kernels,
         "kernel_timing": ("second pass over the same steps with library CUDA events between "
-                          "kernels (defeats launch overlap); that pass's ms_per_step: "
-                          f"{res['ms_per_step_profiled']:.4f}"),
+                          "kernels, each step on one stream (every kernel timed alone); that "
+                          f"pass's ms_per_step: {res['ms_per_step_profiled']:.4f}"),
         "gpu_launches": int(round(res["launches_per_step"] * K)),
         "clocks": res["clocks"],
     }
