@@ -53,6 +53,10 @@ SMALL = {
     # one CTA per (unit, token) over a ragged 20-row tile: output written without a merge
     "latent_one_tile": W.get_workload("latent", requests=2, context=4096, k=20, slots=64, steps=6,
                                       forced="none"),
+    # three query tokens per step (one reservation over their union, token bits in the
+    # staged gather, one cluster per (unit, token))
+    "latent_mtp": W.get_workload("latent", requests=2, context=8192, k=200, slots=1024, steps=6,
+                                 tokens_per_step=3),
     # 19 splits of 106 rows each: four tiles per CTA, the last one ragged
     "latent_multi_tile": W.get_workload("latent", requests=8, context=16384, k=2000, slots=2048,
                                         steps=4),
