@@ -37,15 +37,18 @@ def distinct_hits(sel_u, hit_u):
 
 
 class Parity:
-    """GPU and oracle over the same inputs; ``units`` limits the oracle side."""
+    """GPU and oracle over the same inputs; ``units`` limits the oracle side,
+    ``attn_units`` (default: all of ``units``) the units whose attention
+    output the oracle computes and compares."""
 
     def __init__(self, w, steps=None, units=None, sel=None, q=None, no_reuse=False, seed=W.DEFAULT_SEED,
-                 request_gather=False, initial_entries=0):
+                 request_gather=False, initial_entries=0, attn_units=None):
         self.w = w
         self.steps = w.steps if steps is None else steps
         self.sel = W.selections(w, self.steps, seed=seed) if sel is None else sel
         self.q = W.queries(w, self.steps, seed=seed) if q is None else q
         self.units = list(range(w.units)) if units is None else list(units)
+        self.attn_units = None if attn_units is None else set(attn_units)
         self.no_reuse = no_reuse
         self.hk, self.hv = make_host_kv(w)
         self.sess = make_session(w, self.hk, self.hv, no_reuse, request_gather, initial_entries)
@@ -90,7 +93,16 @@ class Parity:
                     self.max_err = max(self.max_err, float(np.abs(out[u, j] - o).max()))
             assert self.max_err <= ATTN_TOL, self.max_err
             return None
-        res = self.ref.step(t, sel_t, q_t)
+        if self.attn_units is None:
+            res = self.ref.step(t, sel_t, q_t)
+        else:
+            res = self.ref.step(t, sel_t, q_t, attention=False)
+            for u in self.attn_units:
+                st = self.ref.state[u]
+                res[u] = (res[u][0], np.stack([
+                    oracle.attention_from_host(q_t[u][j], st.host_k, st.host_v, sel_t[u][j],
+                                               w.softmax_scale, w.head_dim, w.v_dim)
+                    for j in range(w.tokens_per_step)]))
         for u in self.units:
             r, o = res[u]
             for j in range(w.tokens_per_step):
@@ -100,6 +112,8 @@ class Parity:
             assert g == r.hits, f"distinct hits t={t} unit={u}: {g} vs {r.hits}"
             self.gpu_hits += g
             self.ref_hits += r.hits
+            if o is None:
+                continue
             err = float(np.abs(out[u] - o).max())
             self.max_err = max(self.max_err, err)
             assert err <= ATTN_TOL, f"attention error {err} t={t} unit={u}"
@@ -123,11 +137,15 @@ class Parity:
                 if vr is not None:
                     assert (vr == st.v_rows).all(), f"V rows unit={u}"
 
-    def run(self, state_every=8):
+    def run(self, state_every=8, rows_every=True):
+        """All steps; tags and last_step compared every ``state_every`` steps
+        and after the last, buffer rows with them (``rows_every``) or only
+        after the last step."""
         for t in range(self.steps):
             self.step(t)
-            if not self.no_reuse and (t % state_every == state_every - 1 or t == self.steps - 1):
-                self.check_state()
+            last = t == self.steps - 1
+            if not self.no_reuse and (t % state_every == state_every - 1 or last):
+                self.check_state(rows=rows_every or last)
         return self
 
     def close(self):
