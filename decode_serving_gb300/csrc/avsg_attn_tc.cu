@@ -479,22 +479,21 @@ __device__ __forceinline__ void tc_write_partial(float* pp, const float* cm, con
   }
 }
 
-// Merges nseg partials of a pair into its output (run by one CTA).  Every
-// partial's (m, l) and the first QB partials' output rows are loaded at once;
-// later partials take one more round of loads per QB.  wseg: 2 * nseg * G
-// floats of shared memory.
-template <int G, int D>
-__device__ void tc_merge_partials(const float* pbase, int nseg, float* out, float* wseg) {
+// Merges nseg partials of a pair into its output (run by one CTA); partial
+// q2 starts at part_at(q2).  Every partial's (m, l) and the first QB
+// partials' output rows are loaded at once; later partials take one more
+// round of loads per QB.  wseg: 2 * nseg * G floats of shared memory.
+template <int G, int D, class PartAt>
+__device__ void tc_merge_partials(PartAt part_at, int nseg, float* out, float* wseg) {
   constexpr int R = (G * D + kThreadsTc - 1) / kThreadsTc;  // outputs per thread
   constexpr int QB = 8;                                     // partials per round of loads
-  const size_t stride = (size_t)G * (D + 2);
   const int tid = threadIdx.x;
   float* wm = wseg;             // [nseg][G]: m, then the normalised weight
   float* wl = wseg + nseg * G;  // [nseg][G]: l
   for (int i = tid; i < nseg * G; i += kThreadsTc) {
     const int q2 = i / G, h = i - q2 * G;
-    wm[i] = __ldcg(pbase + q2 * stride + h);
-    wl[i] = __ldcg(pbase + q2 * stride + G + h);
+    wm[i] = __ldcg(part_at(q2) + h);
+    wl[i] = __ldcg(part_at(q2) + G + h);
   }
   float v[QB][R];
   auto load_round = [&](int q0) {
@@ -503,7 +502,7 @@ __device__ void tc_merge_partials(const float* pbase, int nseg, float* out, floa
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int o = tid + r * kThreadsTc;
-        v[j][r] = (q0 + j < nseg && o < G * D) ? __ldcg(pbase + (q0 + j) * stride + 2 * G + o) : 0.f;
+        v[j][r] = (q0 + j < nseg && o < G * D) ? __ldcg(part_at(q0 + j) + 2 * G + o) : 0.f;
       }
   };
   load_round(0);
@@ -541,6 +540,11 @@ __device__ void tc_merge_partials(const float* pbase, int nseg, float* out, floa
 }
 
 // Single pass, persistent: 2 CTAs per SM, each an equal share of all tiles.
+// A pair covered by several CTAs is merged from their partials.  A CTA's
+// range cuts at most two pairs (its first and its last segment; the pairs in
+// between it covers whole), so partials are stored by CTA: slot 2c for CTA
+// c's first segment, 2c + 1 for its last one -- 2 * CTAs partials however
+// many pairs there are.
 template <class SH>
 __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcParams p) {
   constexpr int D = SH::D, G = SH::G;
@@ -580,6 +584,7 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
     a.rows = p.rows_per_pair;
     a.ta = (int)(t - pair_t0);
     a.tb = (int)(min(t_end, pair_t0 + p.tiles_per_pair) - pair_t0);
+    const bool first_seg = t == t_begin;
     t = pair_t0 + a.tb;
     tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
 
@@ -593,15 +598,21 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
         out[o] = L > 0.f ? co[o] / L : 0.f;
       }
     } else {
-      float* pbase = s.part + (size_t)pair * p.max_seg * stride;
-      tc_write_partial<G, D>(pbase + (size_t)(blockIdx.x - first) * stride, cm, cl, co);
+      tc_write_partial<G, D>(s.part + (2 * (size_t)blockIdx.x + (first_seg ? 0 : 1)) * stride, cm,
+                             cl, co);
       __threadfence();
       __syncthreads();
       if (tid == 0) s_last = atomicAdd(&s.part_count[a.u * kMaxTokens + a.tok], 1) == nseg - 1;
       __syncthreads();
       if (s_last) {
         __threadfence();
-        tc_merge_partials<G, D>(pbase, nseg, out, co + G * D);
+        // CTA `first` may have begun in an earlier pair (then this pair is its
+        // last segment); every later CTA of the pair begins in it.
+        const size_t slot0 = 2 * (size_t)first + ((long long)first * T / C == pair_t0 ? 0 : 1);
+        const float* part = s.part;
+        tc_merge_partials<G, D>(
+            [&](int q2) { return part + (q2 == 0 ? slot0 : 2 * (size_t)(first + q2)) * stride; },
+            nseg, out, co + G * D);
         if (tid == 0) s.part_count[a.u * kMaxTokens + a.tok] = 0;
       }
     }
@@ -766,7 +777,9 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_finish_kernel(DeviceState 
   if (s_stop) return;
   const int nseg = p.splits_h + p.splits_m;
   float* out = load_io(s.io).out + (size_t)pair * G * D;
-  tc_merge_partials<G, D>(s.part + (size_t)pair * nseg * G * (D + 2), nseg, out, wseg);
+  const float* pbase = s.part + (size_t)pair * nseg * G * (D + 2);
+  tc_merge_partials<G, D>([&](int q2) { return pbase + (size_t)q2 * G * (D + 2); }, nseg, out,
+                          wseg);
 }
 
 template <class SH>
@@ -797,12 +810,13 @@ cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaS
   const size_t stride = (size_t)SH::G * (SH::D + 2);
   for (;;) {
     const long long per = p.tiles / C;  // fewest tiles a CTA gets
-    p.max_seg = (int)((p.tiles_per_pair + per - 1) / per + 1);
-    if (((size_t)pairs * p.max_seg * stride <= a.part_capacity && p.max_seg <= SH::MAX_SEG) ||
-        C == 1)
-      break;
+    p.max_seg = (int)((p.tiles_per_pair + per - 1) / per + 1);  // most CTAs on one pair
+    // partials: two per CTA (see attn_tc_kernel); the merge's weights fit
+    // the staging while max_seg <= MAX_SEG
+    if ((2 * (size_t)C * stride <= a.part_capacity && p.max_seg <= SH::MAX_SEG) || C == 1) break;
     C = C * 3 / 4 > 0 ? C * 3 / 4 : 1;
   }
+  (void)pairs;
   p.ctas = (int)C;
   cudaError_t e = ensure_smem((const void*)attn_tc_kernel<SH>, SH::SMEM, &smem_done);
   if (e != cudaSuccess) return e;

@@ -39,7 +39,7 @@ unsigned char* g_scratch_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 
 // Marks the call failed when an index is outside [0, rows).
-__global__ void check_index_kernel(const int32_t* __restrict__ idx, size_t n, int32_t per_unit,
+__global__ void check_index_kernel(const int32_t* __restrict__ idx, size_t n, size_t per_unit,
                                    int32_t rows, DevErr* err) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -93,7 +93,7 @@ extern "C" int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, 
       (!kv_shared && !d_v_rows) || (k > 0 && (!d_index || !d_q)) || !(softmax_scale >= 0.f) ||
       isinf(softmax_scale))
     return AVSG_ERR_INVALID_ARG;
-  if (num_units > kMaxUnits) return AVSG_ERR_CAPACITY;
+  if (num_units > kMaxUnits || k > rows_per_unit) return AVSG_ERR_CAPACITY;
   if (!attention_supported(head_dim, v_dim, q_per_kv, kv_shared)) return AVSG_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t n_out = (size_t)num_units * n_tok * q_per_kv * v_dim;
@@ -105,8 +105,10 @@ extern "C" int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, 
   int rc = setup_device(&dev, &scratch, &sms);
   if (rc != AVSG_OK) return rc;
 
-  // Splits: about 4 CTAs per SM in all, at least one tile of rows each, and
-  // no more partials than the array holds.
+  // Splits (read by the CUDA-core and 16-head launchers; the tensor-core
+  // launcher sizes its own persistent grid against part_capacity): about 4
+  // CTAs per SM in all, at least one tile of rows each, and no more partials
+  // than the array holds.
   const int tr = attention_rows_per_tile(head_dim, v_dim, q_per_kv, kv_shared);
   const int64_t pairs = (int64_t)num_units * n_tok;
   int64_t splits = (4LL * sms + pairs - 1) / pairs;
@@ -139,8 +141,8 @@ extern "C" int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, 
   const size_t n_idx = (size_t)num_units * n_tok * k;
   const int check_blocks = (int)((n_idx + 255) / 256 < (size_t)sms * 4 ? (n_idx + 255) / 256 : sms * 4);
   if (e == cudaSuccess) {
-    check_index_kernel<<<check_blocks, 256, 0, st>>>(d_index, n_idx, n_tok * k, rows_per_unit,
-                                                     s.err);
+    check_index_kernel<<<check_blocks, 256, 0, st>>>(d_index, n_idx, (size_t)n_tok * k,
+                                                     rows_per_unit, s.err);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {

@@ -3,10 +3,13 @@
 It serves callers that cannot call cudaMalloc -- code inside another
 framework's memory pool or a serving process that must not allocate once it
 runs.  Its split-K scratch is a fixed array inside the library.  These tests
-check, through the C interface, that it returns what the existing entry point
-(avsg_step) returns for the same selection and queries, on two calls in a
-row (the second call reuses the scratch the first one left behind), and that
-it rejects sizes beyond its limit and flags bad row indices.
+check, through the C interface, that on two calls in a row (the second call
+reuses the scratch the first one left behind) it returns the fp64 oracle's
+attention over the selected host rows and what the existing entry point
+(avsg_step) returns for the same selection and queries, that a call with
+more (unit, token) pairs than the fixed scratch has partials for still runs
+on a full grid, and that it rejects sizes beyond its limit and flags bad row
+indices.
 
 This file is collected last on purpose: a run that stops at the first failure
 has already run every other test when it gets here.
@@ -15,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workload as W
 from decode_serving_gb300 import avsg
 from decode_serving_gb300.avsg import AvsgError
@@ -69,6 +73,14 @@ def test_matches_the_step_entry_point_on_two_calls(name):
             assert torch.isfinite(got).all()
             err = (got - ref).abs().max().item()
             assert err <= ATTN_TOL, (name, t, err)
+            got_h = got.cpu().numpy()
+            for u in range(w.units):
+                for j in range(w.tokens_per_step):
+                    o = oracle.attention_from_host(q[t][u][j], hk.array[u],
+                                                   None if hv is None else hv.array[u], sel[t][u][j],
+                                                   w.softmax_scale, w.head_dim, w.v_dim)
+                    e2 = float(np.abs(got_h[u, j] - o).max())
+                    assert e2 <= ATTN_TOL, (name, t, u, j, e2)
     finally:
         sess.close()
         hk.free()
@@ -76,9 +88,63 @@ def test_matches_the_step_entry_point_on_two_calls(name):
             hv.free()
 
 
+def test_many_pairs_run_on_a_full_grid():
+    """2048 (unit, token) pairs: more than the fixed scratch would hold as one
+    block of partials per pair.  The result matches the oracle on sampled
+    units, and the call takes about as long per pair as one with 256 units
+    (a grid that had collapsed to a few CTAs would take orders of magnitude
+    longer)."""
+    units, rows, k, G, D = 2048, 256, 64, 4, 128
+    rng = np.random.default_rng(11)
+    k_h = W.fill_normal(np.empty((units, rows, D), np.uint16).reshape(-1), rows * D, W.PURPOSE_K)
+    v_h = W.fill_normal(np.empty((units, rows, D), np.uint16).reshape(-1), rows * D, W.PURPOSE_V)
+    k_h, v_h = k_h.reshape(units, rows, D), v_h.reshape(units, rows, D)
+    idx = np.stack([rng.permutation(rows)[:k] for _ in range(units)]).astype(np.int32)
+    idx = idx.reshape(units, 1, k)
+    q = W.fill_normal(np.empty((units, 1, G, D), np.float32).reshape(-1), G * D, W.PURPOSE_Q)
+    q = q.reshape(units, 1, G, D)
+    kd = torch.from_numpy(k_h.view(np.int16)).cuda()
+    vd = torch.from_numpy(v_h.view(np.int16)).cuda()
+    idx_d, q_d = torch.from_numpy(idx).cuda(), torch.from_numpy(q).cuda()
+    out = torch.full((units, 1, G, D), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def call(n):
+        avsg.avsg_attention_noalloc(n, rows, G, D, D, 1, False, 1, k, kd.data_ptr(), vd.data_ptr(),
+                                    idx_d.data_ptr(), q_d.data_ptr(), out.data_ptr(), 0.0,
+                                    st.cuda_stream)
+
+    def timed(n):
+        call(n)
+        best = float("inf")
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            call(n)
+            b.record(st)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    small, full = timed(256), timed(units)
+    assert full <= 16 * small + 0.5, (full, small)
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all()
+    for u in [0, 1, 1023, 2046, 2047]:
+        o = oracle.attention_from_host(q[u][0], k_h[u], v_h[u], idx[u][0], D ** -0.5, D, D)
+        assert float(np.abs(got[u, 0] - o).max()) <= ATTN_TOL, u
+
+
 def test_rejects_too_many_units():
     with pytest.raises(AvsgError) as e:
         avsg.avsg_attention_noalloc(5000, 16, 4, 128, 128, 1, False, 1, 4, 1 << 20, 1 << 20,
+                                    1 << 20, 1 << 20, 1 << 20)
+    assert e.value.code == avsg.AVSG_ERR_CAPACITY
+
+
+def test_rejects_more_selected_than_rows():
+    with pytest.raises(AvsgError) as e:
+        avsg.avsg_attention_noalloc(4, 16, 4, 128, 128, 1, False, 1, 17, 1 << 20, 1 << 20,
                                     1 << 20, 1 << 20, 1 << 20)
     assert e.value.code == avsg.AVSG_ERR_CAPACITY
 
