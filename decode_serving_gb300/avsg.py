@@ -112,6 +112,7 @@ SIGNATURES = {
     "avsg_cuda_error": [_P],
     "avsg_attention_noalloc": [_I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P,
                                _P, _P, ctypes.c_float, _P],
+    "avsg_read_rows": [_P, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int64, _I32, _P, _P],
 }
 
 _lib = None
@@ -244,6 +245,12 @@ def avsg_attention_noalloc(num_units, rows_per_unit, q_per_kv, head_dim, v_dim, 
         num_units, rows_per_unit, q_per_kv, head_dim, v_dim, entry_tokens, 1 if kv_shared else 0,
         n_tok, k, d_k_rows, d_v_rows or None, d_index or None, d_q or None, d_out,
         float(softmax_scale), stream or None), "avsg_attention_noalloc")
+
+
+def avsg_read_rows(src, num_rows, row_bytes, d_idx, n, d_sink, ctas=0, stream=0) -> None:
+    """Reads n rows at the given indices and discards them (a measurement aid)."""
+    _check(load_library().avsg_read_rows(src, int(num_rows), int(row_bytes), d_idx, int(n),
+                                         int(ctas), d_sink, stream or None), "avsg_read_rows")
 
 
 def avsg_strerror(code: int) -> str:

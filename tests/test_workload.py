@@ -85,3 +85,20 @@ def test_generator_rejects_bad_parameters(bad):
     w = W.get_workload("tiny", **bad)
     with pytest.raises((RuntimeError, ValueError)):
         W.selections(w)
+
+
+def test_unit_offset_draws_the_units_of_a_larger_job():
+    """A rank holding units [2, 4) of a 4-unit job draws exactly those units'
+    selections, queries and K/V rows."""
+    whole = W.get_workload("tiny", requests=4, steps=5)
+    part = W.get_workload("tiny", requests=2, steps=5)
+    s_all, s_part = W.selections(whole), W.selections(part, unit_base=2)
+    assert (s_all[:, 2:4] == s_part).all()
+    q_all = W.queries(whole)
+    q_part = W.queries(part, unit_base=2, units_total=4)
+    assert (q_all[:, 2:4] == q_part).all()
+    k_all, v_all = W.host_kv(whole)
+    k_p = np.empty(W.host_kv_shape(part), np.uint16)
+    v_p = np.empty_like(k_p)
+    W.fill_host_kv(part, k_p, v_p, unit_base=2)
+    assert (k_all[2:4] == k_p).all() and (v_all[2:4] == v_p).all()

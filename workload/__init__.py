@@ -41,6 +41,7 @@ class _SelParams(ctypes.Structure):
         ("num_forced", ctypes.c_int32),
         ("forced", ctypes.POINTER(ctypes.c_int32)),
         ("seed", ctypes.c_uint64),
+        ("unit_base", ctypes.c_int32),
     ]
 
 
@@ -74,6 +75,10 @@ def _load():
 
 
 def _threads() -> int:
+    """Generator threads: WORKLOAD_THREADS if set, else every core (at most 64)."""
+    env = os.environ.get("WORKLOAD_THREADS", "")
+    if env.isdigit() and int(env) > 0:
+        return int(env)
     return max(1, min(64, os.cpu_count() or 1))
 
 
@@ -100,14 +105,16 @@ def fill_normal(out: np.ndarray, per_stream: int, purpose: int, seed: int = DEFA
     return out
 
 
-def selections(w: Workload, steps: int | None = None, seed: int = DEFAULT_SEED) -> np.ndarray:
-    """Top-k selections, int32 [steps][units][tokens_per_step][k]."""
+def selections(w: Workload, steps: int | None = None, seed: int = DEFAULT_SEED,
+               unit_base: int = 0) -> np.ndarray:
+    """Top-k selections, int32 [steps][units][tokens_per_step][k]; unit u is
+    drawn as unit ``unit_base + u`` of a larger job."""
     steps = w.steps if steps is None else steps
     out = np.empty((steps, w.units, w.tokens_per_step, w.k), dtype=np.int32)
     forced = np.ascontiguousarray(w.forced_ids(), dtype=np.int32)
     p = _SelParams(w.units, w.num_entries, w.k, steps, w.tokens_per_step,
                    w.p_keep, w.p_keep_token, w.zipf_frac, w.zipf_s, len(forced),
-                   forced.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), seed)
+                   forced.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), seed, int(unit_base))
     rc = _load().gen_selections(out.ctypes.data, ctypes.byref(p), _threads())
     if rc:
         raise RuntimeError(f"gen_selections failed ({rc})")
@@ -115,13 +122,20 @@ def selections(w: Workload, steps: int | None = None, seed: int = DEFAULT_SEED) 
 
 
 def queries(w: Workload, steps: int | None = None, seed: int = DEFAULT_SEED,
-            step_base: int = 0) -> np.ndarray:
-    """Queries, float32 [steps][units][tokens_per_step][q_per_kv][head_dim]."""
+            step_base: int = 0, unit_base: int = 0, units_total: int | None = None) -> np.ndarray:
+    """Queries, float32 [steps][units][tokens_per_step][q_per_kv][head_dim].
+    The stream of (step t, unit u) is t * units_total + unit_base + u: the
+    units are units [unit_base, unit_base + units) of a job of units_total."""
     steps = w.steps if steps is None else steps
+    total = w.units if units_total is None else int(units_total)
     out = np.empty((steps, w.units, w.tokens_per_step, w.q_per_kv, w.head_dim),
                    dtype=np.float32)
     per = w.tokens_per_step * w.q_per_kv * w.head_dim
-    return fill_normal(out, per, PURPOSE_Q, seed, stream_base=step_base * w.units)
+    if unit_base == 0 and total == w.units:
+        return fill_normal(out, per, PURPOSE_Q, seed, stream_base=step_base * w.units)
+    for t in range(steps):
+        fill_normal(out[t], per, PURPOSE_Q, seed, stream_base=(step_base + t) * total + unit_base)
+    return out
 
 
 def host_kv_shape(w: Workload) -> tuple:
@@ -130,16 +144,17 @@ def host_kv_shape(w: Workload) -> tuple:
 
 
 def fill_host_kv(w: Workload, k_out: np.ndarray, v_out: np.ndarray | None,
-                 seed: int = DEFAULT_SEED) -> None:
+                 seed: int = DEFAULT_SEED, unit_base: int = 0) -> None:
     """Fill caller-owned host K (and V unless K and V are shared) bf16 arrays,
-    uint16 storage, shape ``host_kv_shape(w)`` (V uses v_dim)."""
+    uint16 storage, shape ``host_kv_shape(w)`` (V uses v_dim); unit u's rows
+    are those of unit ``unit_base + u``."""
     per_unit = w.num_entries * w.entry_tokens * w.head_dim
-    fill_normal(k_out.reshape(-1), per_unit, PURPOSE_K, seed)
+    fill_normal(k_out.reshape(-1), per_unit, PURPOSE_K, seed, stream_base=unit_base)
     if not w.kv_shared:
         if v_out is None:
             raise ValueError("V output required when K and V are separate")
         fill_normal(v_out.reshape(-1), w.num_entries * w.entry_tokens * w.v_dim,
-                    PURPOSE_V, seed)
+                    PURPOSE_V, seed, stream_base=unit_base)
 
 
 def host_kv(w: Workload, seed: int = DEFAULT_SEED):

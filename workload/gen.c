@@ -135,6 +135,7 @@ typedef struct {
   int32_t num_forced;
   const int32_t* forced;
   uint64_t seed;
+  int32_t unit_base; /* unit u draws from the stream of unit unit_base + u */
 } sel_params;
 
 typedef struct {
@@ -169,7 +170,8 @@ static void* sel_worker(void* arg) {
     for (int32_t t = 0; t < p->steps; ++t) {
       for (int32_t tok = 0; tok < p->tokens; ++tok) {
         int32_t* cur = j->out + (((int64_t)t * p->units + u) * p->tokens + tok) * (int64_t)k;
-        uint64_t key = stream_key(p->seed, 4, (uint64_t)u, (uint64_t)t, (uint64_t)tok);
+        uint64_t key = stream_key(p->seed, 4, (uint64_t)(u + p->unit_base), (uint64_t)t,
+                                  (uint64_t)tok);
         uint64_t ctr = 0;
         ++stamp;
         if (stamp == 0) { memset(mark, 0, (size_t)L * 4); stamp = 1; }
@@ -230,6 +232,7 @@ static void* sel_worker(void* arg) {
 int gen_selections(int32_t* out, const sel_params* p, int nthreads) {
   if (!out || !p || p->units < 0 || p->num_entries <= 0 || p->k < 0 ||
       p->k > p->num_entries || p->steps < 0 || p->tokens < 1 || p->num_forced < 0 ||
+      p->unit_base < 0 ||
       (p->num_forced > 0 && !p->forced))
     return -1;
   if (p->units == 0 || p->steps == 0 || p->k == 0) return 0;
