@@ -279,17 +279,22 @@ int avsg_profile_read(avsg_handle h, avsg_kernel_times* out);
  *   d_v_rows   : device bf16 [num_units][rows_per_unit][entry_tokens][v_dim],
  *                ignored (may be NULL) when kv_shared (V is the K row).
  *   d_index    : device int32 [num_units][n_tok][k], row of each selected
- *                entry, each in [0, rows_per_unit).
+ *                entry, each in [0, rows_per_unit).  Repeats within one
+ *                (unit, token) list are not detected: such a row counts once
+ *                per occurrence (avsg_step rejects them).
  *   d_q, d_out : as in avsg_step.  softmax_scale 0 selects 1/sqrt(head_dim).
- * Shapes: those avsg_create accepts for attention; num_units <= 4096
- * (AVSG_ERR_CAPACITY beyond), n_tok <= 8.
+ * Shapes: those avsg_create accepts for attention; num_units <= 4096 and
+ * k <= rows_per_unit (AVSG_ERR_CAPACITY beyond), n_tok <= 8.
  * Scratch: a fixed 8 MiB device array inside the library, held by every GPU
  * that loads it until the process exits.  The first call on a device looks
  * up that array's address (cudaGetSymbolAddress); make the first call before
  * any stream capture.  Every call shares the array and clears what must start
  * at zero; calls that overlap on the GPU race, so serialise them.
  * An index outside [0, rows_per_unit) makes the call fill d_out with NaN.
- * Returns after enqueueing on `stream`; host-side errors change nothing.
+ * Returns after enqueueing on `stream`.  The argument errors (INVALID_ARG,
+ * CAPACITY, UNSUPPORTED) are found before anything is enqueued and change
+ * nothing; after AVSG_ERR_CUDA part of the work may have been enqueued and
+ * d_out is undefined.
  */
 int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, int32_t q_per_kv,
                            int32_t head_dim, int32_t v_dim, int32_t entry_tokens,
@@ -300,6 +305,26 @@ int avsg_attention_noalloc(int32_t num_units, int32_t rows_per_unit, int32_t q_p
 /* Pinned, mapped, portable host memory for the KV cache (cudaHostAlloc). */
 int avsg_host_alloc(size_t bytes, void** out);
 int avsg_host_free(void* p);
+
+/*
+ * avsg_read_rows -- a measurement aid: reads n rows at scattered positions and
+ * discards them, to measure the ceiling of the step's row reads.  The
+ * attention reads the selected entries' rows from slots scattered over the
+ * device buffer, and the miss gather reads the missed entries' rows from ids
+ * scattered over the host store (AVSG page, arxivdaily 2609.37538, English
+ * abstract: only the selected entries are read; only the misses cross the
+ * host link); the rate of this read alone, at the same row size, bounds both.
+ *   src      : rows [num_rows][row_bytes], device memory or the device pointer
+ *              of mapped host memory; 16-byte aligned.
+ *   row_bytes: a multiple of 16.
+ *   d_idx    : device int32 [n], the rows to read; an index outside
+ *              [0, num_rows) is skipped.
+ *   ctas     : grid size, 0 for 4 per SM.
+ *   d_sink   : device uint32 the kernel may write (it practically never does).
+ * Enqueued on `stream`; INVALID_ARG for bad arguments, CUDA if the launch fails.
+ */
+int avsg_read_rows(const void* src, int64_t num_rows, int64_t row_bytes, const int32_t* d_idx,
+                   int64_t n, int32_t ctas, uint32_t* d_sink, void* stream);
 
 /* Error text, and the cudaError_t behind the last AVSG_ERR_CUDA of a handle. */
 const char* avsg_strerror(int code);
