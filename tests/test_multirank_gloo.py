@@ -59,3 +59,25 @@ def test_whole_job_value_counts_every_rank():
     assert bench.whole_job_value(w, 4, 0.1) == pytest.approx(4 * one)
     # weak scaling with a slower slowest rank lowers the job value
     assert bench.whole_job_value(w, 2, 0.2) == pytest.approx(one)
+
+
+def test_bench_starts_its_own_ranks():
+    """`python bench.py --gpus 2` without torchrun starts two ranks itself;
+    each takes its own contiguous range of units (rank r: units
+    [r*U, (r+1)*U) of the job), and rank 0 reports the job over both."""
+    import json
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--gpus", "2",
+                        "--_dry", "--workload", "tiny", "--steps", "3", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2
+    w = W.get_workload("tiny")
+    assert line["rank_units"] == [[0, w.units], [w.units, 2 * w.units]]
+    assert line["value"] == pytest.approx(bench.whole_job_value(w, 2, line["ms_per_step"]))
