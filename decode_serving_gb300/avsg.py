@@ -24,11 +24,12 @@ AVSG_ERR_TIMEOUT = -5
 AVSG_ERR_BAD_STEP = -6
 AVSG_ERR_UNSUPPORTED = -7
 AVSG_ERR_LATCHED = -8
+AVSG_ERR_INTERNAL = -9
 AVSG_FLAG_NO_REUSE = 1
 AVSG_FLAG_REQUEST_GATHER = 2
 
 ERROR_NAMES = {0: "OK", -1: "INVALID_ARG", -2: "CAPACITY", -3: "CUDA", -4: "BAD_SELECTION",
-               -5: "TIMEOUT", -6: "BAD_STEP", -7: "UNSUPPORTED", -8: "LATCHED"}
+               -5: "TIMEOUT", -6: "BAD_STEP", -7: "UNSUPPORTED", -8: "LATCHED", -9: "INTERNAL"}
 
 
 class avsg_config(ctypes.Structure):
@@ -128,11 +129,13 @@ class AvsgError(RuntimeError):
         self.cuda = cuda
 
 
-def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libavsg.so; raises if it has not been built (no fallback)."""
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libavsg.so (or the library AVSG_LIBRARY names, e.g. the
+    bounds-checked build); raises if it has not been built (no fallback)."""
     global _lib
     if _lib is not None:
         return _lib
+    path = path or os.environ.get("AVSG_LIBRARY") or LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(f"libavsg.so is not built ({path}); run __graft_entry__.build()")
     lib = ctypes.CDLL(path)

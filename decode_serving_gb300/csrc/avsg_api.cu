@@ -6,6 +6,8 @@
 
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "avsg_internal.cuh"
 
 using namespace avsg;
@@ -54,8 +56,10 @@ struct avsg_handle_s {
   // caller's stream runs attention over the hit rows
   cudaStream_t side = nullptr, side2 = nullptr, side3 = nullptr;  // side3: lowest priority
   cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_reserve = nullptr, ev_commit = nullptr,
-              ev_staged = nullptr, ev_place = nullptr;
+              ev_staged = nullptr, ev_place = nullptr, ev_hits = nullptr;
   bool staged = false;  // staging area allocated: the two-pass pipeline is available
+  uint64_t seq = 0;     // steps enqueued since create/reset (their parity alternates)
+  bool pending_place = false;  // the last step's staged rows await the place its next step runs
   bool overlap = false;  // steps run the two-pass pipeline
   bool overlap_h16 = false;  // ... in its 16-head form (one attention launch after the staged gather)
   // Captured steps: one CUDA graph per (tokens, k), re-pointed at each step
@@ -153,7 +157,8 @@ void release(avsg_handle h) {
   }
   if (h->cap) cudaStreamDestroy(h->cap);
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
-  for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_reserve, h->ev_commit, h->ev_staged, h->ev_place})
+  for (cudaEvent_t e : {h->ev_fork, h->ev_gather, h->ev_reserve, h->ev_commit, h->ev_staged, h->ev_place,
+                        h->ev_hits})
     if (e) cudaEventDestroy(e);
   if (h->side) cudaStreamDestroy(h->side);
   if (h->side2) cudaStreamDestroy(h->side2);
@@ -164,23 +169,15 @@ void release(avsg_handle h) {
   delete h;
 }
 
-// CTAs per (unit, token) of the two attention passes: the hit pass fills
-// about two CTAs per SM; the miss pass scans at most kMissScanMax miss-set
-// cells per CTA (and at least AVSG_MISS_SPLITS CTAs); together they stay
-// within what one merge takes.
-void two_pass_splits(const avsg_handle h, int n_tok, int k, int* splits_h, int* splits_m) {
+// Miss-pass CTAs per (unit, token): each scans at most the shape's scan
+// limit of miss-set cells, and at least AVSG_MISS_SPLITS CTAs (default 1,
+// which lets that CTA merge the pair's partials itself).
+int miss_splits(const avsg_handle h) {
   const DeviceState& s = h->ds;
-  const int pairs = s.U * n_tok;
   const int scan = attention_tc_scan_max(s.D, s.G, s.kv_shared);
   int sm = scan > 0 && s.MS > scan ? s.MS / scan : 1;
   while (sm < h->miss_splits && s.MS / sm > 2) sm *= 2;
-  int sh = 2 * h->num_sms / pairs > 0 ? 2 * h->num_sms / pairs : 1;
-  const int tiles = (int)(((int64_t)k * s.ET + 15) / 16);  // 16-row tiles of a pair
-  if (sh > tiles / 2) sh = tiles / 2 > 1 ? tiles / 2 : 1;  // two tiles or more per CTA
-  const int cap = attention_tc_max_segments(s.D, s.G, s.kv_shared);
-  if (sh + sm > cap) sh = cap - sm > 1 ? cap - sm : 1;
-  *splits_h = sh;
-  *splits_m = sm;
+  return sm;
 }
 
 // Splits of a (unit, token)'s entries over CTAs: about target_ctas CTAs in all,
@@ -266,7 +263,8 @@ int init_state(avsg_handle h, cudaStream_t st) {
       e = cudaMemcpyAsync(s.budget, h->budget.data(), (size_t)s.U * 4, cudaMemcpyHostToDevice, st);
     AVSG_SET(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
   }
-  AVSG_SET(s.desc_count, 0, 4);
+  AVSG_SET(s.desc_count, 0, 2 * 4);
+  AVSG_SET(s.dcount, 0, 2 * (size_t)s.U * 4);
   AVSG_SET(s.part_count, 0, (size_t)s.U * kMaxTokens * kCountsPerPair * 4);
   AVSG_SET(s.counters, 0, (size_t)s.U * sizeof(DevCounters));
   AVSG_SET(s.err, 0, sizeof(DevErr));
@@ -276,6 +274,8 @@ int init_state(avsg_handle h, cudaStream_t st) {
   h->last_t = -1;
   h->latched = false;
   h->steps = h->selected = h->host_misses = 0;
+  h->seq = 0;
+  h->pending_place = false;
   return AVSG_OK;
 }
 
@@ -306,7 +306,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   // match keeps a step's miss set and hit bitmaps in one CTA's shared memory
   if (!no_reuse && (max_union > (int64_t)kMatchCluster * kMatchThreads * kMatchPerThread ||
                     match_smem_bytes(pow2_at_least(2 * max_union), c.max_tokens_per_step,
-                                     (c.buffer_slots + 31) / 32) > kMatchSmemMax))
+                                     (c.buffer_slots + 31) / 32, kMatchCluster) > kMatchSmemMax))
     return AVSG_ERR_CAPACITY;
   if (!attention_supported(c.head_dim, c.v_dim, c.q_per_kv, c.kv_shared)) return AVSG_ERR_UNSUPPORTED;
   // shapes with a staging area: the tensor-core two-pass pipeline and the
@@ -362,7 +362,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   // with one CTA per request each CTA's range is exactly one request's units.
   h->stage_ctas = (c.flags & AVSG_FLAG_REQUEST_GATHER) ? c.num_requests
                                                        : env_int("AVSG_STAGE_CTAS", h->num_sms / 2);
-  h->miss_splits = env_int("AVSG_MISS_SPLITS", 2);  // at least this many miss-pass CTAs per pair
+  h->miss_splits = env_int("AVSG_MISS_SPLITS", 1);  // at least this many miss-pass CTAs per pair
   {
     int64_t cap = (h->target_ctas + U - 1) / U;
     const int64_t by_rows = ((int64_t)c.max_select * c.entry_tokens + h->tile_rows - 1) / h->tile_rows;
@@ -389,8 +389,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.vbuf, (size_t)U * s.B * ev);
   // staging rows for the two-pass pipeline (one per miss-set cell)
   h->staged = !no_reuse && (tc_shape || h16_shape);
-  cv.take(&s.kstage, h->staged ? (size_t)U * s.MS * ek : 0);
-  cv.take(&s.vstage, h->staged ? (size_t)U * s.MS * ev : 0);
+  cv.take(&s.kstage, h->staged ? 2 * (size_t)U * s.MS * ek : 0);  // a half per step parity
+  cv.take(&s.vstage, h->staged ? 2 * (size_t)U * s.MS * ev : 0);
   cv.take(&s.tag, ub);
   cv.take(&s.last, ub);
   cv.take(&s.hitbits, st_arrays ? (size_t)U * s.HT * s.HW : 0);
@@ -399,24 +399,23 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.mset, st_arrays ? (size_t)U * s.MS : 0);
   cv.take(&s.hslot, (size_t)U * max_union);
   cv.take(&s.mslot, st_arrays ? (size_t)U * s.MS : 0);
-  cv.take(&s.desc, (size_t)U * max_union);
-  cv.take(&s.desc_count, 1);
+  cv.take(&s.desc, 2 * (size_t)U * max_union);
+  cv.take(&s.desc_count, 2);
   cv.take(&s.io, 1);
   cv.take(&s.qbuf, st_arrays ? (size_t)U * c.max_tokens_per_step * s.G * s.D : 0);
-  cv.take(&s.dbase, (size_t)U);
-  cv.take(&s.dcount, (size_t)U);
+  cv.take(&s.dbase, 2 * (size_t)U);
+  cv.take(&s.dcount, 2 * (size_t)U);
 
   {
     size_t part = (size_t)U * c.max_tokens_per_step * h->splits_cap * s.G * (s.DV + 2);
     const size_t tc = attention_tc_part_floats((int)U, c.max_tokens_per_step, s.G, s.DV, h->num_sms);
-    size_t two = 0;  // two-pass attention: pairs * (hit splits + miss splits)
-    for (int nt = 1; nt <= c.max_tokens_per_step; ++nt) {
-      const int pairs = (int)U * nt;
-      int sh = 0, sm = 0;
-      two_pass_splits(h, nt, c.max_select, &sh, &sm);
-      const size_t need = (size_t)pairs * (sh + sm) * s.G * (s.DV + 2);
-      two = need > two ? need : two;
-    }
+    size_t two = 0;  // two-pass attention (most at max_tokens_per_step * max_select)
+    if (tc_shape)
+      for (int nt = 1; nt <= c.max_tokens_per_step; ++nt) {
+        const size_t need = attention_tc_two_pass_floats((int)U * nt, c.max_select, s.ET, s.G,
+                                                         s.DV, h->num_sms, miss_splits(h));
+        two = need > two ? need : two;
+      }
     h->part_floats = part > tc ? part : tc;
     h->part_floats = h->part_floats > two ? h->part_floats : two;
     h->overlap = h->staged && overlap_enabled() && (h16_shape || attention_tc_enabled());
@@ -466,7 +465,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   if (e == cudaSuccess)
     e = cudaStreamCreateWithPriority(&h->side3, cudaStreamNonBlocking, prio_low);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking);
-  for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_gather, &h->ev_reserve, &h->ev_commit, &h->ev_staged, &h->ev_place})
+  for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_gather, &h->ev_reserve, &h->ev_commit, &h->ev_staged,
+                          &h->ev_place, &h->ev_hits})
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     release(h);
@@ -480,7 +480,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     unsigned* sink = reinterpret_cast<unsigned*>(s.desc_count);  // zeroed again below
     e = launch_host_touch(s.host_k, kb, sink, h->num_sms, nullptr);
     if (e == cudaSuccess) e = launch_host_touch(s.host_v, vb, sink, h->num_sms, nullptr);
-    if (e == cudaSuccess) e = cudaMemsetAsync(s.desc_count, 0, 4, nullptr);
+    if (e == cudaSuccess) e = cudaMemsetAsync(s.desc_count, 0, 2 * 4, nullptr);
     if (e != cudaSuccess) rc = AVSG_ERR_CUDA;
   }
   if (rc == AVSG_OK) {
@@ -535,6 +535,12 @@ struct Prof {
   }
 };
 
+// NVTX range names of the launches (a profiler attached to the process shows
+// each launch, or its capture into a step graph, under these).
+const char* const kKernelNames[AVSG_NUM_KERNELS] = {
+    "avsg_match", "avsg_victims", "avsg_gather", "avsg_attn", "avsg_attn_miss", "avsg_commit",
+    "avsg_finish", "avsg_place"};
+
 // Enqueues the kernels of one step on st (and the side streams, forked from
 // and joined back into st); the step's pointers come in v.  With first !=
 // null (capture), returns the graph node of the first kernel there.
@@ -556,12 +562,14 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   a.part_capacity = h->part_floats;
   a.count_capacity = (size_t)s.U * kMaxTokens * kCountsPerPair;
   Prof pf{h};
-#define AVSG_RUN(kernel_index, stream, call) \
-  do {                                       \
-    pf.begin(kernel_index, stream);          \
-    e = (call);                              \
-    if (e != cudaSuccess) return fail_cuda(h, e); \
-    pf.end(stream);                          \
+#define AVSG_RUN(kernel_index, stream, call)         \
+  do {                                               \
+    nvtxRangePushA(kKernelNames[kernel_index]);      \
+    pf.begin(kernel_index, stream);                  \
+    e = (call);                                      \
+    nvtxRangePop();                                  \
+    if (e != cudaSuccess) return fail_cuda(h, e);    \
+    pf.end(stream);                                  \
   } while (0)
   // The graph node of the kernel just captured on st.
   auto take_first = [&]() -> cudaError_t {
@@ -629,7 +637,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
     e = cudaEventRecord(h->ev_reserve, side2);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_staged, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
-    AVSG_RUN(AVSG_KERNEL_PLACE, side2, launch_place(sc, side2));
+    AVSG_RUN(AVSG_KERNEL_PLACE, side2, launch_place(sc, 0, side2));
     e = cudaEventRecord(h->ev_commit, side2);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_reserve, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
@@ -639,53 +647,56 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
     if (e != cudaSuccess) return fail_cuda(h, e);
     return AVSG_OK;
   }
-  // Two-pass pipeline (the tensor-core shapes).  After match, three
+  // Two-pass pipeline (the tensor-core shapes).  After match, four
   // streams run side by side:
-  //   st:     attention over the hit rows (their slots are known);
-  //   side:   the missed rows, host -> staging area (host link), then the
-  //           attention over them (launched early: it lists its rows while
-  //           the gather drains);
+  //   side3:  the rows the previous step staged, into the slots its
+  //           reservation gave them (the deferred place: off the previous
+  //           step's critical path, beside this step's link-bound gather);
+  //   st:     once they are in place, attention over the hit rows;
+  //   side:   the missed rows, host -> this step's half of the staging area
+  //           (host link), then the attention over them;
   //   side2:  the reservation, then the hash-table update.
-  // Once the gather has staged the rows, a place kernel moves them into the
-  // slots the reservation gave them (on side3, beside the miss pass); the
-  // finish kernel merges the two passes' partials into the output.
-  int splits_h = 0, splits_m = 0;
-  two_pass_splits(h, n_tok, k, &splits_h, &splits_m);
+  // With one miss-pass CTA per (unit, token) that CTA merges the two passes'
+  // partials into the output; otherwise a finish kernel does.  This step's
+  // staged rows reach their slots early in the next step (or when an entry
+  // point that reads the buffer flushes them).
+  const int splits_m = miss_splits(h);
+  const bool fused = splits_m == 1;
   e = cudaEventRecord(h->ev_fork, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_fork, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_fork, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side3, h->ev_fork, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
   DeviceState staged = sc;  // miss rows are read from the staging area, by cell
   staged.kbuf = s.kstage;
   staged.vbuf = s.vstage;
   staged.B = s.MS;
+  // Launched in this order, so the gather's CTAs are placed first (on SMs of
+  // their own), then the reservation's, then the place and the hit pass.
   AVSG_RUN(AVSG_KERNEL_GATHER, side, launch_gather_stage(sc, h->stage_ctas, side));
-  e = cudaEventRecord(h->ev_staged, side);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, side,
-           launch_attention_tc_pass(staged, a, 1, splits_h, splits_m, side));
-  e = cudaEventRecord(h->ev_gather, side);
-  if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_RESERVE, side2, launch_victims(sc, n_tok, k, side2));
   e = cudaEventRecord(h->ev_reserve, side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
   e = cudaEventRecord(h->ev_commit, side2);
-  // Staged rows -> slots, beside the miss pass, on the lowest-priority stream:
-  // both become ready when the gather ends, and the miss pass (on the
-  // critical path) gets the SMs first; the place is needed by the next step.
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(side3, h->ev_reserve, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(side3, h->ev_staged, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_PLACE, side3, launch_place(sc, side3));
+  AVSG_RUN(AVSG_KERNEL_PLACE, side3, launch_place(sc, 1, side3));
   e = cudaEventRecord(h->ev_place, side3);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, splits_h, splits_m, st));
-  e = cudaStreamWaitEvent(st, h->ev_gather, 0);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_FINISH, st, launch_attention_tc_finish(sc, a, splits_h, splits_m, st));
-  e = cudaStreamWaitEvent(st, h->ev_commit, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_place, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, splits_m, st));
+  e = cudaEventRecord(h->ev_hits, st);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  if (fused) e = cudaStreamWaitEvent(side, h->ev_hits, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, side,
+           launch_attention_tc_pass(staged, a, 1, splits_m, side));
+  e = cudaEventRecord(h->ev_gather, side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_gather, 0);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  if (!fused)
+    AVSG_RUN(AVSG_KERNEL_FINISH, st, launch_attention_tc_finish(sc, a, splits_m, st));
+  e = cudaStreamWaitEvent(st, h->ev_commit, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
 #undef AVSG_RUN
   return AVSG_OK;
@@ -756,6 +767,10 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
   }
   if (h->no_reuse) h->host_misses += (uint64_t)s.U * n_tok * k;
   StepIO v{};
+  v.parity = (int32_t)(h->seq & 1);
+  h->seq += 1;
+  // the two-pass pipeline leaves this step's staged rows to the next step
+  h->pending_place = h->overlap && !h->overlap_h16;
   v.sel = d_sel;
   v.q = d_q;
   v.out = d_out;
@@ -777,6 +792,19 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
   return e == cudaSuccess ? AVSG_OK : fail_cuda(h, e);
 }
 
+// Places the rows the last step staged, if the next step has not yet (for
+// the entry points that read or change the buffer between steps).
+// Synchronises.
+int flush_place(avsg_handle h) {
+  if (!h->pending_place) return AVSG_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = launch_place(h->ds, 0, nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  h->pending_place = false;
+  return AVSG_OK;
+}
+
 int check_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k) {
   if (!h) return AVSG_ERR_INVALID_ARG;
   if (h->latched) return AVSG_ERR_LATCHED;
@@ -796,8 +824,11 @@ extern "C" int avsg_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, con
   const int rc = check_step(h, t, n_tok, k);
   if (rc != AVSG_OK) return rc;
   if (!d_out || (k > 0 && (!d_sel || !d_q))) return AVSG_ERR_INVALID_ARG;
-  return enqueue_step(h, t, n_tok, k, d_sel, d_q, d_out, d_slot_map, d_hit,
-                      static_cast<cudaStream_t>(stream));
+  nvtxRangePushA("avsg_step");
+  const int r = enqueue_step(h, t, n_tok, k, d_sel, d_q, d_out, d_slot_map, d_hit,
+                             static_cast<cudaStream_t>(stream));
+  nvtxRangePop();
+  return r;
 }
 
 extern "C" int avsg_step_host(avsg_handle h, int32_t t, int32_t n_tok, int32_t k,
@@ -860,6 +891,8 @@ extern "C" int avsg_set_budget(avsg_handle h, const int32_t* slots_per_unit, voi
     if (slots_per_unit[u] < 1 || slots_per_unit[u] > s.B) return AVSG_ERR_INVALID_ARG;
     lo = slots_per_unit[u] < lo ? slots_per_unit[u] : lo;
   }
+  const int rc = flush_place(h);
+  if (rc != AVSG_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(h->budget_new, slots_per_unit, (size_t)s.U * sizeof(int32_t),
                                   cudaMemcpyHostToDevice, st);
@@ -940,6 +973,8 @@ extern "C" int avsg_read_state(avsg_handle h, int32_t unit, int32_t* tag, int32_
                                void* k_rows, void* v_rows) {
   if (!h || unit < 0 || unit >= h->ds.U) return AVSG_ERR_INVALID_ARG;
   if (h->no_reuse && (tag || last_step)) return AVSG_ERR_INVALID_ARG;
+  const int rc = flush_place(h);
+  if (rc != AVSG_OK) return rc;
   const DeviceState& s = h->ds;
   cudaError_t e = cudaDeviceSynchronize();
   const size_t ub = (size_t)unit * s.B;
@@ -960,13 +995,16 @@ extern "C" int avsg_reset(avsg_handle h, void* stream) {
 
 extern "C" int avsg_clear_error(avsg_handle h) {
   if (!h) return AVSG_ERR_INVALID_ARG;
+  const int rc = flush_place(h);
+  if (rc != AVSG_OK) return rc;
   const DeviceState& s = h->ds;
   cudaError_t e = cudaDeviceSynchronize();
   if (!h->no_reuse) {
     if (e == cudaSuccess) e = cudaMemset(s.hitbits, 0, (size_t)s.U * s.HT * s.HW * 4);
     if (e == cudaSuccess) e = cudaMemset(s.mset, 0xFF, (size_t)s.U * s.MS * 8);
   }
-  if (e == cudaSuccess) e = cudaMemset(s.desc_count, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(s.desc_count, 0, 2 * 4);
+  if (e == cudaSuccess) e = cudaMemset(s.dcount, 0, 2 * (size_t)s.U * 4);
   if (e == cudaSuccess) e = cudaMemset(s.part_count, 0, (size_t)s.U * kMaxTokens * kCountsPerPair * 4);
   if (e == cudaSuccess) e = cudaMemset(s.err, 0, sizeof(DevErr));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -1033,6 +1071,7 @@ extern "C" const char* avsg_strerror(int code) {
     case AVSG_ERR_BAD_STEP: return "step index not strictly increasing";
     case AVSG_ERR_UNSUPPORTED: return "no compiled attention kernel for this shape";
     case AVSG_ERR_LATCHED: return "a device error is pending; call avsg_clear_error";
+    case AVSG_ERR_INTERNAL: return "an index check of the bounds-checked build failed";
     default: return "unknown error";
   }
 }

@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(SH::NT) attn_kernel(DeviceState s, AttnLaunch 
       const int row = r0 + r;
       if (row < rows) {
         const int ent = row / ET, sub = row - ent * ET;
+        if (!AVSG_IN_BOUNDS(slots[ent] >= 0 && slots[ent] < s.B, s.err, u, ent)) continue;
         const size_t srow = ((size_t)u * s.B + slots[ent]) * ET + sub;
         if (w < KCH)
           cp_async16(kt + ((size_t)(buf * TR + r) * D) * 2 + w * 16, s.kbuf + srow * row_k + w * 16);

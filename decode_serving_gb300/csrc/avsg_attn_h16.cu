@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
   const size_t sel_base = ((size_t)u * a.n_tok + tok) * (size_t)k;
   const uint32_t stage_u = smem_u32(stage);
   const unsigned char* kb = s.kbuf;
+  const unsigned char* kstg = s.kstage;  // this step's half of the staging area (set below)
   // slots[e]: >= 0 the slot of a row resident before this step (a hit);
   // -1 not known yet; <= -2 for a row this step's gather writes: its slot
   // (-2 - value), or with staged misses its miss-set cell.  which: 0 every
@@ -194,9 +195,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
         const bool stg = late && staged;  // a missed row, at its cell of the staging area
         const int nb = stg ? s.MS : s.B;
         if (sl >= 0 && sl < nb)
-          src = (stg ? s.kstage : kb) + (((size_t)u * nb + sl) * ET + sub) * (size_t)(2 * D) + lane * 16;
+          src = (stg ? kstg : kb) + (((size_t)u * nb + sl) * ET + sub) * (size_t)(2 * D) + lane * 16;
       } else if (which == 2) {
         continue;
+      }
+      if (row < rows && !src) {
+        const int ent = ET == 1 ? row : row / ET;
+        const int sl = slots[ent] <= -2 ? -2 - slots[ent] : slots[ent];
+        (void)AVSG_IN_BOUNDS(sl < 0 || sl < (slots[ent] <= -2 && staged ? s.MS : s.B), s.err, u, ent);
       }
 #pragma unroll
       for (int j = 0; j < SH::CPL; ++j)
@@ -213,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_h16_kernel(DeviceState s, At
     const StepIO io = load_io(a.io);
     a.out = io.out;
     a.slot_map = io.slot_map;
+    if (staged) kstg = step_bufs(s, io.parity).kstage;
     for (int i = tid; i < ne; i += kThreads) {
       const int sl = __ldcg(s.hslot + sel_base + e0 + i);
       slots[i] = sl >= 0 ? sl : !staged ? -1 : sl <= -2 ? sl : -2 - s.MS;

@@ -22,11 +22,13 @@
 //   taking an equal contiguous share of all 16-row tiles of all (unit, token)
 //   pairs; a CTA writes one partial (max, sum, acc) per pair segment it
 //   covers and the last CTA to finish a pair merges its segments.
-// * Two passes (attn_tc_pass_kernel): pass 0 covers the selected rows that
-//   were already resident (the hit slots match wrote; misses are masked) and
-//   runs beside the gather and the reservation; pass 1 covers the missed rows,
-//   read from the staging area by miss-set cell (each CTA scans a share of the
-//   unit's cells for the ones its token selected), and merges both passes.
+// * Two passes: the hit pass (attn_tc_hits_kernel, persistent like the
+//   single pass) covers the selected rows that were already resident (the
+//   hit slots match wrote; misses are masked) and runs beside the gather and
+//   the reservation; the miss pass (attn_tc_miss_kernel) covers the missed
+//   rows, read from the staging area by miss-set cell (each CTA scans a share
+//   of the unit's cells for the ones its token selected), and, with one CTA
+//   per (unit, token), merges both passes (else attn_tc_finish_kernel does).
 // No CTA waits for another.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -147,8 +149,12 @@ struct TcParams {
   int rows_per_pair, tiles_per_pair;
   long long tiles;              // all pairs
   int ctas, max_seg;
-  // two passes (hits, then misses)
-  int splits_h, splits_m;
+  // two passes: the hit pass is persistent (hit_ctas CTAs over all pairs'
+  // tiles, like the single pass), the miss pass has splits_m CTAs per pair
+  int hit_ctas, splits_m;
+  // with one miss-pass CTA per pair, that CTA merges the pair's partials
+  // into the output
+  int fuse_finish;
 };
 
 struct SegArgs {
@@ -231,6 +237,7 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
                    : p.identity ? tok * p.k + ent
                                 : __ldg(p.slots + (size_t)pair * p.k + ent);
     if (slot < 0) return -1;  // not a row of this pass (a miss in the pass over hit rows)
+    if (!AVSG_IN_BOUNDS(slot < s.B, s.err, u, ent)) return -1;
     return ((long long)u * s.B + slot) * p.ET + sub;
   };
   constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
@@ -620,10 +627,36 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
   }
 }
 
-// Hit pass: every selected position of a (unit, token), with the hit slots
-// that match wrote (a miss has slot -1 and is masked); runs while the missed
-// rows are still crossing the host link.  CTA (sp, pair) takes an equal
-// share of the pair's tiles and writes partial sp of the pair.
+// Partials of the two-pass attention, G * (D + 2) floats each, in three
+// groups: [pairs] the hit-pass partial of a pair one CTA covered whole;
+// [2 * hit_ctas] the hit-pass partials of the pairs a CTA cut (its first and
+// its last segment, as in the single pass); [pairs][splits_m] the miss-pass
+// partials.
+__device__ __forceinline__ int hit_segments(const TcParams& p, int pair, long long* slot0) {
+  const long long T = p.tiles, t0 = (long long)pair * p.tiles_per_pair;
+  const int C = p.hit_ctas;
+  const int first = cta_of_tile(t0, C, T), last = cta_of_tile(t0 + p.tiles_per_pair - 1, C, T);
+  const long long pairs = T / p.tiles_per_pair;
+  *slot0 = first == last ? pair : pairs + 2LL * first + ((long long)first * T / C == t0 ? 0 : 1);
+  return last - first + 1;
+}
+// Slot of a pair's partial q2: its hit-pass partials first, then its
+// splits_m miss-pass partials.
+__device__ __forceinline__ long long two_pass_slot(const TcParams& p, int pair, int nseg_h,
+                                                   long long slot0, int q2) {
+  const long long pairs = p.tiles / p.tiles_per_pair;
+  if (q2 >= nseg_h) return pairs + 2LL * p.hit_ctas + (long long)pair * p.splits_m + (q2 - nseg_h);
+  if (q2 == 0) return slot0;
+  const int first = (int)((slot0 - pairs) >> 1);
+  return pairs + 2LL * (first + q2);
+}
+
+// Hit pass: every selected position of every (unit, token), with the hit
+// slots that match wrote (a miss has slot -1 and is masked); runs while the
+// missed rows are still crossing the host link.  Persistent: 2 CTAs per SM,
+// each an equal contiguous share of all pairs' 16-row tiles, so every SM
+// gets the same work whatever the pair count.  A CTA writes one partial per
+// pair segment it covers (see hit_segments).
 template <class SH>
 __global__ void __launch_bounds__(kThreadsTc) attn_tc_hits_kernel(DeviceState s, TcParams p) {
   constexpr int D = SH::D, G = SH::G;
@@ -633,43 +666,57 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_hits_kernel(DeviceState s,
   __shared__ __align__(16) float s_q[G * D];
   __shared__ int s_stop;
   const int tid = threadIdx.x;
-  const int sp = blockIdx.x, pair = blockIdx.y;
   griddep_wait();
   griddep_launch();
-  // q (the copy match made) -> shared memory, in flight while the rest starts
-  for (int i = tid; i < G * D / 4; i += kThreadsTc) cp_async16(s_q + 4 * i, p.q + (size_t)pair * G * D + 4 * i);
-  cp_async_commit();
   if (tid == 0) s_stop = load_err(s.err);
-  cp_async_wait<0>();
   __syncthreads();
   if (s_stop) return;
   float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
-
-  SegArgs a;
-  a.pair = pair;
-  a.u = pair / p.n_tok;
-  a.tok = pair - a.u * p.n_tok;
-  a.ent_base = 0;
-  a.list = nullptr;
-  a.qs = s_q;
-  a.rows = p.k * p.ET;
-  const int tiles = (a.rows + kTileRows - 1) / kTileRows;
-  a.ta = (int)((long long)sp * tiles / p.splits_h);
-  a.tb = (int)((long long)(sp + 1) * tiles / p.splits_h);
-  tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
+  const long long T = p.tiles, pairs = T / p.tiles_per_pair;
+  const int C = p.hit_ctas;
+  const long long t_begin = (long long)blockIdx.x * T / C;
+  const long long t_end = (long long)(blockIdx.x + 1) * T / C;
   const size_t stride = (size_t)G * (D + 2);
-  float* pbase = s.part + (size_t)pair * (p.splits_h + p.splits_m) * stride;
-  tc_write_partial<G, D>(pbase + (size_t)sp * stride, cm, cl, co);
+  for (long long t = t_begin; t < t_end;) {
+    const int pair = (int)(t / p.tiles_per_pair);
+    const long long pair_t0 = (long long)pair * p.tiles_per_pair;
+    // this pair's q (the copy match made) -> shared memory
+    for (int i = tid; i < G * D / 4; i += kThreadsTc)
+      cp_async16(s_q + 4 * i, p.q + (size_t)pair * G * D + 4 * i);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    SegArgs a;
+    a.pair = pair;
+    a.u = pair / p.n_tok;
+    a.tok = pair - a.u * p.n_tok;
+    a.ent_base = 0;
+    a.list = nullptr;
+    a.qs = s_q;
+    a.rows = p.k * p.ET;
+    a.ta = (int)(t - pair_t0);
+    a.tb = (int)(min(t_end, pair_t0 + p.tiles_per_pair) - pair_t0);
+    const bool first_seg = t == t_begin;
+    const bool whole = a.ta == 0 && a.tb == p.tiles_per_pair;
+    t = pair_t0 + a.tb;
+    tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
+    const long long slot = whole ? pair : pairs + 2LL * blockIdx.x + (first_seg ? 0 : 1);
+    tc_write_partial<G, D>(s.part + (size_t)slot * stride, cm, cl, co);
+    __syncthreads();  // the staging (and s_q) is reused by the next segment
+  }
 }
 
 // Miss pass: CTA (sp, pair) copies its range of the unit's miss set into
 // shared memory (one round of 16-byte async copies), lists the claimed cells
 // that carry this token (a fixed order: by thread, then by stride), attends
-// over their rows in the staging area and writes partial splits_h + sp of the
-// pair (the finish kernel merges).  It follows the staged gather on the same
+// over their rows in this step's half of the staging area and writes its
+// miss-pass partial sp of the pair.  It follows the staged gather on the same
 // stream: the list is built while the gather's last copies drain, and the
-// rows are read after the grid-dependency wait.  `s` is the staged view of
-// the state: kbuf/vbuf are the staging rows and B the miss-set capacity.
+// rows are read after the grid-dependency wait (which, with one CTA per
+// pair, also covers the hit pass: that CTA then merges the pair's partials
+// into the output).  The rows reach their slots later, in the place that
+// the next step runs early.  `s` is the staged view of the state: kbuf/vbuf
+// are the staging area's first half and B the miss-set capacity.
 template <class SH>
 __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s, TcParams p) {
   constexpr int D = SH::D, G = SH::G;
@@ -741,6 +788,11 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
   griddep_wait();  // the gather's rows are in the staging area
   griddep_launch();
   if (tid == 0) s_stop = load_err(s.err);
+  {  // this step's half of the staging area
+    const StepBufs sb = step_bufs(s, load_io(s.io).parity);
+    s.kbuf = sb.kstage;
+    s.vbuf = sb.vstage;
+  }
   __syncthreads();
   if (s_stop) return;
 
@@ -757,9 +809,18 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
   a.tb = (a.rows + kTileRows - 1) / kTileRows;
   tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
 
-  const int nseg = p.splits_h + p.splits_m;
+  long long slot0 = 0;
+  const int nseg_h = hit_segments(p, pair, &slot0);
   const size_t stride = (size_t)G * (D + 2);
-  tc_write_partial<G, D>(s.part + ((size_t)pair * nseg + p.splits_h + sp) * stride, cm, cl, co);
+  tc_write_partial<G, D>(
+      s.part + (size_t)two_pass_slot(p, pair, nseg_h, slot0, nseg_h + sp) * stride, cm, cl, co);
+  if (!p.fuse_finish) return;
+  __threadfence();
+  __syncthreads();  // this CTA's partial is written; the hit pass's were before the launch
+  const float* part = s.part;
+  tc_merge_partials<G, D>(
+      [&](int q2) { return part + (size_t)two_pass_slot(p, pair, nseg_h, slot0, q2) * stride; },
+      nseg_h + p.splits_m, load_io(s.io).out + (size_t)pair * G * D, co + G * D);
 }
 
 // Finish of a step, one CTA per (unit, token): merges the pair's partials
@@ -775,11 +836,14 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_finish_kernel(DeviceState 
   if (tid == 0) s_stop = load_err(s.err);
   __syncthreads();
   if (s_stop) return;
-  const int nseg = p.splits_h + p.splits_m;
+  long long slot0 = 0;
+  const int nseg_h = hit_segments(p, pair, &slot0);
   float* out = load_io(s.io).out + (size_t)pair * G * D;
-  const float* pbase = s.part + (size_t)pair * nseg * G * (D + 2);
-  tc_merge_partials<G, D>([&](int q2) { return pbase + (size_t)q2 * G * (D + 2); }, nseg, out,
-                          wseg);
+  const float* part = s.part;
+  const size_t stride = (size_t)G * (D + 2);
+  tc_merge_partials<G, D>(
+      [&](int q2) { return part + (size_t)two_pass_slot(p, pair, nseg_h, slot0, q2) * stride; },
+      nseg_h + p.splits_m, out, wseg);
 }
 
 template <class SH>
@@ -823,26 +887,58 @@ cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaS
   return launch_pdl(attn_tc_kernel<SH>, dim3(p.ctas), dim3(kThreadsTc), SH::SMEM, st, s, p);
 }
 
+// The persistent hit pass's shape for a step: tiles per pair, all tiles,
+// CTAs, and the most hit-pass partials one pair has.
+struct HitGrid {
+  int tiles_per_pair, ctas, max_seg;
+  long long tiles;
+};
+inline HitGrid hit_grid(int pairs, int k, int ET, int num_sms) {
+  HitGrid g;
+  g.tiles_per_pair = (k * ET + kTileRows - 1) / kTileRows;
+  g.tiles = (long long)pairs * g.tiles_per_pair;
+  long long C = (long long)num_sms * kCtasPerSm;
+  if (C > g.tiles) C = g.tiles;
+  g.ctas = (int)(C < 1 ? 1 : C);
+  const long long per = g.tiles / g.ctas;  // fewest tiles a CTA gets
+  g.max_seg = (int)((g.tiles_per_pair + per - 1) / per + 1);
+  return g;
+}
+
 template <class SH>
-cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int splits_h,
-                        int splits_m, cudaStream_t st) {
-  static int smem_hits = 0, smem_miss = 0;
+TcParams two_pass_params(const DeviceState& s, const AttnLaunch& a, int splits_m) {
   TcParams p = tc_params<SH>(s, a);
   p.slots = s.hslot;
   p.identity = 0;
-  p.splits_h = splits_h;
+  const HitGrid g = hit_grid(s.U * a.n_tok, a.k, s.ET, a.num_sms);
+  p.tiles_per_pair = g.tiles_per_pair;
+  p.tiles = g.tiles;
+  p.hit_ctas = g.ctas;
   p.splits_m = splits_m;
-  dim3 grid((unsigned)(pass ? splits_m : splits_h), (unsigned)(s.U * a.n_tok));
+  return p;
+}
+
+template <class SH>
+cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int splits_m,
+                        cudaStream_t st) {
+  static int smem_hits = 0, smem_miss = 0;
+  TcParams p = two_pass_params<SH>(s, a, splits_m);
+  const HitGrid g = hit_grid(s.U * a.n_tok, a.k, s.ET, a.num_sms);
+  const size_t parts = (size_t)s.U * a.n_tok * (1 + splits_m) + 2 * (size_t)g.ctas;
+  if (parts * SH::G * (SH::D + 2) > a.part_capacity || g.max_seg + splits_m > SH::MAX_SEG)
+    return cudaErrorInvalidValue;
   if (pass == 0) {
     cudaError_t e = ensure_smem((const void*)attn_tc_hits_kernel<SH>, SH::SMEM, &smem_hits);
     if (e != cudaSuccess) return e;
     // Not launched early: its CTAs would take every SM while match runs,
     // ahead of the reservation and the gather on the other streams.
-    return launch_ex(false, attn_tc_hits_kernel<SH>, grid, dim3(kThreadsTc), SH::SMEM, st, s, p);
+    return launch_ex(false, attn_tc_hits_kernel<SH>, dim3((unsigned)g.ctas), dim3(kThreadsTc),
+                     SH::SMEM, st, s, p);
   }
-  if (s.MS % splits_m != 0 || s.MS / splits_m > SH::SCAN_MAX || (s.MS / splits_m) % 2 != 0 ||
-      splits_h + splits_m > SH::MAX_SEG)
+  dim3 grid((unsigned)splits_m, (unsigned)(s.U * a.n_tok));
+  if (s.MS % splits_m != 0 || s.MS / splits_m > SH::SCAN_MAX || (s.MS / splits_m) % 2 != 0)
     return cudaErrorInvalidValue;
+  p.fuse_finish = splits_m == 1 ? 1 : 0;
   const size_t smem = SH::SMEM + (size_t)(s.MS / splits_m) * sizeof(int32_t);
   cudaError_t e = ensure_smem((const void*)attn_tc_miss_kernel<SH>,
                               SH::SMEM + (size_t)SH::SCAN_MAX * sizeof(int32_t), &smem_miss);
@@ -856,13 +952,12 @@ cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int
 }
 
 template <class SH>
-cudaError_t run_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_h, int splits_m,
+cudaError_t run_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_m,
                           cudaStream_t st) {
   static int smem_done = 0;
-  TcParams p = tc_params<SH>(s, a);
-  p.splits_h = splits_h;
-  p.splits_m = splits_m;
-  const size_t smem = 2 * (size_t)(splits_h + splits_m) * SH::G * sizeof(float);
+  TcParams p = two_pass_params<SH>(s, a, splits_m);
+  const HitGrid g = hit_grid(s.U * a.n_tok, a.k, s.ET, a.num_sms);
+  const size_t smem = 2 * (size_t)(g.max_seg + splits_m) * SH::G * sizeof(float);
   cudaError_t e = ensure_smem((const void*)attn_tc_finish_kernel<SH>, smem, &smem_done);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_tc_finish_kernel<SH>, dim3((unsigned)(s.U * a.n_tok)), dim3(kThreadsTc),
@@ -898,6 +993,12 @@ bool attention_tc_supported(int D, int DV, int G, int kv_shared) {
   return D == DV && (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
+size_t attention_tc_two_pass_floats(int pairs, int k, int ET, int G, int DV, int num_sms,
+                                    int splits_m) {
+  const HitGrid g = hit_grid(pairs, k, ET, num_sms);
+  return ((size_t)pairs * (1 + splits_m) + 2 * (size_t)g.ctas) * (size_t)G * (DV + 2);
+}
+
 size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sms) {
   // pairs * max_seg <= T / floor(T / C) + 2 * pairs <= 2 * C + 2 * pairs (see run_tc)
   const size_t pairs = (size_t)U * max_tokens;
@@ -905,10 +1006,10 @@ size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sm
 }
 
 cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
-                                     int splits_h, int splits_m, cudaStream_t st) {
+                                     int splits_m, cudaStream_t st) {
 #define X(d, g, sh)                                                         \
   if (s.D == d && s.G == g && (s.kv_shared != 0) == sh)                     \
-    return run_tc_pass<TcShape<d, g, sh>>(s, a, pass, splits_h, splits_m, st);
+    return run_tc_pass<TcShape<d, g, sh>>(s, a, pass, splits_m, st);
   X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
   X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
   X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)
@@ -917,11 +1018,11 @@ cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, 
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attention_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_h,
-                                       int splits_m, cudaStream_t st) {
+cudaError_t launch_attention_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_m,
+                                       cudaStream_t st) {
 #define X(d, g, sh)                                                         \
   if (s.D == d && s.G == g && (s.kv_shared != 0) == sh)                     \
-    return run_tc_finish<TcShape<d, g, sh>>(s, a, splits_h, splits_m, st);
+    return run_tc_finish<TcShape<d, g, sh>>(s, a, splits_m, st);
   X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
   X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
   X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)

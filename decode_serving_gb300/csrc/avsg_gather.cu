@@ -70,19 +70,22 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(DeviceState s) {
   griddep_wait();
   griddep_launch();
   if (load_err(s.err) != 0) return;  // no barriers below: a per-thread exit is safe
-  const uint32_t n = (uint32_t)*(volatile int32_t*)s.desc_count;
+  const StepBufs sb = step_bufs(s, load_io(s.io).parity);
+  const uint32_t n = (uint32_t)*(volatile int32_t*)sb.desc_count;
   const uint32_t cpe = (uint32_t)((s.ek + s.ev) >> 4);
   const uint32_t total = n * cpe;
   const uint32_t per = (total + gridDim.x - 1) / gridDim.x;
   const uint32_t begin = blockIdx.x * per;
   const uint32_t end = min(total, begin + per);
-  const GatherDesc* desc = s.desc;
+  const GatherDesc* desc = sb.desc;
   copy_chunks(s, begin, end, [&](uint32_t d, int& unit, int& id, int& slot) {
     const int4 g = __ldcg(reinterpret_cast<const int4*>(desc + d));
     unit = g.x;
     id = g.y;
     slot = g.z;
-    return true;
+    return AVSG_IN_BOUNDS(unit >= 0 && unit < s.U && id >= 0 && id < s.L && slot >= 0 &&
+                              slot < s.B,
+                          s.err, unit, (int)d);
   });
 }
 
@@ -105,6 +108,7 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
   // (dependents are released when the last round begins: the miss pass that
   // follows prepares its lists meanwhile, but must not take SMs any earlier)
   if (load_err(s.err) != 0) return;  // uniform over the CTA
+  const StepBufs sb = step_bufs(s, load_io(s.io).parity);
   const int lane = threadIdx.x & 31;
   const long long ncell = (long long)s.U * s.MS;
   const long long c_begin = blockIdx.x * ncell / gridDim.x;
@@ -149,14 +153,17 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
           const uint32_t r = it / cpe, j = it - r * cpe;
           const long long cg = r0 + s_off[r];
           const long long unit = cg / s.MS;
+          if (!AVSG_IN_BOUNDS(cg < (long long)s.U * s.MS && s_id[r] >= 0 && s_id[r] < s.L, s.err,
+                              (int)unit, (int)(cg - unit * s.MS)))
+            continue;
           const long long hrow = unit * s.L + s_id[r];
           const unsigned char* src;
           if (j < cpk) {
             src = s.host_k + hrow * s.ek + ((size_t)j << 4);
-            dst[q] = s.kstage + cg * s.ek + ((size_t)j << 4);
+            dst[q] = sb.kstage + cg * s.ek + ((size_t)j << 4);
           } else {
             src = s.host_v + hrow * s.ev + ((size_t)(j - cpk) << 4);
-            dst[q] = s.vstage + cg * s.ev + ((size_t)(j - cpk) << 4);
+            dst[q] = sb.vstage + cg * s.ev + ((size_t)(j - cpk) << 4);
           }
           v[q] = load_host16(src);
         }
@@ -171,21 +178,23 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
 }
 
 // Place: every miss's staged row (by miss-set cell) into its reserved slot
-// (device to device), grid (U, kPlaceSplit).  The unit's work is its
-// descriptors' (row, 16-byte chunk) items in row order; the unit's
-// kPlaceSplit * 256 threads take consecutive items (coalesced), kPlaceRows
-// items each per round: the rows' descriptors, then all the loads, then the
-// stores.  Rows of any size keep every thread busy (8 KiB page entries as
-// much as 512-byte token rows).
+// (device to device), grid (U, kPlaceSplit), for the step of parity
+// io.parity ^ which (see launch_place).  The unit's work is its descriptors'
+// (row, 16-byte chunk) items in row order; the unit's kPlaceSplit * 256
+// threads take consecutive items (coalesced), kPlaceRows items each per
+// round: the rows' descriptors, then all the loads, then the stores.  Rows of
+// any size keep every thread busy (8 KiB page entries as much as 512-byte
+// token rows).  It ignores the error word: a step whose reservation did not
+// run left no descriptors of its parity.
 constexpr int kPlaceSplit = 4;
 constexpr int kPlaceRows = 8;
 
-__global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s) {
+__global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s, int which) {
   griddep_wait();
   griddep_launch();
-  if (load_err(s.err) != 0) return;
+  const StepBufs sb = step_bufs(s, load_io(s.io).parity ^ which);
   const int u = blockIdx.x;
-  const int base = s.dbase[u], cnt = s.dcount[u];
+  const int base = __ldcg(sb.dbase + u), cnt = __ldcg(sb.dcount + u);
   const uint32_t cpk = (uint32_t)(s.ek >> 4), cpe = cpk + (uint32_t)(s.ev >> 4);
   const uint32_t total = (uint32_t)cnt * cpe;
   const uint32_t nthr = (uint32_t)kPlaceSplit * kThreads;
@@ -201,14 +210,17 @@ __global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s) {
       src[r] = nullptr;
       if (item < total) {
         const uint32_t d = item / cpe, c = item - d * cpe;
-        const GatherDesc* g = s.desc + base + d;
-        const size_t srow = (size_t)u * s.MS + __ldcg(&g->cell);
-        const size_t drow = (size_t)u * s.B + __ldcg(&g->slot);
+        const GatherDesc* g = sb.desc + base + d;
+        const int cell = __ldcg(&g->cell), slot = __ldcg(&g->slot);
+        if (!AVSG_IN_BOUNDS(cell >= 0 && cell < s.MS && slot >= 0 && slot < s.B, s.err, u, (int)d))
+          continue;
+        const size_t srow = (size_t)u * s.MS + cell;
+        const size_t drow = (size_t)u * s.B + slot;
         if (c < cpk) {
-          src[r] = reinterpret_cast<const uint4*>(s.kstage + srow * s.ek) + c;
+          src[r] = reinterpret_cast<const uint4*>(sb.kstage + srow * s.ek) + c;
           dst[r] = reinterpret_cast<uint4*>(s.kbuf + drow * s.ek) + c;
         } else {
-          src[r] = reinterpret_cast<const uint4*>(s.vstage + srow * s.ev) + (c - cpk);
+          src[r] = reinterpret_cast<const uint4*>(sb.vstage + srow * s.ev) + (c - cpk);
           dst[r] = reinterpret_cast<uint4*>(s.vbuf + drow * s.ev) + (c - cpk);
         }
       }
@@ -297,11 +309,11 @@ cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st)
 
 static_assert(kStageCells % kThreads == 0, "a round is whole passes of the CTA");
 
-cudaError_t launch_place(const DeviceState& s, cudaStream_t st) {
+cudaError_t launch_place(const DeviceState& s, int which, cudaStream_t st) {
   static int attr_done = 0;
   const cudaError_t e = ensure_smem((const void*)place_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(place_kernel, dim3(s.U, kPlaceSplit), dim3(kThreads), 0, st, s);
+  return launch_pdl(place_kernel, dim3(s.U, kPlaceSplit), dim3(kThreads), 0, st, s, which);
 }
 
 cudaError_t launch_gather_all(const DeviceState& s, const StepIO& v, int n_tok, int k, int ctas,

@@ -51,6 +51,9 @@ struct StepIO {
   uint8_t* hit;
   int32_t t;
   int32_t live;                    // entries per unit selectable this step (ids below it)
+  int32_t parity;                  // 0 / 1 alternating by step: which half of the per-step
+                                   // staging and descriptor arrays this step writes
+  int32_t pad_;
 };
 
 struct DeviceState {
@@ -68,8 +71,9 @@ struct DeviceState {
   const unsigned char* host_v;
   unsigned char* kbuf;             // [U][B][ek]
   unsigned char* vbuf;             // [U][B][ev]
-  unsigned char* kstage;           // [U][MS][ek] missed rows by miss-set cell (staged gather)
-  unsigned char* vstage;           // [U][MS][ev]
+  unsigned char* kstage;           // [2][U][MS][ek] missed rows by miss-set cell (staged
+                                   // gather), one half per step parity
+  unsigned char* vstage;           // [2][U][MS][ev]
   int32_t* tag;                    // [U][B] resident id or kEmpty
   int32_t* last;                   // [U][B] step of last selection, -1 never
   uint32_t* hitbits;               // [U][HT][HW] this step's hit slots per token (written by match)
@@ -80,10 +84,10 @@ struct DeviceState {
   int32_t* hslot;                  // [U][n_tok][k] slot of each selected id if it was a hit,
                                    // else -2 - its miss-set cell (-1 if it has none)
   int32_t* mslot;                  // [U][MS] slot reserved for the miss in that cell
-  GatherDesc* desc;                // [U * max_union]
-  int32_t* desc_count;             // [1]
-  int32_t* dbase;                  // [U] first descriptor of the unit this step
-  int32_t* dcount;                 // [U] descriptors of the unit this step
+  GatherDesc* desc;                // [2][U * max_union]     (halves by step parity)
+  int32_t* desc_count;             // [2]
+  int32_t* dbase;                  // [2][U] first descriptor of the unit that step
+  int32_t* dcount;                 // [2][U] descriptors of the unit that step (0: none)
   float* part;                     // split-K partials
   int32_t* part_count;             // [U][max_tokens][8] arrival counters, 0 between steps
   DevCounters* counters;           // [U] distinct hits / misses, summed over steps
@@ -91,10 +95,45 @@ struct DeviceState {
   int32_t* budget;                 // [U] usable slots per unit (buffer elasticity), <= B
 };
 
+// The per-step arrays of one parity.
+struct StepBufs {
+  GatherDesc* desc;
+  int32_t* desc_count;
+  int32_t* dbase;
+  int32_t* dcount;
+  unsigned char* kstage;
+  unsigned char* vstage;
+};
+__host__ __device__ __forceinline__ StepBufs step_bufs(const DeviceState& s, int parity) {
+  const size_t half = (size_t)s.U * s.MS;
+  StepBufs b;
+  b.desc = s.desc + (size_t)parity * s.U * s.max_union;
+  b.desc_count = s.desc_count + parity;
+  b.dbase = s.dbase + (size_t)parity * s.U;
+  b.dcount = s.dcount + (size_t)parity * s.U;
+  b.kstage = s.kstage ? s.kstage + (size_t)parity * half * s.ek : nullptr;
+  b.vstage = s.vstage ? s.vstage + (size_t)parity * half * (s.ev ? s.ev : s.ek) : nullptr;
+  return b;
+}
+
 __device__ __forceinline__ uint32_t fib_hash(int32_t id, int shift) {
   // Knuth's multiplicative (Fibonacci) hashing: top bits of id * 2^32/phi.
   return ((uint32_t)id * 2654435769u) >> shift;
 }
+
+// Bounds-checked build (a separate library compiled with -DAVSG_DEBUG_BOUNDS,
+// the stand-in for a memory checker): an index a kernel takes from the step's
+// data or the buffer state -- a slot, a selected id, a miss-set cell, a
+// descriptor -- is checked against its array before the access; a failed
+// check latches AVSG_ERR_INTERNAL with the unit and position in the device
+// error word, and the access is skipped.  In the product build the check is
+// the constant true and costs nothing.
+#ifdef AVSG_DEBUG_BOUNDS
+__device__ __forceinline__ bool bound_ok(bool ok, DevErr* e, int unit, int pos);
+#define AVSG_IN_BOUNDS(cond, err, unit, pos) ::avsg::bound_ok((cond), (err), (unit), (pos))
+#else
+#define AVSG_IN_BOUNDS(cond, err, unit, pos) true
+#endif
 
 // Programmatic dependent launch: a kernel may be scheduled while the previous
 // one in the stream drains; griddep_wait() blocks until that grid has finished
@@ -130,6 +169,13 @@ __device__ __forceinline__ void raise_error(DevErr* e, int code, int unit, int p
   }
 }
 
+#ifdef AVSG_DEBUG_BOUNDS
+__device__ __forceinline__ bool bound_ok(bool ok, DevErr* e, int unit, int pos) {
+  if (!ok) raise_error(e, AVSG_ERR_INTERNAL, unit, pos);
+  return ok;
+}
+#endif
+
 // Launch with programmatic stream serialization (see griddep_wait).
 bool pdl_enabled();
 template <typename... Params, typename... Args>
@@ -159,8 +205,12 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 cudaError_t ensure_smem(const void* kernel, size_t bytes, int* done_bytes);
 
 // Kernel launchers (one per .cu file).
-// Shared memory of match: the miss set (MS cells) and n_tok hit bitmaps.
-size_t match_smem_bytes(int MS, int n_tok, int HW);
+// Shared memory of one match CTA in a cluster of `cl`: its part of the miss
+// set (MS cells) and of n_tok hit bitmaps.
+size_t match_smem_bytes(int MS, int n_tok, int HW, int cl);
+// CTAs per unit (a cluster) of a match over n selected ids per unit: about
+// one id per thread, more where shared memory or the ids per thread need it.
+int match_cluster_size(int MS, int n_tok, int HW, int n);
 cudaError_t launch_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st);
 size_t victims_smem_bytes(const DeviceState& s);
 cudaError_t launch_victims(const DeviceState& s, int n_tok, int k, cudaStream_t st);
@@ -174,8 +224,12 @@ cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
 // Staged gather: right after match, the host row of every claimed miss-set
 // cell is copied to kstage/vstage at that cell (no slot needed yet).
 cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st);
-// Staged rows -> their reserved slots (after the gather and the reservation).
-cudaError_t launch_place(const DeviceState& s, cudaStream_t st);
+// Staged rows -> their reserved slots.  which: 0 the rows the current (or
+// last) step staged; 1 the rows the step before it staged (the deferred place
+// of the two-pass pipeline, run early in the next step).  Runs whatever the
+// error word says: a step whose reservation did not run has no descriptors
+// (match zeroes the counts of its parity first).
+cudaError_t launch_place(const DeviceState& s, int which, cudaStream_t st);
 // Reads one word of every 4 KiB page of a mapped host range (sink: a device
 // word it may write), so the device's translations of the range are in place.
 cudaError_t launch_host_touch(const unsigned char* p, size_t bytes, unsigned* sink, int num_sms,
@@ -218,15 +272,20 @@ bool attention_tc_supported(int D, int DV, int G, int kv_shared);
 size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sms);
 cudaError_t launch_attention_tc(const DeviceState& s, const AttnLaunch& a, int num_sms,
                                 cudaStream_t st);
-// pass 0: hit rows of every (unit, token), splits_h CTAs per pair.  pass 1:
-// miss rows from the staging area (s is the staged view), splits_m CTAs per
+// pass 0: hit rows of every (unit, token), a persistent grid of 2 CTAs per
+// SM, each an equal share of all pairs' tiles.  pass 1: miss rows from this
+// step's half of the staging area (s is the staged view), splits_m CTAs per
 // pair (MS / splits_m <= the shape's scan limit), launched right after the
-// staged gather on its stream.  Each writes partials; the finish kernel
-// merges them (s: real state).
+// staged gather on its stream (and, with splits_m == 1, once the hit pass is
+// done).  Each pass writes partials; with splits_m == 1 the miss pass merges
+// them into the output, else the finish kernel does (s: real state).
 cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
-                                     int splits_h, int splits_m, cudaStream_t st);
-cudaError_t launch_attention_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_h,
-                                       int splits_m, cudaStream_t st);
+                                     int splits_m, cudaStream_t st);
+cudaError_t launch_attention_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_m,
+                                       cudaStream_t st);
+// Floats of partials a two-pass step over `pairs` (unit, token) pairs needs.
+size_t attention_tc_two_pass_floats(int pairs, int k, int ET, int G, int DV, int num_sms,
+                                    int splits_m);
 // Most partials (hit + miss splits) one pair's merge takes.
 int attention_tc_max_segments(int D, int G, int kv_shared);
 // Most miss-set cells one miss-pass CTA scans (a power of two).

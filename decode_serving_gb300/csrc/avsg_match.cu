@@ -4,13 +4,15 @@
 // selected tokens against the entries retained in the HBM buffer identifies
 // the reusable slots.
 //
-// A cluster of kMatchCluster CTAs per unit; the unit's miss set (cells in
+// A cluster of CL CTAs per unit, CL in {1, 2, 4, 8} sized to the step (about
+// one selected id per thread, so a unit with few ids takes one CTA and a
+// large step spreads its probes over 8 SMs); the unit's miss set (cells in
 // contiguous blocks) and hit bitmaps (32-slot words dealt round-robin) are
 // spread over the cluster's shared memories and updated with atomics on
-// distributed shared memory.  A thread takes every (kMatchCluster * 256)-th
-// position of the unit's n_tok * k selected ids (at most kMatchPerThread),
-// loads all of them and then all of their first hash windows before it
-// resolves any.  Per id:
+// distributed shared memory.  A thread takes every (CL * 256)-th position of
+// the unit's n_tok * k selected ids (at most kMatchPerThread), loads all of
+// them and then all of their first hash windows before it resolves any.
+// Per id:
 //   * range check (id in [0, live), the entries live this step), else BAD_SELECTION;
 //   * lookup in the unit's open-addressed table (linear probing, Fibonacci
 //     hash; a probe reads a 16-byte window of two cells);
@@ -38,8 +40,8 @@ namespace avsg {
 namespace {
 
 constexpr int kThreads = kMatchThreads;
-constexpr int kC = kMatchCluster;
 
+template <int kC>
 __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v, int n_tok,
                                                          int k) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -63,9 +65,12 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
   griddep_wait();
   griddep_launch();
   if (u == 0 && rank == 0 && tid == 0) {
-    *s.desc_count = 0;
+    s.desc_count[v.parity] = 0;
     *s.io = v;  // for the kernels after this one
   }
+  // No descriptors of this step's parity until its reservation writes them
+  // (a step that fails leaves none for the place that follows it).
+  if (rank == 0 && tid == 0) s.dcount[(size_t)v.parity * s.U + u] = 0;
   {  // this unit's q, copied to a buffer the attention kernels read at a fixed place
     const int nq = n_tok * s.G * s.D;
     const float* src = v.q + (size_t)u * nq;
@@ -126,6 +131,7 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
       skip_first = false;
       cell += 2;
     }
+    if (slot >= 0 && !AVSG_IN_BOUNDS(slot < s.B, s.err, u, pos)) continue;
     if (slot >= 0) {
       const int word = slot >> 5;
       uint32_t* bits = cl.map_shared_rank(lbits, (unsigned)(word % kC));
@@ -189,35 +195,60 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
 
 }  // namespace
 
-size_t match_smem_bytes(int MS, int n_tok, int HW) {
-  return (size_t)(MS / kMatchCluster) * sizeof(unsigned long long) +
-         (size_t)n_tok * ((HW + kMatchCluster - 1) / kMatchCluster) * sizeof(uint32_t);
+size_t match_smem_bytes(int MS, int n_tok, int HW, int cl) {
+  return (size_t)(MS / cl) * sizeof(unsigned long long) +
+         (size_t)n_tok * ((HW + cl - 1) / cl) * sizeof(uint32_t);
 }
 
-cudaError_t launch_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st) {
-  if ((int64_t)n_tok * k > (int64_t)kMatchCluster * kMatchThreads * kMatchPerThread ||
-      s.MS < 2 * kMatchCluster || n_tok > s.HT)
-    return cudaErrorInvalidValue;
-  const size_t smem = match_smem_bytes(s.MS, n_tok, s.HW);
+int match_cluster_size(int MS, int n_tok, int HW, int n) {
+  int cl = 1;
+  while (cl < kMatchCluster && (int64_t)cl * kThreads < n) cl *= 2;  // about one id per thread
+  while (cl < kMatchCluster && (match_smem_bytes(MS, n_tok, HW, cl) > kMatchSmemMax ||
+                                (int64_t)cl * kThreads * kMatchPerThread < n || MS < 2 * cl))
+    cl *= 2;
+  return cl;
+}
+
+namespace {
+
+template <int CL>
+cudaError_t run_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st) {
+  const size_t smem = match_smem_bytes(s.MS, n_tok, s.HW, CL);
   static int attr_done = 0;
-  const cudaError_t e = ensure_smem((const void*)match_kernel, match_smem_bytes(s.MS, s.HT, s.HW),
-                                    &attr_done);
+  const cudaError_t e = ensure_smem((const void*)match_kernel<CL>,
+                                    match_smem_bytes(s.MS, s.HT, s.HW, CL), &attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(s.U * kMatchCluster));
+  cfg.gridDim = dim3((unsigned)(s.U * CL));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kMatchCluster;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, match_kernel, s, v, n_tok, k);
+  return cudaLaunchKernelEx(&cfg, match_kernel<CL>, s, v, n_tok, k);
+}
+
+}  // namespace
+
+cudaError_t launch_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st) {
+  const int n = n_tok * k;
+  const int cl = match_cluster_size(s.MS, s.HT, s.HW, n);
+  if ((int64_t)n > (int64_t)cl * kThreads * kMatchPerThread || s.MS < 2 * cl || n_tok > s.HT ||
+      match_smem_bytes(s.MS, s.HT, s.HW, cl) > kMatchSmemMax)
+    return cudaErrorInvalidValue;
+  switch (cl) {
+    case 1: return run_match<1>(s, v, n_tok, k, st);
+    case 2: return run_match<2>(s, v, n_tok, k, st);
+    case 4: return run_match<4>(s, v, n_tok, k, st);
+    default: return run_match<8>(s, v, n_tok, k, st);
+  }
 }
 
 }  // namespace avsg

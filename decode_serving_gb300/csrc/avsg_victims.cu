@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   griddep_launch();
   const StepIO io = load_io(s.io);
   const int t = io.t;
+  const StepBufs sb = step_bufs(s, io.parity);
   const int budget = __ldcg(s.budget + u);  // this unit's usable slots (buffer elasticity)
   int32_t* __restrict__ slot_map = io.slot_map;
   if (tid == 0) {
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
       }
     }
   }
-  if (tid == 0) s_base = m > 0 ? atomicAdd(s.desc_count, m) : 0;
+  if (tid == 0) s_base = m > 0 ? atomicAdd(sb.desc_count, m) : 0;
   __syncthreads();
 
   // 5. Reserve: new tags and last_step, gather descriptors (with the evicted
@@ -347,12 +348,17 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     const int32_t id = (int32_t)(key >> 32);
     const int cell = (int)(uint32_t)key;
     const int r = rank[i];
+    if (!AVSG_IN_BOUNDS(r >= 0 && r < m, s.err, u, i)) continue;
     const int v = victim[r];
+    if (!AVSG_IN_BOUNDS(v >= 0 && v < budget && cell >= 0 && cell < s.MS && id >= 0 &&
+                            id < io.live && s_base + r < s.U * s.max_union,
+                        s.err, u, i))
+      continue;
     const int32_t old = s.tag[ub + v];
     s.tag[ub + v] = id;
     s.last[ub + v] = t;
     s.mslot[(size_t)u * s.MS + cell] = v;
-    s.desc[s_base + r] = GatherDesc{u, id, v, old, cell, 0, 0, 0};
+    sb.desc[s_base + r] = GatherDesc{u, id, v, old, cell, 0, 0, 0};
   }
   __syncthreads();
 
@@ -371,15 +377,15 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
 #pragma unroll
     for (int e = 0; e < kRun; ++e) {
       const int p = c0 + e * kThreads + tid;
-      if (p < n && sm[e] <= -2)
+      if (p < n && sm[e] <= -2 && AVSG_IN_BOUNDS(-2 - sm[e] < s.MS, s.err, u, p))
         slot_map[(size_t)u * n + p] = s.mslot[(size_t)u * s.MS + (-2 - sm[e])];
     }
   }
 
   // 7. Statistics and this step's descriptor range (for the table update).
   if (tid == 0) {
-    s.dbase[u] = s_base;
-    s.dcount[u] = m;
+    sb.dbase[u] = s_base;
+    sb.dcount[u] = m;
     s.counters[u].hits += (unsigned long long)s_hits;
     s.counters[u].misses += (unsigned long long)m;
   }
@@ -403,12 +409,14 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
   }
   __syncthreads();
   if (s_stop) return;
-  const int m = s.dcount[u], base = s.dbase[u];
+  const StepBufs sb = step_bufs(s, load_io(s.io).parity);
+  const int m = sb.dcount[u], base = sb.dbase[u];
   int2* tab = s.htab + (size_t)u * s.HS;
   const uint32_t hmask = (uint32_t)s.HS - 1u;
   int freed = 0;
   for (int i = tid; i < m; i += kCommitThreads) {
-    const int32_t old = s.desc[base + i].old_id;
+    if (!AVSG_IN_BOUNDS(base + i < s.U * s.max_union, s.err, u, i)) continue;
+    const int32_t old = sb.desc[base + i].old_id;
     if (old != kEmpty) freed += hash_erase(tab, hmask, s.hs_shift, old);
   }
   freed = __reduce_add_sync(0xffffffffu, freed);
@@ -416,7 +424,10 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
   __syncthreads();
   int used = 0;
   for (int i = tid; i < m; i += kCommitThreads) {
-    const GatherDesc d = s.desc[base + i];
+    if (!AVSG_IN_BOUNDS(base + i < s.U * s.max_union, s.err, u, i)) continue;
+    const GatherDesc d = sb.desc[base + i];
+    if (!AVSG_IN_BOUNDS(d.slot >= 0 && d.slot < s.B && d.id >= 0 && d.id < s.L, s.err, u, i))
+      continue;
     used += hash_insert(tab, hmask, s.hs_shift, d.id, d.slot, s.err, u);
   }
   used = __reduce_add_sync(0xffffffffu, used);

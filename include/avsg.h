@@ -56,6 +56,7 @@ extern "C" {
 #define AVSG_ERR_BAD_STEP (-6)      /* t is negative or not larger than the previous step's t */
 #define AVSG_ERR_UNSUPPORTED (-7)   /* shape without a compiled attention kernel */
 #define AVSG_ERR_LATCHED (-8)       /* a device error is pending; call avsg_clear_error */
+#define AVSG_ERR_INTERNAL (-9)      /* device: an index check of the bounds-checked build failed */
 
 /* avsg_config.flags */
 #define AVSG_FLAG_NO_REUSE 1u /* no buffer reuse: copy every selected row every step */
