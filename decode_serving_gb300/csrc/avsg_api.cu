@@ -17,7 +17,6 @@ struct avsg_handle_s {
   DeviceState ds{};
   int device = 0, num_sms = 0, gather_ctas = 0, splits_cap = 0, target_ctas = 0, tile_rows = 0;
   int stage_ctas = 0;  // CTAs of the staged gather (it shares the GPU with the reservation)
-  int miss_splits = 1;
   void* dev_block = nullptr;
   size_t dev_bytes = 0;
   const void* host_k = nullptr;
@@ -58,6 +57,7 @@ struct avsg_handle_s {
   cudaEvent_t ev_fork = nullptr, ev_gather = nullptr, ev_reserve = nullptr, ev_commit = nullptr,
               ev_staged = nullptr, ev_place = nullptr, ev_hits = nullptr;
   bool staged = false;  // staging area allocated: the two-pass pipeline is available
+  bool by_request = false;  // staged gather assigned by request (AVSG_FLAG_REQUEST_GATHER)
   uint64_t seq = 0;     // steps enqueued since create/reset (their parity alternates)
   bool pending_place = false;  // the last step's staged rows await the place its next step runs
   bool overlap = false;  // steps run the two-pass pipeline
@@ -169,17 +169,6 @@ void release(avsg_handle h) {
   delete h;
 }
 
-// Miss-pass CTAs per (unit, token): each scans at most the shape's scan
-// limit of miss-set cells, and at least AVSG_MISS_SPLITS CTAs (default 1,
-// which lets that CTA merge the pair's partials itself).
-int miss_splits(const avsg_handle h) {
-  const DeviceState& s = h->ds;
-  const int scan = attention_tc_scan_max(s.D, s.G, s.kv_shared);
-  int sm = scan > 0 && s.MS > scan ? s.MS / scan : 1;
-  while (sm < h->miss_splits && s.MS / sm > 2) sm *= 2;
-  return sm;
-}
-
 // Splits of a (unit, token)'s entries over CTAs: about target_ctas CTAs in all,
 // each with at least one tile of rows.
 int attn_splits(const avsg_handle h, int n_tok, int k) {
@@ -255,6 +244,7 @@ int init_state(avsg_handle h, cudaStream_t st) {
   if (s.ev) AVSG_SET(s.vbuf, 0, (size_t)s.U * s.B * s.ev);
   if (!h->no_reuse) {
     AVSG_SET(s.tag, 0xFF, ub * 4);
+    AVSG_SET(s.pend, 0xFF, ub * 8);
     AVSG_SET(s.last, 0xFF, ub * 4);
     AVSG_SET(s.hitbits, 0, (size_t)s.U * s.HT * s.HW * 4);
     AVSG_SET(s.htab, 0xFF, (size_t)s.U * s.HS * sizeof(int2));
@@ -360,9 +350,8 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   h->gather_ctas = h->num_sms * env_int("AVSG_GATHER_CTAS_PER_SM", 4);
   // The staged gather splits all units' miss-set cells evenly over its CTAs;
   // with one CTA per request each CTA's range is exactly one request's units.
-  h->stage_ctas = (c.flags & AVSG_FLAG_REQUEST_GATHER) ? c.num_requests
-                                                       : env_int("AVSG_STAGE_CTAS", h->num_sms / 2);
-  h->miss_splits = env_int("AVSG_MISS_SPLITS", 1);  // at least this many miss-pass CTAs per pair
+  h->by_request = (c.flags & AVSG_FLAG_REQUEST_GATHER) != 0;
+  h->stage_ctas = h->by_request ? c.num_requests : env_int("AVSG_STAGE_CTAS", h->num_sms / 2);
   {
     int64_t cap = (h->target_ctas + U - 1) / U;
     const int64_t by_rows = ((int64_t)c.max_select * c.entry_tokens + h->tile_rows - 1) / h->tile_rows;
@@ -384,13 +373,25 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
 
   const bool st_arrays = !no_reuse;
   const size_t ub = st_arrays ? (size_t)U * s.B : 0;
-  Carver cv;
-  cv.take(&s.kbuf, (size_t)U * s.B * ek);
-  cv.take(&s.vbuf, (size_t)U * s.B * ev);
-  // staging rows for the two-pass pipeline (one per miss-set cell)
+  // staging rows for the two-pass pipeline (one per miss-set cell, a half per
+  // step parity), each right after its buffer: the buffer is padded to whole
+  // entries and 256 bytes, so a staged entry is also an entry index counted
+  // from kbuf (and from vbuf, at the same distance)
   h->staged = !no_reuse && (tc_shape || h16_shape);
-  cv.take(&s.kstage, h->staged ? 2 * (size_t)U * s.MS * ek : 0);  // a half per step parity
+  size_t unit = (size_t)ek;
+  while (unit % kAlign) unit += (size_t)ek;
+  const size_t kbuf_bytes = ((size_t)U * s.B * ek + unit - 1) / unit * unit;
+  Carver cv;
+  cv.take(&s.kbuf, kbuf_bytes);
+  cv.take(&s.kstage, h->staged ? 2 * (size_t)U * s.MS * ek : 0);
+  cv.take(&s.vbuf, ev ? kbuf_bytes : 0);
   cv.take(&s.vstage, h->staged ? 2 * (size_t)U * s.MS * ev : 0);
+  s.stage_entry0 = (int64_t)(kbuf_bytes / (size_t)ek);
+  s.deferred = 0;  // set below for the two-pass pipeline
+  if ((double)U * s.B + 2.0 * U * s.MS >= 2147483647.0) {
+    release(h);
+    return AVSG_ERR_INVALID_ARG;
+  }
   cv.take(&s.tag, ub);
   cv.take(&s.last, ub);
   cv.take(&s.hitbits, st_arrays ? (size_t)U * s.HT * s.HW : 0);
@@ -401,6 +402,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.mslot, st_arrays ? (size_t)U * s.MS : 0);
   cv.take(&s.desc, 2 * (size_t)U * max_union);
   cv.take(&s.desc_count, 2);
+  cv.take(&s.gather_next, 1);
   cv.take(&s.io, 1);
   cv.take(&s.qbuf, st_arrays ? (size_t)U * c.max_tokens_per_step * s.G * s.D : 0);
   cv.take(&s.dbase, 2 * (size_t)U);
@@ -413,19 +415,21 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     if (tc_shape)
       for (int nt = 1; nt <= c.max_tokens_per_step; ++nt) {
         const size_t need = attention_tc_two_pass_floats((int)U * nt, c.max_select, s.ET, s.G,
-                                                         s.DV, h->num_sms, miss_splits(h));
+                                                         s.DV, h->num_sms);
         two = need > two ? need : two;
       }
     h->part_floats = part > tc ? part : tc;
     h->part_floats = h->part_floats > two ? h->part_floats : two;
     h->overlap = h->staged && overlap_enabled() && (h16_shape || attention_tc_enabled());
     h->overlap_h16 = h->overlap && !tc_shape;
+    s.deferred = h->overlap && !h->overlap_h16 ? 1 : 0;
     cv.take(&s.part, h->part_floats);
   }
   cv.take(&s.part_count, (size_t)U * kMaxTokens * kCountsPerPair);
   cv.take(&s.counters, (size_t)U);
   cv.take(&s.err, 1);
   cv.take(&s.budget, (size_t)U);
+  cv.take(&s.pend, st_arrays ? (size_t)U * s.B : 0);
   cv.take(&h->budget_new, (size_t)U);
   cv.take(&h->slot_scratch, (size_t)U * max_union);
   cv.take(&h->hit_scratch, (size_t)U * max_union);
@@ -443,10 +447,11 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   rebase(&s.kstage, b); rebase(&s.vstage, b);
   rebase(&s.hitbits, b); rebase(&s.htab, b); rebase(&s.hused, b); rebase(&s.io, b); rebase(&s.qbuf, b);
   rebase(&s.mslot, b); rebase(&s.desc, b);
-  rebase(&s.desc_count, b); rebase(&s.part, b);
+  rebase(&s.desc_count, b); rebase(&s.gather_next, b); rebase(&s.part, b);
   rebase(&s.dbase, b); rebase(&s.dcount, b); rebase(&s.mset, b); rebase(&s.hslot, b);
   rebase(&s.part_count, b);
   rebase(&s.counters, b); rebase(&s.err, b); rebase(&s.budget, b); rebase(&h->budget_new, b);
+  rebase(&s.pend, b);
   rebase(&h->slot_scratch, b); rebase(&h->hit_scratch, b); rebase(&h->stage_sel, b);
   rebase(&h->stage_q, b); rebase(&h->stage_out, b);
   if (shared) {
@@ -627,7 +632,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_fork, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_fork, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
-    AVSG_RUN(AVSG_KERNEL_GATHER, side, launch_gather_stage(sc, h->stage_ctas, side));
+    AVSG_RUN(AVSG_KERNEL_GATHER, side, launch_gather_stage(sc, h->stage_ctas, h->by_request, side));
     e = cudaEventRecord(h->ev_staged, side);
     if (e != cudaSuccess) return fail_cuda(h, e);
     AVSG_RUN(AVSG_KERNEL_ATTENTION, side, launch_attention(sc, a, side));
@@ -652,51 +657,43 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   //   side3:  the rows the previous step staged, into the slots its
   //           reservation gave them (the deferred place: off the previous
   //           step's critical path, beside this step's link-bound gather);
-  //   st:     once they are in place, attention over the hit rows;
+  //   st:     attention over the hit rows (a hit on a row the previous step
+  //           loaded reads its staged copy: match points it there);
   //   side:   the missed rows, host -> this step's half of the staging area
-  //           (host link), then the attention over them;
+  //           (host link), then the attention over them, which also merges
+  //           both passes into the output (it waits for the hit pass);
   //   side2:  the reservation, then the hash-table update.
-  // With one miss-pass CTA per (unit, token) that CTA merges the two passes'
-  // partials into the output; otherwise a finish kernel does.  This step's
-  // staged rows reach their slots early in the next step (or when an entry
-  // point that reads the buffer flushes them).
-  const int splits_m = miss_splits(h);
-  const bool fused = splits_m == 1;
+  // This step's staged rows reach their slots early in the next step (or
+  // when an entry point that reads the buffer flushes them).
   e = cudaEventRecord(h->ev_fork, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_fork, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_fork, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side3, h->ev_fork, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  DeviceState staged = sc;  // miss rows are read from the staging area, by cell
-  staged.kbuf = s.kstage;
-  staged.vbuf = s.vstage;
-  staged.B = s.MS;
-  // Launched in this order, so the gather's CTAs are placed first (on SMs of
-  // their own), then the reservation's, then the place and the hit pass.
-  AVSG_RUN(AVSG_KERNEL_GATHER, side, launch_gather_stage(sc, h->stage_ctas, side));
+  // Launched in this order, so the CTAs of the kernels the miss pass needs
+  // are placed first: the gather's (on SMs of their own), the reservation's,
+  // the hit pass's; then the hash update and, on the lowest-priority stream,
+  // the place, which only has to end with the step.
+  AVSG_RUN(AVSG_KERNEL_GATHER, side, launch_gather_stage(sc, h->stage_ctas, h->by_request, side));
   AVSG_RUN(AVSG_KERNEL_RESERVE, side2, launch_victims(sc, n_tok, k, side2));
   e = cudaEventRecord(h->ev_reserve, side2);
+  if (e != cudaSuccess) return fail_cuda(h, e);
+  AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, st));
+  e = cudaEventRecord(h->ev_hits, st);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
   e = cudaEventRecord(h->ev_commit, side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_PLACE, side3, launch_place(sc, 1, side3));
   e = cudaEventRecord(h->ev_place, side3);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_place, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_hits, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_reserve, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, splits_m, st));
-  e = cudaEventRecord(h->ev_hits, st);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  if (fused) e = cudaStreamWaitEvent(side, h->ev_hits, 0);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, side,
-           launch_attention_tc_pass(staged, a, 1, splits_m, side));
+  AVSG_RUN(AVSG_KERNEL_ATTENTION_MISS, side, launch_attention_tc_pass(sc, a, 1, side));
   e = cudaEventRecord(h->ev_gather, side);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_gather, 0);
-  if (e != cudaSuccess) return fail_cuda(h, e);
-  if (!fused)
-    AVSG_RUN(AVSG_KERNEL_FINISH, st, launch_attention_tc_finish(sc, a, splits_m, st));
-  e = cudaStreamWaitEvent(st, h->ev_commit, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_commit, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_place, 0);
   if (e != cudaSuccess) return fail_cuda(h, e);
 #undef AVSG_RUN
   return AVSG_OK;
@@ -767,6 +764,7 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
   }
   if (h->no_reuse) h->host_misses += (uint64_t)s.U * n_tok * k;
   StepIO v{};
+  v.seq = (uint32_t)h->seq;
   v.parity = (int32_t)(h->seq & 1);
   h->seq += 1;
   // the two-pass pipeline leaves this step's staged rows to the next step

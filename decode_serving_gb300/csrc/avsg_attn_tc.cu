@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "avsg_internal.cuh"
 
 namespace avsg {
@@ -43,13 +45,6 @@ constexpr int kThreadsTc = kWarpsTc * 32;
 constexpr int kTileRows = 16;
 constexpr int kStages = 3;
 constexpr int kCtasPerSm = 2;
-constexpr int kScanMax = kMissScanMax;          // miss-set cells one miss-pass CTA scans
-
-constexpr int pow2_floor_capped(int x, int cap) {
-  int q = 1;
-  while (q * 2 <= x && q * 2 <= cap) q *= 2;
-  return q;
-}
 
 template <int D_, int G_, bool SHARED_>
 struct TcShape {
@@ -71,9 +66,6 @@ struct TcShape {
   // Most partials one merge takes: the four warps' outputs, the CTA's own
   // and 2 floats per partial and head must fit in the warps' staging.
   static constexpr int MAX_SEG = (kWarpsTc * WARP_BYTES / 4 - (kWarpsTc + 1) * G * D) / (2 * G);
-  // Most miss-set cells one miss-pass CTA scans: they are staged in the tile
-  // staging (8 bytes each); a power of two, at most kScanMax.
-  static constexpr int SCAN_MAX = pow2_floor_capped(kWarpsTc * WARP_BYTES / 8, kScanMax);
   static_assert(MAX_SEG >= 16, "merge scratch");
 };
 
@@ -150,11 +142,8 @@ struct TcParams {
   long long tiles;              // all pairs
   int ctas, max_seg;
   // two passes: the hit pass is persistent (hit_ctas CTAs over all pairs'
-  // tiles, like the single pass), the miss pass has splits_m CTAs per pair
-  int hit_ctas, splits_m;
-  // with one miss-pass CTA per pair, that CTA merges the pair's partials
-  // into the output
-  int fuse_finish;
+  // tiles, like the single pass)
+  int hit_ctas;
 };
 
 struct SegArgs {
@@ -237,7 +226,11 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
                    : p.identity ? tok * p.k + ent
                                 : __ldg(p.slots + (size_t)pair * p.k + ent);
     if (slot < 0) return -1;  // not a row of this pass (a miss in the pass over hit rows)
-    if (!AVSG_IN_BOUNDS(slot < s.B, s.err, u, ent)) return -1;
+    // (a slot of B or more is a row still staged by the previous step)
+    if (!AVSG_IN_BOUNDS(slot < s.B || (s.deferred && (long long)u * s.B + slot >= s.stage_entry0 &&
+                                       (long long)u * s.B + slot < s.stage_entry0 + 2LL * s.U * s.MS),
+                        s.err, u, ent))
+      return -1;
     return ((long long)u * s.B + slot) * p.ET + sub;
   };
   constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
@@ -475,6 +468,330 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
   __syncthreads();
 }
 
+// The union of NT query tokens of a multi-token step: one pass over the rows
+// the NT tokens selected together, every row staged once and attended by the
+// query heads of each token that selected it (bit j of masks[e], the token
+// bits of entry e; for the other tokens the row is masked).  Same tiles,
+// pipeline and MMA layout as tc_segment, with NT sets of q fragments (q of
+// token j at qs + j * G * D), softmax state and accumulators; the K and V
+// fragments of a tile are loaded once for all tokens.  Per-warp shared
+// memory: the stages, then NT P tiles.  Results, in shared memory: cm[j * G
+// + h], cl[j * G + h], co[(j * G + h) * D + d].
+template <class SH, int NT>
+__device__ void tc_segment_union(const DeviceState& s, const TcParams& p, const SegArgs& a,
+                                 const uint8_t* masks, unsigned char* smem, float* cm, float* cl,
+                                 float* co, float (*s_m)[NT * SH::G],
+                                 float (*s_l)[NT * SH::G]) {
+  constexpr int D = SH::D, G = SH::G, NTN = SH::NTN, KS = SH::KS, MT = SH::MT;
+  constexpr int PITCH = SH::PITCH;
+  constexpr int NH = G == 1 ? 1 : 2;              // heads per thread
+  constexpr int OWNERS = G >= 2 ? G / 2 : 1;      // lanes c < OWNERS own their heads
+  constexpr int WB = kStages * SH::STAGE_BYTES + NT * SH::PTILE_BYTES;
+  static_assert(NT * 16 <= 64, "token row masks of a stage fit 64 bits");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int head_base = G == 1 ? 0 : 2 * (c % OWNERS);
+  const bool owner = c < OWNERS;
+  unsigned char* wbase = smem + warp * WB;
+  unsigned char* ptile0 = wbase + kStages * SH::STAGE_BYTES;
+  const int u = a.u;
+
+  float m[NT][NH], l[NT][NH];
+  float acc[NT][MT][NTN][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      m[j][h] = -INFINITY;
+      l[j][h] = 0.f;
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[j][mt][nt][i] = 0.f;
+  }
+
+  const int n_my = a.tb - a.ta - warp > 0 ? (a.tb - a.ta - warp + kWarpsTc - 1) / kWarpsTc : 0;
+  // Buffer row of row (lane & 15) of this warp's i-th tile (or -1) and its token bits.
+  auto row_index = [&](int i, uint32_t& tok_bits) -> long long {
+    tok_bits = 0u;
+    const int row = (a.ta + warp + i * kWarpsTc) * kTileRows + (lane & 15);
+    if (i >= n_my || row >= a.rows) return -1;
+    const int ent = a.ent_base + (p.ET == 1 ? row : row / p.ET);
+    const int sub = row - (ent - a.ent_base) * p.ET;
+    const int slot = a.list[ent];
+    if (slot < 0 || !AVSG_IN_BOUNDS(slot < s.B, s.err, u, ent)) return -1;
+    tok_bits = masks[ent];
+    return ((long long)u * s.B + slot) * p.ET + sub;
+  };
+  constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
+  constexpr int RPI = 32 / CPR;    // rows per warp instruction
+  // Per stage: bits [16 j, 16 j + 16) mark the tile's rows token j selected.
+  unsigned long long tm0 = 0, tm1 = 0, tm2 = 0;
+  static_assert(kStages == 3, "three stage masks");
+  auto issue = [&](long long myrow, uint32_t mybits, int st) {
+    unsigned long long tm = 0;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+      tm |= (unsigned long long)(__ballot_sync(0xffffffffu, myrow >= 0 && ((mybits >> j) & 1u)) &
+                                 0xFFFFu)
+            << (16 * j);
+    if (st == 0) tm0 = tm; else if (st == 1) tm1 = tm; else tm2 = tm;
+    unsigned char* kst = wbase + st * SH::STAGE_BYTES;
+    unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
+    const int ch = lane % CPR, rsub = lane / CPR;
+#pragma unroll
+    for (int it = 0; it < kTileRows / RPI; ++it) {
+      const int r = it * RPI + rsub;
+      const long long srow = __shfl_sync(0xffffffffu, myrow, r);
+      if (srow >= 0) {
+        cp_async16(kst + r * PITCH + ch * 16, s.kbuf + srow * (2 * D) + ch * 16);
+        if (!SH::SHARED) cp_async16(vst + r * PITCH + ch * 16, s.vbuf + srow * (2 * D) + ch * 16);
+      } else {
+        *reinterpret_cast<uint4*>(kst + r * PITCH + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+        if (!SH::SHARED) *reinterpret_cast<uint4*>(vst + r * PITCH + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    cp_async_commit();
+  };
+
+  long long next_row;
+  uint32_t next_bits;
+  {
+    long long first_rows[kStages + 1];
+    uint32_t first_bits[kStages + 1];
+#pragma unroll
+    for (int i = 0; i <= kStages; ++i) first_rows[i] = row_index(i, first_bits[i]);
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) issue(first_rows[i], first_bits[i], i);
+    next_row = first_rows[kStages];
+    next_bits = first_bits[kStages];
+  }
+  // q fragments of every token: column n < G is hi(q_n), G <= n < 2G is lo(q_{n-G})
+  uint32_t qb[NT][KS][NTN][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) {
+      const int col = g + 8 * nt;
+      const int head = col < G ? col : col - G;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint16_t e[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int d = 16 * ks + 2 * c + (i & 1) + 8 * (i >> 1);
+          uint16_t hi = 0, lo = 0;
+          if (col < 2 * G) split_bf16(a.qs[(j * G + head) * D + d] * p.scale_log2, hi, lo);
+          e[i] = col < G ? hi : lo;
+        }
+        qb[j][ks][nt][0] = pack2(e[0], e[1]);
+        qb[j][ks][nt][1] = pack2(e[2], e[3]);
+      }
+    }
+
+  for (int i = 0; i < n_my; ++i) {
+    const int st = i % kStages;
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const unsigned long long tm = st == 0 ? tm0 : st == 1 ? tm1 : tm2;
+    const unsigned char* kst = wbase + st * SH::STAGE_BYTES;
+    const unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
+    const uint32_t kaddr = smem_u32(kst), vaddr = smem_u32(vst);
+
+    // scores^T of every token; K fragments loaded once per k-step
+    float sc[NT][NTN][4], sc2[NT][NTN][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) sc[j][nt][i2] = sc2[j][nt][i2] = 0.f;
+    {
+      const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int acol = (lane >> 4) * 8;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kaddr + arow * PITCH + (16 * ks + acol) * 2, a0, a1, a2, a3);
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int nt = 0; nt < NTN; ++nt)
+            mma_bf16((ks & 1) ? sc2[j][nt] : sc[j][nt], a0, a1, a2, a3, qb[j][ks][nt][0],
+                     qb[j][ks][nt][1]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) sc[j][nt][i2] += sc2[j][nt][i2];
+      float sv[2][2];
+      if (G == 8) {
+        sv[0][0] = sc[j][0][0] + sc[j][NTN - 1][0];
+        sv[0][1] = sc[j][0][1] + sc[j][NTN - 1][1];
+        sv[1][0] = sc[j][0][2] + sc[j][NTN - 1][2];
+        sv[1][1] = sc[j][0][3] + sc[j][NTN - 1][3];
+      } else if (G == 1) {
+        sv[0][0] = sc[j][0][0] + sc[j][0][1];
+        sv[1][0] = sc[j][0][2] + sc[j][0][3];
+        sv[0][1] = sv[1][1] = -INFINITY;
+      } else {
+        const int xm = G / 2;
+        sv[0][0] = sc[j][0][0] + __shfl_xor_sync(0xffffffffu, sc[j][0][0], xm);
+        sv[0][1] = sc[j][0][1] + __shfl_xor_sync(0xffffffffu, sc[j][0][1], xm);
+        sv[1][0] = sc[j][0][2] + __shfl_xor_sync(0xffffffffu, sc[j][0][2], xm);
+        sv[1][1] = sc[j][0][3] + __shfl_xor_sync(0xffffffffu, sc[j][0][3], xm);
+      }
+      const unsigned vmask = (unsigned)(tm >> (16 * j)) & 0xFFFFu;  // rows token j selected
+      if (!((vmask >> g) & 1u)) sv[0][0] = sv[0][1] = -INFINITY;
+      if (!((vmask >> (g + 8)) & 1u)) sv[1][0] = sv[1][1] = -INFINITY;
+
+      float pv[2][2], alpha[2] = {1.f, 1.f};
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        float mx = fmaxf(sv[0][h], sv[1][h]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(m[j][h], mx);
+        float p0 = 0.f, p1 = 0.f;
+        if (m_new != -INFINITY) {
+          alpha[h] = exp2f(m[j][h] - m_new);
+          p0 = exp2f(sv[0][h] - m_new);
+          p1 = exp2f(sv[1][h] - m_new);
+        }
+        float sum = p0 + p1;
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+        l[j][h] = l[j][h] * alpha[h] + sum;
+        m[j][h] = m_new;
+        pv[0][h] = p0;
+        pv[1][h] = p1;
+      }
+      if (NH == 1) alpha[1] = alpha[0];
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NTN; ++nt) {
+            acc[j][mt][nt][0] *= alpha[0];
+            acc[j][mt][nt][1] *= alpha[1];
+            acc[j][mt][nt][2] *= alpha[0];
+            acc[j][mt][nt][3] *= alpha[1];
+          }
+      }
+      unsigned char* ptile = ptile0 + j * SH::PTILE_BYTES;
+      if (owner) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int rr = g + 8 * h;
+          uint16_t hi0, lo0, hi1 = 0, lo1 = 0;
+          split_bf16(pv[h][0], hi0, lo0);
+          if (NH == 2) split_bf16(pv[h][1], hi1, lo1);
+          if (G == 1) {
+            *reinterpret_cast<uint32_t*>(ptile + rr * 16) = pack2(hi0, lo0);
+          } else {
+            const int chi = head_base, clo = G + head_base;
+            *reinterpret_cast<uint32_t*>(ptile + (chi >> 3) * 256 + rr * 16 + (chi & 7) * 2) =
+                pack2(hi0, hi1);
+            *reinterpret_cast<uint32_t*>(ptile + (clo >> 3) * 256 + rr * 16 + (clo & 7) * 2) =
+                pack2(lo0, lo1);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    uint32_t pb[NT][NTN][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int nt = 0; nt < NTN; ++nt)
+        ldsm_x2_t(smem_u32(ptile0 + j * SH::PTILE_BYTES + nt * 256 + (lane & 15) * 16), pb[j][nt][0],
+                  pb[j][nt][1]);
+    {
+      const int vrow = (lane & 7) + ((lane >> 4) << 3);
+      const int vcol = ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vaddr + vrow * PITCH + (16 * mt + vcol) * 2, a0, a1, a2, a3);
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int nt = 0; nt < NTN; ++nt)
+            mma_bf16(acc[j][mt][nt], a0, a1, a2, a3, pb[j][nt][0], pb[j][nt][1]);
+      }
+    }
+    __syncwarp();  // every lane has read stage st and the P tiles
+    issue(next_row, next_bits, st);
+    next_row = row_index(i + kStages + 1, next_bits);
+  }
+  cp_async_wait<0>();
+
+  // Per-warp results -> shared memory [warp][token][head][D], then merge the 4 warps.
+  __syncthreads();
+  float* mo = reinterpret_cast<float*>(smem);
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int dv = 16 * mt + g + 8 * (i >> 1);
+        float v;
+        int head;
+        if (G == 8) {
+          v = acc[j][mt][0][i] + acc[j][mt][NTN - 1][i];
+          head = 2 * c + (i & 1);
+        } else if (G == 1) {
+          v = (i & 1) ? 0.f : acc[j][mt][0][i] + acc[j][mt][0][i + 1];
+          head = 0;
+        } else {
+          v = acc[j][mt][0][i] + __shfl_xor_sync(0xffffffffu, acc[j][mt][0][i], G / 2);
+          head = head_base + (i & 1);
+        }
+        if (owner && (G != 1 || (i & 1) == 0)) mo[((warp * NT + j) * G + head) * D + dv] = v;
+      }
+  if (owner && g == 0) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        s_m[warp][j * G + head_base + h] = m[j][h];
+        s_l[warp][j * G + head_base + h] = l[j][h];
+      }
+  }
+  __syncthreads();
+  if (tid < NT * G) {
+    float M = -INFINITY, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarpsTc; ++w) M = fmaxf(M, s_m[w][tid]);
+    if (M != -INFINITY)
+#pragma unroll
+      for (int w = 0; w < kWarpsTc; ++w) L = fmaf(s_l[w][tid], exp2f(s_m[w][tid] - M), L);
+    cm[tid] = M;
+    cl[tid] = L;
+  }
+  __syncthreads();
+  for (int o = tid; o < NT * G * D; o += kThreadsTc) {
+    const int jh = o / D;  // token * G + head
+    const float M = cm[jh];
+    float O = 0.f;
+    if (M != -INFINITY)
+#pragma unroll
+      for (int w = 0; w < kWarpsTc; ++w)
+        O = fmaf(mo[(w * NT * G + jh) * D + (o - jh * D)], exp2f(s_m[w][jh] - M), O);
+    co[o] = O;
+  }
+  __syncthreads();
+}
+
 // Writes this CTA's segment result as partial `idx` of a pair.
 template <int G, int D>
 __device__ __forceinline__ void tc_write_partial(float* pp, const float* cm, const float* cl,
@@ -486,12 +803,13 @@ __device__ __forceinline__ void tc_write_partial(float* pp, const float* cm, con
   }
 }
 
-// Merges nseg partials of a pair into its output (run by one CTA); partial
-// q2 starts at part_at(q2).  Every partial's (m, l) and the first QB
-// partials' output rows are loaded at once; later partials take one more
-// round of loads per QB.  wseg: 2 * nseg * G floats of shared memory.
-template <int G, int D, class PartAt>
-__device__ void tc_merge_partials(PartAt part_at, int nseg, float* out, float* wseg) {
+// Merges nseg partials of a pair into its output (run by one CTA); value i
+// of partial q2 (m of head h at i = h, l at G + h, output o at 2G + o) is
+// part(q2, i).  Every partial's (m, l) and the first QB partials' output rows
+// are loaded at once; later partials take one more round of loads per QB.
+// wseg: 2 * nseg * G floats of shared memory.
+template <int G, int D, class Part>
+__device__ void tc_merge_partials(Part part, int nseg, float* out, float* wseg) {
   constexpr int R = (G * D + kThreadsTc - 1) / kThreadsTc;  // outputs per thread
   constexpr int QB = 8;                                     // partials per round of loads
   const int tid = threadIdx.x;
@@ -499,8 +817,8 @@ __device__ void tc_merge_partials(PartAt part_at, int nseg, float* out, float* w
   float* wl = wseg + nseg * G;  // [nseg][G]: l
   for (int i = tid; i < nseg * G; i += kThreadsTc) {
     const int q2 = i / G, h = i - q2 * G;
-    wm[i] = __ldcg(part_at(q2) + h);
-    wl[i] = __ldcg(part_at(q2) + G + h);
+    wm[i] = part(q2, h);
+    wl[i] = part(q2, G + h);
   }
   float v[QB][R];
   auto load_round = [&](int q0) {
@@ -509,7 +827,7 @@ __device__ void tc_merge_partials(PartAt part_at, int nseg, float* out, float* w
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int o = tid + r * kThreadsTc;
-        v[j][r] = (q0 + j < nseg && o < G * D) ? __ldcg(part_at(q0 + j) + 2 * G + o) : 0.f;
+        v[j][r] = (q0 + j < nseg && o < G * D) ? part(q0 + j, 2 * G + o) : 0.f;
       }
   };
   load_round(0);
@@ -618,7 +936,9 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
         const size_t slot0 = 2 * (size_t)first + ((long long)first * T / C == pair_t0 ? 0 : 1);
         const float* part = s.part;
         tc_merge_partials<G, D>(
-            [&](int q2) { return part + (q2 == 0 ? slot0 : 2 * (size_t)(first + q2)) * stride; },
+            [&](int q2, int i) {
+              return __ldcg(part + (q2 == 0 ? slot0 : 2 * (size_t)(first + q2)) * stride + i);
+            },
             nseg, out, co + G * D);
         if (tid == 0) s.part_count[a.u * kMaxTokens + a.tok] = 0;
       }
@@ -627,11 +947,11 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_kernel(DeviceState s, TcPa
   }
 }
 
-// Partials of the two-pass attention, G * (D + 2) floats each, in three
-// groups: [pairs] the hit-pass partial of a pair one CTA covered whole;
-// [2 * hit_ctas] the hit-pass partials of the pairs a CTA cut (its first and
-// its last segment, as in the single pass); [pairs][splits_m] the miss-pass
-// partials.
+// Hit-pass partials of the two-pass attention, G * (D + 2) floats each, in
+// two groups: [pairs] the partial of a pair one CTA covered whole;
+// [2 * hit_ctas] the partials of the pairs a CTA cut (its first and its last
+// segment, as in the single pass).  The miss pass merges them with its own
+// result, which never leaves its shared memory.
 __device__ __forceinline__ int hit_segments(const TcParams& p, int pair, long long* slot0) {
   const long long T = p.tiles, t0 = (long long)pair * p.tiles_per_pair;
   const int C = p.hit_ctas;
@@ -640,12 +960,11 @@ __device__ __forceinline__ int hit_segments(const TcParams& p, int pair, long lo
   *slot0 = first == last ? pair : pairs + 2LL * first + ((long long)first * T / C == t0 ? 0 : 1);
   return last - first + 1;
 }
-// Slot of a pair's partial q2: its hit-pass partials first, then its
-// splits_m miss-pass partials.
+// Slot of a pair's hit-pass partial q2 (q2 < its hit_segments).
 __device__ __forceinline__ long long two_pass_slot(const TcParams& p, int pair, int nseg_h,
                                                    long long slot0, int q2) {
+  (void)nseg_h;
   const long long pairs = p.tiles / p.tiles_per_pair;
-  if (q2 >= nseg_h) return pairs + 2LL * p.hit_ctas + (long long)pair * p.splits_m + (q2 - nseg_h);
   if (q2 == 0) return slot0;
   const int first = (int)((slot0 - pairs) >> 1);
   return pairs + 2LL * (first + q2);
@@ -667,10 +986,12 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_hits_kernel(DeviceState s,
   __shared__ int s_stop;
   const int tid = threadIdx.x;
   griddep_wait();
-  griddep_launch();
   if (tid == 0) s_stop = load_err(s.err);
   __syncthreads();
-  if (s_stop) return;
+  if (s_stop) {
+    griddep_launch();
+    return;
+  }
   float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
   const long long T = p.tiles, pairs = T / p.tiles_per_pair;
   const int C = p.hit_ctas;
@@ -704,146 +1025,163 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_hits_kernel(DeviceState s,
     tc_write_partial<G, D>(s.part + (size_t)slot * stride, cm, cl, co);
     __syncthreads();  // the staging (and s_q) is reused by the next segment
   }
+  griddep_launch();  // dependents launch as this pass ends, not while it needs the SMs
 }
 
-// Miss pass: CTA (sp, pair) copies its range of the unit's miss set into
-// shared memory (one round of 16-byte async copies), lists the claimed cells
-// that carry this token (a fixed order: by thread, then by stride), attends
-// over their rows in this step's half of the staging area and writes its
-// miss-pass partial sp of the pair.  It follows the staged gather on the same
-// stream: the list is built while the gather's last copies drain, and the
-// rows are read after the grid-dependency wait (which, with one CTA per
-// pair, also covers the hit pass: that CTA then merges the pair's partials
-// into the output).  The rows reach their slots later, in the place that
-// the next step runs early.  `s` is the staged view of the state: kbuf/vbuf
-// are the staging area's first half and B the miss-set capacity.
-template <class SH>
+// Miss pass: the rows this step copied from host into its half of the
+// staging area, attended once the gather is done.  The list comes from the
+// reservation's descriptors of the unit (each with the row's miss-set cell
+// and the bits of the tokens that selected it), in chunks of kMissChunk
+// entries whose results are merged as they come.  NT == 1: CTA = one (unit,
+// token), over the unit's misses that token selected.  NT > 1 (a step of NT
+// query tokens): CTA = one unit, over the union of its misses, each row
+// attended by the tokens that selected it (tc_segment_union).  The CTA then
+// writes the pair's (pairs') miss partial and merges it with the hit pass's
+// into the output: the grid-dependency wait covers the gather, and the launch
+// follows the reservation and the hit pass.  `s` is the real state.
+constexpr int kMissChunk = 512;
+
+template <class SH, int NT>
+struct MissSmem {
+  static constexpr int WB = kStages * SH::STAGE_BYTES + NT * SH::PTILE_BYTES;  // per warp
+  static constexpr int LIST = kWarpsTc * WB;                                  // [kMissChunk] cells
+  static constexpr int MASKS = LIST + kMissChunk * 4;                         // [kMissChunk] bits
+  static constexpr int RUN = MASKS + (NT > 1 ? kMissChunk : 0);                // [NT][G][D]
+  static constexpr int BYTES = RUN + NT * SH::G * SH::D * 4 + 128;
+  static_assert(kWarpsTc * NT * SH::G * SH::D * 4 + NT * SH::G * SH::D * 4 <= kWarpsTc * WB,
+                "per-warp results and the segment result fit the staging");
+  static_assert(MASKS % 16 == 0 && RUN % 16 == 0, "alignment");
+};
+
+template <class SH, int NT>
 __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s, TcParams p) {
   constexpr int D = SH::D, G = SH::G;
+  using L = MissSmem<SH, NT>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
-  // The range's cells are staged in the warps' tile staging (free until the
-  // first tile is issued); the list follows the staging.
-  unsigned long long* cells = reinterpret_cast<unsigned long long*>(smem);           // [span]
-  int32_t* list = reinterpret_cast<int32_t*>(smem + kWarpsTc * SH::WARP_BYTES);       // [span]
-  __shared__ float s_m[kWarpsTc][G], s_l[kWarpsTc][G], cm[G], cl[G];
-  __shared__ __align__(16) float s_q[G * D];
+  int32_t* list = reinterpret_cast<int32_t*>(smem + L::LIST);
+  uint8_t* masks = smem + L::MASKS;
+  float* run_o = reinterpret_cast<float*>(smem + L::RUN);
+  __shared__ float s_m[kWarpsTc][NT * G], s_l[kWarpsTc][NT * G], cm[NT * G], cl[NT * G];
+  __shared__ float run_m[NT * G], run_l[NT * G], wa[NT * G], wb[NT * G];
+  __shared__ __align__(16) float s_q[NT * G * D];
   __shared__ int s_stop, s_wsum[kWarpsTc];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int sp = blockIdx.x, pair = blockIdx.y;
-  const int u = pair / p.n_tok, tok = pair - u * p.n_tok;
-  const int span = s.MS / p.splits_m;  // both powers of two, span <= SH::SCAN_MAX
-  const int c_lo = sp * span;
-  // The miss set and the q copy were written by match, which completed before
-  // the gather began: they are read before the wait on the gather.
-  {  // the range of the miss set, and q, in one group
-    const unsigned long long* src = s.mset + (size_t)u * s.MS + c_lo;
-    for (int i = tid; i < span / 2; i += kThreadsTc) cp_async16(cells + 2 * i, src + 2 * i);
-    for (int i = tid; i < G * D / 4; i += kThreadsTc) cp_async16(s_q + 4 * i, p.q + (size_t)pair * G * D + 4 * i);
-    cp_async_commit();
+  const int u = NT == 1 ? (int)blockIdx.y / p.n_tok : (int)blockIdx.y;
+  const int tok0 = NT == 1 ? (int)blockIdx.y - u * p.n_tok : 0;
+  // q of the CTA's token(s): match wrote it before the gather began
+  for (int i = tid; i < NT * G * D / 4; i += kThreadsTc)
+    cp_async16(s_q + 4 * i, p.q + ((size_t)u * p.n_tok + tok0) * G * D + 4 * i);
+  cp_async_commit();
+  for (int i = tid; i < NT * G; i += kThreadsTc) {
+    run_m[i] = -INFINITY;
+    run_l[i] = 0.f;
   }
-  cp_async_wait<0>();
-  __syncthreads();
-
-  // cells tid, tid + 128, ... of the range: those carrying this token, in a
-  // fixed order (thread, then stride)
-  const unsigned long long tokbit = 1ull << (32 + tok);
-  int cnt = 0;
-  for (int c0 = tid; c0 < span; c0 += 8 * kThreadsTc) {
-    unsigned long long w[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = c0 + j * kThreadsTc;
-      w[j] = c < span ? cells[c] : kMissEmpty;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) cnt += (w[j] != kMissEmpty && (w[j] & tokbit)) ? 1 : 0;
-  }
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) s_wsum[warp] = incl;
-  __syncthreads();
-  int base = incl - cnt, nlist = 0;
-#pragma unroll
-  for (int w2 = 0; w2 < kWarpsTc; ++w2) {
-    base += w2 < warp ? s_wsum[w2] : 0;
-    nlist += s_wsum[w2];
-  }
-  for (int c0 = tid; c0 < span; c0 += 8 * kThreadsTc) {
-    unsigned long long w[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = c0 + j * kThreadsTc;
-      w[j] = c < span ? cells[c] : kMissEmpty;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (w[j] != kMissEmpty && (w[j] & tokbit)) list[base++] = c_lo + c0 + j * kThreadsTc;
-  }
-  __syncthreads();
+  for (int i = tid; i < NT * G * D; i += kThreadsTc) run_o[i] = 0.f;
   griddep_wait();  // the gather's rows are in the staging area
   griddep_launch();
   if (tid == 0) s_stop = load_err(s.err);
-  {  // this step's half of the staging area
-    const StepBufs sb = step_bufs(s, load_io(s.io).parity);
-    s.kbuf = sb.kstage;
-    s.vbuf = sb.vstage;
+  cp_async_wait<0>();
+  __syncthreads();
+  if (s_stop) return;
+  const StepIO io = load_io(s.io);
+  const StepBufs sb = step_bufs(s, io.parity);
+  DeviceState sv = s;  // the staged view: rows by miss-set cell in this step's half
+  sv.kbuf = sb.kstage;
+  sv.vbuf = sb.vstage;
+  sv.B = s.MS;
+  const int m = __ldcg(sb.dcount + u), base = __ldcg(sb.dbase + u);
+  const GatherDesc* desc = sb.desc + base;
+  float* co = reinterpret_cast<float*>(smem) + kWarpsTc * NT * G * D;
+
+  for (int c0 = 0; c0 < m; c0 += kMissChunk) {
+    const int cn = min(kMissChunk, m - c0);
+    int nlist = cn;
+    if (NT == 1) {
+      // the chunk's entries this token selected, in descriptor order
+      const uint32_t tokbit = 1u << tok0;
+      constexpr int kPer = kMissChunk / kThreadsTc;
+      int2 e[kPer];
+      int cnt = 0;
+#pragma unroll
+      for (int r = 0; r < kPer; ++r) {
+        const int i = tid * kPer + r;
+        e[r] = i < cn ? __ldcg(reinterpret_cast<const int2*>(&desc[c0 + i].cell)) : make_int2(-1, 0);
+        cnt += ((uint32_t)e[r].y & tokbit) ? 1 : 0;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) s_wsum[warp] = incl;
+      __syncthreads();
+      int pos = incl - cnt;
+      nlist = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarpsTc; ++w2) {
+        pos += w2 < warp ? s_wsum[w2] : 0;
+        nlist += s_wsum[w2];
+      }
+#pragma unroll
+      for (int r = 0; r < kPer; ++r)
+        if ((uint32_t)e[r].y & tokbit) list[pos++] = e[r].x;
+    } else {
+      for (int i = tid; i < cn; i += kThreadsTc) {
+        const int2 e = __ldcg(reinterpret_cast<const int2*>(&desc[c0 + i].cell));
+        list[i] = e.x;
+        masks[i] = (uint8_t)e.y;
+      }
+    }
+    __syncthreads();
+    SegArgs a;
+    a.pair = u * p.n_tok + tok0;
+    a.u = u;
+    a.tok = tok0;
+    a.ent_base = 0;
+    a.list = list;
+    a.qs = s_q;
+    a.rows = nlist * p.ET;
+    a.ta = 0;
+    a.tb = (a.rows + kTileRows - 1) / kTileRows;
+    if constexpr (NT == 1)
+      tc_segment<SH>(sv, p, a, smem, cm, cl, co, s_m, s_l);
+    else
+      tc_segment_union<SH, NT>(sv, p, a, masks, smem, cm, cl, co, s_m, s_l);
+    // fold the chunk's result into the running one
+    if (tid < NT * G) {
+      const float M = fmaxf(run_m[tid], cm[tid]);
+      const float x = M == -INFINITY ? 0.f : exp2f(run_m[tid] - M);
+      const float y = M == -INFINITY ? 0.f : exp2f(cm[tid] - M);
+      run_l[tid] = run_l[tid] * x + cl[tid] * y;
+      run_m[tid] = M;
+      wa[tid] = x;
+      wb[tid] = y;
+    }
+    __syncthreads();
+    for (int o = tid; o < NT * G * D; o += kThreadsTc) run_o[o] = run_o[o] * wa[o / D] + co[o] * wb[o / D];
+    __syncthreads();
   }
-  __syncthreads();
-  if (s_stop) return;
 
-  float* co = reinterpret_cast<float*>(smem) + kWarpsTc * G * D;
-  SegArgs a;
-  a.pair = pair;
-  a.u = u;
-  a.tok = tok;
-  a.ent_base = 0;
-  a.list = list;
-  a.qs = s_q;
-  a.rows = nlist * p.ET;
-  a.ta = 0;
-  a.tb = (a.rows + kTileRows - 1) / kTileRows;
-  tc_segment<SH>(s, p, a, smem, cm, cl, co, s_m, s_l);
-
-  long long slot0 = 0;
-  const int nseg_h = hit_segments(p, pair, &slot0);
+  // each pair's hit-pass partials (global) merged with its miss result (here)
   const size_t stride = (size_t)G * (D + 2);
-  tc_write_partial<G, D>(
-      s.part + (size_t)two_pass_slot(p, pair, nseg_h, slot0, nseg_h + sp) * stride, cm, cl, co);
-  if (!p.fuse_finish) return;
-  __threadfence();
-  __syncthreads();  // this CTA's partial is written; the hit pass's were before the launch
-  const float* part = s.part;
-  tc_merge_partials<G, D>(
-      [&](int q2) { return part + (size_t)two_pass_slot(p, pair, nseg_h, slot0, q2) * stride; },
-      nseg_h + p.splits_m, load_io(s.io).out + (size_t)pair * G * D, co + G * D);
-}
-
-// Finish of a step, one CTA per (unit, token): merges the pair's partials
-// (hit pass, then miss pass) into the output.
-template <class SH>
-__global__ void __launch_bounds__(kThreadsTc) attn_tc_finish_kernel(DeviceState s, TcParams p) {
-  constexpr int D = SH::D, G = SH::G;
-  extern __shared__ float wseg[];  // [2][nseg][G]
-  __shared__ int s_stop;
-  const int pair = blockIdx.x, tid = threadIdx.x;
-  griddep_wait();
-  griddep_launch();
-  if (tid == 0) s_stop = load_err(s.err);
-  __syncthreads();
-  if (s_stop) return;
-  long long slot0 = 0;
-  const int nseg_h = hit_segments(p, pair, &slot0);
-  float* out = load_io(s.io).out + (size_t)pair * G * D;
-  const float* part = s.part;
-  const size_t stride = (size_t)G * (D + 2);
-  tc_merge_partials<G, D>(
-      [&](int q2) { return part + (size_t)two_pass_slot(p, pair, nseg_h, slot0, q2) * stride; },
-      nseg_h + p.splits_m, out, wseg);
+  for (int j = 0; j < NT; ++j) {
+    const int pair = u * p.n_tok + tok0 + j;
+    long long slot0 = 0;
+    const int nseg_h = hit_segments(p, pair, &slot0);
+    const float* part = s.part;
+    const float* rm = run_m + j * G;
+    const float* rl = run_l + j * G;
+    const float* ro = run_o + j * G * D;
+    tc_merge_partials<G, D>(
+        [&](int q2, int i) -> float {
+          if (q2 == nseg_h) return i < G ? rm[i] : i < 2 * G ? rl[i - G] : ro[i - 2 * G];
+          return __ldcg(part + (size_t)two_pass_slot(p, pair, nseg_h, slot0, q2) * stride + i);
+        },
+        nseg_h + 1, io.out + (size_t)pair * G * D, co);
+    __syncthreads();
+  }
 }
 
 template <class SH>
@@ -906,7 +1244,7 @@ inline HitGrid hit_grid(int pairs, int k, int ET, int num_sms) {
 }
 
 template <class SH>
-TcParams two_pass_params(const DeviceState& s, const AttnLaunch& a, int splits_m) {
+TcParams two_pass_params(const DeviceState& s, const AttnLaunch& a) {
   TcParams p = tc_params<SH>(s, a);
   p.slots = s.hslot;
   p.identity = 0;
@@ -914,18 +1252,16 @@ TcParams two_pass_params(const DeviceState& s, const AttnLaunch& a, int splits_m
   p.tiles_per_pair = g.tiles_per_pair;
   p.tiles = g.tiles;
   p.hit_ctas = g.ctas;
-  p.splits_m = splits_m;
   return p;
 }
 
 template <class SH>
-cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int splits_m,
-                        cudaStream_t st) {
-  static int smem_hits = 0, smem_miss = 0;
-  TcParams p = two_pass_params<SH>(s, a, splits_m);
+cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, cudaStream_t st) {
+  static int smem_hits = 0;
+  TcParams p = two_pass_params<SH>(s, a);
   const HitGrid g = hit_grid(s.U * a.n_tok, a.k, s.ET, a.num_sms);
-  const size_t parts = (size_t)s.U * a.n_tok * (1 + splits_m) + 2 * (size_t)g.ctas;
-  if (parts * SH::G * (SH::D + 2) > a.part_capacity || g.max_seg + splits_m > SH::MAX_SEG)
+  const size_t parts = (size_t)s.U * a.n_tok * 2 + 2 * (size_t)g.ctas;
+  if (parts * SH::G * (SH::D + 2) > a.part_capacity || g.max_seg + 1 > SH::MAX_SEG)
     return cudaErrorInvalidValue;
   if (pass == 0) {
     cudaError_t e = ensure_smem((const void*)attn_tc_hits_kernel<SH>, SH::SMEM, &smem_hits);
@@ -935,68 +1271,40 @@ cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, int
     return launch_ex(false, attn_tc_hits_kernel<SH>, dim3((unsigned)g.ctas), dim3(kThreadsTc),
                      SH::SMEM, st, s, p);
   }
-  dim3 grid((unsigned)splits_m, (unsigned)(s.U * a.n_tok));
-  if (s.MS % splits_m != 0 || s.MS / splits_m > SH::SCAN_MAX || (s.MS / splits_m) % 2 != 0)
-    return cudaErrorInvalidValue;
-  p.fuse_finish = splits_m == 1 ? 1 : 0;
-  const size_t smem = SH::SMEM + (size_t)(s.MS / splits_m) * sizeof(int32_t);
-  cudaError_t e = ensure_smem((const void*)attn_tc_miss_kernel<SH>,
-                              SH::SMEM + (size_t)SH::SCAN_MAX * sizeof(int32_t), &smem_miss);
-  if (e != cudaSuccess) return e;
-  // Launched early (behind the gather, waiting on it) only while its grid
-  // fits one CTA per SM: resident early, a larger grid would hold every SM's
-  // shared memory for the whole gather and keep the hit pass and the
-  // reservation's kernels off the GPU until it ends.
-  const bool early = a.num_sms > 0 && (long long)grid.x * grid.y <= a.num_sms;
-  return launch_ex(early, attn_tc_miss_kernel<SH>, grid, dim3(kThreadsTc), smem, st, s, p);
-}
-
-template <class SH>
-cudaError_t run_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_m,
-                          cudaStream_t st) {
-  static int smem_done = 0;
-  TcParams p = two_pass_params<SH>(s, a, splits_m);
-  const HitGrid g = hit_grid(s.U * a.n_tok, a.k, s.ET, a.num_sms);
-  const size_t smem = 2 * (size_t)(g.max_seg + splits_m) * SH::G * sizeof(float);
-  cudaError_t e = ensure_smem((const void*)attn_tc_finish_kernel<SH>, smem, &smem_done);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(attn_tc_finish_kernel<SH>, dim3((unsigned)(s.U * a.n_tok)), dim3(kThreadsTc),
-                    smem, st, s, p);
+  // Miss pass: one CTA per unit over the union of its tokens' misses (2 or 3
+  // tokens), else one per (unit, token).
+  auto launch_miss = [&](auto nt_tag) -> cudaError_t {
+    constexpr int NT = decltype(nt_tag)::value;
+    static int smem_miss = 0;
+    using L = MissSmem<SH, NT>;
+    cudaError_t e = ensure_smem((const void*)attn_tc_miss_kernel<SH, NT>, L::BYTES, &smem_miss);
+    if (e != cudaSuccess) return e;
+    dim3 grid(1u, (unsigned)(NT == 1 ? s.U * a.n_tok : s.U));
+    // Launched early behind the gather (its CTAs wait for it): the launch
+    // also follows the hit pass and the reservation, which release their
+    // dependents only as they end, so the early CTAs take no SM the hit
+    // pass still needs.
+    return launch_pdl(attn_tc_miss_kernel<SH, NT>, grid, dim3(kThreadsTc), L::BYTES, st, s, p);
+  };
+  // (the union keeps NT sets of accumulators in registers: shapes with one
+  // n-tile of query columns only)
+  if constexpr (SH::NTN == 1) {
+    if (a.n_tok == 2) return launch_miss(std::integral_constant<int, 2>());
+    if (a.n_tok == 3) return launch_miss(std::integral_constant<int, 3>());
+  }
+  return launch_miss(std::integral_constant<int, 1>());
 }
 
 }  // namespace
-
-int attention_tc_scan_max(int D, int G, int kv_shared) {
-#define X(d, g, sh) \
-  if (D == d && G == g && (kv_shared != 0) == sh) return TcShape<d, g, sh>::SCAN_MAX;
-  X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
-  X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
-  X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)
-  X(64, 1, true) X(64, 2, true) X(64, 4, true) X(64, 8, true)
-#undef X
-  return 0;
-}
-
-int attention_tc_max_segments(int D, int G, int kv_shared) {
-#define X(d, g, sh) \
-  if (D == d && G == g && (kv_shared != 0) == sh) return TcShape<d, g, sh>::MAX_SEG;
-  X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
-  X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
-  X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)
-  X(64, 1, true) X(64, 2, true) X(64, 4, true) X(64, 8, true)
-#undef X
-  return 0;
-}
 
 bool attention_tc_supported(int D, int DV, int G, int kv_shared) {
   (void)kv_shared;
   return D == DV && (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
-size_t attention_tc_two_pass_floats(int pairs, int k, int ET, int G, int DV, int num_sms,
-                                    int splits_m) {
+size_t attention_tc_two_pass_floats(int pairs, int k, int ET, int G, int DV, int num_sms) {
   const HitGrid g = hit_grid(pairs, k, ET, num_sms);
-  return ((size_t)pairs * (1 + splits_m) + 2 * (size_t)g.ctas) * (size_t)G * (DV + 2);
+  return ((size_t)pairs * 2 + 2 * (size_t)g.ctas) * (size_t)G * (DV + 2);
 }
 
 size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sms) {
@@ -1006,23 +1314,10 @@ size_t attention_tc_part_floats(int U, int max_tokens, int G, int DV, int num_sm
 }
 
 cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
-                                     int splits_m, cudaStream_t st) {
+                                     cudaStream_t st) {
 #define X(d, g, sh)                                                         \
   if (s.D == d && s.G == g && (s.kv_shared != 0) == sh)                     \
-    return run_tc_pass<TcShape<d, g, sh>>(s, a, pass, splits_m, st);
-  X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
-  X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
-  X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)
-  X(64, 1, true) X(64, 2, true) X(64, 4, true) X(64, 8, true)
-#undef X
-  return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_attention_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_m,
-                                       cudaStream_t st) {
-#define X(d, g, sh)                                                         \
-  if (s.D == d && s.G == g && (s.kv_shared != 0) == sh)                     \
-    return run_tc_finish<TcShape<d, g, sh>>(s, a, splits_m, st);
+    return run_tc_pass<TcShape<d, g, sh>>(s, a, pass, st);
   X(128, 1, false) X(128, 2, false) X(128, 4, false) X(128, 8, false)
   X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
   X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false)

@@ -90,8 +90,10 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(DeviceState s) {
 }
 
 // Staged gather: runs right after match, before any slot is reserved.  Each
-// CTA takes an equal contiguous range of all units' miss-set cells (hashing
-// spreads the claimed cells evenly) and walks it in rounds of kStageCells:
+// CTA takes an equal contiguous range of all units' miss-set cells (with one
+// CTA per request, exactly that request's units: the request-level
+// assignment the AVSG page compares against) and walks it in rounds of
+// kStageCells:
 // the claimed cells of a round are compacted into a shared list, then the
 // whole CTA copies the listed host rows into the staging area at their
 // cells, consecutive threads on consecutive 16-byte chunks of a row and
@@ -175,6 +177,121 @@ __global__ void __launch_bounds__(kThreads) gather_stage_kernel(DeviceState s) {
     __syncthreads();  // the list is rewritten by the next round
   }
   griddep_launch();  // (no round at all)
+}
+
+// Copies the listed host rows of one chunk of miss-set cells into the
+// staging area at their cells: consecutive threads on consecutive 16-byte
+// chunks of a row, kUnroll chunks in flight per thread.  off[r]: cell of row
+// r counted from c0; id[r]: its entry id.
+__device__ __forceinline__ void copy_staged_rows(const DeviceState& s, const StepBufs& sb,
+                                                 long long c0, const uint32_t* off,
+                                                 const int32_t* id, int n) {
+  const uint32_t cpk = (uint32_t)(s.ek >> 4), cpv = (uint32_t)(s.ev >> 4), cpe = cpk + cpv;
+  const uint32_t items = (uint32_t)n * cpe;  // (row, 16-byte chunk) pairs
+  for (uint32_t it0 = threadIdx.x; it0 < items; it0 += kThreads * kUnroll) {
+    uint4 v[kUnroll];
+    unsigned char* dst[kUnroll];
+#pragma unroll
+    for (int q = 0; q < kUnroll; ++q) {
+      const uint32_t it = it0 + (uint32_t)(q * kThreads);
+      dst[q] = nullptr;
+      if (it < items) {
+        const uint32_t r = it / cpe, j = it - r * cpe;
+        const long long cg = c0 + off[r];
+        const long long unit = cg / s.MS;
+        if (!AVSG_IN_BOUNDS(cg < (long long)s.U * s.MS && id[r] >= 0 && id[r] < s.L, s.err,
+                            (int)unit, (int)(cg - unit * s.MS)))
+          continue;
+        const long long hrow = unit * s.L + id[r];
+        const unsigned char* src;
+        if (j < cpk) {
+          src = s.host_k + hrow * s.ek + ((size_t)j << 4);
+          dst[q] = sb.kstage + cg * s.ek + ((size_t)j << 4);
+        } else {
+          src = s.host_v + hrow * s.ev + ((size_t)(j - cpk) << 4);
+          dst[q] = sb.vstage + cg * s.ev + ((size_t)(j - cpk) << 4);
+        }
+        v[q] = load_host16(src);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kUnroll; ++q)
+      if (dst[q]) store16(dst[q], v[q]);
+  }
+}
+
+// Staged gather, balanced: the same copy, with the cells of all units cut
+// into chunks of kStageChunk that the CTAs take one at a time from a counter
+// (match zeroes it), so a CTA whose chunks held more misses simply takes
+// fewer of them and the CTAs end together.  A chunk's cells are loaded, and
+// the next chunk taken, while the previous chunk's rows are in flight, so
+// the host link sees no gap between chunks.  Dependents (the miss pass) are
+// released when a CTA finds no chunk left.
+constexpr int kStageChunk = 512;
+
+__global__ void __launch_bounds__(kThreads) gather_stage_dyn_kernel(DeviceState s) {
+  __shared__ uint32_t s_off[2][kStageChunk];  // claimed cells of a chunk (offset in the chunk)
+  __shared__ int32_t s_id[2][kStageChunk];
+  __shared__ int s_n[2];
+  __shared__ long long s_chunk[2];
+  constexpr int kPer = kStageChunk / kThreads;
+  griddep_wait();
+  if (load_err(s.err) != 0) {  // uniform over the CTA
+    griddep_launch();
+    return;
+  }
+  const StepBufs sb = step_bufs(s, load_io(s.io).parity);
+  const int lane = threadIdx.x & 31;
+  const long long ncell = (long long)s.U * s.MS;
+  const long long nchunk = (ncell + kStageChunk - 1) / kStageChunk;
+  unsigned long long w[kPer];
+  // claimed cells of chunk c (held in w) -> list b
+  auto compact = [&](long long c, int b) {
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const bool claimed = w[e] != kMissEmpty;
+      const unsigned bal = __ballot_sync(0xffffffffu, claimed);
+      if (bal == 0u) continue;  // uniform over the warp
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&s_n[b], __popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (claimed) {
+        const int r = base + __popc(bal & ((1u << lane) - 1u));
+        s_off[b][r] = (uint32_t)(e * kThreads + (int)threadIdx.x);
+        s_id[b][r] = (int32_t)(uint32_t)w[e];
+      }
+    }
+    (void)c;
+  };
+  auto load_cells = [&](long long c) {
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const long long cell = c * kStageChunk + e * kThreads + (int)threadIdx.x;
+      w[e] = c < nchunk && cell < ncell ? __ldcg(s.mset + cell) : kMissEmpty;
+    }
+  };
+  if (threadIdx.x == 0) {
+    s_chunk[0] = atomicAdd(s.gather_next, 1);
+    s_n[0] = 0;
+  }
+  __syncthreads();
+  load_cells(s_chunk[0]);
+  compact(s_chunk[0], 0);
+  __syncthreads();
+  for (int b = 0; s_chunk[b] < nchunk; b ^= 1) {
+    if (threadIdx.x == 0) {
+      s_chunk[b ^ 1] = atomicAdd(s.gather_next, 1);
+      s_n[b ^ 1] = 0;
+    }
+    __syncthreads();
+    const long long next = s_chunk[b ^ 1];
+    if (next >= nchunk) griddep_launch();  // this CTA's last chunk
+    load_cells(next);                      // in flight beside this chunk's copies
+    copy_staged_rows(s, sb, s_chunk[b] * kStageChunk, s_off[b], s_id[b], s_n[b]);
+    compact(next, b ^ 1);
+    __syncthreads();  // list b ^ 1 complete; list b is rewritten two chunks on
+  }
+  griddep_launch();  // (no chunk at all)
 }
 
 // Place: every miss's staged row (by miss-set cell) into its reserved slot
@@ -299,15 +416,21 @@ cudaError_t launch_host_touch(const unsigned char* p, size_t bytes, unsigned* si
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st) {
-  static int attr_done = 0;
-  const cudaError_t e = ensure_smem((const void*)gather_stage_kernel, 0, &attr_done);
+cudaError_t launch_gather_stage(const DeviceState& s, int ctas, bool by_request, cudaStream_t st) {
+  static int attr_done = 0, attr_dyn = 0;
+  if (by_request) {
+    const cudaError_t e = ensure_smem((const void*)gather_stage_kernel, 0, &attr_done);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(gather_stage_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
+  }
+  const cudaError_t e = ensure_smem((const void*)gather_stage_dyn_kernel, 0, &attr_dyn);
   if (e != cudaSuccess) return e;
-  return launch_pdl(gather_stage_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
+  return launch_pdl(gather_stage_dyn_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
 }
 
 
 static_assert(kStageCells % kThreads == 0, "a round is whole passes of the CTA");
+static_assert(kStageChunk % kThreads == 0, "a chunk is whole passes of the CTA");
 
 cudaError_t launch_place(const DeviceState& s, int which, cudaStream_t st) {
   static int attr_done = 0;

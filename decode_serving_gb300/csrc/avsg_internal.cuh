@@ -15,7 +15,6 @@ constexpr int kOrders = 64;                    // reservation classes 0..63
 constexpr int kNotCandidate = 255;
 constexpr int kMaxTokens = 8;
 constexpr int kCountsPerPair = 8;              // arrival counters per (unit, token)
-constexpr int kMissScanMax = 4096;             // most miss-set cells one miss-pass CTA scans
 constexpr int kMatchCluster = 8;               // match: one cluster of CTAs per unit
 constexpr int kMatchThreads = 256;             // threads per match CTA
 constexpr int kMatchPerThread = 4;             // selected ids per match thread (n_tok * k <= 8192)
@@ -33,9 +32,10 @@ struct DevCounters {
 
 // One miss to copy: host row `id` of `unit` into buffer slot `slot`, which
 // held `old_id` (kEmpty if none) before this step; `cell` is the id's
-// miss-set cell (and its row in the staging area).
+// miss-set cell (and its row in the staging area); bit j of `tokens` is set
+// when query token j selected the id.
 struct GatherDesc {
-  int32_t unit, id, slot, old_id, cell, pad0, pad1, pad2;
+  int32_t unit, id, slot, old_id, cell, tokens, pad1, pad2;
 };
 
 // Everything a kernel needs about a handle: sizes and device pointers.
@@ -53,7 +53,7 @@ struct StepIO {
   int32_t live;                    // entries per unit selectable this step (ids below it)
   int32_t parity;                  // 0 / 1 alternating by step: which half of the per-step
                                    // staging and descriptor arrays this step writes
-  int32_t pad_;
+  uint32_t seq;                    // steps since create / reset (parity = seq & 1)
 };
 
 struct DeviceState {
@@ -86,6 +86,7 @@ struct DeviceState {
   int32_t* mslot;                  // [U][MS] slot reserved for the miss in that cell
   GatherDesc* desc;                // [2][U * max_union]     (halves by step parity)
   int32_t* desc_count;             // [2]
+  int32_t* gather_next;            // [1] chunks of miss-set cells handed to the gather (zeroed by match)
   int32_t* dbase;                  // [2][U] first descriptor of the unit that step
   int32_t* dcount;                 // [2][U] descriptors of the unit that step (0: none)
   float* part;                     // split-K partials
@@ -93,6 +94,15 @@ struct DeviceState {
   DevCounters* counters;           // [U] distinct hits / misses, summed over steps
   DevErr* err;
   int32_t* budget;                 // [U] usable slots per unit (buffer elasticity), <= B
+  // Deferred place (two-pass pipeline): a step's missed rows reach their
+  // slots during the next step, so that step's hits on them read the staged
+  // copy.  pend[u][slot] = (seq of the step that reserved the slot) << 32 |
+  // its miss-set cell; stage_entry0 = entry index, counted from kbuf (and
+  // from vbuf: the staging area follows each buffer at the same distance), of
+  // the first staged entry.  deferred = 0: no pend (the other pipelines).
+  unsigned long long* pend;
+  int64_t stage_entry0;
+  int32_t deferred;
 };
 
 // The per-step arrays of one parity.
@@ -114,6 +124,20 @@ __host__ __device__ __forceinline__ StepBufs step_bufs(const DeviceState& s, int
   b.kstage = s.kstage ? s.kstage + (size_t)parity * half * s.ek : nullptr;
   b.vstage = s.vstage ? s.vstage + (size_t)parity * half * (s.ev ? s.ev : s.ek) : nullptr;
   return b;
+}
+
+// The slot value the hit pass reads for a hit on `slot` at step `seq`: the
+// slot itself, or, when the previous step reserved it (its row is still in
+// that step's half of the staging area until the deferred place), the
+// staged entry expressed as a slot of unit u counted from kbuf.
+__device__ __forceinline__ int32_t hit_row_slot(const DeviceState& s, int u, int32_t slot,
+                                                uint32_t seq) {
+  if (!s.deferred || seq == 0) return slot;
+  const unsigned long long p = __ldcg(s.pend + (size_t)u * s.B + slot);
+  if (p == ~0ull || (uint32_t)(p >> 32) != seq - 1) return slot;
+  const int64_t e = s.stage_entry0 + (int64_t)((seq - 1) & 1) * s.U * s.MS +
+                    (int64_t)u * s.MS + (int64_t)(uint32_t)p - (int64_t)u * s.B;
+  return (int32_t)e;
 }
 
 __device__ __forceinline__ uint32_t fib_hash(int32_t id, int shift) {
@@ -222,8 +246,10 @@ cudaError_t launch_budget(const DeviceState& s, const int32_t* budget_new, cudaS
 cudaError_t launch_commit(const DeviceState& s, cudaStream_t st);
 cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
 // Staged gather: right after match, the host row of every claimed miss-set
-// cell is copied to kstage/vstage at that cell (no slot needed yet).
-cudaError_t launch_gather_stage(const DeviceState& s, int ctas, cudaStream_t st);
+// cell is copied to kstage/vstage at that cell (no slot needed yet); chunks
+// of cells handed out by a counter, or with by_request an equal range of
+// cells per CTA (one CTA per request).
+cudaError_t launch_gather_stage(const DeviceState& s, int ctas, bool by_request, cudaStream_t st);
 // Staged rows -> their reserved slots.  which: 0 the rows the current (or
 // last) step staged; 1 the rows the step before it staged (the deferred place
 // of the two-pass pipeline, run early in the next step).  Runs whatever the
@@ -274,22 +300,14 @@ cudaError_t launch_attention_tc(const DeviceState& s, const AttnLaunch& a, int n
                                 cudaStream_t st);
 // pass 0: hit rows of every (unit, token), a persistent grid of 2 CTAs per
 // SM, each an equal share of all pairs' tiles.  pass 1: miss rows from this
-// step's half of the staging area (s is the staged view), splits_m CTAs per
-// pair (MS / splits_m <= the shape's scan limit), launched right after the
-// staged gather on its stream (and, with splits_m == 1, once the hit pass is
-// done).  Each pass writes partials; with splits_m == 1 the miss pass merges
-// them into the output, else the finish kernel does (s: real state).
+// step's half of the staging area, listed from the reservation's
+// descriptors: one CTA per unit over the union of a 2- or 3-token step's
+// misses, else one per (unit, token); launched after the gather, the
+// reservation and the hit pass, it merges both passes into the output.
 cudaError_t launch_attention_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass,
-                                     int splits_m, cudaStream_t st);
-cudaError_t launch_attention_tc_finish(const DeviceState& s, const AttnLaunch& a, int splits_m,
-                                       cudaStream_t st);
+                                     cudaStream_t st);
 // Floats of partials a two-pass step over `pairs` (unit, token) pairs needs.
-size_t attention_tc_two_pass_floats(int pairs, int k, int ET, int G, int DV, int num_sms,
-                                    int splits_m);
-// Most partials (hit + miss splits) one pair's merge takes.
-int attention_tc_max_segments(int D, int G, int kv_shared);
-// Most miss-set cells one miss-pass CTA scans (a power of two).
-int attention_tc_scan_max(int D, int G, int kv_shared);
+size_t attention_tc_two_pass_floats(int pairs, int k, int ET, int G, int DV, int num_sms);
 bool attention_tc_enabled();
 
 }  // namespace avsg

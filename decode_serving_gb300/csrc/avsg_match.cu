@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
   griddep_launch();
   if (u == 0 && rank == 0 && tid == 0) {
     s.desc_count[v.parity] = 0;
+    *s.gather_next = 0;
     *s.io = v;  // for the kernels after this one
   }
   // No descriptors of this step's parity until its reservation writes them
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
       const uint32_t old = atomicOr(&bits[tok * HWL + word / kC], b);
       if (old & b) raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
       slot_map[off] = slot;
-      s.hslot[off] = slot;
+      s.hslot[off] = hit_row_slot(s, u, slot, v.seq);
       if (hit) hit[off] = 1;
     } else {
       const uint32_t mmask = (uint32_t)s.MS - 1u;

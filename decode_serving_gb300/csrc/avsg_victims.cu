@@ -133,7 +133,6 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   uint8_t* ord = smem + lay.ord;
 
   griddep_wait();
-  griddep_launch();
   const StepIO io = load_io(s.io);
   const int t = io.t;
   const StepBufs sb = step_bufs(s, io.parity);
@@ -144,7 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     s_hits = 0;
   }
   __syncthreads();
-  if (s_stop) return;
+  if (s_stop) {
+    griddep_launch();
+    return;
+  }
 
   const int B = s.B;
   const size_t ub = (size_t)u * B;
@@ -355,10 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
                         s.err, u, i))
       continue;
     const int32_t old = s.tag[ub + v];
+    const int32_t toks = (int32_t)(__ldcg(ms + cell) >> 32);
     s.tag[ub + v] = id;
     s.last[ub + v] = t;
     s.mslot[(size_t)u * s.MS + cell] = v;
-    sb.desc[s_base + r] = GatherDesc{u, id, v, old, cell, 0, 0, 0};
+    if (s.deferred) s.pend[ub + v] = ((unsigned long long)io.seq << 32) | (uint32_t)cell;
+    sb.desc[s_base + r] = GatherDesc{u, id, v, old, cell, toks, 0, 0};
   }
   __syncthreads();
 
@@ -389,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     s.counters[u].hits += (unsigned long long)s_hits;
     s.counters[u].misses += (unsigned long long)m;
   }
+  griddep_launch();  // dependents launch as this kernel ends
 }
 
 // Hash-table update of one unit: erase the ids this step evicted, insert the

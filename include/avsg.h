@@ -133,7 +133,7 @@ typedef struct avsg_info {
 #define AVSG_KERNEL_ATTENTION 3      /* single pass, or the pass over hit rows */
 #define AVSG_KERNEL_ATTENTION_MISS 4 /* pass over miss rows */
 #define AVSG_KERNEL_COMMIT 5         /* hash-table update */
-#define AVSG_KERNEL_FINISH 6         /* merge of the two attention passes */
+#define AVSG_KERNEL_FINISH 6         /* reserved (the miss pass merges the two passes) */
 #define AVSG_KERNEL_PLACE 7          /* staged missed rows into their slots */
 #define AVSG_NUM_KERNELS 8
 typedef struct avsg_kernel_times {
