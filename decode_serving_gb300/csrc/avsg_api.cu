@@ -642,7 +642,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
     e = cudaEventRecord(h->ev_reserve, side2);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_staged, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
-    AVSG_RUN(AVSG_KERNEL_PLACE, side2, launch_place(sc, 0, side2));
+    AVSG_RUN(AVSG_KERNEL_PLACE, side2, launch_place(sc, 0, h->num_sms, side2));
     e = cudaEventRecord(h->ev_commit, side2);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_reserve, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
@@ -654,17 +654,18 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   }
   // Two-pass pipeline (the tensor-core shapes).  After match, four
   // streams run side by side:
-  //   side3:  the rows the previous step staged, into the slots its
-  //           reservation gave them (the deferred place: off the previous
-  //           step's critical path, beside this step's link-bound gather);
+  //   side3:  (lowest priority) the rows the previous step staged, into the
+  //           slots its reservation gave them: the deferred place, off the
+  //           previous step's critical path, in the SMs this step's kernels
+  //           leave free;
   //   st:     attention over the hit rows (a hit on a row the previous step
   //           loaded reads its staged copy: match points it there);
   //   side:   the missed rows, host -> this step's half of the staging area
   //           (host link), then the attention over them, which also merges
   //           both passes into the output (it waits for the hit pass);
   //   side2:  the reservation, then the hash-table update.
-  // This step's staged rows reach their slots early in the next step (or
-  // when an entry point that reads the buffer flushes them).
+  // This step's staged rows reach their slots in the next step (or when an
+  // entry point that reads the buffer flushes them).
   e = cudaEventRecord(h->ev_fork, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_fork, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_fork, 0);
@@ -672,8 +673,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   if (e != cudaSuccess) return fail_cuda(h, e);
   // Launched in this order, so the CTAs of the kernels the miss pass needs
   // are placed first: the gather's (on SMs of their own), the reservation's,
-  // the hit pass's; then the hash update and, on the lowest-priority stream,
-  // the place, which only has to end with the step.
+  // the hit pass's; then the hash update and the place.
   AVSG_RUN(AVSG_KERNEL_GATHER, side, launch_gather_stage(sc, h->stage_ctas, h->by_request, side));
   AVSG_RUN(AVSG_KERNEL_RESERVE, side2, launch_victims(sc, n_tok, k, side2));
   e = cudaEventRecord(h->ev_reserve, side2);
@@ -684,7 +684,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
   e = cudaEventRecord(h->ev_commit, side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_PLACE, side3, launch_place(sc, 1, side3));
+  AVSG_RUN(AVSG_KERNEL_PLACE, side3, launch_place(sc, 1, h->num_sms, side3));
   e = cudaEventRecord(h->ev_place, side3);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_hits, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->ev_reserve, 0);
@@ -796,7 +796,7 @@ int enqueue_step(avsg_handle h, int32_t t, int32_t n_tok, int32_t k, const int32
 int flush_place(avsg_handle h) {
   if (!h->pending_place) return AVSG_OK;
   cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = launch_place(h->ds, 0, nullptr);
+  if (e == cudaSuccess) e = launch_place(h->ds, 0, h->num_sms, nullptr);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail_cuda(h, e);
   h->pending_place = false;

@@ -295,41 +295,42 @@ __global__ void __launch_bounds__(kThreads) gather_stage_dyn_kernel(DeviceState 
 }
 
 // Place: every miss's staged row (by miss-set cell) into its reserved slot
-// (device to device), grid (U, kPlaceSplit), for the step of parity
-// io.parity ^ which (see launch_place).  The unit's work is its descriptors'
-// (row, 16-byte chunk) items in row order; the unit's kPlaceSplit * 256
-// threads take consecutive items (coalesced), kPlaceRows items each per
-// round: the rows' descriptors, then all the loads, then the stores.  Rows of
-// any size keep every thread busy (8 KiB page entries as much as 512-byte
-// token rows).  It ignores the error word: a step whose reservation did not
-// run left no descriptors of its parity.
-constexpr int kPlaceSplit = 4;
+// (device to device), for the step of parity io.parity ^ which (see
+// launch_place).  A persistent grid of one CTA per SM, each an equal
+// contiguous share of all the step's (descriptor, 16-byte chunk) items,
+// kPlaceRows items per thread in flight (the descriptors, then all the loads,
+// then the stores); consecutive threads take consecutive chunks of a row, so
+// 8 KiB page entries and 512-byte token rows both keep every thread busy.
+// Few CTAs on the lowest-priority stream: it fills the SMs the other kernels
+// of the step leave free.  It ignores the error word: a step whose
+// reservation did not run has no descriptors (match zeroes the count).
 constexpr int kPlaceRows = 8;
 
 __global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s, int which) {
   griddep_wait();
   griddep_launch();
   const StepBufs sb = step_bufs(s, load_io(s.io).parity ^ which);
-  const int u = blockIdx.x;
-  const int base = __ldcg(sb.dbase + u), cnt = __ldcg(sb.dcount + u);
   const uint32_t cpk = (uint32_t)(s.ek >> 4), cpe = cpk + (uint32_t)(s.ev >> 4);
-  const uint32_t total = (uint32_t)cnt * cpe;
-  const uint32_t nthr = (uint32_t)kPlaceSplit * kThreads;
-  const uint32_t me = blockIdx.y * kThreads + threadIdx.x;
-  for (uint32_t i0 = me; i0 < total; i0 += nthr * kPlaceRows) {
+  const long long total = (long long)__ldcg(sb.desc_count) * cpe;
+  const long long begin = (long long)blockIdx.x * total / gridDim.x;
+  const long long end = (long long)(blockIdx.x + 1) * total / gridDim.x;
+  for (long long i0 = begin + threadIdx.x; i0 < end; i0 += (long long)kThreads * kPlaceRows) {
     uint4 v[kPlaceRows];
     void* dst[kPlaceRows];
     const uint4* src[kPlaceRows];
 #pragma unroll
     for (int r = 0; r < kPlaceRows; ++r) {
-      const uint32_t item = i0 + (uint32_t)r * nthr;
+      const long long item = i0 + (long long)r * kThreads;
       dst[r] = nullptr;
       src[r] = nullptr;
-      if (item < total) {
-        const uint32_t d = item / cpe, c = item - d * cpe;
-        const GatherDesc* g = sb.desc + base + d;
-        const int cell = __ldcg(&g->cell), slot = __ldcg(&g->slot);
-        if (!AVSG_IN_BOUNDS(cell >= 0 && cell < s.MS && slot >= 0 && slot < s.B, s.err, u, (int)d))
+      if (item < end) {
+        const long long d = item / cpe;
+        const uint32_t c = (uint32_t)(item - d * cpe);
+        const GatherDesc* g = sb.desc + d;
+        const int u = __ldcg(&g->unit), cell = __ldcg(&g->cell), slot = __ldcg(&g->slot);
+        if (!AVSG_IN_BOUNDS(u >= 0 && u < s.U && cell >= 0 && cell < s.MS && slot >= 0 &&
+                                slot < s.B,
+                            s.err, u, (int)d))
           continue;
         const size_t srow = (size_t)u * s.MS + cell;
         const size_t drow = (size_t)u * s.B + slot;
@@ -395,23 +396,34 @@ cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st) {
   return launch_pdl(gather_kernel, dim3(ctas), dim3(kThreads), 0, st, s);
 }
 
-// One 4-byte read in every 4 KiB page of a mapped host range.  The first
-// device access to a region of the host store costs a translation the
-// device then keeps; taking them all at once when a handle is created keeps
-// them out of the first decode steps (4.5 GiB: about 0.3 ms).
+// Warms the device's path to a mapped host range before the first step: the
+// whole range is read once (coalesced 16-byte loads, four in flight per
+// thread).  The first device reads of host memory the host has just written
+// pay for translations and for the state the host keeps about those lines,
+// which later reads do not: on a 17 GB store the first tens of steps ran up
+// to 3x slower, unevenly from run to run, when the store was only sampled
+// here; read whole, the first steps run as fast as the later ones.  About
+// 90 ms for 17 GB (once per handle).
 __global__ void host_touch_kernel(const unsigned char* __restrict__ p, size_t bytes,
                                   unsigned* __restrict__ sink) {
-  constexpr size_t kPage = 4096;
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  const size_t n = bytes / 16;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
   unsigned acc = 0;
-  for (size_t off = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * kPage; off + 4 <= bytes;
-       off += (size_t)gridDim.x * blockDim.x * kPage)
-    acc += __ldcg(reinterpret_cast<const unsigned*>(p + off));
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      v[j] = i + j * stride < n ? __ldcg(q + i + j * stride) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc += v[j].x ^ v[j].y ^ v[j].z ^ v[j].w;
+  }
   if (acc == 0x9E3779B9u) *sink = acc;  // keeps the loads; practically never taken
 }
 
 cudaError_t launch_host_touch(const unsigned char* p, size_t bytes, unsigned* sink, int num_sms,
                               cudaStream_t st) {
-  if (!p || bytes < 4) return cudaSuccess;
+  if (!p || bytes < 16 || ((uintptr_t)p & 15)) return cudaSuccess;
   host_touch_kernel<<<dim3((unsigned)(num_sms * 8)), dim3(256), 0, st>>>(p, bytes, sink);
   return cudaGetLastError();
 }
@@ -432,11 +444,11 @@ cudaError_t launch_gather_stage(const DeviceState& s, int ctas, bool by_request,
 static_assert(kStageCells % kThreads == 0, "a round is whole passes of the CTA");
 static_assert(kStageChunk % kThreads == 0, "a chunk is whole passes of the CTA");
 
-cudaError_t launch_place(const DeviceState& s, int which, cudaStream_t st) {
+cudaError_t launch_place(const DeviceState& s, int which, int ctas, cudaStream_t st) {
   static int attr_done = 0;
   const cudaError_t e = ensure_smem((const void*)place_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(place_kernel, dim3(s.U, kPlaceSplit), dim3(kThreads), 0, st, s, which);
+  return launch_pdl(place_kernel, dim3((unsigned)ctas), dim3(kThreads), 0, st, s, which);
 }
 
 cudaError_t launch_gather_all(const DeviceState& s, const StepIO& v, int n_tok, int k, int ctas,

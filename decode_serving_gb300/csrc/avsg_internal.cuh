@@ -255,9 +255,9 @@ cudaError_t launch_gather_stage(const DeviceState& s, int ctas, bool by_request,
 // of the two-pass pipeline, run early in the next step).  Runs whatever the
 // error word says: a step whose reservation did not run has no descriptors
 // (match zeroes the counts of its parity first).
-cudaError_t launch_place(const DeviceState& s, int which, cudaStream_t st);
-// Reads one word of every 4 KiB page of a mapped host range (sink: a device
-// word it may write), so the device's translations of the range are in place.
+cudaError_t launch_place(const DeviceState& s, int which, int ctas, cudaStream_t st);
+// Warms the device's path to a mapped host range (reads it whole once; sink:
+// a device word it may write), so the first steps do not pay for first accesses.
 cudaError_t launch_host_touch(const unsigned char* p, size_t bytes, unsigned* sink, int num_sms,
                               cudaStream_t st);
 cudaError_t launch_gather_all(const DeviceState& s, const StepIO& v, int n_tok, int k, int ctas,

@@ -10,8 +10,9 @@
 // contiguous blocks) and hit bitmaps (32-slot words dealt round-robin) are
 // spread over the cluster's shared memories and updated with atomics on
 // distributed shared memory.  A thread takes every (CL * 256)-th position of
-// the unit's n_tok * k selected ids (at most kMatchPerThread), loads all of
-// them and then all of their first hash windows before it resolves any.
+// the unit's n_tok * k selected ids (at most kPer, 1 .. kMatchPerThread),
+// loads all of them and then all of their first hash windows before it
+// resolves any.
 // Per id:
 //   * range check (id in [0, live), the entries live this step), else BAD_SELECTION;
 //   * lookup in the unit's open-addressed table (linear probing, Fibonacci
@@ -41,7 +42,7 @@ namespace {
 
 constexpr int kThreads = kMatchThreads;
 
-template <int kC>
+template <int kC, int kPer>
 __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v, int n_tok,
                                                          int k) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -81,9 +82,9 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
   if (tid == 0) s_stop = load_err(s.err);  // a latched error from an earlier step
   const size_t ubase = (size_t)u * n;
   const int first = rank * kThreads + tid;
-  int32_t id[kMatchPerThread];
+  int32_t id[kPer];
 #pragma unroll
-  for (int j = 0; j < kMatchPerThread; ++j) {
+  for (int j = 0; j < kPer; ++j) {
     const int pos = first + j * kC * kThreads;
     id[j] = pos < n ? __ldcg(sel + ubase + pos) : kEmpty;
   }
@@ -92,15 +93,15 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
 
   const int2* tab = s.htab + (size_t)u * s.HS;
   const uint32_t mask = (uint32_t)s.HS - 1u;
-  int4 win[kMatchPerThread];
+  int4 win[kPer];
 #pragma unroll
-  for (int j = 0; j < kMatchPerThread; ++j) {
+  for (int j = 0; j < kPer; ++j) {
     const bool valid = !stop && first + j * kC * kThreads < n && id[j] >= 0 && id[j] < v.live;
     win[j] = valid ? __ldcg(reinterpret_cast<const int4*>(tab + (fib_hash(id[j], s.hs_shift) & ~1u)))
                    : make_int4(kEmpty, -1, kEmpty, -1);
   }
 #pragma unroll
-  for (int j = 0; j < kMatchPerThread; ++j) {
+  for (int j = 0; j < kPer; ++j) {
     const int pos = first + j * kC * kThreads;
     if (stop || pos >= n) continue;
     const size_t off = ubase + pos;
@@ -212,11 +213,11 @@ int match_cluster_size(int MS, int n_tok, int HW, int n) {
 
 namespace {
 
-template <int CL>
+template <int CL, int PER>
 cudaError_t run_match(const DeviceState& s, const StepIO& v, int n_tok, int k, cudaStream_t st) {
   const size_t smem = match_smem_bytes(s.MS, n_tok, s.HW, CL);
   static int attr_done = 0;
-  const cudaError_t e = ensure_smem((const void*)match_kernel<CL>,
+  const cudaError_t e = ensure_smem((const void*)match_kernel<CL, PER>,
                                     match_smem_bytes(s.MS, s.HT, s.HW, CL), &attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -233,7 +234,17 @@ cudaError_t run_match(const DeviceState& s, const StepIO& v, int n_tok, int k, c
   attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, match_kernel<CL>, s, v, n_tok, k);
+  return cudaLaunchKernelEx(&cfg, match_kernel<CL, PER>, s, v, n_tok, k);
+}
+
+// ids per thread: 1, 2 or 4 (kMatchPerThread), the fewest that cover n
+template <int CL>
+cudaError_t run_match_per(const DeviceState& s, const StepIO& v, int n_tok, int k,
+                          cudaStream_t st) {
+  const int n = n_tok * k;
+  if (n <= CL * kThreads) return run_match<CL, 1>(s, v, n_tok, k, st);
+  if (n <= 2 * CL * kThreads) return run_match<CL, 2>(s, v, n_tok, k, st);
+  return run_match<CL, kMatchPerThread>(s, v, n_tok, k, st);
 }
 
 }  // namespace
@@ -245,10 +256,10 @@ cudaError_t launch_match(const DeviceState& s, const StepIO& v, int n_tok, int k
       match_smem_bytes(s.MS, s.HT, s.HW, cl) > kMatchSmemMax)
     return cudaErrorInvalidValue;
   switch (cl) {
-    case 1: return run_match<1>(s, v, n_tok, k, st);
-    case 2: return run_match<2>(s, v, n_tok, k, st);
-    case 4: return run_match<4>(s, v, n_tok, k, st);
-    default: return run_match<8>(s, v, n_tok, k, st);
+    case 1: return run_match_per<1>(s, v, n_tok, k, st);
+    case 2: return run_match_per<2>(s, v, n_tok, k, st);
+    case 4: return run_match_per<4>(s, v, n_tok, k, st);
+    default: return run_match_per<8>(s, v, n_tok, k, st);
   }
 }
 

@@ -6,7 +6,7 @@
 // the GPU) combined with the AVSG page's slot reservation for entries that
 // need a transfer (arxivdaily 2609.37538, English abstract).
 //
-// One CTA of 1024 threads per unit.  Slots are put in 64 reservation orders:
+// One CTA of 512 threads per unit.  Slots are put in 64 reservation orders:
 //   order 0      : empty slot;
 //   order 64 - b : occupied, not selected this step, bucket b = min(63, t - last);
 //   excluded     : selected this step (a hit; its last_step becomes t).
@@ -15,11 +15,12 @@
 // owns a contiguous slot range), one exclusive scan over (order, warp), and,
 // only for the orders that can hold one of the m victims, an in-order ballot
 // count within each 32-slot chunk -- no sort of the slots.  The m distinct
-// missing ids are ranked in ascending id order (counting, or a bitonic sort
-// for very many); the i-th takes the slot of rank i: its tag and last_step are
-// set, a gather descriptor (with the evicted id) is appended, the slot map
-// entries that pointed at its miss-set cell are resolved, and, for the
-// two-pass attention, each token's slots are listed hits first.
+// missing ids are ranked in ascending id order (a bit per entry of the unit
+// and a prefix popcount when the unit has at most 2^17 entries, else by
+// counting, or a bitonic sort for very many); the i-th takes the slot of
+// rank i: its tag and last_step are set, a gather descriptor (with the
+// evicted id and the tokens that selected it) is appended, and the slot map
+// entries that pointed at its miss-set cell are resolved.
 //
 // The hash-table update of the step (commit_kernel below) runs separately:
 // only the next step's match needs it.
@@ -28,8 +29,9 @@
 namespace avsg {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;   // 2 per SM, or 1 beside a gather CTA
 constexpr int kWarps = kThreads / 32;
+static_assert(kOrders * kWarps == 2 * kThreads, "the (order, warp) scan takes 2 values per thread");
 
 __device__ __forceinline__ int next_pow2(int x) {
   int p = 1;
@@ -96,36 +98,59 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 namespace {
 
 constexpr int kCountRankMax = 2048;  // above this many misses, sort instead of counting
+constexpr int kCountRankCheap = 64;  // up to this many misses, counting is cheapest
+constexpr int64_t kRankBitmapMax = 1 << 17;  // entries per unit a shared id bitmap covers
 
 struct VictimsSmem {
-  size_t keys, rank, victim, wstart, ord, total;
+  size_t keys, rank, victim, wstart, ord, bits, pre, total;
+  int bitmap_words;  // 0: no id bitmap (more entries per unit than it covers)
 };
 
-__host__ __device__ inline VictimsSmem victims_layout(int max_union, int B) {
+__host__ __device__ inline VictimsSmem victims_layout(int max_union, int B, int64_t L) {
   int p = 1;
   while (p < max_union) p <<= 1;
   VictimsSmem l;
   const size_t mu = ((sizeof(int32_t) * (size_t)max_union + 15) & ~(size_t)15);
+  l.bitmap_words = L <= kRankBitmapMax ? (int)((L + 31) / 32) : 0;
   l.keys = 0;
   l.rank = l.keys + sizeof(unsigned long long) * (size_t)p;
   l.victim = l.rank + mu;
   l.wstart = l.victim + mu;
   l.ord = l.wstart + sizeof(int32_t) * kOrders * kWarps;
-  l.total = l.ord + (((size_t)B + 15) & ~(size_t)15);
+  l.bits = l.ord + (((size_t)B + 15) & ~(size_t)15);
+  l.pre = l.bits + sizeof(uint32_t) * (size_t)l.bitmap_words;
+  l.total = l.pre + sizeof(int32_t) * (size_t)l.bitmap_words;
   return l;
+}
+
+// Exclusive prefix sum of v over the CTA (all threads call it); wsum: kWarps ints.
+__device__ __forceinline__ int block_excl_scan(int v, int* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int incl = warp_incl_scan(v, lane);
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = lane < kWarps ? wsum[lane] : 0;
+    const int y = warp_incl_scan(x, lane) - x;
+    if (lane < kWarps) wsum[lane] = y;
+  }
+  __syncthreads();
+  const int r = wsum[warp] + incl - v;
+  __syncthreads();  // wsum is free again
+  return r;
 }
 
 constexpr int kBatch = 8;  // 32-slot chunks whose state one warp loads before using it
 static_assert(kBatch == 8, "the hit-word loads map lane & 7 to a chunk, lane >> 3 to a token");
 
-__global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int n_tok,
+__global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int n_tok,
                                                               int k) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int s_stop, s_base, s_hits, s_omax, s_m;
   __shared__ int wsum[kWarps];
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const VictimsSmem lay = victims_layout(s.max_union, s.B);
+  const VictimsSmem lay = victims_layout(s.max_union, s.B, s.L);
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem + lay.keys);
   int32_t* rank = reinterpret_cast<int32_t*>(smem + lay.rank);
   int32_t* victim = reinterpret_cast<int32_t*>(smem + lay.victim);
@@ -229,7 +254,33 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
   for (int i = m + tid; i < P; i += kThreads) keys[i] = ~0ull;
   for (int i = tid; i < kOrders * kWarps; i += kThreads) wstart[i] = 0;
   __syncthreads();
-  if (counting) {
+  if (lay.bitmap_words > 0 && m > kCountRankCheap) {
+    // The distinct missing ids as bits of a bitmap over the unit's entries;
+    // the rank of an id is the number of bits below it (a prefix popcount).
+    uint32_t* bits = reinterpret_cast<uint32_t*>(smem + lay.bits);
+    int32_t* pre = reinterpret_cast<int32_t*>(smem + lay.pre);
+    const int W = lay.bitmap_words;
+    for (int i = tid; i < W; i += kThreads) bits[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < m; i += kThreads) {
+      const uint32_t id = (uint32_t)(keys[i] >> 32);
+      atomicOr(&bits[id >> 5], 1u << (id & 31));
+    }
+    __syncthreads();
+    const int wpt = (W + kThreads - 1) / kThreads;  // words per thread, contiguous
+    int cnt = 0;
+    for (int w2 = tid * wpt; w2 < min(W, (tid + 1) * wpt); ++w2) cnt += __popc(bits[w2]);
+    int run = block_excl_scan(cnt, wsum);
+    for (int w2 = tid * wpt; w2 < min(W, (tid + 1) * wpt); ++w2) {
+      pre[w2] = run;
+      run += __popc(bits[w2]);
+    }
+    __syncthreads();
+    for (int i = tid; i < m; i += kThreads) {
+      const uint32_t id = (uint32_t)(keys[i] >> 32);
+      rank[i] = pre[id >> 5] + __popc(bits[id >> 5] & ((1u << (id & 31)) - 1u));
+    }
+  } else if (counting) {
     // tpk threads per key, each counting smaller keys over a strided share.
     int tpk = 1;
     while (tpk < 32 && tpk * 2 * (m > 0 ? m : 1) <= kThreads) tpk <<= 1;
@@ -302,8 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1) victims_kernel(DeviceState s, int
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      const int v = wsum[lane];
-      wsum[lane] = warp_incl_scan(v, lane) - v;
+      const int v = lane < kWarps ? wsum[lane] : 0;
+      const int x = warp_incl_scan(v, lane) - v;
+      if (lane < kWarps) wsum[lane] = x;
     }
     __syncthreads();
     const int excl = wsum[warp] + incl - (a + b);
@@ -468,7 +520,9 @@ int g_victims_smem = 0;
 
 }  // namespace
 
-size_t victims_smem_bytes(const DeviceState& s) { return victims_layout(s.max_union, s.B).total; }
+size_t victims_smem_bytes(const DeviceState& s) {
+  return victims_layout(s.max_union, s.B, s.L).total;
+}
 
 namespace {
 
