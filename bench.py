@@ -281,11 +281,15 @@ def algorithmic_bytes(w, hits, misses, steps, num_sms=152) -> dict:
 
     attention: slot id + K row + V row per selected entry, plus q and out
            (both passes together);
-    match: id (4) + one 16-byte probe window + slot map (4) + hit flag (1)
-           per selected id, + 8 per distinct miss (miss-set cell) + the hit
-           bitmaps (1 bit per slot);
+    match: id (4) + one 32-byte probe window (two 16-byte hash cells) +
+           slot map (4) + hit-slot list (4) + hit flag (1) per selected id,
+           + 8 per distinct miss (miss-set cell) + the hit bitmaps (1 bit per
+           slot) + q read and copied;
     victims: tag and last_step (8 bytes) per slot + the hit bitmaps, + 40 per
-           miss (sorted key, tag/last/slot writes, descriptor, slot map fix-up);
+           miss (miss-set cell, descriptor, last_step, cell -> slot, marker);
+    commit: the slot map read (4 per selected id), + 112 per miss
+           (descriptor, evicted and new tag, cell -> slot, slot map write,
+           evicted-id and new-id probe windows);
     gather: one entry (K + V) per miss, read over the host link and written
            to HBM (host-link bytes are the read half);
     finish: the partials it merges (about 2 * SMs / pairs hit-pass partials
@@ -297,10 +301,11 @@ def algorithmic_bytes(w, hits, misses, steps, num_sms=152) -> dict:
     miss_ps = misses / steps
     row_b = w.entry_k_bytes + w.entry_v_bytes
     attn = sel * 4 + sel * row_b + U * n_tok * w.q_per_kv * (w.head_dim + w.v_dim) * 4
-    match = sel * (4 + 16 + 4 + 1) + miss_ps * 8 + U * n_tok * w.slots / 8
+    q_bytes = U * n_tok * w.q_per_kv * w.head_dim * 4
+    match = sel * (4 + 32 + 4 + 4 + 1) + miss_ps * 8 + U * n_tok * w.slots / 8 + 2 * q_bytes
     victims = U * w.slots * 8 + U * n_tok * w.slots / 8 + miss_ps * 40
     gather_host = miss_ps * w.entry_bytes
-    commit = miss_ps * 40   # descriptor, evicted-id probe window, new-id probe window
+    commit = sel * 4 + miss_ps * 112
     return {"attention": attn, "match": match, "victims": victims, "gather": 2 * gather_host,
             "gather_host_link": gather_host, "commit": commit,
             "finish": U * n_tok * (max(1, 2 * num_sms // (U * n_tok)) + 1) * w.q_per_kv

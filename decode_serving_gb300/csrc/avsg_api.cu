@@ -247,7 +247,7 @@ int init_state(avsg_handle h, cudaStream_t st) {
     AVSG_SET(s.pend, 0xFF, ub * 8);
     AVSG_SET(s.last, 0xFF, ub * 4);
     AVSG_SET(s.hitbits, 0, (size_t)s.U * s.HT * s.HW * 4);
-    AVSG_SET(s.htab, 0xFF, (size_t)s.U * s.HS * sizeof(int2));
+    AVSG_SET(s.htab, 0xFF, (size_t)s.U * s.HS * sizeof(int4));
     AVSG_SET(s.hused, 0, (size_t)s.U * 4);
     if (e == cudaSuccess && !h->budget.empty())
       e = cudaMemcpyAsync(s.budget, h->budget.data(), (size_t)s.U * 4, cudaMemcpyHostToDevice, st);
@@ -388,6 +388,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
   cv.take(&s.vstage, h->staged ? 2 * (size_t)U * s.MS * ev : 0);
   s.stage_entry0 = (int64_t)(kbuf_bytes / (size_t)ek);
   s.deferred = 0;  // set below for the two-pass pipeline
+  s.late_commit = 0;  // set below for the overlapped pipelines
   if ((double)U * s.B + 2.0 * U * s.MS >= 2147483647.0) {
     release(h);
     return AVSG_ERR_INVALID_ARG;
@@ -423,6 +424,7 @@ extern "C" int avsg_create(const avsg_config* cfg, const void* host_k, const voi
     h->overlap = h->staged && overlap_enabled() && (h16_shape || attention_tc_enabled());
     h->overlap_h16 = h->overlap && !tc_shape;
     s.deferred = h->overlap && !h->overlap_h16 ? 1 : 0;
+    s.late_commit = h->overlap ? 1 : 0;
     cv.take(&s.part, h->part_floats);
   }
   cv.take(&s.part_count, (size_t)U * kMaxTokens * kCountsPerPair);
@@ -612,7 +614,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
     e = cudaEventRecord(h->ev_reserve, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side2, h->ev_reserve, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
-    AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
+    AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, n_tok, k, side2));
     e = cudaEventRecord(h->ev_commit, side2);
     if (e != cudaSuccess) return fail_cuda(h, e);
     AVSG_RUN(AVSG_KERNEL_GATHER, st, launch_gather(sc, h->gather_ctas, st));
@@ -646,7 +648,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
     e = cudaEventRecord(h->ev_commit, side2);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_reserve, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
-    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(sc, st));
+    AVSG_RUN(AVSG_KERNEL_COMMIT, st, launch_commit(sc, n_tok, k, st));
     e = cudaStreamWaitEvent(st, h->ev_gather, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_commit, 0);
     if (e != cudaSuccess) return fail_cuda(h, e);
@@ -681,7 +683,7 @@ int enqueue_dag(avsg_handle h, int32_t n_tok, int32_t k, const StepIO& v, cudaSt
   AVSG_RUN(AVSG_KERNEL_ATTENTION, st, launch_attention_tc_pass(sc, a, 0, st));
   e = cudaEventRecord(h->ev_hits, st);
   if (e != cudaSuccess) return fail_cuda(h, e);
-  AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, side2));
+  AVSG_RUN(AVSG_KERNEL_COMMIT, side2, launch_commit(sc, n_tok, k, side2));
   e = cudaEventRecord(h->ev_commit, side2);
   if (e != cudaSuccess) return fail_cuda(h, e);
   AVSG_RUN(AVSG_KERNEL_PLACE, side3, launch_place(sc, 1, h->num_sms, side3));

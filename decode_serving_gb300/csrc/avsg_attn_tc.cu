@@ -26,9 +26,10 @@
 //   single pass) covers the selected rows that were already resident (the
 //   hit slots match wrote; misses are masked) and runs beside the gather and
 //   the reservation; the miss pass (attn_tc_miss_kernel) covers the missed
-//   rows, read from the staging area by miss-set cell (each CTA scans a share
-//   of the unit's cells for the ones its token selected), and, with one CTA
-//   per (unit, token), merges both passes (else attn_tc_finish_kernel does).
+//   rows, read from the staging area by miss-set cell from the reservation's
+//   descriptors, with one CTA per (unit, token) -- or per unit, over the
+//   union of a multi-token step's misses -- and merges both passes into the
+//   output.
 // No CTA waits for another.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -44,6 +45,7 @@ constexpr int kWarpsTc = 4;
 constexpr int kThreadsTc = kWarpsTc * 32;
 constexpr int kTileRows = 16;
 constexpr int kStages = 3;
+constexpr int kAhead = 3;  // tiles whose slot ids are loaded beyond the staged ones
 constexpr int kCtasPerSm = 2;
 
 template <int D_, int G_, bool SHARED_>
@@ -257,14 +259,17 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
     cp_async_commit();  // one group per tile (empty past the end) keeps the count uniform
   };
 
-  long long next_row;
+  // Rows of the tiles after the staged ones, kAhead tiles ahead (their slot
+  // loads in flight while the staged tiles are computed).
+  long long next_row[kAhead];
   {
-    long long first_rows[kStages + 1];  // slot loads issued together, then the copies
+    long long first_rows[kStages + kAhead];  // slot loads issued together, then the copies
 #pragma unroll
-    for (int i = 0; i <= kStages; ++i) first_rows[i] = row_index(i);
+    for (int i = 0; i < kStages + kAhead; ++i) first_rows[i] = row_index(i);
 #pragma unroll
     for (int i = 0; i < kStages; ++i) issue(first_rows[i], i);
-    next_row = first_rows[kStages];
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) next_row[j] = first_rows[kStages + j];
   }
   uint32_t qb[KS][NTN][2];
 #pragma unroll
@@ -410,8 +415,10 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
       }
     }
     __syncwarp();  // every lane has read stage st
-    issue(next_row, st);
-    next_row = row_index(i + kStages + 1);
+    issue(next_row[0], st);
+#pragma unroll
+    for (int j = 0; j + 1 < kAhead; ++j) next_row[j] = next_row[j + 1];
+    next_row[kAhead - 1] = row_index(i + kStages + kAhead);
   }
   cp_async_wait<0>();
 

@@ -221,9 +221,10 @@ __device__ __forceinline__ void copy_staged_rows(const DeviceState& s, const Ste
 }
 
 // Staged gather, balanced: the same copy, with the cells of all units cut
-// into chunks of kStageChunk that the CTAs take one at a time from a counter
-// (match zeroes it), so a CTA whose chunks held more misses simply takes
-// fewer of them and the CTAs end together.  A chunk's cells are loaded, and
+// into chunks (a power of two of 128 .. kStageChunk cells, about two per CTA
+// at least, so a small step still spreads over every CTA) that the CTAs take
+// one at a time from a counter (match zeroes it): a CTA whose chunks held
+// more misses simply takes fewer of them and the CTAs end together.  A chunk's cells are loaded, and
 // the next chunk taken, while the previous chunk's rows are in flight, so
 // the host link sees no gap between chunks.  Dependents (the miss pass) are
 // released when a CTA finds no chunk left.
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kThreads) gather_stage_dyn_kernel(DeviceState 
   __shared__ int s_n[2];
   __shared__ long long s_chunk[2];
   constexpr int kPer = kStageChunk / kThreads;
+  constexpr int kMinChunk = 128;
   griddep_wait();
   if (load_err(s.err) != 0) {  // uniform over the CTA
     griddep_launch();
@@ -243,7 +245,9 @@ __global__ void __launch_bounds__(kThreads) gather_stage_dyn_kernel(DeviceState 
   const StepBufs sb = step_bufs(s, load_io(s.io).parity);
   const int lane = threadIdx.x & 31;
   const long long ncell = (long long)s.U * s.MS;
-  const long long nchunk = (ncell + kStageChunk - 1) / kStageChunk;
+  int chunk = kStageChunk;
+  while (chunk > kMinChunk && ncell < 2LL * chunk * gridDim.x) chunk >>= 1;
+  const long long nchunk = (ncell + chunk - 1) / chunk;
   unsigned long long w[kPer];
   // claimed cells of chunk c (held in w) -> list b
   auto compact = [&](long long c, int b) {
@@ -266,8 +270,9 @@ __global__ void __launch_bounds__(kThreads) gather_stage_dyn_kernel(DeviceState 
   auto load_cells = [&](long long c) {
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
-      const long long cell = c * kStageChunk + e * kThreads + (int)threadIdx.x;
-      w[e] = c < nchunk && cell < ncell ? __ldcg(s.mset + cell) : kMissEmpty;
+      const int off = e * kThreads + (int)threadIdx.x;
+      const long long cell = c * chunk + off;
+      w[e] = c < nchunk && off < chunk && cell < ncell ? __ldcg(s.mset + cell) : kMissEmpty;
     }
   };
   if (threadIdx.x == 0) {
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) gather_stage_dyn_kernel(DeviceState 
     const long long next = s_chunk[b ^ 1];
     if (next >= nchunk) griddep_launch();  // this CTA's last chunk
     load_cells(next);                      // in flight beside this chunk's copies
-    copy_staged_rows(s, sb, s_chunk[b] * kStageChunk, s_off[b], s_id[b], s_n[b]);
+    copy_staged_rows(s, sb, s_chunk[b] * chunk, s_off[b], s_id[b], s_n[b]);
     compact(next, b ^ 1);
     __syncthreads();  // list b ^ 1 complete; list b is rewritten two chunks on
   }
@@ -448,7 +453,9 @@ cudaError_t launch_place(const DeviceState& s, int which, int ctas, cudaStream_t
   static int attr_done = 0;
   const cudaError_t e = ensure_smem((const void*)place_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(place_kernel, dim3((unsigned)ctas), dim3(kThreads), 0, st, s, which);
+  // Not launched early: resident early behind match, its CTAs would hold
+  // registers on every SM that the hit pass needs when match ends.
+  return launch_ex(false, place_kernel, dim3((unsigned)ctas), dim3(kThreads), 0, st, s, which);
 }
 
 cudaError_t launch_gather_all(const DeviceState& s, const StepIO& v, int n_tok, int k, int ctas,

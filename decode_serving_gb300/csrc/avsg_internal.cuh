@@ -77,7 +77,7 @@ struct DeviceState {
   int32_t* tag;                    // [U][B] resident id or kEmpty
   int32_t* last;                   // [U][B] step of last selection, -1 never
   uint32_t* hitbits;               // [U][HT][HW] this step's hit slots per token (written by match)
-  int2* htab;                      // [U][HS] {key, slot}
+  int4* htab;                      // [U][HS] {key, slot, seq, cell}: seq and cell as in pend
   int32_t* hused;                  // [U] non-empty hash cells (live + erased)
   unsigned long long* mset;        // [U][MS] {id | token bits << 32}: this step's miss set
                                    // (two sets alternate by step; each is empty when its step starts)
@@ -97,12 +97,21 @@ struct DeviceState {
   // Deferred place (two-pass pipeline): a step's missed rows reach their
   // slots during the next step, so that step's hits on them read the staged
   // copy.  pend[u][slot] = (seq of the step that reserved the slot) << 32 |
-  // its miss-set cell; stage_entry0 = entry index, counted from kbuf (and
-  // from vbuf: the staging area follows each buffer at the same distance), of
-  // the first staged entry.  deferred = 0: no pend (the other pipelines).
+  // its miss-set cell; the hash-table update copies it into the id's cell,
+  // where match finds it in the window it already read (pend itself is read
+  // only to rebuild the table).  stage_entry0 = entry index, counted from
+  // kbuf (and from vbuf: the staging area follows each buffer at the same
+  // distance), of the first staged entry.  deferred = 0: no pend, and the
+  // hash cells' seq stays -1 (the other pipelines).
   unsigned long long* pend;
   int64_t stage_entry0;
   int32_t deferred;
+  // late_commit = 1 (the overlapped pipelines, where no kernel of the step
+  // reads them before the hash-table update): the update, not the
+  // reservation, writes the reserved slots' new tags and resolves the slot
+  // map's miss entries, so the reservation that the miss pass waits for
+  // keeps only what that pass and the place need.
+  int32_t late_commit;
 };
 
 // The per-step arrays of one parity.
@@ -126,18 +135,26 @@ __host__ __device__ __forceinline__ StepBufs step_bufs(const DeviceState& s, int
   return b;
 }
 
-// The slot value the hit pass reads for a hit on `slot` at step `seq`: the
-// slot itself, or, when the previous step reserved it (its row is still in
-// that step's half of the staging area until the deferred place), the
-// staged entry expressed as a slot of unit u counted from kbuf.
+// The slot value the hit pass reads for a hit on `slot` at step `seq`, from
+// the id's hash cell {key, slot, mseq, mcell}: the slot itself, or, when the
+// previous step reserved it (mseq == seq - 1: its row is still in that
+// step's half of the staging area until the deferred place), the staged
+// entry expressed as a slot of unit u counted from kbuf.
 __device__ __forceinline__ int32_t hit_row_slot(const DeviceState& s, int u, int32_t slot,
-                                                uint32_t seq) {
-  if (!s.deferred || seq == 0) return slot;
-  const unsigned long long p = __ldcg(s.pend + (size_t)u * s.B + slot);
-  if (p == ~0ull || (uint32_t)(p >> 32) != seq - 1) return slot;
+                                                int32_t mseq, int32_t mcell, uint32_t seq) {
+  if (!s.deferred || seq == 0 || mseq != (int32_t)(seq - 1) || mcell < 0) return slot;
   const int64_t e = s.stage_entry0 + (int64_t)((seq - 1) & 1) * s.U * s.MS +
-                    (int64_t)u * s.MS + (int64_t)(uint32_t)p - (int64_t)u * s.B;
+                    (int64_t)u * s.MS + (int64_t)mcell - (int64_t)u * s.B;
   return (int32_t)e;
+}
+
+// Two adjacent 16-byte hash cells in one 32-byte load, cached in L2 only (a
+// window of the table; p is 32-byte aligned).
+__device__ __forceinline__ void ldcg_cells2(const int4* p, int4& a, int4& b) {
+  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                 "=r"(b.w)
+               : "l"(p));
 }
 
 __device__ __forceinline__ uint32_t fib_hash(int32_t id, int shift) {
@@ -223,6 +240,7 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   return launch_ex(true, kernel, grid, block, smem, st, args...);
 }
 
+
 // Raises a kernel's dynamic shared memory limit once per size, and asks for
 // the largest shared-memory carveout so consecutive kernels of a step keep
 // one L1/shared split.
@@ -243,7 +261,7 @@ cudaError_t launch_budget(const DeviceState& s, const int32_t* budget_new, cudaS
 // Hash-table update of a step (erase evicted ids, insert new ones, rebuild):
 // needed only by the next step's match, so it may run beside the gather and
 // the attention.
-cudaError_t launch_commit(const DeviceState& s, cudaStream_t st);
+cudaError_t launch_commit(const DeviceState& s, int n_tok, int k, cudaStream_t st);
 cudaError_t launch_gather(const DeviceState& s, int ctas, cudaStream_t st);
 // Staged gather: right after match, the host row of every claimed miss-set
 // cell is copied to kstage/vstage at that cell (no slot needed yet); chunks

@@ -16,9 +16,11 @@
 // Per id:
 //   * range check (id in [0, live), the entries live this step), else BAD_SELECTION;
 //   * lookup in the unit's open-addressed table (linear probing, Fibonacci
-//     hash; a probe reads a 16-byte window of two cells);
+//     hash; a probe reads a 32-byte window of two 16-byte cells {key, slot,
+//     seq, cell}, one DRAM sector);
 //   * a hit writes its slot (slot map and the hit-slot list the attention
-//     over hit rows reads) and sets the slot's bit in the token's hit bitmap
+//     over hit rows reads: the staged copy when the cell's seq names the
+//     previous step) and sets the slot's bit in the token's hit bitmap
 //     (a bit already set means the id repeats within one token's list);
 //   * a miss is entered in the step's miss set (one cell per distinct id,
 //     claimed or extended with one compare-and-swap; token bits merged, so a
@@ -73,12 +75,6 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
   // No descriptors of this step's parity until its reservation writes them
   // (a step that fails leaves none for the place that follows it).
   if (rank == 0 && tid == 0) s.dcount[(size_t)v.parity * s.U + u] = 0;
-  {  // this unit's q, copied to a buffer the attention kernels read at a fixed place
-    const int nq = n_tok * s.G * s.D;
-    const float* src = v.q + (size_t)u * nq;
-    float* dst = s.qbuf + (size_t)u * nq;
-    for (int i = rank * kThreads + tid; i < nq; i += kC * kThreads) dst[i] = __ldcg(src + i);
-  }
   if (tid == 0) s_stop = load_err(s.err);  // a latched error from an earlier step
   const size_t ubase = (size_t)u * n;
   const int first = rank * kThreads + tid;
@@ -91,14 +87,23 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
   __syncthreads();
   const bool stop = s_stop != 0;  // uniform over the cluster's work below
 
-  const int2* tab = s.htab + (size_t)u * s.HS;
+  // First windows of two 16-byte cells (one 32-byte sector), starting at the
+  // even cell at or before the home cell.
+  const int4* tab = s.htab + (size_t)u * s.HS;
   const uint32_t mask = (uint32_t)s.HS - 1u;
-  int4 win[kPer];
+  int4 wa[kPer], wb[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const bool valid = !stop && first + j * kC * kThreads < n && id[j] >= 0 && id[j] < v.live;
-    win[j] = valid ? __ldcg(reinterpret_cast<const int4*>(tab + (fib_hash(id[j], s.hs_shift) & ~1u)))
-                   : make_int4(kEmpty, -1, kEmpty, -1);
+    wa[j] = wb[j] = make_int4(kEmpty, -1, -1, -1);
+    if (valid) ldcg_cells2(tab + (fib_hash(id[j], s.hs_shift) & ~1u), wa[j], wb[j]);
+  }
+  {  // this unit's q, copied to a buffer the attention kernels read at a fixed
+     // place (its loads in flight beside the windows)
+    const int nq = n_tok * s.G * s.D;
+    const float* src = v.q + (size_t)u * nq;
+    float* dst = s.qbuf + (size_t)u * nq;
+    for (int i = rank * kThreads + tid; i < nq; i += kC * kThreads) dst[i] = __ldcg(src + i);
   }
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
@@ -114,25 +119,25 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
       if (hit) hit[off] = 0;
       continue;
     }
-    // Windows of two cells, starting at the even cell at or before the home
-    // cell: a cell before the home cell never holds this id, and an empty
-    // one there does not end the probe.
+    // Windows of two cells: a cell before the home cell never holds this id,
+    // and an empty one there does not end the probe.
     const uint32_t home = fib_hash(x, s.hs_shift);
     uint32_t cell = home & ~1u;
     bool skip_first = (home & 1u) != 0;
-    int4 w = win[j];
-    int slot = -1;
+    int4 a = wa[j], b = wb[j];
+    int4 found = make_int4(kEmpty, -1, -1, -1);
     for (int probes = 0; probes < s.HS; probes += 2) {
-      if (probes) w = __ldcg(reinterpret_cast<const int4*>(tab + (cell & mask)));
+      if (probes) ldcg_cells2(tab + (cell & mask), a, b);  // cell is even: no wrap inside
       if (!skip_first) {
-        if (w.x == x) { slot = w.y; break; }
-        if (w.x == kEmpty) break;
+        if (a.x == x) { found = a; break; }
+        if (a.x == kEmpty) break;
       }
-      if (w.z == x) { slot = w.w; break; }
-      if (w.z == kEmpty) break;
+      if (b.x == x) { found = b; break; }
+      if (b.x == kEmpty) break;
       skip_first = false;
       cell += 2;
     }
+    const int slot = found.x == x ? found.y : -1;
     if (slot >= 0 && !AVSG_IN_BOUNDS(slot < s.B, s.err, u, pos)) continue;
     if (slot >= 0) {
       const int word = slot >> 5;
@@ -141,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) match_kernel(DeviceState s, StepIO v
       const uint32_t old = atomicOr(&bits[tok * HWL + word / kC], b);
       if (old & b) raise_error(s.err, AVSG_ERR_BAD_SELECTION, u, pos);
       slot_map[off] = slot;
-      s.hslot[off] = hit_row_slot(s, u, slot, v.seq);
+      s.hslot[off] = hit_row_slot(s, u, slot, found.z, found.w, v.seq);
       if (hit) hit[off] = 1;
     } else {
       const uint32_t mmask = (uint32_t)s.MS - 1u;

@@ -44,10 +44,10 @@ __device__ __forceinline__ int next_pow2(int x) {
 // stored further on would have stopped at that empty cell), otherwise a
 // tombstone.  Concurrent erases stay valid: a cell only turns empty behind an
 // empty cell.  Returns 1 when a cell was freed.
-__device__ int hash_erase(int2* tab, uint32_t mask, int shift, int32_t key) {
+__device__ int hash_erase(int4* tab, uint32_t mask, int shift, int32_t key) {
   uint32_t c = fib_hash(key, shift);
   for (uint32_t i = 0; i <= mask; ++i, ++c) {
-    int2* p = tab + (c & mask);
+    int4* p = tab + (c & mask);
     const int32_t kk = *(volatile int32_t*)&p->x;
     if (kk == key) {
       const int32_t next = *(volatile int32_t*)&tab[(c + 1) & mask].x;
@@ -64,16 +64,20 @@ __device__ int hash_erase(int2* tab, uint32_t mask, int shift, int32_t key) {
 }
 
 // Linear-probing insert of a key known to be absent; takes the first empty or
-// erased cell on the probe path.  Returns 1 if it consumed an empty cell.
-__device__ int hash_insert(int2* tab, uint32_t mask, int shift, int32_t key, int32_t slot,
-                           DevErr* err, int unit) {
+// erased cell on the probe path and stores {key, slot, mseq, mcell} there
+// (mseq, mcell: the deferred-place marker, -1 when none).  Returns 1 if it
+// consumed an empty cell.
+__device__ int hash_insert(int4* tab, uint32_t mask, int shift, int32_t key, int32_t slot,
+                           int32_t mseq, int32_t mcell, DevErr* err, int unit) {
   uint32_t c = fib_hash(key, shift);
   for (uint32_t i = 0; i <= 2 * mask + 2 * kThreads; ++i) {
-    int2* p = tab + (c & mask);
+    int4* p = tab + (c & mask);
     const int32_t kk = *(volatile int32_t*)&p->x;
     if (kk == kEmpty || kk == kTomb) {
       if (atomicCAS(&p->x, kk, key) == kk) {
         p->y = slot;
+        p->z = mseq;
+        p->w = mcell;
         return kk == kEmpty ? 1 : 0;
       }
       continue;  // another insert took this cell; look at it again
@@ -140,6 +144,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum) {
   return r;
 }
 
+// A reservation key packs id << 32 | token bits << 24 | miss-set cell.
+static_assert(kMaxTokens <= 8, "token bits fit the key's 8 bits");
+static_assert(2LL * kMatchCluster * kMatchThreads * kMatchPerThread <= (1LL << 24),
+              "a miss-set cell fits the key's 24 bits");
+
 constexpr int kBatch = 8;  // 32-slot chunks whose state one warp loads before using it
 static_assert(kBatch == 8, "the hit-word loads map lane & 7 to a chunk, lane >> 3 to a token");
 
@@ -158,27 +167,20 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
   uint8_t* ord = smem + lay.ord;
 
   griddep_wait();
-  const StepIO io = load_io(s.io);
-  const int t = io.t;
-  const StepBufs sb = step_bufs(s, io.parity);
-  const int budget = __ldcg(s.budget + u);  // this unit's usable slots (buffer elasticity)
-  int32_t* __restrict__ slot_map = io.slot_map;
-  if (tid == 0) {
-    s_stop = load_err(s.err);
-    s_hits = 0;
-  }
-  __syncthreads();
-  if (s_stop) {
-    griddep_launch();
-    return;
-  }
-
   const int B = s.B;
   const size_t ub = (size_t)u * B;
   unsigned long long* ms = s.mset + (size_t)u * s.MS;
+  // Issued before anything waits: the step's record and the error word, this
+  // unit's budget, the slot state of the first kBatch chunks and the first
+  // round of the unit's miss-set cells.
+  const StepIO io = load_io(s.io);
+  const int budget = __ldcg(s.budget + u);  // this unit's usable slots (buffer elasticity)
+  if (tid == 0) {
+    s_stop = load_err(s.err);
+    s_hits = 0;
+    s_m = 0;
+  }
 
-  // The slot state of the first kBatch chunks is loaded now, so that its
-  // latency overlaps phase 1's dependent loads.
   const int chunk = ((B + kWarps * 32 - 1) / (kWarps * 32)) * 32;  // slots per warp
   const int w_begin = warp * chunk, w_end = min(B, w_begin + chunk);
   int sn[kBatch], tg[kBatch], ls[kBatch];
@@ -217,38 +219,52 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
     }
   };
   load_batch(w_begin);
-
-  // 1. Distinct missing ids: every claimed cell of the unit's miss set, as
-  //    key = id << 32 | cell (one coalesced pass, compacted by ballots), and
-  //    the rank of each in ascending id order: counted directly when there
-  //    are few, otherwise by a bitonic sort.
-  if (tid == 0) s_m = 0;
-  __syncthreads();
-  constexpr int kCellsAhead = 4;  // miss-set cells a thread loads before compacting
-  for (int c0 = 0; c0 < s.MS; c0 += kThreads * kCellsAhead) {
-    unsigned long long wv[kCellsAhead];
+  constexpr int kCellsAhead = 8;  // miss-set cells a thread loads before compacting
+  unsigned long long wv[kCellsAhead];
+  auto load_cells = [&](int c0) {
 #pragma unroll
     for (int e = 0; e < kCellsAhead; ++e) {
       const int cell = c0 + e * kThreads + tid;
       wv[e] = cell < s.MS ? __ldcg(ms + cell) : kMissEmpty;
     }
+  };
+  load_cells(0);
+  __syncthreads();
+  if (s_stop) {
+    griddep_launch();
+    return;
+  }
+  const int t = io.t;
+  const StepBufs sb = step_bufs(s, io.parity);
+  int32_t* __restrict__ slot_map = io.slot_map;
+
+  // 1. Distinct missing ids: every claimed cell of the unit's miss set, as
+  //    key = id << 32 | token bits << 24 | cell (one coalesced pass,
+  //    compacted by ballots), and the rank of each in ascending id order:
+  //    counted directly when there are few, otherwise by a bitonic sort.
+  for (int c0 = 0; c0 < s.MS; c0 += kThreads * kCellsAhead) {
+    if (c0) load_cells(c0);
 #pragma unroll
     for (int e = 0; e < kCellsAhead; ++e) {
-    if (c0 + e * kThreads >= s.MS) break;  // warp-uniform
-    const int cell = c0 + e * kThreads + tid;
-    const unsigned long long w = wv[e];
-    const bool used = w != kMissEmpty;
-    const unsigned bal = __ballot_sync(0xffffffffu, used);
-    int wbase = 0;
-    if (lane == 0 && bal) wbase = atomicAdd(&s_m, __popc(bal));
-    wbase = __shfl_sync(0xffffffffu, wbase, 0);
-    if (used)
-      keys[wbase + __popc(bal & ((1u << lane) - 1u))] =
-          ((unsigned long long)(uint32_t)w << 32) | (uint32_t)cell;
+      if (c0 + e * kThreads >= s.MS) break;  // warp-uniform
+      const int cell = c0 + e * kThreads + tid;
+      const unsigned long long w = wv[e];
+      const bool used = w != kMissEmpty;
+      const unsigned bal = __ballot_sync(0xffffffffu, used);
+      int wbase = 0;
+      if (lane == 0 && bal) wbase = atomicAdd(&s_m, __popc(bal));
+      wbase = __shfl_sync(0xffffffffu, wbase, 0);
+      if (used)
+        keys[wbase + __popc(bal & ((1u << lane) - 1u))] =
+            ((unsigned long long)(uint32_t)w << 32) | (((w >> 32) & 0xFFull) << 24) |
+            (uint32_t)cell;
     }
   }
   __syncthreads();
   const int m = s_m;
+  // this unit's descriptor range, claimed now (its latency overlaps the ranking)
+  int base_claim = 0;
+  if (tid == 0 && m > 0) base_claim = atomicAdd(sb.desc_count, m);
   const bool counting = m <= kCountRankMax;
   const int P = counting ? m : next_pow2(m);
   for (int i = m + tid; i < P; i += kThreads) keys[i] = ~0ull;
@@ -314,8 +330,9 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
   }
 
   // 2. Reservation order of every slot; per-warp histogram over orders (each
-  //    warp owns a contiguous slot range and a private row of counters, so
-  //    plain shared-memory atomics need no ordering).
+  //    warp owns a contiguous slot range and a private row of counters; the
+  //    lanes of a chunk are grouped by order with one match, and each group's
+  //    lowest lane adds its size with a shared-memory atomic).
   int hits = 0;
   for (int base = w_begin; base < w_begin + chunk; base += 32 * kBatch) {
     if (base != w_begin) load_batch(base);
@@ -323,21 +340,22 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int sl = base + b * 32 + lane;
-      if (sl >= w_end || base + b * 32 >= w_begin + chunk) continue;
+      const bool in = sl < w_end && base + b * 32 < w_begin + chunk;  // uniform but the tail
       int o = kNotCandidate;
-      if (sn[b] > 0) {
+      if (in && sn[b] > 0) {
         s.last[ub + sl] = t;  // selected this step: refreshed, never a victim
         ++hits;
-      } else if (sn[b] == 0 && sl < budget) {  // slots at or above the budget are not used
+      } else if (in && sn[b] == 0 && sl < budget) {  // slots at or above the budget are not used
         if (tg[b] == kEmpty) {
           o = 0;
         } else {
           const int age = max(1, t - ls[b]);
           o = kOrders - min(kOrders - 1, age);
         }
-        atomicAdd(&wstart[o * kWarps + warp], 1);
       }
-      ord[sl] = (uint8_t)o;
+      const unsigned grp = __match_any_sync(0xffffffffu, o);
+      if (o != kNotCandidate && lane == __ffs(grp) - 1) atomicAdd(&wstart[o * kWarps + warp], __popc(grp));
+      if (in) ord[sl] = (uint8_t)o;
     }
   }
   hits = __reduce_add_sync(0xffffffffu, hits);
@@ -369,38 +387,38 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
   const int o_max = s_omax;
 
   // 4. Rank within order by slot index, only for orders <= o_max; the first
-  //    m ranks are the victims.  Lanes of a chunk are grouped by order with a
-  //    ballot per distinct order present (usually one or two).
+  //    m ranks are the victims.  The lanes of a chunk are grouped by order
+  //    with one match: a lane's rank is its group's running start plus the
+  //    group's lanes below it, and the group's lowest lane advances the start.
   if (o_max >= 0) {
     for (int base = w_begin; base < w_begin + chunk; base += 32) {
       const int sl = base + lane;
       const int o = sl < w_end ? (int)ord[sl] : kNotCandidate;
-      unsigned todo = __ballot_sync(0xffffffffu, o <= o_max);
-      while (todo) {
-        const int leader = __ffs(todo) - 1;
-        const int ol = __shfl_sync(0xffffffffu, o, leader);
-        const unsigned peers = __ballot_sync(0xffffffffu, o == ol && o <= o_max);
-        const int start = wstart[ol * kWarps + warp];
-        if (o == ol) {
-          const int r = start + __popc(peers & ((1u << lane) - 1u));
-          if (r < m) victim[r] = sl;
-        }
-        __syncwarp();
-        if (lane == leader) wstart[ol * kWarps + warp] = start + __popc(peers);
-        __syncwarp();
-        todo &= ~peers;
+      const bool cand = o <= o_max;
+      if (__ballot_sync(0xffffffffu, cand) == 0u) continue;  // uniform over the warp
+      const unsigned grp = __match_any_sync(0xffffffffu, cand ? o : -1);
+      const int start = cand ? wstart[o * kWarps + warp] : 0;
+      __syncwarp();  // every lane has read its group's start
+      if (cand) {
+        const int r = start + __popc(grp & ((1u << lane) - 1u));
+        if (r < m) victim[r] = sl;
+        if (lane == __ffs(grp) - 1) wstart[o * kWarps + warp] = start + __popc(grp);
       }
+      __syncwarp();
     }
   }
-  if (tid == 0) s_base = m > 0 ? atomicAdd(sb.desc_count, m) : 0;
+  if (tid == 0) s_base = base_claim;
   __syncthreads();
 
-  // 5. Reserve: new tags and last_step, gather descriptors (with the evicted
-  //    id, for the hash-table update that runs later), miss-set cells freed.
+  // 5. Reserve: last_step, gather descriptors (with the tokens that selected
+  //    the id), the cell -> slot map and the deferred-place marker; the new
+  //    tags (and the evicted ids, for the hash-table update) here only when
+  //    the update does not write them itself (late_commit = 0).
   for (int i = tid; i < m; i += kThreads) {
     const unsigned long long key = keys[i];
     const int32_t id = (int32_t)(key >> 32);
-    const int cell = (int)(uint32_t)key;
+    const int cell = (int)(key & 0xFFFFFFu);
+    const int32_t toks = (int32_t)((key >> 24) & 0xFFu);
     const int r = rank[i];
     if (!AVSG_IN_BOUNDS(r >= 0 && r < m, s.err, u, i)) continue;
     const int v = victim[r];
@@ -408,9 +426,11 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
                             id < io.live && s_base + r < s.U * s.max_union,
                         s.err, u, i))
       continue;
-    const int32_t old = s.tag[ub + v];
-    const int32_t toks = (int32_t)(__ldcg(ms + cell) >> 32);
-    s.tag[ub + v] = id;
+    int32_t old = kEmpty;
+    if (!s.late_commit) {
+      old = s.tag[ub + v];
+      s.tag[ub + v] = id;
+    }
     s.last[ub + v] = t;
     s.mslot[(size_t)u * s.MS + cell] = v;
     if (s.deferred) s.pend[ub + v] = ((unsigned long long)io.seq << 32) | (uint32_t)cell;
@@ -418,10 +438,11 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
   }
   __syncthreads();
 
-  // 6. Resolve slot-map entries of misses (-2 - cell -> reserved slot).
-  //    Thread t takes positions t, t + 1024, ... (coalesced) and issues its
-  //    loads before using them.
-  const int n = n_tok * k;
+  // 6. Resolve slot-map entries of misses (-2 - cell -> reserved slot),
+  //    unless the hash-table update does (late_commit).  Thread t takes
+  //    positions t, t + kThreads, ... (coalesced) and issues its loads
+  //    before using them.
+  const int n = s.late_commit ? 0 : n_tok * k;
   constexpr int kRun = 4;
   for (int c0 = 0; c0 < n; c0 += kThreads * kRun) {
     int sm[kRun];
@@ -452,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
 // ids it loaded, rebuild from the tags when erased cells pile up.
 constexpr int kCommitThreads = 256;  // small CTAs: they share SMs with the attention
 
-__global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
+__global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s, int n_tok, int k) {
   __shared__ int s_stop, s_used, s_freed, s_rebuild, s_live;
   const int u = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -466,14 +487,37 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
   }
   __syncthreads();
   if (s_stop) return;
-  const StepBufs sb = step_bufs(s, load_io(s.io).parity);
+  const StepIO io = load_io(s.io);
+  const StepBufs sb = step_bufs(s, io.parity);
   const int m = sb.dcount[u], base = sb.dbase[u];
-  int2* tab = s.htab + (size_t)u * s.HS;
+  const size_t ub = (size_t)u * s.B;
+  int4* tab = s.htab + (size_t)u * s.HS;
   const uint32_t hmask = (uint32_t)s.HS - 1u;
+  // the marker of an id this step loaded: its row stays staged until the
+  // next step's place
+  const int32_t mseq = s.deferred ? (int32_t)io.seq : -1;
+  if (s.late_commit) {
+    // the slot map's miss entries (-2 - cell -> the slot reserved for the cell)
+    const int n = n_tok * k;
+    int32_t* slot_map = io.slot_map + (size_t)u * n;
+    for (int p = tid; p < n; p += kCommitThreads) {
+      const int sm = slot_map[p];
+      if (sm <= -2 && AVSG_IN_BOUNDS(-2 - sm < s.MS, s.err, u, p))
+        slot_map[p] = s.mslot[(size_t)u * s.MS + (-2 - sm)];
+    }
+  }
   int freed = 0;
   for (int i = tid; i < m; i += kCommitThreads) {
     if (!AVSG_IN_BOUNDS(base + i < s.U * s.max_union, s.err, u, i)) continue;
-    const int32_t old = sb.desc[base + i].old_id;
+    int32_t old;
+    if (s.late_commit) {  // the reserved slot's evicted id, then its new one
+      const GatherDesc d = sb.desc[base + i];
+      if (!AVSG_IN_BOUNDS(d.slot >= 0 && d.slot < s.B, s.err, u, i)) continue;
+      old = s.tag[ub + d.slot];
+      s.tag[ub + d.slot] = d.id;
+    } else {
+      old = sb.desc[base + i].old_id;
+    }
     if (old != kEmpty) freed += hash_erase(tab, hmask, s.hs_shift, old);
   }
   freed = __reduce_add_sync(0xffffffffu, freed);
@@ -485,7 +529,8 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
     const GatherDesc d = sb.desc[base + i];
     if (!AVSG_IN_BOUNDS(d.slot >= 0 && d.slot < s.B && d.id >= 0 && d.id < s.L, s.err, u, i))
       continue;
-    used += hash_insert(tab, hmask, s.hs_shift, d.id, d.slot, s.err, u);
+    used += hash_insert(tab, hmask, s.hs_shift, d.id, d.slot, mseq, s.deferred ? d.cell : -1,
+                        s.err, u);
   }
   used = __reduce_add_sync(0xffffffffu, used);
   if (lane == 0 && used) atomicAdd(&s_used, used);
@@ -498,14 +543,21 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s) {
   __syncthreads();
   if (s_rebuild) {
     const int B = s.B;
-    const size_t ub = (size_t)u * B;
-    for (int i = tid; i < s.HS; i += kCommitThreads) tab[i] = make_int2(kEmpty, kEmpty);
+    for (int i = tid; i < s.HS; i += kCommitThreads) tab[i] = make_int4(kEmpty, -1, -1, -1);
     __syncthreads();
     int live = 0;
     for (int sl = tid; sl < B; sl += kCommitThreads) {
       const int32_t tg = s.tag[ub + sl];
       if (tg != kEmpty) {
-        hash_insert(tab, hmask, s.hs_shift, tg, sl, s.err, u);
+        int32_t ms = -1, mc = -1;  // this step's loads keep their marker (from pend)
+        if (s.deferred) {
+          const unsigned long long pm = s.pend[ub + sl];
+          if (pm != ~0ull && (int32_t)(pm >> 32) == mseq) {
+            ms = mseq;
+            mc = (int32_t)(uint32_t)pm;
+          }
+        }
+        hash_insert(tab, hmask, s.hs_shift, tg, sl, ms, mc, s.err, u);
         ++live;
       }
     }
@@ -537,7 +589,7 @@ __global__ void __launch_bounds__(kCommitThreads) budget_kernel(DeviceState s,
   griddep_launch();
   if (load_err(s.err) != 0) return;
   const int old_b = __ldcg(s.budget + u), new_b = budget_new[u];
-  int2* tab = s.htab + (size_t)u * s.HS;
+  int4* tab = s.htab + (size_t)u * s.HS;
   const uint32_t hmask = (uint32_t)s.HS - 1u;
   const size_t ub = (size_t)u * s.B;
   int freed = 0;
@@ -567,11 +619,11 @@ cudaError_t launch_victims(const DeviceState& s, int n_tok, int k, cudaStream_t 
   return launch_pdl(victims_kernel, dim3(s.U), dim3(kThreads), smem, st, s, n_tok, k);
 }
 
-cudaError_t launch_commit(const DeviceState& s, cudaStream_t st) {
+cudaError_t launch_commit(const DeviceState& s, int n_tok, int k, cudaStream_t st) {
   static int attr_done = 0;
   const cudaError_t e = ensure_smem((const void*)commit_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(commit_kernel, dim3(s.U), dim3(kCommitThreads), 0, st, s);
+  return launch_pdl(commit_kernel, dim3(s.U), dim3(kCommitThreads), 0, st, s, n_tok, k);
 }
 
 }  // namespace avsg
