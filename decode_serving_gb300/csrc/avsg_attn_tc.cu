@@ -79,6 +79,20 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src)
                : "memory");
 }
+// The same with an L2 cache policy (from l2_evict_first_policy).
+__device__ __forceinline__ void cp_async16_hint(void* smem_dst, const void* gmem_src,
+                                                unsigned long long policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(gmem_src), "l"(policy)
+               : "memory");
+}
+// Lines read under this policy are the first the L2 evicts.
+__device__ __forceinline__ unsigned long long l2_evict_first_policy() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -146,6 +160,11 @@ struct TcParams {
   // two passes: the hit pass is persistent (hit_ctas CTAs over all pairs'
   // tiles, like the single pass)
   int hit_ctas;
+  // 1: rows are read as the L2's first eviction candidates.  The hit pass
+  // streams every hit row once per step, beside the gather writing the
+  // staging rows the miss pass reads next: read this way, the hit rows do
+  // not push the staged rows out of the L2 before the miss pass gets them.
+  int evict_first;
 };
 
 struct SegArgs {
@@ -238,6 +257,7 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
   constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
   constexpr int RPI = 32 / CPR;    // rows per warp instruction
   unsigned long long vmasks = 0;  // 16 bits per stage: which rows of the staged tile are real
+  const unsigned long long policy = p.evict_first ? l2_evict_first_policy() : 0ull;
   auto issue = [&](long long myrow, int st) {
     const unsigned long long vm = __ballot_sync(0xffffffffu, myrow >= 0) & 0xFFFFu;
     vmasks = (vmasks & ~(0xFFFFull << (16 * st))) | (vm << (16 * st));
@@ -248,7 +268,11 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
     for (int it = 0; it < kTileRows / RPI; ++it) {
       const int r = it * RPI + rsub;
       const long long srow = __shfl_sync(0xffffffffu, myrow, r);
-      if (srow >= 0) {
+      if (srow >= 0 && p.evict_first) {
+        cp_async16_hint(kst + r * PITCH + ch * 16, s.kbuf + srow * (2 * D) + ch * 16, policy);
+        if (!SH::SHARED)
+          cp_async16_hint(vst + r * PITCH + ch * 16, s.vbuf + srow * (2 * D) + ch * 16, policy);
+      } else if (srow >= 0) {
         cp_async16(kst + r * PITCH + ch * 16, s.kbuf + srow * (2 * D) + ch * 16);
         if (!SH::SHARED) cp_async16(vst + r * PITCH + ch * 16, s.vbuf + srow * (2 * D) + ch * 16);
       } else {  // no row: zeros (finite values, which P = 0 cancels)
@@ -1088,16 +1112,20 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
   griddep_wait();  // the gather's rows are in the staging area
   griddep_launch();
   if (tid == 0) s_stop = load_err(s.err);
+  // the step's record and this unit's descriptor range of both parities,
+  // loaded together (the range of the step's parity is then picked)
+  const StepIO io = load_io(s.io);
+  const int m_p[2] = {__ldcg(s.dcount + u), __ldcg(s.dcount + s.U + u)};
+  const int b_p[2] = {__ldcg(s.dbase + u), __ldcg(s.dbase + s.U + u)};
   cp_async_wait<0>();
   __syncthreads();
   if (s_stop) return;
-  const StepIO io = load_io(s.io);
   const StepBufs sb = step_bufs(s, io.parity);
   DeviceState sv = s;  // the staged view: rows by miss-set cell in this step's half
   sv.kbuf = sb.kstage;
   sv.vbuf = sb.vstage;
   sv.B = s.MS;
-  const int m = __ldcg(sb.dcount + u), base = __ldcg(sb.dbase + u);
+  const int m = io.parity ? m_p[1] : m_p[0], base = io.parity ? b_p[1] : b_p[0];
   const GatherDesc* desc = sb.desc + base;
   float* co = reinterpret_cast<float*>(smem) + kWarpsTc * NT * G * D;
 
@@ -1266,6 +1294,7 @@ template <class SH>
 cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, cudaStream_t st) {
   static int smem_hits = 0;
   TcParams p = two_pass_params<SH>(s, a);
+  p.evict_first = pass == 0 ? 1 : 0;
   const HitGrid g = hit_grid(s.U * a.n_tok, a.k, s.ET, a.num_sms);
   const size_t parts = (size_t)s.U * a.n_tok * 2 + 2 * (size_t)g.ctas;
   if (parts * SH::G * (SH::D + 2) > a.part_capacity || g.max_seg + 1 > SH::MAX_SEG)
