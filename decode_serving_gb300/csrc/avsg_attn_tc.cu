@@ -1243,7 +1243,8 @@ cudaError_t run_tc(const DeviceState& s, const AttnLaunch& a, int num_sms, cudaS
   const long long pairs = (long long)s.U * a.n_tok;
   p.tiles = pairs * p.tiles_per_pair;
   long long C = (long long)num_sms * kCtasPerSm;
-  if (C > p.tiles) C = p.tiles;
+  if (C > (p.tiles + kWarpsTc - 1) / kWarpsTc) C = (p.tiles + kWarpsTc - 1) / kWarpsTc;  // a tile per warp
+  if (C < 1) C = 1;
   const size_t stride = (size_t)SH::G * (SH::D + 2);
   for (;;) {
     const long long per = p.tiles / C;  // fewest tiles a CTA gets
@@ -1270,8 +1271,9 @@ inline HitGrid hit_grid(int pairs, int k, int ET, int num_sms) {
   HitGrid g;
   g.tiles_per_pair = (k * ET + kTileRows - 1) / kTileRows;
   g.tiles = (long long)pairs * g.tiles_per_pair;
+  // at least one tile per warp: fewer, fuller CTAs leave fewer partials
   long long C = (long long)num_sms * kCtasPerSm;
-  if (C > g.tiles) C = g.tiles;
+  if (C > (g.tiles + kWarpsTc - 1) / kWarpsTc) C = (g.tiles + kWarpsTc - 1) / kWarpsTc;
   g.ctas = (int)(C < 1 ? 1 : C);
   const long long per = g.tiles / g.ctas;  // fewest tiles a CTA gets
   g.max_seg = (int)((g.tiles_per_pair + per - 1) / per + 1);

@@ -330,9 +330,8 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
   }
 
   // 2. Reservation order of every slot; per-warp histogram over orders (each
-  //    warp owns a contiguous slot range and a private row of counters; the
-  //    lanes of a chunk are grouped by order with one match, and each group's
-  //    lowest lane adds its size with a shared-memory atomic).
+  //    warp owns a contiguous slot range and a private row of counters, so
+  //    plain shared-memory atomics need no ordering).
   int hits = 0;
   for (int base = w_begin; base < w_begin + chunk; base += 32 * kBatch) {
     if (base != w_begin) load_batch(base);
@@ -340,22 +339,21 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int sl = base + b * 32 + lane;
-      const bool in = sl < w_end && base + b * 32 < w_begin + chunk;  // uniform but the tail
+      if (sl >= w_end || base + b * 32 >= w_begin + chunk) continue;
       int o = kNotCandidate;
-      if (in && sn[b] > 0) {
+      if (sn[b] > 0) {
         s.last[ub + sl] = t;  // selected this step: refreshed, never a victim
         ++hits;
-      } else if (in && sn[b] == 0 && sl < budget) {  // slots at or above the budget are not used
+      } else if (sn[b] == 0 && sl < budget) {  // slots at or above the budget are not used
         if (tg[b] == kEmpty) {
           o = 0;
         } else {
           const int age = max(1, t - ls[b]);
           o = kOrders - min(kOrders - 1, age);
         }
+        atomicAdd(&wstart[o * kWarps + warp], 1);
       }
-      const unsigned grp = __match_any_sync(0xffffffffu, o);
-      if (o != kNotCandidate && lane == __ffs(grp) - 1) atomicAdd(&wstart[o * kWarps + warp], __popc(grp));
-      if (in) ord[sl] = (uint8_t)o;
+      ord[sl] = (uint8_t)o;
     }
   }
   hits = __reduce_add_sync(0xffffffffu, hits);
@@ -387,24 +385,27 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
   const int o_max = s_omax;
 
   // 4. Rank within order by slot index, only for orders <= o_max; the first
-  //    m ranks are the victims.  The lanes of a chunk are grouped by order
-  //    with one match: a lane's rank is its group's running start plus the
-  //    group's lanes below it, and the group's lowest lane advances the start.
+  //    m ranks are the victims.  Lanes of a chunk are grouped by order with a
+  //    ballot per distinct order present (usually one or two).
   if (o_max >= 0) {
     for (int base = w_begin; base < w_begin + chunk; base += 32) {
       const int sl = base + lane;
       const int o = sl < w_end ? (int)ord[sl] : kNotCandidate;
-      const bool cand = o <= o_max;
-      if (__ballot_sync(0xffffffffu, cand) == 0u) continue;  // uniform over the warp
-      const unsigned grp = __match_any_sync(0xffffffffu, cand ? o : -1);
-      const int start = cand ? wstart[o * kWarps + warp] : 0;
-      __syncwarp();  // every lane has read its group's start
-      if (cand) {
-        const int r = start + __popc(grp & ((1u << lane) - 1u));
-        if (r < m) victim[r] = sl;
-        if (lane == __ffs(grp) - 1) wstart[o * kWarps + warp] = start + __popc(grp);
+      unsigned todo = __ballot_sync(0xffffffffu, o <= o_max);
+      while (todo) {
+        const int leader = __ffs(todo) - 1;
+        const int ol = __shfl_sync(0xffffffffu, o, leader);
+        const unsigned peers = __ballot_sync(0xffffffffu, o == ol && o <= o_max);
+        const int start = wstart[ol * kWarps + warp];
+        if (o == ol) {
+          const int r = start + __popc(peers & ((1u << lane) - 1u));
+          if (r < m) victim[r] = sl;
+        }
+        __syncwarp();
+        if (lane == leader) wstart[ol * kWarps + warp] = start + __popc(peers);
+        __syncwarp();
+        todo &= ~peers;
       }
-      __syncwarp();
     }
   }
   if (tid == 0) s_base = base_claim;
@@ -470,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, 2) victims_kernel(DeviceState s, int
 }
 
 // Hash-table update of one unit: erase the ids this step evicted, insert the
-// ids it loaded, rebuild from the tags when erased cells pile up.
+// ids it loaded, rebuild from the tags when erased cells pile up.  With
+// late_commit, CTA (u, 0) also moves the reserved slots' tags and CTA (u, 1)
+// resolves the unit's slot-map entries of misses.
 constexpr int kCommitThreads = 256;  // small CTAs: they share SMs with the attention
 
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s, int n_tok, int k) {
@@ -496,8 +499,9 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s, i
   // the marker of an id this step loaded: its row stays staged until the
   // next step's place
   const int32_t mseq = s.deferred ? (int32_t)io.seq : -1;
-  if (s.late_commit) {
-    // the slot map's miss entries (-2 - cell -> the slot reserved for the cell)
+  if (blockIdx.y == 1) {
+    // (late_commit) the slot map's miss entries, -2 - cell -> the slot
+    // reserved for the cell: a CTA of its own beside the hash update
     const int n = n_tok * k;
     int32_t* slot_map = io.slot_map + (size_t)u * n;
     for (int p = tid; p < n; p += kCommitThreads) {
@@ -505,6 +509,7 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(DeviceState s, i
       if (sm <= -2 && AVSG_IN_BOUNDS(-2 - sm < s.MS, s.err, u, p))
         slot_map[p] = s.mslot[(size_t)u * s.MS + (-2 - sm)];
     }
+    return;
   }
   int freed = 0;
   for (int i = tid; i < m; i += kCommitThreads) {
@@ -623,7 +628,8 @@ cudaError_t launch_commit(const DeviceState& s, int n_tok, int k, cudaStream_t s
   static int attr_done = 0;
   const cudaError_t e = ensure_smem((const void*)commit_kernel, 0, &attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(commit_kernel, dim3(s.U), dim3(kCommitThreads), 0, st, s, n_tok, k);
+  return launch_pdl(commit_kernel, dim3(s.U, s.late_commit ? 2 : 1), dim3(kCommitThreads), 0, st, s,
+                    n_tok, k);
 }
 
 }  // namespace avsg
