@@ -31,12 +31,15 @@
 //   union of a multi-token step's misses -- and merges both passes into the
 //   output.
 // No CTA waits for another.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math.h>
 
 #include <type_traits>
 
 #include "avsg_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace avsg {
 namespace {
@@ -508,7 +511,7 @@ __device__ void tc_segment(const DeviceState& s, const TcParams& p, const SegArg
 // fragments of a tile are loaded once for all tokens.  Per-warp shared
 // memory: the stages, then NT P tiles.  Results, in shared memory: cm[j * G
 // + h], cl[j * G + h], co[(j * G + h) * D + d].
-template <class SH, int NT>
+template <class SH, int NT, int ST>
 __device__ void tc_segment_union(const DeviceState& s, const TcParams& p, const SegArgs& a,
                                  const uint8_t* masks, unsigned char* smem, float* cm, float* cl,
                                  float* co, float (*s_m)[NT * SH::G],
@@ -517,14 +520,14 @@ __device__ void tc_segment_union(const DeviceState& s, const TcParams& p, const 
   constexpr int PITCH = SH::PITCH;
   constexpr int NH = G == 1 ? 1 : 2;              // heads per thread
   constexpr int OWNERS = G >= 2 ? G / 2 : 1;      // lanes c < OWNERS own their heads
-  constexpr int WB = kStages * SH::STAGE_BYTES + NT * SH::PTILE_BYTES;
+  constexpr int WB = ST * SH::STAGE_BYTES + NT * SH::PTILE_BYTES;
   static_assert(NT * 16 <= 64, "token row masks of a stage fit 64 bits");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int head_base = G == 1 ? 0 : 2 * (c % OWNERS);
   const bool owner = c < OWNERS;
   unsigned char* wbase = smem + warp * WB;
-  unsigned char* ptile0 = wbase + kStages * SH::STAGE_BYTES;
+  unsigned char* ptile0 = wbase + ST * SH::STAGE_BYTES;
   const int u = a.u;
 
   float m[NT][NH], l[NT][NH];
@@ -561,7 +564,7 @@ __device__ void tc_segment_union(const DeviceState& s, const TcParams& p, const 
   constexpr int RPI = 32 / CPR;    // rows per warp instruction
   // Per stage: bits [16 j, 16 j + 16) mark the tile's rows token j selected.
   unsigned long long tm0 = 0, tm1 = 0, tm2 = 0;
-  static_assert(kStages == 3, "three stage masks");
+  static_assert(ST == 2 || ST == 3, "two or three stage masks");
   auto issue = [&](long long myrow, uint32_t mybits, int st) {
     unsigned long long tm = 0;
 #pragma unroll
@@ -569,7 +572,7 @@ __device__ void tc_segment_union(const DeviceState& s, const TcParams& p, const 
       tm |= (unsigned long long)(__ballot_sync(0xffffffffu, myrow >= 0 && ((mybits >> j) & 1u)) &
                                  0xFFFFu)
             << (16 * j);
-    if (st == 0) tm0 = tm; else if (st == 1) tm1 = tm; else tm2 = tm;
+    if (st == 0) tm0 = tm; else if (st == 1) tm1 = tm; else tm2 = tm;  // (tm2 unused at ST = 2)
     unsigned char* kst = wbase + st * SH::STAGE_BYTES;
     unsigned char* vst = SH::SHARED ? kst : kst + kTileRows * PITCH;
     const int ch = lane % CPR, rsub = lane / CPR;
@@ -591,14 +594,14 @@ __device__ void tc_segment_union(const DeviceState& s, const TcParams& p, const 
   long long next_row;
   uint32_t next_bits;
   {
-    long long first_rows[kStages + 1];
-    uint32_t first_bits[kStages + 1];
+    long long first_rows[ST + 1];
+    uint32_t first_bits[ST + 1];
 #pragma unroll
-    for (int i = 0; i <= kStages; ++i) first_rows[i] = row_index(i, first_bits[i]);
+    for (int i = 0; i <= ST; ++i) first_rows[i] = row_index(i, first_bits[i]);
 #pragma unroll
-    for (int i = 0; i < kStages; ++i) issue(first_rows[i], first_bits[i], i);
-    next_row = first_rows[kStages];
-    next_bits = first_bits[kStages];
+    for (int i = 0; i < ST; ++i) issue(first_rows[i], first_bits[i], i);
+    next_row = first_rows[ST];
+    next_bits = first_bits[ST];
   }
   // q fragments of every token: column n < G is hi(q_n), G <= n < 2G is lo(q_{n-G})
   uint32_t qb[NT][KS][NTN][2];
@@ -624,8 +627,8 @@ __device__ void tc_segment_union(const DeviceState& s, const TcParams& p, const 
     }
 
   for (int i = 0; i < n_my; ++i) {
-    const int st = i % kStages;
-    cp_async_wait<kStages - 1>();
+    const int st = i % ST;
+    cp_async_wait<ST - 1>();
     __syncwarp();
     const unsigned long long tm = st == 0 ? tm0 : st == 1 ? tm1 : tm2;
     const unsigned char* kst = wbase + st * SH::STAGE_BYTES;
@@ -761,7 +764,7 @@ __device__ void tc_segment_union(const DeviceState& s, const TcParams& p, const 
     }
     __syncwarp();  // every lane has read stage st and the P tiles
     issue(next_row, next_bits, st);
-    next_row = row_index(i + kStages + 1, next_bits);
+    next_row = row_index(i + ST + 1, next_bits);
   }
   cp_async_wait<0>();
 
@@ -1072,9 +1075,15 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_hits_kernel(DeviceState s,
 // follows the reservation and the hit pass.  `s` is the real state.
 constexpr int kMissChunk = 512;
 
+// Stages per warp of the union pass: two, so that two of its CTAs share an
+// SM; and CTAs per unit (a cluster, merged through distributed shared memory).
+constexpr int kUnionStages = 2;
+constexpr int kUnionCluster = 2;
+
 template <class SH, int NT>
 struct MissSmem {
-  static constexpr int WB = kStages * SH::STAGE_BYTES + NT * SH::PTILE_BYTES;  // per warp
+  static constexpr int ST = NT > 1 ? kUnionStages : kStages;               // stages per warp
+  static constexpr int WB = ST * SH::STAGE_BYTES + NT * SH::PTILE_BYTES;  // per warp
   static constexpr int LIST = kWarpsTc * WB;                                  // [kMissChunk] cells
   static constexpr int MASKS = LIST + kMissChunk * 4;                         // [kMissChunk] bits
   static constexpr int RUN = MASKS + (NT > 1 ? kMissChunk : 0);                // [NT][G][D]
@@ -1097,6 +1106,8 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
   __shared__ float run_m[NT * G], run_l[NT * G], wa[NT * G], wb[NT * G];
   __shared__ __align__(16) float s_q[NT * G * D];
   __shared__ int s_stop, s_wsum[kWarpsTc];
+  cg::cluster_group clu = cg::this_cluster();
+  const int cs = (int)clu.num_blocks(), crank = (int)clu.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int u = NT == 1 ? (int)blockIdx.y / p.n_tok : (int)blockIdx.y;
   const int tok0 = NT == 1 ? (int)blockIdx.y - u * p.n_tok : 0;
@@ -1119,18 +1130,21 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
   const int b_p[2] = {__ldcg(s.dbase + u), __ldcg(s.dbase + s.U + u)};
   cp_async_wait<0>();
   __syncthreads();
-  if (s_stop) return;
+  // (a CTA that stops skips its work, not the cluster barriers)
+  const bool stop = s_stop != 0;
   const StepBufs sb = step_bufs(s, io.parity);
   DeviceState sv = s;  // the staged view: rows by miss-set cell in this step's half
   sv.kbuf = sb.kstage;
   sv.vbuf = sb.vstage;
   sv.B = s.MS;
-  const int m = io.parity ? m_p[1] : m_p[0], base = io.parity ? b_p[1] : b_p[0];
+  const int m = stop ? 0 : io.parity ? m_p[1] : m_p[0], base = io.parity ? b_p[1] : b_p[0];
   const GatherDesc* desc = sb.desc + base;
   float* co = reinterpret_cast<float*>(smem) + kWarpsTc * NT * G * D;
+  // this CTA's contiguous share of the unit's descriptors
+  const int d0 = (int)((long long)crank * m / cs), d1 = (int)((long long)(crank + 1) * m / cs);
 
-  for (int c0 = 0; c0 < m; c0 += kMissChunk) {
-    const int cn = min(kMissChunk, m - c0);
+  for (int c0 = d0; c0 < d1; c0 += kMissChunk) {
+    const int cn = min(kMissChunk, d1 - c0);
     int nlist = cn;
     if (NT == 1) {
       // the chunk's entries this token selected, in descriptor order
@@ -1183,7 +1197,7 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
     if constexpr (NT == 1)
       tc_segment<SH>(sv, p, a, smem, cm, cl, co, s_m, s_l);
     else
-      tc_segment_union<SH, NT>(sv, p, a, masks, smem, cm, cl, co, s_m, s_l);
+      tc_segment_union<SH, NT, L::ST>(sv, p, a, masks, smem, cm, cl, co, s_m, s_l);
     // fold the chunk's result into the running one
     if (tid < NT * G) {
       const float M = fmaxf(run_m[tid], cm[tid]);
@@ -1199,24 +1213,30 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_miss_kernel(DeviceState s,
     __syncthreads();
   }
 
-  // each pair's hit-pass partials (global) merged with its miss result (here)
+  clu.sync();  // every CTA's miss result is in its shared memory
+
+  // each pair's hit-pass partials (global) merged with the cluster's miss
+  // results (shared memory of its CTAs): CTA j of the cluster merges token j
   const size_t stride = (size_t)G * (D + 2);
-  for (int j = 0; j < NT; ++j) {
+  for (int j = crank; j < NT && !stop; j += cs) {
     const int pair = u * p.n_tok + tok0 + j;
     long long slot0 = 0;
     const int nseg_h = hit_segments(p, pair, &slot0);
     const float* part = s.part;
-    const float* rm = run_m + j * G;
-    const float* rl = run_l + j * G;
-    const float* ro = run_o + j * G * D;
     tc_merge_partials<G, D>(
         [&](int q2, int i) -> float {
-          if (q2 == nseg_h) return i < G ? rm[i] : i < 2 * G ? rl[i - G] : ro[i - 2 * G];
+          if (q2 >= nseg_h) {
+            const unsigned r = (unsigned)(q2 - nseg_h);
+            if (i < G) return *clu.map_shared_rank(run_m + j * G + i, r);
+            if (i < 2 * G) return *clu.map_shared_rank(run_l + j * G + i - G, r);
+            return *clu.map_shared_rank(run_o + j * G * D + i - 2 * G, r);
+          }
           return __ldcg(part + (size_t)two_pass_slot(p, pair, nseg_h, slot0, q2) * stride + i);
         },
-        nseg_h + 1, io.out + (size_t)pair * G * D, co);
+        nseg_h + cs, io.out + (size_t)pair * G * D, co);
     __syncthreads();
   }
+  clu.sync();  // no CTA leaves while another reads its shared memory
 }
 
 template <class SH>
@@ -1299,7 +1319,7 @@ cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, cud
   p.evict_first = pass == 0 ? 1 : 0;
   const HitGrid g = hit_grid(s.U * a.n_tok, a.k, s.ET, a.num_sms);
   const size_t parts = (size_t)s.U * a.n_tok * 2 + 2 * (size_t)g.ctas;
-  if (parts * SH::G * (SH::D + 2) > a.part_capacity || g.max_seg + 1 > SH::MAX_SEG)
+  if (parts * SH::G * (SH::D + 2) > a.part_capacity || g.max_seg + kUnionCluster > SH::MAX_SEG)
     return cudaErrorInvalidValue;
   if (pass == 0) {
     cudaError_t e = ensure_smem((const void*)attn_tc_hits_kernel<SH>, SH::SMEM, &smem_hits);
@@ -1317,12 +1337,16 @@ cudaError_t run_tc_pass(const DeviceState& s, const AttnLaunch& a, int pass, cud
     using L = MissSmem<SH, NT>;
     cudaError_t e = ensure_smem((const void*)attn_tc_miss_kernel<SH, NT>, L::BYTES, &smem_miss);
     if (e != cudaSuccess) return e;
-    dim3 grid(1u, (unsigned)(NT == 1 ? s.U * a.n_tok : s.U));
+    // The union pass: a cluster of kUnionCluster CTAs per unit, each on a
+    // share of the unit's rows (two of its CTAs fit an SM).
+    const int cs = NT > 1 ? kUnionCluster : 1;
+    dim3 grid((unsigned)cs, (unsigned)(NT == 1 ? s.U * a.n_tok : s.U));
     // Launched early behind the gather (its CTAs wait for it): the launch
     // also follows the hit pass and the reservation, which release their
     // dependents only as they end, so the early CTAs take no SM the hit
     // pass still needs.
-    return launch_pdl(attn_tc_miss_kernel<SH, NT>, grid, dim3(kThreadsTc), L::BYTES, st, s, p);
+    return launch_pdl_cluster(cs, attn_tc_miss_kernel<SH, NT>, grid, dim3(kThreadsTc), L::BYTES,
+                              st, s, p);
   };
   // (the union keeps NT sets of accumulators in registers: shapes with one
   // n-tile of query columns only)

@@ -239,6 +239,26 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
                        cudaStream_t st, Args... args) {
   return launch_ex(true, kernel, grid, block, smem, st, args...);
 }
+// The same with thread-block clusters of cluster_x CTAs along x.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl_cluster(int cluster_x, void (*kernel)(Params...), dim3 grid, dim3 block,
+                               size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
 
 
 // Raises a kernel's dynamic shared memory limit once per size, and asks for

@@ -57,6 +57,12 @@ SMALL = {
     # staged gather, one cluster per (unit, token))
     "latent_mtp": W.get_workload("latent", requests=2, context=8192, k=200, slots=1024, steps=6,
                                  tokens_per_step=3),
+    # two query tokens per step (the union miss pass with two sets of accumulators)
+    "mtp2_small": W.get_workload("mtp", requests=2, kv_heads=2, context=8192, k=300, slots=1024,
+                                 steps=10, tokens_per_step=2),
+    # the union miss pass at D = 64, one query head per kv-head
+    "mtp_d64_g1": W.get_workload("mtp", requests=2, kv_heads=3, context=8192, k=200, slots=1024,
+                                 steps=8, head_dim=64, v_dim=64, q_per_kv=1),
     # 19 splits of 106 rows each: four tiles per CTA, the last one ragged
     "latent_multi_tile": W.get_workload("latent", requests=8, context=16384, k=2000, slots=2048,
                                         steps=4),
