@@ -26,6 +26,27 @@ __device__ __forceinline__ uint4 load_host16(const void* p) {
   return v;
 }
 
+// 16-byte load and store marked as the L2's first eviction candidates (the
+// place: its rows are not read again this step, and the staged rows the miss
+// pass is about to read should stay in the L2 instead).
+__device__ __forceinline__ unsigned long long l2_evict_first() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 load16_evict_first(const uint4* p, unsigned long long pol) {
+  uint4 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void store16_evict_first(void* p, uint4 v, unsigned long long pol) {
+  asm volatile("st.global.cg.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
 __device__ __forceinline__ void store16(void* p, uint4 v) {
   asm volatile("st.global.cg.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
@@ -317,6 +338,7 @@ __global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s, int whic
   const StepBufs sb = step_bufs(s, load_io(s.io).parity ^ which);
   const uint32_t cpk = (uint32_t)(s.ek >> 4), cpe = cpk + (uint32_t)(s.ev >> 4);
   const long long total = (long long)__ldcg(sb.desc_count) * cpe;
+  const unsigned long long pol = l2_evict_first();
   const long long begin = (long long)blockIdx.x * total / gridDim.x;
   const long long end = (long long)(blockIdx.x + 1) * total / gridDim.x;
   for (long long i0 = begin + threadIdx.x; i0 < end; i0 += (long long)kThreads * kPlaceRows) {
@@ -350,10 +372,10 @@ __global__ void __launch_bounds__(kThreads) place_kernel(DeviceState s, int whic
     }
 #pragma unroll
     for (int r = 0; r < kPlaceRows; ++r)
-      if (src[r]) v[r] = __ldcg(src[r]);
+      if (src[r]) v[r] = load16_evict_first(src[r], pol);
 #pragma unroll
     for (int r = 0; r < kPlaceRows; ++r)
-      if (dst[r]) store16(dst[r], v[r]);
+      if (dst[r]) store16_evict_first(dst[r], v[r], pol);
   }
 }
 

@@ -19,8 +19,12 @@
  * Within a step the copy of the misses (bound by the host link) overlaps the
  * reservation and the attention over the selected rows that were already
  * resident: the library runs the gather (into a staging area), the
- * reservation and the hash-table update on two internal streams, forked from
- * and joined back into the caller's stream with events.
+ * reservation, the hash-table update and the move of the previous step's
+ * staged rows into their slots on three internal streams, forked from and
+ * joined back into the caller's stream with events.  A step's missed rows
+ * reach their slots during the next step (its hits on them read the staged
+ * copy); avsg_read_state, avsg_set_budget and avsg_clear_error move them
+ * first, so every entry point sees the buffer of the step-by-step order.
  *
  * Reservation order (the pages give no formula; this is the reading the
  * library implements): empty slots first, by ascending slot index; then the
