@@ -27,10 +27,11 @@
 //   hit slots match wrote; misses are masked) and runs beside the gather and
 //   the reservation; the miss pass (attn_tc_miss_kernel) covers the missed
 //   rows, read from the staging area by miss-set cell from the reservation's
-//   descriptors, with one CTA per (unit, token) -- or per unit, over the
-//   union of a multi-token step's misses -- and merges both passes into the
-//   output.
-// No CTA waits for another.
+//   descriptors, with one CTA per (unit, token) -- or a cluster of two CTAs
+//   per unit, over the union of a multi-token step's misses -- and merges
+//   both passes into the output.
+// No CTA waits for another kernel's CTAs; the union pass's cluster barriers
+// are hardware barriers over co-scheduled CTAs.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -1068,11 +1069,14 @@ __global__ void __launch_bounds__(kThreadsTc) attn_tc_hits_kernel(DeviceState s,
 // and the bits of the tokens that selected it), in chunks of kMissChunk
 // entries whose results are merged as they come.  NT == 1: CTA = one (unit,
 // token), over the unit's misses that token selected.  NT > 1 (a step of NT
-// query tokens): CTA = one unit, over the union of its misses, each row
-// attended by the tokens that selected it (tc_segment_union).  The CTA then
-// writes the pair's (pairs') miss partial and merges it with the hit pass's
-// into the output: the grid-dependency wait covers the gather, and the launch
-// follows the reservation and the hit pass.  `s` is the real state.
+// query tokens): a cluster of kUnionCluster CTAs per unit, CTA r on the r-th
+// contiguous share of the unit's descriptors, over the union of its misses,
+// each row attended by the tokens that selected it (tc_segment_union).  After
+// a cluster barrier, CTA j merges token j's hit-pass partials with the
+// cluster's miss results (read from the CTAs' shared memories) into the
+// output; a second barrier keeps every CTA's shared memory alive until then.
+// The grid-dependency wait covers the gather, and the launch follows the
+// reservation and the hit pass.  `s` is the real state.
 constexpr int kMissChunk = 512;
 
 // Stages per warp of the union pass: two, so that two of its CTAs share an
